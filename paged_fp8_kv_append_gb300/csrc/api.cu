@@ -1,0 +1,317 @@
+// api.cu -- the C ABI declared in include/kvfp8.h: argument validation,
+// launch configuration and workspace carve-up.  All compute is in the
+// kernels of append.cu, verify.cu, decode_gqa.cu and decode_latent.cu.
+#include <math.h>
+
+#include <new>
+
+#include "internal.h"
+
+using namespace kvfp8;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+namespace kvfp8 {
+
+kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig* cfg) {
+  const kv_pool_desc& d = pool->d;
+  if (B < 0 || Hq <= 0 || T <= 0) return KV_ERR_INVALID_ARG;
+  if (d.layout == KV_LAYOUT_GQA) {
+    if (Hq % d.num_kv_heads != 0) return KV_ERR_INVALID_ARG;
+    const int G = Hq / d.num_kv_heads;
+    if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || T * G > 8)
+      return KV_ERR_UNSUPPORTED;
+    cfg->kind = d.dtype == KV_DTYPE_E4M3 ? 0 : 1;
+    const int sms = sm_count();
+    const int per_sm = sms > 0 ? gqa_split_ctas_per_sm(cfg->kind) : 0;
+    if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
+    cfg->grid = sms * per_sm;
+    if (cfg->grid > 4000) cfg->grid = 4000;  // the combine holds <= 4096 piece weights
+    cfg->R8 = 8;
+    return KV_OK;
+  }
+  // latent layout
+  if (d.head_dim_k != 576 || d.head_dim_v != 512 || d.page_size != 64 || T * Hq % 128 != 0)
+    return KV_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  const int per_sm = sms > 0 ? latent_split_ctas_per_sm() : 0;
+  if (sms <= 0 || per_sm <= 0) return KV_ERR_UNSUPPORTED;
+  cfg->kind = 2;
+  cfg->grid = sms * per_sm;
+  cfg->R8 = T * Hq;
+  return KV_OK;
+}
+
+size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
+                        void* base, DecodeWs* ws) {
+  const long long slots = (long long)B * Hkv + cfg.grid;
+  size_t off = 0;
+  const size_t o_pfx = off;
+  off = align256(off + sizeof(int32_t) * (size_t)(B + 1));
+  const size_t o_skip = off;
+  off = align256(off + (size_t)B);
+  const size_t o_bad = off;
+  off = align256(off + (size_t)B);
+  const size_t o_ml = off;
+  off = align256(off + sizeof(float) * 2 * (size_t)slots * cfg.R8);
+  const size_t o_o = off;
+  off = align256(off + sizeof(float) * (size_t)slots * cfg.R8 * d.head_dim_v);
+  if (ws) {
+    uint8_t* b = static_cast<uint8_t*>(base);
+    ws->pfx = reinterpret_cast<int32_t*>(b + o_pfx);
+    ws->rq_skip = b + o_skip;
+    ws->rq_bad = b + o_bad;
+    ws->ml_part = reinterpret_cast<float*>(b + o_ml);
+    ws->o_part = reinterpret_cast<float*>(b + o_o);
+    ws->bytes = off;
+  }
+  return off;
+}
+
+}  // namespace kvfp8
+
+namespace {
+
+kv_status decode_prepare(kv_pool* pool, int32_t B, int32_t Hq, int32_t T, const void* q,
+                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                         const uint8_t* abort_mask, float sm_scale, void* out, void* workspace,
+                         size_t workspace_bytes, bool need_inputs, bool need_out,
+                         DecodeArgs* a, int* kind) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  const kv_pool_desc& d = pool->d;
+  if (B < 0 || Hq <= 0 || T <= 0) return KV_ERR_INVALID_ARG;
+  if (B > 0) {
+    if (need_inputs && (!q || !page_table || !seq_lens || max_pages <= 0 || !aligned16(q) ||
+                        !isfinite(sm_scale)))
+      return KV_ERR_INVALID_ARG;
+    if (need_out && !out) return KV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return KV_ERR_INVALID_ARG;
+  }
+  DecodeConfig cfg;
+  const kv_status st = decode_config(pool, B, Hq, T, &cfg);
+  if (st != KV_OK) return st;
+  const int Hkv = d.num_kv_heads;
+  DecodeArgs& x = *a;
+  x.d = d;
+  x.B = B;
+  x.Hq = Hq;
+  x.T = T;
+  x.G = Hq / Hkv;
+  x.R = (d.layout == KV_LAYOUT_GQA) ? T * x.G : T * Hq;
+  x.q = static_cast<const uint16_t*>(q);
+  x.page_table = page_table;
+  x.max_pages = max_pages;
+  x.seq_lens = seq_lens;
+  x.abort_mask = abort_mask;
+  x.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  x.out = static_cast<uint16_t*>(out);
+  x.grid = cfg.grid;
+  x.R8 = cfg.R8;
+  const size_t need = decode_ws_layout(d, B, Hkv, cfg, workspace, &x.ws);
+  if (B > 0 && workspace_bytes < need) return KV_ERR_INVALID_ARG;
+  *kind = cfg.kind;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status kv_pool_create(const kv_pool_desc* desc, kv_pool** out) {
+  if (!desc || !out) return KV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const kv_pool_desc& d = *desc;
+  if (d.num_pages <= 0 || d.page_size <= 0 || d.page_size > 1024 || d.num_kv_heads <= 0 ||
+      d.head_dim_k <= 0 || d.head_dim_v <= 0 || d.head_dim_k % 16 != 0 ||
+      d.head_dim_v % 16 != 0 || d.head_dim_k > 1024 || d.head_dim_v > 1024)
+    return KV_ERR_INVALID_ARG;
+  if (d.dtype != KV_DTYPE_E4M3 && d.dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (d.layout != KV_LAYOUT_GQA && d.layout != KV_LAYOUT_LATENT) return KV_ERR_INVALID_ARG;
+  if (!d.k_cache || !d.tags || !d.free_list || !d.ctl) return KV_ERR_INVALID_ARG;
+  if (!aligned16(d.k_cache) || !aligned16(d.tags) || !aligned16(d.free_list) ||
+      !aligned16(d.ctl))
+    return KV_ERR_INVALID_ARG;
+  if (d.layout == KV_LAYOUT_GQA) {
+    if (!d.v_cache || !aligned16(d.v_cache)) return KV_ERR_INVALID_ARG;
+    if (d.dtype == KV_DTYPE_E4M3 && (!d.k_scale || !d.v_scale)) return KV_ERR_INVALID_ARG;
+    // the dim-major V tile of one page must fit the append kernel's staging
+    if ((long long)d.head_dim_v * d.page_size * (d.dtype == KV_DTYPE_E4M3 ? 1 : 2) > 160 * 1024)
+      return KV_ERR_UNSUPPORTED;
+  } else {
+    if (d.dtype != KV_DTYPE_E4M3) return KV_ERR_UNSUPPORTED;
+    if (d.num_kv_heads != 1 || d.head_dim_v > d.head_dim_k || !d.k_scale)
+      return KV_ERR_INVALID_ARG;
+  }
+  kv_pool* p = new (std::nothrow) kv_pool;
+  if (!p) return KV_ERR_INVALID_ARG;
+  p->d = d;
+  p->last_launches = 0;
+  *out = p;
+  return KV_OK;
+}
+
+kv_status kv_pool_destroy(kv_pool* pool) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  delete pool;
+  return KV_OK;
+}
+
+kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B, const void* k_new,
+                             const void* v_new, const int32_t* new_indptr,
+                             int32_t max_new_per_req, int32_t* page_table, uint32_t* exp_tags,
+                             int32_t max_pages_per_req, int32_t* seq_lens) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  const kv_pool_desc& d = pool->d;
+  if (B < 0 || max_new_per_req < 0 || max_pages_per_req <= 0) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!new_indptr || !page_table || !exp_tags || !seq_lens) return KV_ERR_INVALID_ARG;
+  if (max_new_per_req > 0) {
+    if (!k_new || !aligned16(k_new)) return KV_ERR_INVALID_ARG;
+    if (d.layout == KV_LAYOUT_GQA && (!v_new || !aligned16(v_new))) return KV_ERR_INVALID_ARG;
+  }
+  AppendArgs a;
+  a.d = d;
+  a.B = B;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.new_indptr = new_indptr;
+  a.max_new = max_new_per_req;
+  a.page_table = page_table;
+  a.exp_tags = exp_tags;
+  a.max_pages = max_pages_per_req;
+  a.seq_lens = seq_lens;
+  int n = 0;
+  const cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status kv_verify_tags(kv_pool* pool, void* stream, int32_t B, const int32_t* page_table,
+                         const uint32_t* exp_tags, int32_t max_pages_per_req,
+                         const int32_t* seq_lens, uint8_t* abort_mask) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  if (B < 0 || max_pages_per_req <= 0) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!page_table || !exp_tags || !seq_lens || !abort_mask) return KV_ERR_INVALID_ARG;
+  VerifyArgs a;
+  a.num_pages = pool->d.num_pages;
+  a.page_size = pool->d.page_size;
+  a.B = B;
+  a.max_pages = max_pages_per_req;
+  a.tags = pool->d.tags;
+  a.page_table = page_table;
+  a.exp_tags = exp_tags;
+  a.seq_lens = seq_lens;
+  a.abort_mask = abort_mask;
+  int n = 0;
+  const cudaError_t e = launch_verify(a, static_cast<cudaStream_t>(stream), &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+size_t paged_decode_workspace_size(const kv_pool* pool, int32_t B, int32_t num_q_heads,
+                                   int32_t q_tokens) {
+  if (!pool || B < 0) return 0;
+  DecodeConfig cfg;
+  if (decode_config(pool, B, num_q_heads, q_tokens, &cfg) != KV_OK) return 0;
+  return decode_ws_layout(pool->d, B, pool->d.num_kv_heads, cfg, nullptr, nullptr);
+}
+
+kv_status paged_decode_attn_split(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                                  int32_t q_tokens, const void* q, const int32_t* page_table,
+                                  int32_t max_pages_per_req, const int32_t* seq_lens,
+                                  const uint8_t* abort_mask, float sm_scale, void* workspace,
+                                  size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  DecodeArgs a;
+  int kind = 0;
+  const kv_status st =
+      decode_prepare(pool, B, num_q_heads, q_tokens, q, page_table, max_pages_per_req, seq_lens,
+                     abort_mask, sm_scale, nullptr, workspace, workspace_bytes, true, false, &a,
+                     &kind);
+  if (st != KV_OK || B == 0) return st;
+  int n = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_plan(a, s, &n);
+  if (e == cudaSuccess) e = launch_decode_split(a, kind, s, &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status paged_decode_attn_combine(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                                    int32_t q_tokens, const uint8_t* abort_mask, void* out,
+                                    void* workspace, size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  DecodeArgs a;
+  int kind = 0;
+  const kv_status st =
+      decode_prepare(pool, B, num_q_heads, q_tokens, nullptr, nullptr, 1, nullptr, abort_mask,
+                     1.0f, out, workspace, workspace_bytes, false, true, &a, &kind);
+  if (st != KV_OK || B == 0) return st;
+  int n = 0;
+  const cudaError_t e = launch_decode_combine(a, static_cast<cudaStream_t>(stream), &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status paged_decode_attn(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                            int32_t q_tokens, const void* q, const int32_t* page_table,
+                            int32_t max_pages_per_req, const int32_t* seq_lens,
+                            const uint8_t* abort_mask, float sm_scale, void* out,
+                            void* workspace, size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  if (B > 0 && !out) return KV_ERR_INVALID_ARG;
+  kv_status st = paged_decode_attn_split(pool, stream, B, num_q_heads, q_tokens, q, page_table,
+                                         max_pages_per_req, seq_lens, abort_mask, sm_scale,
+                                         workspace, workspace_bytes);
+  if (st != KV_OK) return st;
+  const int n = pool->last_launches;
+  st = paged_decode_attn_combine(pool, stream, B, num_q_heads, q_tokens, abort_mask, out,
+                                 workspace, workspace_bytes);
+  pool->last_launches += n;
+  return st;
+}
+
+const char* kv_status_string(kv_status s) {
+  switch (s) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+    case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA";
+    case KV_ERR_OUT_OF_PAGES: return "KV_ERR_OUT_OF_PAGES";
+    case KV_ERR_BAD_PAGE_ID: return "KV_ERR_BAD_PAGE_ID";
+    case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
+  }
+  return "KV_ERR_UNKNOWN";
+}
+
+int32_t kv_last_launch_count(const kv_pool* pool) { return pool ? pool->last_launches : 0; }
+
+}  // extern "C"
+
+namespace kvfp8 {
+
+cudaError_t launch_decode_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches) {
+  if (kind == 2) return launch_latent_split(a, s, launches);
+  return launch_gqa_split(a, kind, s, launches);
+}
+
+}  // namespace kvfp8

@@ -1,0 +1,746 @@
+// decode_gqa.cu -- split-K paged decode attention over a GQA cache (e4m3 or
+// bf16), the batch plan it runs on, and the combine step.
+//
+// "Smaller, faster, safer: running Kimi and GLM at scale", section
+// "Quantizing the KV cache": decode attention reads the FP8 e4m3 cache and
+// converts values as it reads them; BF16 is the baseline cache format.
+// Section "Protecting a shared KV cache": aborted requests read nothing and
+// return nothing.
+//
+// Work decomposition.  The unit of work is one (page, kv head) pair.  Units
+// are laid out request-major, kv-head-minor ("segments" of ceil(L_r/P) pages
+// each; aborted requests have none) and cut into gridDim.x equal contiguous
+// ranges, one per persistent CTA, so every CTA streams the same number of
+// bytes whatever the length mix.  A CTA range crosses segment boundaries;
+// each (CTA, segment) piece yields one partial (o, running max, sum) in slot
+// segment + cta (injective because both are sorted along the range), and the
+// combine kernel merges the pieces of a segment.
+//
+// CTA layout: warp 4 is the producer: it reads page ids and scales and moves
+// each (page, kv head) K tile and V tile into a shared-memory ring with bulk
+// async copies (cp.async.bulk, completion on an mbarrier).  Warps 0-3 are
+// consumers: page k of the range goes to warp k % 4, which keeps its own
+// online-softmax state and merges with the others at the end of a piece.
+//
+// Per page a consumer computes S^T = K Q^T (M = 16 tokens, N = 8 query rows,
+// K = 128 dims) and O^T += V^T P^T (M = 128 dims, N = 8 rows, K = 16 tokens)
+// with mma.sync m16n8k16.  At 8 query rows per kv head the work is 16 flop per
+// cache byte, beyond what the fp32 CUDA cores sustain at HBM speed, so the
+// tensor pipe carries the dot products and the CUDA cores only convert and
+// run the softmax.  e4m3 codes convert exactly to f16; the per-page scales are
+// applied to the scores (K) and folded into P (V).
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvfp8 {
+namespace {
+
+// ----------------------------------------------------------- batch plan
+
+constexpr int kPlanThreads = 1024;
+
+// pfx[r] = exclusive prefix of pages over requests that get output, rq_skip,
+// rq_bad cleared.  A request is skipped (no pages, no output) when aborted or
+// when its length is negative or needs more pages than its page table holds
+// (that also sets KV_ERR_INVALID_ARG).
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int P = a.d.page_size;
+  int carry = 0;
+  for (int base = 0; base < a.B; base += kPlanThreads) {
+    const int r = base + threadIdx.x;
+    int np = 0;
+    if (r < a.B) {
+      const int L = a.seq_lens[r];
+      const bool aborted = a.abort_mask != nullptr && a.abort_mask[r] != 0;
+      const bool bad_len = L < 0 || (long long)ceil_div(max(L, 0), P) > a.max_pages;
+      if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+      const bool skip = aborted || bad_len;
+      np = skip ? 0 : ceil_div(L, P);
+      a.ws.rq_skip[r] = skip ? 1 : 0;
+      a.ws.rq_bad[r] = 0;
+    }
+    int v = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += n;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
+    if (r < a.B) a.ws.pfx[r] = carry + incl - np;
+    carry += warp_sums[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.ws.pfx[a.B] = carry;
+}
+
+// ------------------------------------------------- segment cursor
+
+// Walks segments (r, h) of the flattened unit sequence.  pfx may live in
+// shared or global memory.
+struct Cursor {
+  int r, h, np;
+  long long seg_start;
+};
+
+__device__ __forceinline__ Cursor cursor_at(const int32_t* pfx, int B, int Hkv, long long x) {
+  // last r with pfx[r] <= x / Hkv; that request has pages (pfx[r+1] > x/Hkv)
+  const long long v = x / Hkv;
+  int lo = 0, hi = B;  // invariant: pfx[lo] <= v < pfx[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pfx[mid] <= v)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  Cursor c;
+  c.r = lo;
+  c.np = pfx[lo + 1] - pfx[lo];
+  c.h = (int)((x - (long long)Hkv * pfx[lo]) / c.np);
+  c.seg_start = (long long)Hkv * pfx[lo] + (long long)c.h * c.np;
+  return c;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* pfx, int B, int Hkv) {
+  if (++c.h == Hkv) {
+    c.h = 0;
+    do {
+      ++c.r;
+    } while (c.r < B && pfx[c.r + 1] == pfx[c.r]);
+    if (c.r < B) c.np = pfx[c.r + 1] - pfx[c.r];
+  }
+  if (c.r < B) c.seg_start = (long long)Hkv * pfx[c.r] + (long long)c.h * c.np;
+}
+
+// ------------------------------------------------- tensor-core helpers
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  // exact: every e4m3 value is an f16 value
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  return f32x2_to_f16x2(lo, hi);
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// ------------------------------------------------- split kernel
+
+template <bool FP8>
+struct GqaCfg {
+  static constexpr int P = 16;                      // tokens per page
+  static constexpr int D = 128;                     // head dim (K and V)
+  static constexpr int ES = FP8 ? 1 : 2;            // cache element bytes
+  static constexpr int TILE = P * D * ES;           // bytes of one K or V tile
+  static constexpr int STAGE = 2 * TILE;            // K tile + V tile
+  static constexpr int STAGES = FP8 ? 12 : 8;       // ring depth
+  static constexpr int CONSUMERS = 4;               // consumer warps
+  static constexpr int THREADS = (CONSUMERS + 1) * 32;
+  static constexpr int R8 = 8;                      // query rows per kv head (padded)
+  static constexpr int PFX_CACHE = 1024;            // pfx entries cached in smem
+  static constexpr int PBUF = FP8 ? R8 * P * 2 : R8 * P * 4;  // per-warp P transpose
+  // shared memory carve-up (byte offsets)
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_MERGE_O = OFF_RING + STAGES * STAGE;              // [C][R8][D] f32
+  static constexpr int OFF_MERGE_ML = OFF_MERGE_O + CONSUMERS * R8 * D * 4;  // [C][R8][2] f32
+  static constexpr int OFF_PBUF = OFF_MERGE_ML + CONSUMERS * R8 * 2 * 4;
+  static constexpr int OFF_META = OFF_PBUF + CONSUMERS * PBUF;               // [STAGES] int4
+  static constexpr int OFF_BAR = OFF_META + STAGES * 16;                    // full, empty
+  static constexpr int OFF_PFX = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;
+  static constexpr int SMEM = OFF_FLAG + 16;
+};
+
+struct StageMeta {
+  int n_valid;  // tokens of this page below the request length (0: skip page)
+  float ks, vs; // K and V scales (1 for bf16)
+  int pos0;     // position of the page's first token
+};
+
+template <bool FP8>
+__global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
+    gqa_split_kernel(const DecodeArgs a) {
+  using C = GqaCfg<FP8>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem + C::OFF_RING;
+  float* merge_o = reinterpret_cast<float*>(smem + C::OFF_MERGE_O);
+  float* merge_ml = reinterpret_cast<float*>(smem + C::OFF_MERGE_ML);
+  uint8_t* pbuf_all = smem + C::OFF_PBUF;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + C::OFF_META);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  int32_t* pfx_s = reinterpret_cast<int32_t*>(smem + C::OFF_PFX);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = a.B, Hkv = a.d.num_kv_heads;
+  const int32_t* pfx_g = a.ws.pfx;
+  const long long total = (long long)pfx_g[B] * Hkv;
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  const long long x_begin = (long long)blockIdx.x * per;
+  const long long x_end = min(total, x_begin + per);
+  if (x_begin >= x_end) return;
+
+  const bool cached = B + 1 <= C::PFX_CACHE;
+  if (cached)
+    for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int32_t* pfx = cached ? pfx_s : pfx_g;
+  const Cursor start = cursor_at(pfx, B, Hkv, x_begin);
+  const int P = C::P, D = C::D;
+
+  if (warp == C::CONSUMERS) {
+    // ======================= producer warp =======================
+    const uint64_t policy = l2_evict_first_policy();
+    Cursor cur = start;
+    long long x = x_begin;
+    long long k = 0;  // stage sequence number
+    const int maxp = a.max_pages;
+    while (x < x_end && !*abort_flag) {
+      const long long seg_end = cur.seg_start + cur.np;
+      const long long piece_end = min(seg_end, x_end);
+      const int r = cur.r, h = cur.h;
+      const int L = a.seq_lens[r];
+      const int j0 = (int)(x - cur.seg_start), j1 = (int)(piece_end - cur.seg_start);
+      const int32_t* pt = a.page_table + (long long)r * maxp;
+      for (int jb = j0; jb < j1 && !*abort_flag; jb += 32) {
+        const int jj = jb + lane;
+        int p = -1;
+        float ks = 1.0f, vs = 1.0f;
+        bool ok = false;
+        if (jj < j1) {
+          p = pt[jj];
+          ok = p >= 0 && p < a.d.num_pages;
+          if (ok && FP8) {
+            ks = a.d.k_scale[(long long)p * Hkv + h];
+            vs = a.d.v_scale[(long long)p * Hkv + h];
+          }
+          if (!ok) {
+            a.ws.rq_bad[r] = 1;
+            set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
+          }
+        }
+        const int cnt = min(32, j1 - jb);
+        for (int i = 0; i < cnt; ++i) {
+          const int pi = __shfl_sync(0xffffffffu, p, i);
+          const float ksi = __shfl_sync(0xffffffffu, ks, i);
+          const float vsi = __shfl_sync(0xffffffffu, vs, i);
+          const bool oki = __shfl_sync(0xffffffffu, (int)ok, i) != 0;
+          const int stage = (int)(k % C::STAGES);
+          bool go = true;
+          if (k >= C::STAGES)
+            go = mbar_wait(&empty[stage], (uint32_t)(((k / C::STAGES) - 1) & 1), abort_flag,
+                           a.d.ctl);
+          if (!go) break;
+          if (lane == 0) {
+            const int j = jb + i;
+            StageMeta m;
+            m.n_valid = oki ? min(P, L - j * P) : 0;
+            m.ks = ksi;
+            m.vs = vsi;
+            m.pos0 = j * P;
+            meta[stage] = m;
+            if (oki) {
+              uint8_t* dst = ring + stage * C::STAGE;
+              const long long ph = (long long)pi * Hkv + h;
+              mbar_arrive_expect_tx(&full[stage], C::STAGE);
+              bulk_g2s(dst, static_cast<const uint8_t*>(a.d.k_cache) + ph * C::TILE, C::TILE,
+                       &full[stage], policy);
+              bulk_g2s(dst + C::TILE, static_cast<const uint8_t*>(a.d.v_cache) + ph * C::TILE,
+                       C::TILE, &full[stage], policy);
+            } else {
+              mbar_arrive(&full[stage]);
+            }
+          }
+          __syncwarp();
+          ++k;
+        }
+      }
+      x = piece_end;
+      if (x == seg_end) cursor_next(cur, pfx, B, Hkv);
+    }
+    // On abort, copies already issued may still be landing: wait for them
+    // (bounded) before this CTA's shared memory goes away.
+    if (*abort_flag && lane == 0) {
+      for (long long q = max(0ll, k - C::STAGES); q < k; ++q) {
+        const int stage = (int)(q % C::STAGES);
+        const uint32_t par = (uint32_t)((q / C::STAGES) & 1);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&full[stage], par) && global_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ========================= consumer warps =========================
+  const int g = lane >> 2, t = lane & 3;
+  const int odd = g & 1;
+  uint8_t* pbuf = pbuf_all + warp * C::PBUF;
+  const int G = a.G, T = a.T, R = a.R;
+  Cursor cur = start;
+  long long x = x_begin;
+  long long k_base = 0;
+  const float ssl = a.sm_scale_log2;
+
+  while (x < x_end) {
+    const long long seg_end = cur.seg_start + cur.np;
+    const long long piece_end = min(seg_end, x_end);
+    const int npages = (int)(piece_end - x);
+    const int r = cur.r, h = cur.h;
+    const int L = a.seq_lens[r];
+
+    // ---- query fragments for row n = g (zero for padding rows)
+    // dims of k-step j: chunk c = t + 4*(j/4) (fp8) -- 16 dims per chunk --
+    // or chunk c = t + 4*(j/2) (bf16) -- 8 dims per chunk.
+    uint32_t qf[8][2];
+    {
+      const bool live = g < R;
+      const int tq = live ? g / G : 0, hq = live ? h * G + g % G : 0;
+      const uint16_t* qrow = a.q + (((long long)r * T + tq) * a.Hq + hq) * D;
+      if constexpr (FP8) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c = t + 4 * half;  // 16 dims = 32 bytes = 2 uint4
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (live) v = *reinterpret_cast<const uint4*>(qrow + 16 * c + 8 * u);
+            // words of v: dims 16c + 8u + {0,1}, {2,3}, {4,5}, {6,7}
+            const int j0 = 4 * half + 2 * u;
+            qf[j0][0] = bf16x2_to_f16x2(v.x);
+            qf[j0][1] = bf16x2_to_f16x2(v.y);
+            qf[j0 + 1][0] = bf16x2_to_f16x2(v.z);
+            qf[j0 + 1][1] = bf16x2_to_f16x2(v.w);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (live) v = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * m));
+          qf[2 * m][0] = v.x;
+          qf[2 * m][1] = v.y;
+          qf[2 * m + 1][0] = v.z;
+          qf[2 * m + 1][1] = v.w;
+        }
+      }
+    }
+    // visibility limit (inclusive) of rows 2t and 2t+1
+    const int lim0 = L - T + min((2 * t) / G, T - 1);
+    const int lim1 = L - T + min((2 * t + 1) / G, T - 1);
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+    for (int pi = warp; pi < npages; pi += C::CONSUMERS) {
+      const long long kk = k_base + pi;
+      const int stage = (int)(kk % C::STAGES);
+      const bool ok = mbar_wait(&full[stage], (uint32_t)((kk / C::STAGES) & 1), abort_flag,
+                                a.d.ctl);
+      const StageMeta mt = meta[stage];
+      if (ok && mt.n_valid > 0) {
+        const uint8_t* Kt = ring + stage * C::STAGE;
+        const uint8_t* Vt = Kt + C::TILE;
+        // ---------------- S^T = K Q^T
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (FP8) {
+          // row g: chunk t (dims 16t..) and t+4 (dims 64+16t..); odd rows
+          // load them in the other order so a quarter-warp hits 8 banks groups
+          const uint4 x0 = lds128(Kt + g * 128 + 16 * (t + 4 * odd));
+          const uint4 x1 = lds128(Kt + g * 128 + 16 * (t + 4 - 4 * odd));
+          const uint4 y0 = lds128(Kt + (g + 8) * 128 + 16 * (t + 4 * odd));
+          const uint4 y1 = lds128(Kt + (g + 8) * 128 + 16 * (t + 4 - 4 * odd));
+          const uint4 kA = odd ? x1 : x0, kB = odd ? x0 : x1;
+          const uint4 hA = odd ? y1 : y0, hB = odd ? y0 : y1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w = w_of(j < 4 ? kA : kB, j & 3);
+            const uint32_t w8 = w_of(j < 4 ? hA : hB, j & 3);
+            const uint32_t a0 = e4m3x2_to_f16x2(w), a2 = e4m3x2_to_f16x2(w >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(w8), a3 = e4m3x2_to_f16x2(w8 >> 16);
+            if (j & 1)
+              mma16816<true>(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+            else
+              mma16816<true>(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+          }
+        } else {
+          // row g: chunks t, t+4, t+8, t+12 (8 dims each); odd rows swap pairs
+          uint4 cg[4], c8[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            cg[m] = lds128(Kt + g * 256 + 16 * (t + 4 * (m ^ odd)));
+            c8[m] = lds128(Kt + (g + 8) * 256 + 16 * (t + 4 * (m ^ odd)));
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint4 vg = odd ? cg[m ^ 1] : cg[m];
+            const uint4 v8 = odd ? c8[m ^ 1] : c8[m];
+            mma16816<false>(sa, vg.x, v8.x, vg.y, v8.y, qf[2 * m][0], qf[2 * m][1]);
+            mma16816<false>(sb, vg.z, v8.z, vg.w, v8.w, qf[2 * m + 1][0], qf[2 * m + 1][1]);
+          }
+        }
+        // scores (log2 domain) for (token g | g+8, row 2t | 2t+1)
+        const float sc = FP8 ? mt.ks * ssl : ssl;
+        float s[4] = {(sa[0] + sb[0]) * sc, (sa[1] + sb[1]) * sc, (sa[2] + sb[2]) * sc,
+                      (sa[3] + sb[3]) * sc};
+        const int pA = mt.pos0 + g, pB = mt.pos0 + g + 8;
+        const bool vA = g < mt.n_valid, vB = g + 8 < mt.n_valid;
+        s[0] = (vA && pA <= lim0) ? s[0] : -INFINITY;
+        s[1] = (vA && pA <= lim1) ? s[1] : -INFINITY;
+        s[2] = (vB && pB <= lim0) ? s[2] : -INFINITY;
+        s[3] = (vB && pB <= lim1) ? s[3] : -INFINITY;
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        // rows with nothing visible yet keep m = -inf and contribute nothing
+        const float al0 = (n0 == -INFINITY) ? 1.0f : exp2f(m0 - n0);
+        const float al1 = (n1 == -INFINITY) ? 1.0f : exp2f(m1 - n1);
+        const float p0 = (n0 == -INFINITY) ? 0.0f : exp2f(s[0] - n0);
+        const float p1 = (n1 == -INFINITY) ? 0.0f : exp2f(s[1] - n1);
+        const float p2 = (n0 == -INFINITY) ? 0.0f : exp2f(s[2] - n0);
+        const float p3 = (n1 == -INFINITY) ? 0.0f : exp2f(s[3] - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 = l0 * al0 + p0 + p2;
+        l1 = l1 * al1 + p1 + p3;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[i][0] *= al0;
+          acc[i][2] *= al0;
+          acc[i][1] *= al1;
+          acc[i][3] *= al1;
+        }
+        // ---------------- P^T to the B-fragment layout via shared memory
+        // tokens beyond the request length are zeroed in V (stale cache bytes
+        // could be NaN patterns; 0 * NaN would poison the sum)
+        const int nv = mt.n_valid;
+        if constexpr (FP8) {
+          __half* pb = reinterpret_cast<__half*>(pbuf);  // [8 rows][16 tokens]
+          const float vsc = mt.vs;
+          pb[(2 * t) * 16 + g] = __float2half_rn(p0 * vsc);
+          pb[(2 * t + 1) * 16 + g] = __float2half_rn(p1 * vsc);
+          pb[(2 * t) * 16 + g + 8] = __float2half_rn(p2 * vsc);
+          pb[(2 * t + 1) * 16 + g + 8] = __float2half_rn(p3 * vsc);
+          __syncwarp();
+          const uint2 bq = lds64(pbuf + g * 32 + 8 * t);  // row g, tokens 4t..4t+3
+          __syncwarp();
+          uint32_t vmask = 0xFFFFFFFFu;
+          if (nv < P) {
+            const int keep = min(max(nv - 4 * t, 0), 4);  // bytes of tokens 4t.. kept
+            vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t wl = lds32(Vt + (16 * i + g) * 16 + 4 * t) & vmask;
+            const uint32_t wh = lds32(Vt + (16 * i + g + 8) * 16 + 4 * t) & vmask;
+            mma16816<true>(acc[i], e4m3x2_to_f16x2(wl), e4m3x2_to_f16x2(wh),
+                           e4m3x2_to_f16x2(wl >> 16), e4m3x2_to_f16x2(wh >> 16), bq.x, bq.y);
+          }
+        } else {
+          float* pb = reinterpret_cast<float*>(pbuf);  // [8 rows][16 tokens] f32
+          pb[(2 * t) * 16 + g] = p0;
+          pb[(2 * t + 1) * 16 + g] = p1;
+          pb[(2 * t) * 16 + g + 8] = p2;
+          pb[(2 * t + 1) * 16 + g + 8] = p3;
+          __syncwarp();
+          const uint4 pq = lds128(pbuf + g * 64 + 16 * t);  // row g, tokens 4t..4t+3
+          __syncwarp();
+          const float f0 = __uint_as_float(pq.x), f1 = __uint_as_float(pq.y);
+          const float f2 = __uint_as_float(pq.z), f3 = __uint_as_float(pq.w);
+          // P = hi + lo in bf16 keeps ~16 bits of the weights
+          const uint32_t h01 = f32x2_to_bf16x2(f0, f1), h23 = f32x2_to_bf16x2(f2, f3);
+          const uint32_t l01 = f32x2_to_bf16x2(f0 - __uint_as_float(h01 << 16),
+                                               f1 - __uint_as_float(h01 & 0xFFFF0000u));
+          const uint32_t l23 = f32x2_to_bf16x2(f2 - __uint_as_float(h23 << 16),
+                                               f3 - __uint_as_float(h23 & 0xFFFF0000u));
+          uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;  // tokens (4t,4t+1) and (4t+2,4t+3)
+          if (nv < P) {
+            const int keep = min(max(nv - 4 * t, 0), 4);
+            mlo = keep >= 2 ? 0xFFFFFFFFu : (keep == 1 ? 0x0000FFFFu : 0u);
+            mhi = keep >= 4 ? 0xFFFFFFFFu : (keep == 3 ? 0x0000FFFFu : 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint2 vl = lds64(Vt + (16 * i + g) * 32 + 8 * t);
+            const uint2 vh = lds64(Vt + (16 * i + g + 8) * 32 + 8 * t);
+            const uint32_t a0 = vl.x & mlo, a2 = vl.y & mhi, a1 = vh.x & mlo, a3 = vh.y & mhi;
+            mma16816<false>(acc[i], a0, a1, a2, a3, h01, h23);
+            mma16816<false>(acc[i], a0, a1, a2, a3, l01, l23);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // ---- merge the four warps' states of this piece into one partial
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    float* mo = merge_o + warp * C::R8 * D;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mo[(2 * t) * D + 16 * i + g] = acc[i][0];
+      mo[(2 * t + 1) * D + 16 * i + g] = acc[i][1];
+      mo[(2 * t) * D + 16 * i + g + 8] = acc[i][2];
+      mo[(2 * t + 1) * D + 16 * i + g + 8] = acc[i][3];
+    }
+    if (g == 0) {
+      float* ml = merge_ml + warp * C::R8 * 2;
+      ml[(2 * t) * 2 + 0] = m0;
+      ml[(2 * t) * 2 + 1] = l0;
+      ml[(2 * t + 1) * 2 + 0] = m1;
+      ml[(2 * t + 1) * 2 + 1] = l1;
+    }
+    named_bar_sync(1, C::CONSUMERS * 32);
+    {
+      const long long slot = (long long)r * Hkv + h + blockIdx.x;
+      const int tid = threadIdx.x;  // 0..127
+      for (int e = tid; e < C::R8 * D; e += C::CONSUMERS * 32) {
+        const int n = e / D, dd = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::CONSUMERS; ++w) M = fmaxf(M, merge_ml[(w * C::R8 + n) * 2]);
+        float o = 0.0f, lsum = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < C::CONSUMERS; ++w) {
+            const float mw = merge_ml[(w * C::R8 + n) * 2];
+            const float sc = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+            o += merge_o[(w * C::R8 + n) * D + dd] * sc;
+            lsum += merge_ml[(w * C::R8 + n) * 2 + 1] * sc;
+          }
+        }
+        a.ws.o_part[(slot * C::R8 + n) * D + dd] = o;
+        if (dd == 0) {
+          a.ws.ml_part[(slot * C::R8 + n) * 2 + 0] = M;
+          a.ws.ml_part[(slot * C::R8 + n) * 2 + 1] = lsum;
+        }
+      }
+    }
+    named_bar_sync(1, C::CONSUMERS * 32);
+
+    k_base += npages;
+    x = piece_end;
+    if (x == seg_end) cursor_next(cur, pfx, B, Hkv);
+  }
+}
+
+// ------------------------------------------------- combine
+
+constexpr int kCombineThreads = 128;
+constexpr int kMaxPieces = 4096;
+
+// One CTA per (segment, query row).  Merges the pieces of the segment:
+// O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c, written as bf16.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeArgs a) {
+  __shared__ float wgt[kMaxPieces];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float s_M, s_L;
+  const int Hkv = a.d.num_kv_heads;
+  const int seg = blockIdx.x, n = blockIdx.y;
+  const int r = seg / Hkv, h = seg % Hkv;
+  if (n >= a.R) return;
+  if (a.ws.rq_skip[r] || a.ws.rq_bad[r]) return;  // aborted: output left untouched
+  const int Dv = a.d.head_dim_v;
+  const int tq = n / a.G, hq = h * a.G + n % a.G;
+  uint16_t* out = a.out + (((long long)r * a.T + tq) * a.Hq + hq) * Dv;
+  const int32_t* pfx = a.ws.pfx;
+  const int np = pfx[r + 1] - pfx[r];
+  if (np == 0) {
+    for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) out[dd] = 0;
+    return;
+  }
+  const long long total = (long long)pfx[a.B] * Hkv;
+  const long long per = (total + a.grid - 1) / a.grid;
+  const long long start = (long long)Hkv * pfx[r] + (long long)h * np;
+  const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
+  const int npc = c1 - c0 + 1;
+  const long long slot0 = (long long)seg + c0;
+  const int R8 = a.R8;
+  // pass 1: M and L
+  float mloc = -INFINITY;
+  for (int c = threadIdx.x; c < npc; c += kCombineThreads)
+    mloc = fmaxf(mloc, a.ws.ml_part[((slot0 + c) * R8 + n) * 2]);
+  mloc = warp_max(mloc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mloc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+    s_M = M;
+  }
+  __syncthreads();
+  const float M = s_M;
+  if (M == -INFINITY) {  // nothing visible to this row
+    for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) out[dd] = 0;
+    return;
+  }
+  float lloc = 0.0f;
+  for (int c = threadIdx.x; c < npc; c += kCombineThreads) {
+    const float mc = a.ws.ml_part[((slot0 + c) * R8 + n) * 2];
+    const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
+    if (c < kMaxPieces) wgt[c] = w;
+    lloc += w * a.ws.ml_part[((slot0 + c) * R8 + n) * 2 + 1];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lloc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float L = 0.0f;
+    for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
+    s_L = L;
+  }
+  __syncthreads();
+  const float inv = 1.0f / s_L;
+  for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) {
+    float o = 0.0f;
+    for (int c = 0; c < npc; ++c) {
+      const float w = wgt[c];
+      if (w != 0.0f) o += w * a.ws.o_part[((slot0 + c) * R8 + n) * (long long)Dv + dd];
+    }
+    const __nv_bfloat16 b = __float2bfloat16_rn(o * inv);
+    out[dd] = *reinterpret_cast<const uint16_t*>(&b);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------- host side
+
+int gqa_split_ctas_per_sm(int kind) {
+  static int cache[2] = {-1, -1};
+  if (cache[kind] >= 0) return cache[kind];
+  int n = 0;
+  cudaError_t e;
+  if (kind == 0) {
+    cudaFuncSetAttribute(gqa_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         GqaCfg<true>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_kernel<true>,
+                                                      GqaCfg<true>::THREADS, GqaCfg<true>::SMEM);
+  } else {
+    cudaFuncSetAttribute(gqa_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         GqaCfg<false>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_kernel<false>,
+                                                      GqaCfg<false>::THREADS, GqaCfg<false>::SMEM);
+  }
+  if (e != cudaSuccess || n <= 0) return 0;
+  cache[kind] = n;
+  return n;
+}
+
+cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s, int* launches) {
+  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches) {
+  if (kind == 0)
+    gqa_split_kernel<true><<<a.grid, GqaCfg<true>::THREADS, GqaCfg<true>::SMEM, s>>>(a);
+  else
+    gqa_split_kernel<false><<<a.grid, GqaCfg<false>::THREADS, GqaCfg<false>::SMEM, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* launches) {
+  const long long segs = (long long)a.B * a.d.num_kv_heads;
+  if (segs <= 0) return cudaSuccess;
+  dim3 grid((unsigned)segs, (unsigned)a.R);
+  combine_kernel<<<grid, kCombineThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+}  // namespace kvfp8

@@ -1,0 +1,91 @@
+// internal.h -- host-side declarations shared by the C-ABI layer (api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvfp8.h"
+
+struct kv_pool {
+  kv_pool_desc d;
+  int32_t last_launches;
+};
+
+namespace kvfp8 {
+
+// ---- append -------------------------------------------------------------
+struct AppendArgs {
+  kv_pool_desc d;
+  int32_t B;
+  const uint16_t* k_new;  // bf16 bits
+  const uint16_t* v_new;
+  const int32_t* new_indptr;
+  int32_t max_new;
+  int32_t* page_table;
+  uint32_t* exp_tags;
+  int32_t max_pages;
+  int32_t* seq_lens;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
+
+// ---- verify -------------------------------------------------------------
+struct VerifyArgs {
+  int32_t num_pages, page_size, B, max_pages;
+  const uint32_t* tags;
+  const int32_t* page_table;
+  const uint32_t* exp_tags;
+  const int32_t* seq_lens;
+  uint8_t* abort_mask;
+};
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int* launches);
+
+// ---- decode -------------------------------------------------------------
+// Workspace carve-up (all offsets 256-byte aligned).
+struct DecodeWs {
+  int32_t* pfx;       // [B+1] exclusive prefix of pages per request (0 if skipped)
+  uint8_t* rq_skip;   // [B] 1: request gets no output (aborted / invalid)
+  uint8_t* rq_bad;    // [B] 1: a page id out of range was met while reading
+  float* ml_part;     // [slots][R8][2]  running max (log2 domain) and sum
+  float* o_part;      // [slots][R8][Dv] unnormalised partial outputs
+  size_t bytes;
+};
+
+struct DecodeArgs {
+  kv_pool_desc d;
+  int32_t B, Hq, T, G, R;  // R = T*G query rows per kv head (latent: T*Hq)
+  const uint16_t* q;       // bf16 bits [B][T][Hq][Dk]
+  const int32_t* page_table;
+  int32_t max_pages;
+  const int32_t* seq_lens;
+  const uint8_t* abort_mask;
+  float sm_scale_log2;  // sm_scale * log2(e)
+  uint16_t* out;        // bf16 bits [B][T][Hq][Dv]
+  int32_t grid;         // CTAs of the split kernel
+  int32_t R8;           // rows per partial slot (R rounded up)
+  DecodeWs ws;
+};
+
+// Kernel configuration chosen for a pool (shape checks + grid).
+struct DecodeConfig {
+  int kind;   // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3
+  int grid;   // split-kernel CTAs
+  int R8;     // partial rows per slot
+};
+
+kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig* cfg);
+size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
+                        void* base, DecodeWs* ws);
+
+cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_decode_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches);
+cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches);
+cudaError_t launch_latent_split(const DecodeArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* launches);
+
+// Occupancy-derived CTAs per SM for the split kernels (cached per device).
+int gqa_split_ctas_per_sm(int kind);
+int latent_split_ctas_per_sm();
+
+}  // namespace kvfp8

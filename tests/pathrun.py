@@ -1,0 +1,142 @@
+"""Test helpers: run one workload through the CUDA library and through the
+oracle on identical seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+
+TOL_ABS, TOL_REL = 2e-3, 1e-2  # attention output tolerance: |o - r| <= abs + rel * |r|
+
+
+def close(got: np.ndarray, ref: np.ndarray):
+    """Elementwise |got - ref| <= 2e-3 + 1e-2 |ref|; returns (ok, max_abs, max_rel, worst)."""
+    err = np.abs(got.astype(np.float64) - ref)
+    bound = TOL_ABS + TOL_REL * np.abs(ref)
+    ok = bool(np.all(err <= bound))
+    rel = err / np.maximum(np.abs(ref), 1e-30)
+    worst = float(np.max(err - bound)) if err.size else 0.0
+    return ok, float(err.max(initial=0.0)), float(rel.max(initial=0.0)), worst
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+
+
+class Both:
+    """A pool on the device (library) and its host twin (oracle)."""
+
+    def __init__(self, w: wl.Workload, dtype: int, device="cuda", num_pages=None, free=None,
+                 tags=None):
+        import paged_fp8_kv_append_gb300 as kv
+
+        self.kv, self.w, self.dtype = kv, w, dtype
+        npg = num_pages or w.num_pages
+        free = wl.free_list(w) if free is None else free
+        tags = wl.initial_tags(w) if tags is None else tags
+        self.dev = kv.KVPool(npg, w.page_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v,
+                             dtype=dtype, layout=w.layout, device=device, tags=tags,
+                             free_list=free)
+        self.ref = oracle.Pool(npg, w.page_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v,
+                               dtype=dtype, layout=w.layout, tags=tags, free_list=free)
+        B, mp = w.B, w.max_pages
+        self.pt_d = torch.full((B, mp), -1, dtype=torch.int32, device=device)
+        self.et_d = torch.zeros((B, mp), dtype=torch.int32, device=device)
+        self.sl_d = torch.zeros(B, dtype=torch.int32, device=device)
+        self.pt_h = np.full((B, mp), -1, np.int32)
+        self.et_h = np.zeros((B, mp), np.uint32)
+        self.sl_h = np.zeros(B, np.int32)
+        self.device = device
+
+    def append(self, rows_k, rows_v, counts, max_new=None):
+        """Append per-request rows (lists of bf16 device tensors) on both sides."""
+        B = self.w.B
+        counts = np.asarray(counts, np.int64)
+        ind = np.zeros(B + 1, np.int32)
+        ind[1:] = np.cumsum(counts)
+        k = torch.cat([x for x in rows_k if x is not None and x.shape[0] > 0]) if ind[-1] else None
+        v = None
+        if self.w.layout == 0 and ind[-1]:
+            v = torch.cat([x for x in rows_v if x is not None and x.shape[0] > 0])
+        mx = int(counts.max()) if max_new is None else max_new
+        ind_d = torch.from_numpy(ind).to(self.device)
+        if k is None:  # nothing to append: still a valid call
+            k = torch.zeros((1, self.w.num_kv_heads, self.w.head_dim_k), dtype=torch.bfloat16,
+                            device=self.device)
+            v = torch.zeros((1, self.w.num_kv_heads, self.w.head_dim_v), dtype=torch.bfloat16,
+                            device=self.device) if self.w.layout == 0 else None
+        self.dev.append(B, k.contiguous(), None if v is None else v.contiguous(), ind_d, mx,
+                        self.pt_d, self.et_d, self.sl_d)
+        kb = wl.bits_u16(k)
+        vb = wl.bits_u16(v) if v is not None else None
+        st, stop = oracle.append(self.ref, kb, vb, ind, mx, self.pt_h, self.et_h, self.sl_h)
+        return st, stop
+
+    def fill(self, lens=None, tag=0):
+        w = self.w
+        lens = w.lens if lens is None else lens
+        ks, vs = [], []
+        for r in range(w.B):
+            k, v = wl.kv_rows(w, r, int(self.sl_h[r]), int(lens[r]), device=self.device, tag=tag)
+            ks.append(k)
+            vs.append(v)
+        return self.append(ks, vs, lens)
+
+    def make_stale(self):
+        """Give the workload's stale requests one stale expected tag (both sides)."""
+        for r, j in wl.stale_slots(self.w):
+            self.et_h[r, j] = np.uint32(self.et_h[r, j]) - np.uint32(1)
+        self.et_d.copy_(torch.from_numpy(self.et_h.view(np.int32)))
+
+    # ---- state comparison (bit-exact)
+    def assert_state_equal(self):
+        d, r = self.dev, self.ref
+        kc = d.k_cache.cpu()
+        if self.dtype == 1:
+            kc = kc.view(torch.int16)
+        assert np.array_equal(kc.numpy().view(r.k_cache.dtype), r.k_cache), "k_cache"
+        if r.v_cache is not None:
+            vc = d.v_cache.cpu()
+            if self.dtype == 1:
+                vc = vc.view(torch.int16)
+            assert np.array_equal(vc.numpy().view(r.v_cache.dtype), r.v_cache), "v_cache"
+        if self.dtype == 0:
+            assert np.array_equal(d.k_scale.cpu().numpy().view(np.uint32),
+                                  r.k_scale.view(np.uint32)), "k_scale"
+            if r.v_scale is not None:
+                assert np.array_equal(d.v_scale.cpu().numpy().view(np.uint32),
+                                      r.v_scale.view(np.uint32)), "v_scale"
+        assert np.array_equal(d.tags.cpu().numpy().view(np.uint32), r.tags), "tags"
+        assert np.array_equal(self.pt_d.cpu().numpy(), self.pt_h), "page_table"
+        assert np.array_equal(self.et_d.cpu().numpy().view(np.uint32), self.et_h), "exp_tags"
+        assert np.array_equal(self.sl_d.cpu().numpy(), self.sl_h), "seq_lens"
+        assert int(d.ctl[0].item()) == int(r.free_head[0]), "free_head"
+
+    def verify(self):
+        B = self.w.B
+        m_d = torch.zeros(B, dtype=torch.uint8, device=self.device)
+        self.dev.verify(B, self.pt_d, self.et_d, self.sl_d, m_d)
+        m_h = oracle.verify(self.ref.num_pages, self.w.page_size, self.ref.tags, self.pt_h,
+                            self.et_h, self.sl_h)
+        return m_d, m_h
+
+    def attn(self, q, abort_d, abort_h, sentinel=7.0, phases=False):
+        w, B = self.w, self.w.B
+        out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), sentinel,
+                         dtype=torch.bfloat16, device=self.device)
+        ws = torch.empty(self.dev.workspace_size(B, w.num_q_heads, w.q_tokens), dtype=torch.uint8,
+                         device=self.device)
+        if phases:
+            self.kv.paged_decode_attn_split(self.dev.handle, B, w.num_q_heads, w.q_tokens, q,
+                                            self.pt_d, self.sl_d, abort_d, w.sm_scale, ws)
+            self.kv.paged_decode_attn_combine(self.dev.handle, B, w.num_q_heads, w.q_tokens,
+                                              abort_d, out, ws)
+        else:
+            self.dev.attn(B, w.num_q_heads, w.q_tokens, q, self.pt_d, self.sl_d, abort_d,
+                          w.sm_scale, out, ws)
+        ref, written = oracle.attn(self.ref, wl.bits_u16(q), self.pt_h, self.sl_h, abort_h,
+                                   w.sm_scale, w.num_q_heads, w.q_tokens)
+        return out, ref, written

@@ -1,0 +1,83 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments synchronously (no GPU needed: nothing is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kv():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_fp8_kv_append_gb300 as kv
+
+    return kv
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvfp8.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) - {"if", "sizeof"})
+
+
+def test_exports_every_declared_symbol(kv):
+    names = _declared()
+    assert {"kv_pool_create", "kv_append_quantize", "kv_verify_tags", "paged_decode_attn"} <= set(names)
+    lib = ctypes.CDLL(kv.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(kv, **over):
+    d = kv.kv_pool_desc()
+    d.num_pages, d.page_size, d.num_kv_heads, d.head_dim_k, d.head_dim_v = 64, 16, 2, 128, 128
+    d.dtype, d.layout = kv.KV_DTYPE_E4M3, kv.KV_LAYOUT_GQA
+    fake = 0x10000  # 16-byte aligned, never dereferenced by pool creation
+    d.k_cache = d.v_cache = d.k_scale = d.v_scale = d.tags = d.free_list = d.ctl = fake
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_pool_create_validation(kv):
+    h = kv.kv_pool_create(_desc(kv))
+    assert h
+    kv.kv_pool_destroy(h)
+    for bad in [dict(num_pages=0), dict(page_size=0), dict(head_dim_k=100), dict(dtype=7),
+                dict(layout=3), dict(k_cache=None), dict(v_scale=None), dict(ctl=0x10004),
+                dict(layout=1, num_kv_heads=2)]:
+        with pytest.raises(kv.KVError) as e:
+            kv.kv_pool_create(_desc(kv, **bad))
+        assert e.value.status == kv.KV_ERR_INVALID_ARG, bad
+    with pytest.raises(kv.KVError) as e:
+        kv.kv_pool_create(_desc(kv, layout=1, num_kv_heads=1, dtype=kv.KV_DTYPE_BF16))
+    assert e.value.status == kv.KV_ERR_UNSUPPORTED
+    bf = _desc(kv, dtype=kv.KV_DTYPE_BF16, k_scale=None, v_scale=None)
+    kv.kv_pool_destroy(kv.kv_pool_create(bf))
+
+
+def test_entry_points_reject_bad_arguments(kv):
+    lib = kv._lib
+    h = kv.kv_pool_create(_desc(kv))
+    try:
+        assert lib.kv_append_quantize(h, None, -1, None, None, None, 0, None, None, 4, None) == 1
+        assert lib.kv_append_quantize(h, None, 2, None, None, None, 1, None, None, 4, None) == 1
+        assert lib.kv_append_quantize(h, None, 0, None, None, None, 0, None, None, 4, None) == 0
+        assert lib.kv_verify_tags(h, None, 3, None, None, 4, None, None) == 1
+        assert lib.kv_verify_tags(h, None, 0, None, None, 4, None, None) == 0
+        assert lib.paged_decode_attn(h, None, 2, 8, 1, None, None, 4, None, None, 1.0, None,
+                                     None, 0) == 1
+        assert lib.paged_decode_attn_split(h, None, 2, 8, 1, 0x10000, 0x10000, 4, 0x10000, None,
+                                           float("nan"), 0x10000, 1 << 20) == 1
+        # workspace must be 256-byte aligned
+        assert lib.paged_decode_attn_combine(h, None, 2, 8, 1, None, 0x10000, 0x10010, 1 << 20) == 1
+        assert lib.kv_pool_destroy(None) == 1
+        assert kv.kv_status_string(4) == "KV_ERR_OUT_OF_PAGES"
+        assert lib.kv_last_launch_count(h) == 0
+    finally:
+        kv.kv_pool_destroy(h)
