@@ -21,7 +21,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -109,50 +108,73 @@ def smi_index(local: int) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during a timed region."""
+    """SM clock and clock-event (throttle) reasons sampled through NVML
+    (libnvidia-ml, the library nvidia-smi reads) every ~1 ms while a timed
+    region runs: the decode steps last milliseconds, too short for
+    nvidia-smi's 100 ms loop.  Read-only: no clock or setting is changed."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: str, path: str):
-        self.path, self.proc = path, None
+    def __init__(self, gpu_id: str, period_s: float = 0.001):
+        import ctypes
+        import threading
+
+        self.samples, self.masks, self.ok = [], [], False
+        self.max_mhz = None
         try:
-            self.f = open(path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
-                stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if gpu_id.startswith("GPU-"):
+                rc = lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(h))
+            else:
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(int(gpu_id), ctypes.byref(h))
+            if rc != 0:
+                raise OSError(f"nvml handle rc={rc}")
+            self.lib, self.h = lib, h
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.reasons_fn = reasons_fn
+            self.ok = True
+        except Exception as e:  # noqa: BLE001
+            self.err = str(e)
+            return
+        self.stop_flag = False
+        self.period = period_s
+        self.t = threading.Thread(target=self._loop, daemon=True)
+        self.t.start()
+
+    def _loop(self):
+        import ctypes
+
+        c = ctypes.c_uint()
+        m = ctypes.c_ulonglong()
+        while not self.stop_flag:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(float(c.value))
+            if self.reasons_fn(self.h, ctypes.byref(m)) == 0:
+                self.masks.append(int(m.value))
+            time.sleep(self.period)
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": [f"nvml unavailable: {getattr(self, 'err', '')}"]}
+        self.stop_flag = True
+        self.t.join(timeout=2)
+        reasons = set()
+        for m in self.masks:
+            for bit, name in self.REASONS.items():
+                if m & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(reasons), "source": "nvml, ~1 ms period"}
 
 
 # ------------------------------------------------------------ GPU arm
@@ -389,12 +411,10 @@ def main():
     w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + 2)
     if args.batch != w.B:
         w = wl.subset(w, args.batch)
-    clocks_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-    os.makedirs(os.path.dirname(clocks_path), exist_ok=True)
 
     # ---- FP8 (headline)
     arm = Arm(w, 0, device, total_steps)
-    sampler = ClockSampler(smi_index(local), clocks_path)
+    sampler = ClockSampler(smi_index(local))
     total_ms, per, lens_timed, launches = arm.run(args.steps, args.warmup)
     clocks = sampler.stop()
     e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup)

@@ -39,7 +39,6 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     const int per_sm = sms > 0 ? gqa_split_ctas_per_sm(cfg->kind) : 0;
     if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
     cfg->grid = sms * per_sm;
-    if (cfg->grid > 4000) cfg->grid = 4000;  // the combine holds <= 4096 piece weights
     cfg->R8 = 8;
     return KV_OK;
   }

@@ -14,9 +14,9 @@
 //     requests are untouched.  Popped pages get tag += 1; page_table,
 //     exp_tags and seq_lens are updated; ctl gets the new free head, the stop
 //     index and the error code.
-//  2. append_data (one CTA per (request, touched page)): reads the request's
-//     rows for that page, computes amax per kv head for a fresh page (K and V
-//     separately), scale = amax/448 (IEEE division; 1 when 0), and stores
+//  2. append_data (one CTA per (request, touched page, kv head, K|V)): reads
+//     the request's rows for that page, computes the amax of a fresh page
+//     (K and V separately), scale = amax/448 (IEEE division; 1 when 0), and stores
 //     e4m3(x / scale) with round-to-nearest-even and saturation; a page that
 //     already held rows keeps its scale.  bf16 pools copy the bits.
 #include "common.cuh"
@@ -272,7 +272,9 @@ __device__ void append_block(const uint16_t* src, long long src_stride, int nrow
   }
 }
 
-// One (request, touched page) per CTA; every kv head of the page.
+// One (request, touched page, kv head, K|V) per CTA (blockIdx.z = 2 * head +
+// {0: K, 1: V}; latent pools use z = 0 only), so a decode-step append of one
+// row per request is a short chain of memory round trips.
 __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a) {
   __shared__ float red[9];
   extern __shared__ __align__(16) uint8_t tile[];
@@ -286,6 +288,8 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
   const long long L0 = Lnew - n;
   const bool fp8 = d.dtype == KV_DTYPE_E4M3;
   const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
+  const int h = blockIdx.z >> 1;
+  const bool is_v = (blockIdx.z & 1) != 0;
   for (long long jp = L0 / P + blockIdx.y; jp * P < Lnew; jp += gridDim.y) {
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
     const int nrows = (int)(pos_hi - pos_lo);
@@ -304,11 +308,12 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
       continue;
     }
     const int es = fp8 ? 1 : 2;
-    for (int h = 0; h < H; ++h) {
+    if (!is_v) {
       const long long kp = (((long long)p * H + h) * P) * Dk;
       append_block(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
                    fp8 ? d.k_scale + (long long)p * H + h : nullptr,
                    static_cast<uint8_t*>(d.k_cache) + kp * es, false, (int)P, slot0, tile, red);
+    } else {
       const long long vp = ((long long)p * H + h) * (long long)Dv * P;
       append_block(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
                    fp8 ? d.v_scale + (long long)p * H + h : nullptr,
@@ -338,7 +343,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
                              (int)tile_bytes);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((unsigned)a.B, (unsigned)pieces);
+  const unsigned items = a.d.layout == KV_LAYOUT_GQA ? 2u * (unsigned)a.d.num_kv_heads : 1u;
+  dim3 grid((unsigned)a.B, (unsigned)pieces, items);
   append_data_kernel<<<grid, kDataThreads, tile_bytes, s>>>(a);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*launches;

@@ -16,11 +16,12 @@
 // segment + cta (injective because both are sorted along the range), and the
 // combine kernel merges the pieces of a segment.
 //
-// CTA layout: warp 4 is the producer: it reads page ids and scales and moves
-// each (page, kv head) K tile and V tile into a shared-memory ring with bulk
-// async copies (cp.async.bulk, completion on an mbarrier).  Warps 0-3 are
-// consumers: page k of the range goes to warp k % 4, which keeps its own
-// online-softmax state and merges with the others at the end of a piece.
+// CTA layout: the last warp is the producer: it reads page ids and scales
+// and moves each (page, kv head) K tile and V tile into a shared-memory ring
+// with bulk async copies (cp.async.bulk, completion on an mbarrier).  The
+// other warps are consumers: page k of the range goes to consumer k % C,
+// which keeps its own online-softmax state and merges with the others at the
+// end of a piece.
 //
 // Per page a consumer computes S^T = K Q^T (M = 16 tokens, N = 8 query rows,
 // K = 128 dims) and O^T += V^T P^T (M = 128 dims, N = 8 rows, K = 16 tokens)
@@ -194,6 +195,19 @@ __device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
 
 // ------------------------------------------------- split kernel
 
+// Ring depth and consumer warps per CTA.  At these sizes three CTAs share an
+// SM (~144 KB of e4m3 pages in flight per SM); measured faster than one or
+// two larger CTAs per SM with deeper rings.
+#ifndef KV_GQA_CONSUMERS
+#define KV_GQA_CONSUMERS 4
+#endif
+#ifndef KV_GQA_FP8_STAGES
+#define KV_GQA_FP8_STAGES 12
+#endif
+#ifndef KV_GQA_BF16_STAGES
+#define KV_GQA_BF16_STAGES 8
+#endif
+
 template <bool FP8>
 struct GqaCfg {
   static constexpr int P = 16;                      // tokens per page
@@ -201,8 +215,8 @@ struct GqaCfg {
   static constexpr int ES = FP8 ? 1 : 2;            // cache element bytes
   static constexpr int TILE = P * D * ES;           // bytes of one K or V tile
   static constexpr int STAGE = 2 * TILE;            // K tile + V tile
-  static constexpr int STAGES = FP8 ? 12 : 8;       // ring depth
-  static constexpr int CONSUMERS = 4;               // consumer warps
+  static constexpr int STAGES = FP8 ? KV_GQA_FP8_STAGES : KV_GQA_BF16_STAGES;  // ring depth
+  static constexpr int CONSUMERS = KV_GQA_CONSUMERS;                          // consumer warps
   static constexpr int THREADS = (CONSUMERS + 1) * 32;
   static constexpr int R8 = 8;                      // query rows per kv head (padded)
   static constexpr int PFX_CACHE = 1024;            // pfx entries cached in smem
@@ -218,6 +232,9 @@ struct GqaCfg {
   static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;
   static constexpr int SMEM = OFF_FLAG + 16;
 };
+
+// Units a producer warp issues per warp instruction (one per lane).
+constexpr int kIssueGroup = 8;
 
 struct StageMeta {
   int n_valid;  // tokens of this page below the request length (0: skip page)
@@ -267,78 +284,108 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
 
   if (warp == C::CONSUMERS) {
     // ======================= producer warp =======================
+    // Lane l owns unit x0 + l of each batch of 32 consecutive units.  Page
+    // ids (and lengths) are loaded two batches ahead and scales one batch
+    // ahead, so the dependent page-id -> scale loads never hold up the copy
+    // issue; each lane then issues its own unit's copies.
     const uint64_t policy = l2_evict_first_policy();
-    Cursor cur = start;
-    long long x = x_begin;
-    long long k = 0;  // stage sequence number
     const int maxp = a.max_pages;
-    while (x < x_end && !*abort_flag) {
-      const long long seg_end = cur.seg_start + cur.np;
-      const long long piece_end = min(seg_end, x_end);
-      const int r = cur.r, h = cur.h;
-      const int L = a.seq_lens[r];
-      const int j0 = (int)(x - cur.seg_start), j1 = (int)(piece_end - cur.seg_start);
-      const int32_t* pt = a.page_table + (long long)r * maxp;
-      for (int jb = j0; jb < j1 && !*abort_flag; jb += 32) {
-        const int jj = jb + lane;
-        int p = -1;
-        float ks = 1.0f, vs = 1.0f;
-        bool ok = false;
-        if (jj < j1) {
-          p = pt[jj];
-          ok = p >= 0 && p < a.d.num_pages;
-          if (ok && FP8) {
-            ks = a.d.k_scale[(long long)p * Hkv + h];
-            vs = a.d.v_scale[(long long)p * Hkv + h];
-          }
-          if (!ok) {
-            a.ws.rq_bad[r] = 1;
-            set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
-          }
+    Cursor lc = start;  // per-lane cursor, only moves forward
+    struct Unit {
+      int r, h, j, p, L;
+    };
+    auto locate_load = [&](long long xu) {
+      Unit u;
+      u.r = 0;
+      u.h = 0;
+      u.j = 0;
+      u.p = -1;
+      u.L = 0;
+      if (xu < x_end) {
+        while (xu >= lc.seg_start + lc.np) cursor_next(lc, pfx, B, Hkv);
+        u.r = lc.r;
+        u.h = lc.h;
+        u.j = (int)(xu - lc.seg_start);
+        u.p = a.page_table[(long long)u.r * maxp + u.j];
+        u.L = a.seq_lens[u.r];
+      }
+      return u;
+    };
+    auto scales = [&](const Unit& u, long long xu, float& ks, float& vs, bool& ok) {
+      ok = false;
+      ks = vs = 1.0f;
+      if (xu < x_end) {
+        ok = u.p >= 0 && u.p < a.d.num_pages;
+        if (ok && FP8) {
+          ks = a.d.k_scale[(long long)u.p * Hkv + u.h];
+          vs = a.d.v_scale[(long long)u.p * Hkv + u.h];
         }
-        const int cnt = min(32, j1 - jb);
-        for (int i = 0; i < cnt; ++i) {
-          const int pi = __shfl_sync(0xffffffffu, p, i);
-          const float ksi = __shfl_sync(0xffffffffu, ks, i);
-          const float vsi = __shfl_sync(0xffffffffu, vs, i);
-          const bool oki = __shfl_sync(0xffffffffu, (int)ok, i) != 0;
-          const int stage = (int)(k % C::STAGES);
-          bool go = true;
-          if (k >= C::STAGES)
-            go = mbar_wait(&empty[stage], (uint32_t)(((k / C::STAGES) - 1) & 1), abort_flag,
-                           a.d.ctl);
-          if (!go) break;
-          if (lane == 0) {
-            const int j = jb + i;
-            StageMeta m;
-            m.n_valid = oki ? min(P, L - j * P) : 0;
-            m.ks = ksi;
-            m.vs = vsi;
-            m.pos0 = j * P;
-            meta[stage] = m;
-            if (oki) {
-              uint8_t* dst = ring + stage * C::STAGE;
-              const long long ph = (long long)pi * Hkv + h;
-              mbar_arrive_expect_tx(&full[stage], C::STAGE);
-              bulk_g2s(dst, static_cast<const uint8_t*>(a.d.k_cache) + ph * C::TILE, C::TILE,
-                       &full[stage], policy);
-              bulk_g2s(dst + C::TILE, static_cast<const uint8_t*>(a.d.v_cache) + ph * C::TILE,
-                       C::TILE, &full[stage], policy);
-            } else {
-              mbar_arrive(&full[stage]);
-            }
-          }
-          __syncwarp();
-          ++k;
+        if (!ok) {
+          a.ws.rq_bad[u.r] = 1;
+          set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
         }
       }
-      x = piece_end;
-      if (x == seg_end) cursor_next(cur, pfx, B, Hkv);
+    };
+    Unit u0 = locate_load(x_begin + lane);
+    Unit u1 = locate_load(x_begin + 32 + lane);
+    float ks0, vs0, ks1, vs1;
+    bool ok0, ok1;
+    scales(u0, x_begin + lane, ks0, vs0, ok0);
+    long long k = 0;       // stage sequence number of the batch's first unit
+    long long issued = 0;  // units whose copies have been issued
+    static_assert(C::STAGES >= kIssueGroup, "ring shallower than an issue group");
+    for (long long xb = x_begin; xb < x_end && !*abort_flag; xb += 32) {
+      scales(u1, xb + 32 + lane, ks1, vs1, ok1);
+      const Unit u2 = locate_load(xb + 64 + lane);
+      const int cnt = (int)min(32ll, x_end - xb);
+      // lanes issue their own unit's copies, kIssueGroup units per step, so
+      // one warp instruction moves several pages (a group never holds two
+      // units of one stage because kIssueGroup <= STAGES)
+      bool go = true;
+      for (int g0 = 0; g0 < cnt && go; g0 += kIssueGroup) {
+        const bool mine = lane >= g0 && lane < min(g0 + kIssueGroup, cnt);
+        const long long kl = k + lane;
+        const int stage = (int)(kl % C::STAGES);
+        bool ok = true;
+        if (mine && kl >= C::STAGES)
+          ok = mbar_wait(&empty[stage], (uint32_t)(((kl / C::STAGES) - 1) & 1), abort_flag,
+                         a.d.ctl);
+        go = __all_sync(0xffffffffu, ok);
+        if (!go) break;
+        if (mine) {
+          StageMeta m;
+          m.n_valid = ok0 ? min(P, u0.L - u0.j * P) : 0;
+          m.ks = ks0;
+          m.vs = vs0;
+          m.pos0 = u0.j * P;
+          meta[stage] = m;
+          if (ok0) {
+            uint8_t* dst = ring + stage * C::STAGE;
+            const long long ph = (long long)u0.p * Hkv + u0.h;
+            mbar_arrive_expect_tx(&full[stage], C::STAGE);
+            bulk_g2s(dst, static_cast<const uint8_t*>(a.d.k_cache) + ph * C::TILE, C::TILE,
+                     &full[stage], policy);
+            bulk_g2s(dst + C::TILE, static_cast<const uint8_t*>(a.d.v_cache) + ph * C::TILE,
+                     C::TILE, &full[stage], policy);
+          } else {
+            mbar_arrive(&full[stage]);
+          }
+        }
+        __syncwarp();
+        issued = k + min(g0 + kIssueGroup, cnt);
+      }
+      if (!go) break;
+      k += cnt;
+      u0 = u1;
+      ks0 = ks1;
+      vs0 = vs1;
+      ok0 = ok1;
+      u1 = u2;
     }
     // On abort, copies already issued may still be landing: wait for them
     // (bounded) before this CTA's shared memory goes away.
     if (*abort_flag && lane == 0) {
-      for (long long q = max(0ll, k - C::STAGES); q < k; ++q) {
+      for (long long q = max(0ll, issued - C::STAGES); q < issued; ++q) {
         const int stage = (int)(q % C::STAGES);
         const uint32_t par = (uint32_t)((q / C::STAGES) & 1);
         const uint64_t t0 = global_ns();
@@ -580,7 +627,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
     named_bar_sync(1, C::CONSUMERS * 32);
     {
       const long long slot = (long long)r * Hkv + h + blockIdx.x;
-      const int tid = threadIdx.x;  // 0..127
+      const int tid = threadIdx.x;  // consumer thread index
       for (int e = tid; e < C::R8 * D; e += C::CONSUMERS * 32) {
         const int n = e / D, dd = e % D;
         float M = -INFINITY;
@@ -613,81 +660,75 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
 
 // ------------------------------------------------- combine
 
-constexpr int kCombineThreads = 128;
-constexpr int kMaxPieces = 4096;
+constexpr int kCombineWarps = 8;
 
-// One CTA per (segment, query row).  Merges the pieces of the segment:
-// O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c, written as bf16.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeArgs a) {
-  __shared__ float wgt[kMaxPieces];
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ float s_M, s_L;
+// One warp per (segment, query row): merges the pieces of the segment,
+// O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c, with a running max so a
+// single pass over the pieces suffices; lane l owns dims [4l, 4l+4) of every
+// 128-dim group.  Written as bf16 (RNE).
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const int Hkv = a.d.num_kv_heads;
-  const int seg = blockIdx.x, n = blockIdx.y;
-  const int r = seg / Hkv, h = seg % Hkv;
-  if (n >= a.R) return;
+  const long long nitems = (long long)a.B * Hkv * a.R;
+  if (item >= nitems) return;
+  const int n = (int)(item % a.R);
+  const long long seg = item / a.R;
+  const int r = (int)(seg / Hkv), h = (int)(seg % Hkv);
   if (a.ws.rq_skip[r] || a.ws.rq_bad[r]) return;  // aborted: output left untouched
   const int Dv = a.d.head_dim_v;
   const int tq = n / a.G, hq = h * a.G + n % a.G;
   uint16_t* out = a.out + (((long long)r * a.T + tq) * a.Hq + hq) * Dv;
   const int32_t* pfx = a.ws.pfx;
   const int np = pfx[r + 1] - pfx[r];
-  if (np == 0) {
-    for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) out[dd] = 0;
-    return;
-  }
-  const long long total = (long long)pfx[a.B] * Hkv;
-  const long long per = (total + a.grid - 1) / a.grid;
-  const long long start = (long long)Hkv * pfx[r] + (long long)h * np;
-  const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
-  const int npc = c1 - c0 + 1;
-  const long long slot0 = (long long)seg + c0;
-  const int R8 = a.R8;
-  // pass 1: M and L
-  float mloc = -INFINITY;
-  for (int c = threadIdx.x; c < npc; c += kCombineThreads)
-    mloc = fmaxf(mloc, a.ws.ml_part[((slot0 + c) * R8 + n) * 2]);
-  mloc = warp_max(mloc);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mloc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = red[0];
-    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
-    s_M = M;
-  }
-  __syncthreads();
-  const float M = s_M;
-  if (M == -INFINITY) {  // nothing visible to this row
-    for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) out[dd] = 0;
-    return;
-  }
-  float lloc = 0.0f;
-  for (int c = threadIdx.x; c < npc; c += kCombineThreads) {
-    const float mc = a.ws.ml_part[((slot0 + c) * R8 + n) * 2];
-    const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
-    if (c < kMaxPieces) wgt[c] = w;
-    lloc += w * a.ws.ml_part[((slot0 + c) * R8 + n) * 2 + 1];
-  }
+  const int ngroups = Dv / 128;  // Dv is 128 or 512
+  float acc[4][4];
+  float M = -INFINITY, L = 0.0f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lloc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float L = 0.0f;
-    for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
-    s_L = L;
-  }
-  __syncthreads();
-  const float inv = 1.0f / s_L;
-  for (int dd = threadIdx.x; dd < Dv; dd += kCombineThreads) {
-    float o = 0.0f;
-    for (int c = 0; c < npc; ++c) {
-      const float w = wgt[c];
-      if (w != 0.0f) o += w * a.ws.o_part[((slot0 + c) * R8 + n) * (long long)Dv + dd];
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
+  if (np > 0) {
+    const long long total = (long long)pfx[a.B] * Hkv;
+    const long long per = (total + a.grid - 1) / a.grid;
+    const long long start = (long long)Hkv * pfx[r] + (long long)h * np;
+    const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
+    const long long slot0 = seg + c0;
+    const int R8 = a.R8;
+#pragma unroll 2
+    for (int c = 0; c <= c1 - c0; ++c) {
+      const long long rowi = (slot0 + c) * R8 + n;
+      const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
+      float4 o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < ngroups)
+          o[q] = *reinterpret_cast<const float4*>(a.ws.o_part + rowi * Dv + 128 * q + 4 * lane);
+      if (ml.x == -INFINITY) continue;  // piece saw nothing visible
+      const float Mn = fmaxf(M, ml.x);
+      const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
+      L = L * sa + ml.y * sb;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < ngroups) {
+          acc[q][0] = acc[q][0] * sa + o[q].x * sb;
+          acc[q][1] = acc[q][1] * sa + o[q].y * sb;
+          acc[q][2] = acc[q][2] * sa + o[q].z * sb;
+          acc[q][3] = acc[q][3] * sa + o[q].w * sb;
+        }
+      }
+      M = Mn;
     }
-    const __nv_bfloat16 b = __float2bfloat16_rn(o * inv);
-    out[dd] = *reinterpret_cast<const uint16_t*>(&b);
+  }
+  const float inv = (M == -INFINITY) ? 0.0f : 1.0f / L;  // nothing visible: zeros
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q < ngroups) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[q][0] * inv, acc[q][1] * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[q][2] * inv, acc[q][3] * inv);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&lo);
+      w.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + 128 * q + 4 * lane) = w;
+    }
   }
 }
 
@@ -734,10 +775,10 @@ cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int*
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* launches) {
-  const long long segs = (long long)a.B * a.d.num_kv_heads;
-  if (segs <= 0) return cudaSuccess;
-  dim3 grid((unsigned)segs, (unsigned)a.R);
-  combine_kernel<<<grid, kCombineThreads, 0, s>>>(a);
+  const long long items = (long long)a.B * a.d.num_kv_heads * a.R;
+  if (items <= 0) return cudaSuccess;
+  const long long blocks = (items + kCombineWarps - 1) / kCombineWarps;
+  combine_kernel<<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*launches;
   return e;
