@@ -232,6 +232,32 @@ kv_status paged_decode_attn_combine(kv_pool* pool, void* stream, int32_t B,
                                     const uint8_t* abort_mask, void* out,
                                     void* workspace, size_t workspace_bytes);
 
+/*
+ * paged_decode_attn without a caller-provided workspace.  No counterpart in
+ * the post: this entry point exists for callers that cannot allocate device
+ * memory -- a serving runtime (or a plug-in inside one) that owns all of the
+ * GPU's memory and hands out no scratch buffers, and so can neither call
+ * cudaMalloc nor pass `workspace`.  Arguments and results are exactly those of
+ * paged_decode_attn; the caller still provides q, page tables, lengths and
+ * `out`.
+ *   - Scratch comes from one fixed 32 MiB device array compiled into the
+ *     library (held by every GPU that loads the library until the process
+ *     exits).  A batch whose workspace (paged_decode_workspace_size) exceeds
+ *     32 MiB is rejected with KV_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture on that device.
+ *   - All calls share the one array and nothing in it needs clearing between
+ *     calls (each call rewrites what it reads), but calls that overlap on the
+ *     GPU (concurrent streams) race on it: serialise them.
+ */
+kv_status paged_decode_attn_noalloc(kv_pool* pool, void* stream, int32_t B,
+                                    int32_t num_q_heads, int32_t q_tokens, const void* q,
+                                    const int32_t* page_table, int32_t max_pages_per_req,
+                                    const int32_t* seq_lens, const uint8_t* abort_mask,
+                                    float sm_scale, void* out);
+
 /* Human-readable name of a status code (static string). */
 const char* kv_status_string(kv_status status);
 

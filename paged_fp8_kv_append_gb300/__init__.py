@@ -64,6 +64,9 @@ _lib.paged_decode_attn_split.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _
 _lib.paged_decode_attn_split.restype = _i32
 _lib.paged_decode_attn_combine.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz]
 _lib.paged_decode_attn_combine.restype = _i32
+_lib.paged_decode_attn_noalloc.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp,
+                                           _vp, _f32, _vp]
+_lib.paged_decode_attn_noalloc.restype = _i32
 _lib.kv_status_string.argtypes = [_i32]
 _lib.kv_status_string.restype = ctypes.c_char_p
 _lib.kv_last_launch_count.argtypes = [_vp]
@@ -168,6 +171,19 @@ def paged_decode_attn(handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,
         _ptr(out, torch.bfloat16, "out"), _ptr(workspace, torch.uint8, "workspace"),
         int(workspace.numel()))
     _check(st, "paged_decode_attn")
+
+
+def paged_decode_attn_noalloc(handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,
+                              abort_mask, sm_scale, out, stream=None):
+    """paged_decode_attn with the library's fixed device scratch instead of a
+    workspace: for callers that cannot allocate device memory (see kvfp8.h)."""
+    st = _lib.paged_decode_attn_noalloc(
+        handle, _stream(stream), int(B), int(num_q_heads), int(q_tokens),
+        _ptr(q, torch.bfloat16, "q"), _ptr(page_table, torch.int32, "page_table"),
+        int(page_table.shape[-1]), _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(abort_mask, torch.uint8, "abort_mask"), float(sm_scale),
+        _ptr(out, torch.bfloat16, "out"))
+    _check(st, "paged_decode_attn_noalloc")
 
 
 def paged_decode_attn_split(handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,
