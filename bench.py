@@ -275,7 +275,10 @@ class Arm:
         per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])
         err = self.pool.error()
         if err != 0:
-            raise RuntimeError(f"device error during timing: {self.kv.kv_status_string(err)}")
+            info = int(self.pool.ctl[3].item())
+            raise RuntimeError(f"device error during timing: {self.kv.kv_status_string(err)} "
+                               f"(wait info cta={info >> 12} warp={(info >> 7) & 31} "
+                               f"barrier={(info >> 6) & 1} stage={info & 63}; dtype={self.dtype})")
         return total_ms, per, lens_timed, int(sum(launches))
 
     def run_e2e(self, steps: int, warmup: int):

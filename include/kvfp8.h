@@ -54,7 +54,8 @@ typedef enum {
   KV_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute query) */
   KV_ERR_OUT_OF_PAGES = 4,  /* device: free list exhausted during an append */
   KV_ERR_BAD_PAGE_ID = 5,   /* device: a page id outside [0, num_pages) was met */
-  KV_ERR_TIMEOUT = 6        /* device: a bounded wait inside a kernel gave up */
+  KV_ERR_TIMEOUT = 6,       /* device: a bounded wait inside a kernel gave up */
+  KV_ERR_INTERNAL = 7       /* device: an internal consistency check failed (a library bug) */
 } kv_status;
 
 typedef enum { KV_DTYPE_E4M3 = 0, KV_DTYPE_BF16 = 1 } kv_dtype;
@@ -74,6 +75,8 @@ enum {
   KV_CTL_FREE_HEAD = 0,    /* next unused position of free_list */
   KV_CTL_ERROR = 1,        /* first device-side error (kv_status), 0 = none */
   KV_CTL_APPEND_STOP = 2,  /* last append: first request not served (B if all were) */
+  KV_CTL_WAIT_INFO = 3,    /* first timed-out wait: (cta << 12) | (warp << 7) | (barrier << 6) | stage;
+                              barrier 0 = data-ready, 1 = slot-free; 0 = none */
   KV_CTL_WORDS = 4
 };
 

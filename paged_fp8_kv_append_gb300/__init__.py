@@ -28,10 +28,10 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 # status codes
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA = 0, 1, 2, 3
-KV_ERR_OUT_OF_PAGES, KV_ERR_BAD_PAGE_ID, KV_ERR_TIMEOUT = 4, 5, 6
+KV_ERR_OUT_OF_PAGES, KV_ERR_BAD_PAGE_ID, KV_ERR_TIMEOUT, KV_ERR_INTERNAL = 4, 5, 6, 7
 KV_DTYPE_E4M3, KV_DTYPE_BF16 = 0, 1
 KV_LAYOUT_GQA, KV_LAYOUT_LATENT = 0, 1
-KV_CTL_FREE_HEAD, KV_CTL_ERROR, KV_CTL_APPEND_STOP, KV_CTL_WORDS = 0, 1, 2, 4
+KV_CTL_FREE_HEAD, KV_CTL_ERROR, KV_CTL_APPEND_STOP, KV_CTL_WAIT_INFO, KV_CTL_WORDS = 0, 1, 2, 3, 4
 
 
 class kv_pool_desc(ctypes.Structure):

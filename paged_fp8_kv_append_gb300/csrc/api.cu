@@ -35,6 +35,20 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || T * G > 8)
       return KV_ERR_UNSUPPORTED;
     cfg->kind = d.dtype == KV_DTYPE_E4M3 ? 0 : 1;
+    // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
+    // tiles are twice as large) dividing Hkv; ring depth from the ring size
+    int hs = cfg->kind == 0 ? 8 : 4;
+    while (d.num_kv_heads % hs != 0) hs >>= 1;
+    cfg->Hs = hs;
+    const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 0 ? 1 : 2);
+    cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;
+    if (cfg->stages > gqa_max_stages()) cfg->stages = gqa_max_stages();
+    // A consumer warp serves every (consumers/Hs)-th unit; the ring depth must
+    // be a multiple of that stride so each warp sees every phase of the stages
+    // it uses (parity waits cannot tell phase n from phase n-2).
+    const int wph = gqa_consumer_warps() / hs;
+    cfg->stages -= cfg->stages % wph;
+    if (cfg->stages < 2 || cfg->stages < wph) return KV_ERR_UNSUPPORTED;
     const int sms = sm_count();
     const int per_sm = sms > 0 ? gqa_split_ctas_per_sm(cfg->kind) : 0;
     if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
@@ -51,12 +65,16 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
   cfg->kind = 2;
   cfg->grid = sms * per_sm;
   cfg->R8 = T * Hq;
+  cfg->Hs = 1;
+  cfg->stages = 0;
   return KV_OK;
 }
 
 size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
                         void* base, DecodeWs* ws) {
-  const long long slots = (long long)B * Hkv + cfg.grid;
+  // one partial slot per (CTA, segment) piece; segments are (request, head
+  // group); each slot holds Hs heads x R8 rows
+  const long long slots = (long long)B * (Hkv / cfg.Hs) + cfg.grid;
   size_t off = 0;
   const size_t o_pfx = off;
   off = align256(off + sizeof(int32_t) * (size_t)(B + 1));
@@ -65,9 +83,9 @@ size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfi
   const size_t o_bad = off;
   off = align256(off + (size_t)B);
   const size_t o_ml = off;
-  off = align256(off + sizeof(float) * 2 * (size_t)slots * cfg.R8);
+  off = align256(off + sizeof(float) * 2 * (size_t)slots * cfg.Hs * cfg.R8);
   const size_t o_o = off;
-  off = align256(off + sizeof(float) * (size_t)slots * cfg.R8 * d.head_dim_v);
+  off = align256(off + sizeof(float) * (size_t)slots * cfg.Hs * cfg.R8 * d.head_dim_v);
   if (ws) {
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->pfx = reinterpret_cast<int32_t*>(b + o_pfx);
@@ -120,6 +138,9 @@ kv_status decode_prepare(kv_pool* pool, int32_t B, int32_t Hq, int32_t T, const 
   x.out = static_cast<uint16_t*>(out);
   x.grid = cfg.grid;
   x.R8 = cfg.R8;
+  x.Hs = cfg.Hs;
+  x.HG = Hkv / cfg.Hs;
+  x.stages = cfg.stages;
   const size_t need = decode_ws_layout(d, B, Hkv, cfg, workspace, &x.ws);
   if (B > 0 && workspace_bytes < need) return KV_ERR_INVALID_ARG;
   *kind = cfg.kind;
@@ -298,6 +319,7 @@ const char* kv_status_string(kv_status s) {
     case KV_ERR_OUT_OF_PAGES: return "KV_ERR_OUT_OF_PAGES";
     case KV_ERR_BAD_PAGE_ID: return "KV_ERR_BAD_PAGE_ID";
     case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
+    case KV_ERR_INTERNAL: return "KV_ERR_INTERNAL";
   }
   return "KV_ERR_UNKNOWN";
 }

@@ -82,9 +82,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false)
 // when *abort_flag (shared memory) is set by another warp or after
-// kWaitLimitNs, in which case it sets the abort flag and KV_ERR_TIMEOUT.
+// kWaitLimitNs, in which case it sets the abort flag, KV_ERR_TIMEOUT and (first
+// timeout wins) the diagnostic word ctl[KV_CTL_WAIT_INFO] = `info`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, int32_t* ctl) {
+                                          volatile int* abort_flag, int32_t* ctl,
+                                          int info = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
@@ -93,11 +95,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
-        set_error(ctl, KV_ERR_TIMEOUT);
+        if (atomicCAS(reinterpret_cast<int*>(ctl + KV_CTL_ERROR), 0, KV_ERR_TIMEOUT) == 0)
+          ctl[KV_CTL_WAIT_INFO] = info;
         return false;
       }
     }
   }
+}
+
+// Diagnostic word of a wait (see KV_CTL_WAIT_INFO).
+__device__ __forceinline__ int wait_info(int warp, int which, int stage) {
+  return (int)((blockIdx.x << 12) | ((warp & 31) << 7) | ((which & 1) << 6) | (stage & 63));
 }
 
 // ------------------------------------------------------ bulk (TMA) copies

@@ -92,16 +92,17 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
 
 // ------------------------------------------------- segment cursor
 
-// Walks segments (r, h) of the flattened unit sequence.  pfx may live in
-// shared or global memory.
+// Walks segments (request r, head group h) of the flattened unit sequence;
+// `groups` is the number of head groups per request.  pfx may live in shared
+// or global memory.
 struct Cursor {
   int r, h, np;
   long long seg_start;
 };
 
-__device__ __forceinline__ Cursor cursor_at(const int32_t* pfx, int B, int Hkv, long long x) {
-  // last r with pfx[r] <= x / Hkv; that request has pages (pfx[r+1] > x/Hkv)
-  const long long v = x / Hkv;
+__device__ __forceinline__ Cursor cursor_at(const int32_t* pfx, int B, int groups, long long x) {
+  // last r with pfx[r] <= x / groups; that request has pages (pfx[r+1] > x/groups)
+  const long long v = x / groups;
   int lo = 0, hi = B;  // invariant: pfx[lo] <= v < pfx[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -113,20 +114,20 @@ __device__ __forceinline__ Cursor cursor_at(const int32_t* pfx, int B, int Hkv, 
   Cursor c;
   c.r = lo;
   c.np = pfx[lo + 1] - pfx[lo];
-  c.h = (int)((x - (long long)Hkv * pfx[lo]) / c.np);
-  c.seg_start = (long long)Hkv * pfx[lo] + (long long)c.h * c.np;
+  c.h = (int)((x - (long long)groups * pfx[lo]) / c.np);
+  c.seg_start = (long long)groups * pfx[lo] + (long long)c.h * c.np;
   return c;
 }
 
-__device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* pfx, int B, int Hkv) {
-  if (++c.h == Hkv) {
+__device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* pfx, int B, int groups) {
+  if (++c.h == groups) {
     c.h = 0;
     do {
       ++c.r;
     } while (c.r < B && pfx[c.r + 1] == pfx[c.r]);
     if (c.r < B) c.np = pfx[c.r + 1] - pfx[c.r];
   }
-  if (c.r < B) c.seg_start = (long long)Hkv * pfx[c.r] + (long long)c.h * c.np;
+  if (c.r < B) c.seg_start = (long long)groups * pfx[c.r] + (long long)c.h * c.np;
 }
 
 // ------------------------------------------------- tensor-core helpers
@@ -195,55 +196,62 @@ __device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
 
 // ------------------------------------------------- split kernel
 
-// Ring depth and consumer warps per CTA.  At these sizes three CTAs share an
-// SM (~144 KB of e4m3 pages in flight per SM); measured faster than one or
-// two larger CTAs per SM with deeper rings.
+// A unit of work is one page of one request for Hs kv heads (a "head
+// group"; Hs = the largest power of two <= 8 that divides Hkv, <= 4 for
+// bf16).  The Hs K tiles of a page are contiguous in the cache, and so are
+// its Hs V tiles, so one unit is two bulk copies of Hs * P * D elements.
+// One CTA per SM: a producer warp and kConsumers consumer warps; consumer w
+// serves head w % Hs of every (w / Hs)-th unit, so each unit is consumed by
+// exactly Hs warps.  The ring holds kRingBytes of units in flight.
 #ifndef KV_GQA_CONSUMERS
-#define KV_GQA_CONSUMERS 4
+#define KV_GQA_CONSUMERS 8
 #endif
-#ifndef KV_GQA_FP8_STAGES
-#define KV_GQA_FP8_STAGES 12
+#ifndef KV_GQA_RING_KB
+#define KV_GQA_RING_KB 160
 #endif
-#ifndef KV_GQA_BF16_STAGES
-#define KV_GQA_BF16_STAGES 8
-#endif
+
+constexpr int kConsumers = KV_GQA_CONSUMERS;
+constexpr int kMaxStages = 40;
 
 template <bool FP8>
 struct GqaCfg {
   static constexpr int P = 16;                      // tokens per page
   static constexpr int D = 128;                     // head dim (K and V)
   static constexpr int ES = FP8 ? 1 : 2;            // cache element bytes
-  static constexpr int TILE = P * D * ES;           // bytes of one K or V tile
-  static constexpr int STAGE = 2 * TILE;            // K tile + V tile
-  static constexpr int STAGES = FP8 ? KV_GQA_FP8_STAGES : KV_GQA_BF16_STAGES;  // ring depth
-  static constexpr int CONSUMERS = KV_GQA_CONSUMERS;                          // consumer warps
-  static constexpr int THREADS = (CONSUMERS + 1) * 32;
+  static constexpr int TILE = P * D * ES;           // bytes of one head's K or V tile
+  static constexpr int RING = KV_GQA_RING_KB * 1024;
+  static constexpr int THREADS = (kConsumers + 1) * 32;
   static constexpr int R8 = 8;                      // query rows per kv head (padded)
   static constexpr int PFX_CACHE = 1024;            // pfx entries cached in smem
   static constexpr int PBUF = FP8 ? R8 * P * 2 : R8 * P * 4;  // per-warp P transpose
   // shared memory carve-up (byte offsets)
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_MERGE_O = OFF_RING + STAGES * STAGE;              // [C][R8][D] f32
-  static constexpr int OFF_MERGE_ML = OFF_MERGE_O + CONSUMERS * R8 * D * 4;  // [C][R8][2] f32
-  static constexpr int OFF_PBUF = OFF_MERGE_ML + CONSUMERS * R8 * 2 * 4;
-  static constexpr int OFF_META = OFF_PBUF + CONSUMERS * PBUF;               // [STAGES] int4
-  static constexpr int OFF_BAR = OFF_META + STAGES * 16;                    // full, empty
-  static constexpr int OFF_PFX = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int OFF_MERGE_O = OFF_RING + RING;                         // [W][R8][D] f32
+  static constexpr int OFF_MERGE_ML = OFF_MERGE_O + kConsumers * R8 * D * 4;  // [W][R8][2] f32
+  static constexpr int OFF_PBUF = OFF_MERGE_ML + kConsumers * R8 * 2 * 4;
+  static constexpr int OFF_META = OFF_PBUF + kConsumers * PBUF;               // [S] StageMeta
+  static constexpr int OFF_BAR = OFF_META + kMaxStages * 80;                  // full, empty
+  static constexpr int OFF_PFX = OFF_BAR + 2 * kMaxStages * 8;
   static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;
   static constexpr int SMEM = OFF_FLAG + 16;
 };
 
-// Units a producer warp issues per warp instruction (one per lane).
+// Most units a producer warp issues per warp instruction (one per lane; at most
+// a quarter of the ring depth so most stages stay in flight while a group waits).
 constexpr int kIssueGroup = 8;
 
 struct StageMeta {
-  int n_valid;  // tokens of this page below the request length (0: skip page)
-  float ks, vs; // K and V scales (1 for bf16)
-  int pos0;     // position of the page's first token
+  int n_valid;    // tokens of this page below the request length (0: skip page)
+  int pos0;       // position of the page's first token
+  float ks[8];    // K scales of the unit's heads (1 for bf16)
+  float vs[8];    // V scales
+  int unit;       // stage sequence number (low 32 bits): consumers check it
+  int pad;
 };
+static_assert(sizeof(StageMeta) == 80, "StageMeta layout");
 
 template <bool FP8>
-__global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
+__global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
     gqa_split_kernel(const DecodeArgs a) {
   using C = GqaCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -253,14 +261,21 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
   uint8_t* pbuf_all = smem + C::OFF_PBUF;
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + C::OFF_META);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + C::STAGES;
+  uint64_t* empty = full + kMaxStages;
   int32_t* pfx_s = reinterpret_cast<int32_t*>(smem + C::OFF_PFX);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, Hkv = a.d.num_kv_heads;
+  const int Hs = a.Hs, HG = a.HG;              // heads per unit, head groups
+  const int S = a.stages;                      // ring stages (<= kMaxStages)
+  const int stage_bytes = 2 * Hs * C::TILE;
+  if (S < 2 || S > kMaxStages || S % (kConsumers / Hs) != 0 || stage_bytes * S > C::RING) {
+    if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad ring
+    return;
+  }
   const int32_t* pfx_g = a.ws.pfx;
-  const long long total = (long long)pfx_g[B] * Hkv;
+  const long long total = (long long)pfx_g[B] * HG;
   const long long per = (total + gridDim.x - 1) / gridDim.x;
   const long long x_begin = (long long)blockIdx.x * per;
   const long long x_end = min(total, x_begin + per);
@@ -270,55 +285,62 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
   if (cached)
     for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], Hs);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   const int32_t* pfx = cached ? pfx_s : pfx_g;
-  const Cursor start = cursor_at(pfx, B, Hkv, x_begin);
+  const Cursor start = cursor_at(pfx, B, HG, x_begin);
   const int P = C::P, D = C::D;
 
-  if (warp == C::CONSUMERS) {
+  if (warp == kConsumers) {
     // ======================= producer warp =======================
     // Lane l owns unit x0 + l of each batch of 32 consecutive units.  Page
     // ids (and lengths) are loaded two batches ahead and scales one batch
     // ahead, so the dependent page-id -> scale loads never hold up the copy
-    // issue; each lane then issues its own unit's copies.
+    // issue; each lane then issues its own unit's two copies.
     const uint64_t policy = l2_evict_first_policy();
     const int maxp = a.max_pages;
     Cursor lc = start;  // per-lane cursor, only moves forward
     struct Unit {
-      int r, h, j, p, L;
+      int r, hg, j, p, L;
     };
     auto locate_load = [&](long long xu) {
       Unit u;
       u.r = 0;
-      u.h = 0;
+      u.hg = 0;
       u.j = 0;
       u.p = -1;
       u.L = 0;
       if (xu < x_end) {
-        while (xu >= lc.seg_start + lc.np) cursor_next(lc, pfx, B, Hkv);
+        while (xu >= lc.seg_start + lc.np) cursor_next(lc, pfx, B, HG);
         u.r = lc.r;
-        u.h = lc.h;
+        u.hg = lc.h;
         u.j = (int)(xu - lc.seg_start);
         u.p = a.page_table[(long long)u.r * maxp + u.j];
         u.L = a.seq_lens[u.r];
       }
       return u;
     };
-    auto scales = [&](const Unit& u, long long xu, float& ks, float& vs, bool& ok) {
+    auto scales = [&](const Unit& u, long long xu, float (&ks)[8], float (&vs)[8], bool& ok) {
       ok = false;
-      ks = vs = 1.0f;
+#pragma unroll
+      for (int hh = 0; hh < 8; ++hh) ks[hh] = vs[hh] = 1.0f;
       if (xu < x_end) {
         ok = u.p >= 0 && u.p < a.d.num_pages;
         if (ok && FP8) {
-          ks = a.d.k_scale[(long long)u.p * Hkv + u.h];
-          vs = a.d.v_scale[(long long)u.p * Hkv + u.h];
+          const long long base = (long long)u.p * Hkv + (long long)u.hg * Hs;
+#pragma unroll
+          for (int hh = 0; hh < 8; ++hh) {
+            if (hh < Hs) {
+              ks[hh] = a.d.k_scale[base + hh];
+              vs[hh] = a.d.v_scale[base + hh];
+            }
+          }
         }
         if (!ok) {
           a.ws.rq_bad[u.r] = 1;
@@ -328,66 +350,74 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
     };
     Unit u0 = locate_load(x_begin + lane);
     Unit u1 = locate_load(x_begin + 32 + lane);
-    float ks0, vs0, ks1, vs1;
+    float ks0[8], vs0[8], ks1[8], vs1[8];
     bool ok0, ok1;
     scales(u0, x_begin + lane, ks0, vs0, ok0);
+    // issue group: a group waits for the stages of the units S earlier, so it
+    // must stay small next to S or the ring drains before it refills; large
+    // units (S small) need few issues per byte anyway
+    const int grp = max(1, min(kIssueGroup, S / 4));
     long long k = 0;       // stage sequence number of the batch's first unit
     long long issued = 0;  // units whose copies have been issued
-    static_assert(C::STAGES >= kIssueGroup, "ring shallower than an issue group");
     for (long long xb = x_begin; xb < x_end && !*abort_flag; xb += 32) {
       scales(u1, xb + 32 + lane, ks1, vs1, ok1);
       const Unit u2 = locate_load(xb + 64 + lane);
       const int cnt = (int)min(32ll, x_end - xb);
-      // lanes issue their own unit's copies, kIssueGroup units per step, so
-      // one warp instruction moves several pages (a group never holds two
-      // units of one stage because kIssueGroup <= STAGES)
       bool go = true;
-      for (int g0 = 0; g0 < cnt && go; g0 += kIssueGroup) {
-        const bool mine = lane >= g0 && lane < min(g0 + kIssueGroup, cnt);
+      for (int g0 = 0; g0 < cnt && go; g0 += grp) {
+        const bool mine = lane >= g0 && lane < min(g0 + grp, cnt);
         const long long kl = k + lane;
-        const int stage = (int)(kl % C::STAGES);
+        const int stage = (int)(kl % S);
         bool ok = true;
-        if (mine && kl >= C::STAGES)
-          ok = mbar_wait(&empty[stage], (uint32_t)(((kl / C::STAGES) - 1) & 1), abort_flag,
-                         a.d.ctl);
+        if (mine && kl >= S)
+          ok = mbar_wait(&empty[stage], (uint32_t)(((kl / S) - 1) & 1), abort_flag, a.d.ctl,
+                         wait_info(warp, 1, stage));
         go = __all_sync(0xffffffffu, ok);
         if (!go) break;
         if (mine) {
           StageMeta m;
           m.n_valid = ok0 ? min(P, u0.L - u0.j * P) : 0;
-          m.ks = ks0;
-          m.vs = vs0;
           m.pos0 = u0.j * P;
+#pragma unroll
+          for (int hh = 0; hh < 8; ++hh) {
+            m.ks[hh] = ks0[hh];
+            m.vs[hh] = vs0[hh];
+          }
+          m.unit = (int)kl;
+          m.pad = 0;
           meta[stage] = m;
           if (ok0) {
-            uint8_t* dst = ring + stage * C::STAGE;
-            const long long ph = (long long)u0.p * Hkv + u0.h;
-            mbar_arrive_expect_tx(&full[stage], C::STAGE);
-            bulk_g2s(dst, static_cast<const uint8_t*>(a.d.k_cache) + ph * C::TILE, C::TILE,
-                     &full[stage], policy);
-            bulk_g2s(dst + C::TILE, static_cast<const uint8_t*>(a.d.v_cache) + ph * C::TILE,
-                     C::TILE, &full[stage], policy);
+            uint8_t* dst = ring + (size_t)stage * stage_bytes;
+            const long long ph = (long long)u0.p * Hkv + (long long)u0.hg * Hs;
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_bytes);
+            bulk_g2s(dst, static_cast<const uint8_t*>(a.d.k_cache) + ph * C::TILE,
+                     (uint32_t)(Hs * C::TILE), &full[stage], policy);
+            bulk_g2s(dst + Hs * C::TILE, static_cast<const uint8_t*>(a.d.v_cache) + ph * C::TILE,
+                     (uint32_t)(Hs * C::TILE), &full[stage], policy);
           } else {
             mbar_arrive(&full[stage]);
           }
         }
         __syncwarp();
-        issued = k + min(g0 + kIssueGroup, cnt);
+        issued = k + min(g0 + grp, cnt);
       }
       if (!go) break;
       k += cnt;
       u0 = u1;
-      ks0 = ks1;
-      vs0 = vs1;
+#pragma unroll
+      for (int hh = 0; hh < 8; ++hh) {
+        ks0[hh] = ks1[hh];
+        vs0[hh] = vs1[hh];
+      }
       ok0 = ok1;
       u1 = u2;
     }
     // On abort, copies already issued may still be landing: wait for them
     // (bounded) before this CTA's shared memory goes away.
     if (*abort_flag && lane == 0) {
-      for (long long q = max(0ll, issued - C::STAGES); q < issued; ++q) {
-        const int stage = (int)(q % C::STAGES);
-        const uint32_t par = (uint32_t)((q / C::STAGES) & 1);
+      for (long long q = max(0ll, issued - S); q < issued; ++q) {
+        const int stage = (int)(q % S);
+        const uint32_t par = (uint32_t)((q / S) & 1);
         const uint64_t t0 = global_ns();
         while (!mbar_try_wait(&full[stage], par) && global_ns() - t0 < 100000000ull) {
         }
@@ -401,6 +431,8 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
   const int odd = g & 1;
   uint8_t* pbuf = pbuf_all + warp * C::PBUF;
   const int G = a.G, T = a.T, R = a.R;
+  const int WPH = kConsumers / Hs;          // warps per head
+  const int hw = warp % Hs, lg = warp / Hs;  // head within the group, page lane
   Cursor cur = start;
   long long x = x_begin;
   long long k_base = 0;
@@ -410,7 +442,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
     const long long seg_end = cur.seg_start + cur.np;
     const long long piece_end = min(seg_end, x_end);
     const int npages = (int)(piece_end - x);
-    const int r = cur.r, h = cur.h;
+    const int r = cur.r, h = cur.h * Hs + hw;  // request, kv head of this warp
     const int L = a.seq_lens[r];
 
     // ---- query fragments for row n = g (zero for padding rows)
@@ -458,15 +490,21 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 
-    for (int pi = warp; pi < npages; pi += C::CONSUMERS) {
-      const long long kk = k_base + pi;
-      const int stage = (int)(kk % C::STAGES);
-      const bool ok = mbar_wait(&full[stage], (uint32_t)((kk / C::STAGES) & 1), abort_flag,
-                                a.d.ctl);
-      const StageMeta mt = meta[stage];
-      if (ok && mt.n_valid > 0) {
-        const uint8_t* Kt = ring + stage * C::STAGE;
-        const uint8_t* Vt = Kt + C::TILE;
+    // this warp's units of the piece: stage numbers kk == lg (mod WPH)
+    const long long kfirst = k_base + (long long)((lg - (int)(k_base % WPH) + WPH) % WPH);
+    for (long long kk = kfirst; kk < k_base + npages; kk += WPH) {
+      const int stage = (int)(kk % S);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((kk / S) & 1),
+                                                        abort_flag, a.d.ctl,
+                                                        wait_info(warp, 0, stage)));
+      const StageMeta& mt = meta[stage];
+      if (ok && mt.unit != (int)kk) {  // would mean a stale stage: report, never compute on it
+        if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
+        *abort_flag = 1;
+      }
+      if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
+        const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
+        const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
         // ---------------- S^T = K Q^T
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (FP8) {
@@ -506,7 +544,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
           }
         }
         // scores (log2 domain) for (token g | g+8, row 2t | 2t+1)
-        const float sc = FP8 ? mt.ks * ssl : ssl;
+        const float sc = FP8 ? mt.ks[hw] * ssl : ssl;
         float s[4] = {(sa[0] + sb[0]) * sc, (sa[1] + sb[1]) * sc, (sa[2] + sb[2]) * sc,
                       (sa[3] + sb[3]) * sc};
         const int pA = mt.pos0 + g, pB = mt.pos0 + g + 8;
@@ -546,7 +584,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
         const int nv = mt.n_valid;
         if constexpr (FP8) {
           __half* pb = reinterpret_cast<__half*>(pbuf);  // [8 rows][16 tokens]
-          const float vsc = mt.vs;
+          const float vsc = mt.vs[hw];
           pb[(2 * t) * 16 + g] = __float2half_rn(p0 * vsc);
           pb[(2 * t + 1) * 16 + g] = __float2half_rn(p1 * vsc);
           pb[(2 * t) * 16 + g + 8] = __float2half_rn(p2 * vsc);
@@ -603,7 +641,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
 
-    // ---- merge the four warps' states of this piece into one partial
+    // ---- merge the states of the warps that share a head into one partial
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
@@ -624,37 +662,38 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS)
       ml[(2 * t + 1) * 2 + 0] = m1;
       ml[(2 * t + 1) * 2 + 1] = l1;
     }
-    named_bar_sync(1, C::CONSUMERS * 32);
+    named_bar_sync(1, kConsumers * 32);
     {
-      const long long slot = (long long)r * Hkv + h + blockIdx.x;
+      // slot of this (CTA, segment) piece; rows (head in group, query row)
+      const long long slot = (long long)r * HG + cur.h + blockIdx.x;
       const int tid = threadIdx.x;  // consumer thread index
-      for (int e = tid; e < C::R8 * D; e += C::CONSUMERS * 32) {
-        const int n = e / D, dd = e % D;
+      for (int e = tid; e < Hs * C::R8 * D; e += kConsumers * 32) {
+        const int hh = e / (C::R8 * D), n = (e / D) % C::R8, dd = e % D;
         float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::CONSUMERS; ++w) M = fmaxf(M, merge_ml[(w * C::R8 + n) * 2]);
+        for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hs + hh) * C::R8 + n) * 2]);
         float o = 0.0f, lsum = 0.0f;
         if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < C::CONSUMERS; ++w) {
+          for (int q = 0; q < WPH; ++q) {
+            const int w = q * Hs + hh;
             const float mw = merge_ml[(w * C::R8 + n) * 2];
             const float sc = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
             o += merge_o[(w * C::R8 + n) * D + dd] * sc;
             lsum += merge_ml[(w * C::R8 + n) * 2 + 1] * sc;
           }
         }
-        a.ws.o_part[(slot * C::R8 + n) * D + dd] = o;
+        const long long row = (slot * Hs + hh) * C::R8 + n;
+        a.ws.o_part[row * D + dd] = o;
         if (dd == 0) {
-          a.ws.ml_part[(slot * C::R8 + n) * 2 + 0] = M;
-          a.ws.ml_part[(slot * C::R8 + n) * 2 + 1] = lsum;
+          a.ws.ml_part[row * 2 + 0] = M;
+          a.ws.ml_part[row * 2 + 1] = lsum;
         }
       }
     }
-    named_bar_sync(1, C::CONSUMERS * 32);
+    named_bar_sync(1, kConsumers * 32);
 
     k_base += npages;
     x = piece_end;
-    if (x == seg_end) cursor_next(cur, pfx, B, Hkv);
+    if (x == seg_end) cursor_next(cur, pfx, B, HG);
   }
 }
 
@@ -673,8 +712,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
   const long long nitems = (long long)a.B * Hkv * a.R;
   if (item >= nitems) return;
   const int n = (int)(item % a.R);
-  const long long seg = item / a.R;
-  const int r = (int)(seg / Hkv), h = (int)(seg % Hkv);
+  const long long rh = item / a.R;
+  const int r = (int)(rh / Hkv), h = (int)(rh % Hkv);
+  const int Hs = a.Hs, HG = a.HG;
+  const int hg = h / Hs, hw = h % Hs;
+  const long long seg = (long long)r * HG + hg;
   if (a.ws.rq_skip[r] || a.ws.rq_bad[r]) return;  // aborted: output left untouched
   const int Dv = a.d.head_dim_v;
   const int tq = n / a.G, hq = h * a.G + n % a.G;
@@ -687,15 +729,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
   if (np > 0) {
-    const long long total = (long long)pfx[a.B] * Hkv;
+    const long long total = (long long)pfx[a.B] * HG;
     const long long per = (total + a.grid - 1) / a.grid;
-    const long long start = (long long)Hkv * pfx[r] + (long long)h * np;
+    const long long start = (long long)HG * pfx[r] + (long long)hg * np;
     const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
     const long long slot0 = seg + c0;
     const int R8 = a.R8;
 #pragma unroll 2
     for (int c = 0; c <= c1 - c0; ++c) {
-      const long long rowi = (slot0 + c) * R8 + n;
+      const long long rowi = ((slot0 + c) * Hs + hw) * R8 + n;
       const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
       float4 o[4];
 #pragma unroll
@@ -735,6 +777,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
 }  // namespace
 
 // ------------------------------------------------- host side
+
+int gqa_ring_bytes(int kind) { return kind == 0 ? GqaCfg<true>::RING : GqaCfg<false>::RING; }
+int gqa_max_stages() { return kMaxStages; }
+int gqa_consumer_warps() { return kConsumers; }
 
 int gqa_split_ctas_per_sm(int kind) {
   static int cache[2] = {-1, -1};

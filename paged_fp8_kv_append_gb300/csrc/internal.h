@@ -47,8 +47,8 @@ struct DecodeWs {
   int32_t* pfx;       // [B+1] exclusive prefix of pages per request (0 if skipped)
   uint8_t* rq_skip;   // [B] 1: request gets no output (aborted / invalid)
   uint8_t* rq_bad;    // [B] 1: a page id out of range was met while reading
-  float* ml_part;     // [slots][R8][2]  running max (log2 domain) and sum
-  float* o_part;      // [slots][R8][Dv] unnormalised partial outputs
+  float* ml_part;     // [slots][Hs][R8][2]  running max (log2 domain) and sum
+  float* o_part;      // [slots][Hs][R8][Dv] unnormalised partial outputs
   size_t bytes;
 };
 
@@ -63,16 +63,27 @@ struct DecodeArgs {
   float sm_scale_log2;  // sm_scale * log2(e)
   uint16_t* out;        // bf16 bits [B][T][Hq][Dv]
   int32_t grid;         // CTAs of the split kernel
-  int32_t R8;           // rows per partial slot (R rounded up)
+  int32_t R8;           // rows per (partial slot, head) (R rounded up)
+  int32_t Hs;           // kv heads per unit of work (a head group)
+  int32_t HG;           // head groups per request (Hkv / Hs)
+  int32_t stages;       // ring stages of the split kernel
   DecodeWs ws;
 };
 
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {
-  int kind;   // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3
-  int grid;   // split-kernel CTAs
-  int R8;     // partial rows per slot
+  int kind;    // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3
+  int grid;    // split-kernel CTAs
+  int R8;      // partial rows per (slot, head)
+  int Hs;      // kv heads per unit of work
+  int stages;  // ring stages
 };
+
+// Ring bytes and stage limit of the GQA split kernel (for the host-side
+// choice of heads per unit and ring depth).
+int gqa_ring_bytes(int kind);
+int gqa_max_stages();
+int gqa_consumer_warps();
 
 kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig* cfg);
 size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
