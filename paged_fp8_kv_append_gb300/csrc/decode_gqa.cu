@@ -132,11 +132,22 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* pfx, int B
 
 // ------------------------------------------------- tensor-core helpers
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  // exact: every e4m3 value is an f16 value
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+
+// Four e4m3 codes (bytes 0..3 of w) -> two f16x2 words, lo = (b0, b1) and
+// hi = (b2, b3); exact (every e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 2^x on the special-function unit (flushes denormal results to zero, which
+// only drops softmax weights below 2^-126).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
@@ -428,7 +439,6 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
 
   // ========================= consumer warps =========================
   const int g = lane >> 2, t = lane & 3;
-  const int odd = g & 1;
   uint8_t* pbuf = pbuf_all + warp * C::PBUF;
   const int G = a.G, T = a.T, R = a.R;
   const int WPH = kConsumers / Hs;          // warps per head
@@ -505,40 +515,30 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
       if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
         const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
         const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
-        // ---------------- S^T = K Q^T
+        // ---------------- S^T = K Q^T  (two accumulator chains for ILP)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (FP8) {
-          // row g: chunk t (dims 16t..) and t+4 (dims 64+16t..); odd rows
-          // load them in the other order so a quarter-warp hits 8 banks groups
-          const uint4 x0 = lds128(Kt + g * 128 + 16 * (t + 4 * odd));
-          const uint4 x1 = lds128(Kt + g * 128 + 16 * (t + 4 - 4 * odd));
-          const uint4 y0 = lds128(Kt + (g + 8) * 128 + 16 * (t + 4 * odd));
-          const uint4 y1 = lds128(Kt + (g + 8) * 128 + 16 * (t + 4 - 4 * odd));
-          const uint4 kA = odd ? x1 : x0, kB = odd ? x0 : x1;
-          const uint4 hA = odd ? y1 : y0, hB = odd ? y0 : y1;
+          // row g (and g+8): dims 16t..16t+15 and 64+16t..64+16t+15
+          const uint4 kA = lds128(Kt + g * 128 + 16 * t);
+          const uint4 kB = lds128(Kt + g * 128 + 64 + 16 * t);
+          const uint4 hA = lds128(Kt + (g + 8) * 128 + 16 * t);
+          const uint4 hB = lds128(Kt + (g + 8) * 128 + 64 + 16 * t);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t w = w_of(j < 4 ? kA : kB, j & 3);
-            const uint32_t w8 = w_of(j < 4 ? hA : hB, j & 3);
-            const uint32_t a0 = e4m3x2_to_f16x2(w), a2 = e4m3x2_to_f16x2(w >> 16);
-            const uint32_t a1 = e4m3x2_to_f16x2(w8), a3 = e4m3x2_to_f16x2(w8 >> 16);
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16(w_of(j < 4 ? kA : kB, j & 3), a0, a2);
+            e4m3x4_to_f16(w_of(j < 4 ? hA : hB, j & 3), a1, a3);
             if (j & 1)
               mma16816<true>(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
             else
               mma16816<true>(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
           }
         } else {
-          // row g: chunks t, t+4, t+8, t+12 (8 dims each); odd rows swap pairs
-          uint4 cg[4], c8[4];
+          // row g (and g+8): chunks t, t+4, t+8, t+12 (8 dims each)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            cg[m] = lds128(Kt + g * 256 + 16 * (t + 4 * (m ^ odd)));
-            c8[m] = lds128(Kt + (g + 8) * 256 + 16 * (t + 4 * (m ^ odd)));
-          }
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const uint4 vg = odd ? cg[m ^ 1] : cg[m];
-            const uint4 v8 = odd ? c8[m ^ 1] : c8[m];
+            const uint4 vg = lds128(Kt + g * 256 + 16 * (t + 4 * m));
+            const uint4 v8 = lds128(Kt + (g + 8) * 256 + 16 * (t + 4 * m));
             mma16816<false>(sa, vg.x, v8.x, vg.y, v8.y, qf[2 * m][0], qf[2 * m][1]);
             mma16816<false>(sb, vg.z, v8.z, vg.w, v8.w, qf[2 * m + 1][0], qf[2 * m + 1][1]);
           }
@@ -547,12 +547,17 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
         const float sc = FP8 ? mt.ks[hw] * ssl : ssl;
         float s[4] = {(sa[0] + sb[0]) * sc, (sa[1] + sb[1]) * sc, (sa[2] + sb[2]) * sc,
                       (sa[3] + sb[3]) * sc};
-        const int pA = mt.pos0 + g, pB = mt.pos0 + g + 8;
-        const bool vA = g < mt.n_valid, vB = g + 8 < mt.n_valid;
-        s[0] = (vA && pA <= lim0) ? s[0] : -INFINITY;
-        s[1] = (vA && pA <= lim1) ? s[1] : -INFINITY;
-        s[2] = (vB && pB <= lim0) ? s[2] : -INFINITY;
-        s[3] = (vB && pB <= lim1) ? s[3] : -INFINITY;
+        const int nv = mt.n_valid;
+        const bool full_page = nv == P;
+        if (!full_page || mt.pos0 + P - 1 > min(lim0, lim1)) {
+          // partial page or causal edge: mask invisible positions
+          const int pA = mt.pos0 + g, pB = mt.pos0 + g + 8;
+          const bool vA = g < nv, vB = g + 8 < nv;
+          s[0] = (vA && pA <= lim0) ? s[0] : -INFINITY;
+          s[1] = (vA && pA <= lim1) ? s[1] : -INFINITY;
+          s[2] = (vB && pB <= lim0) ? s[2] : -INFINITY;
+          s[3] = (vB && pB <= lim1) ? s[3] : -INFINITY;
+        }
         float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -561,27 +566,28 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
         }
         const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
         // rows with nothing visible yet keep m = -inf and contribute nothing
-        const float al0 = (n0 == -INFINITY) ? 1.0f : exp2f(m0 - n0);
-        const float al1 = (n1 == -INFINITY) ? 1.0f : exp2f(m1 - n1);
-        const float p0 = (n0 == -INFINITY) ? 0.0f : exp2f(s[0] - n0);
-        const float p1 = (n1 == -INFINITY) ? 0.0f : exp2f(s[1] - n1);
-        const float p2 = (n0 == -INFINITY) ? 0.0f : exp2f(s[2] - n0);
-        const float p3 = (n1 == -INFINITY) ? 0.0f : exp2f(s[3] - n1);
+        const float al0 = (n0 == -INFINITY) ? 1.0f : fast_exp2(m0 - n0);
+        const float al1 = (n1 == -INFINITY) ? 1.0f : fast_exp2(m1 - n1);
+        const float p0 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[0] - n0);
+        const float p1 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[1] - n1);
+        const float p2 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[2] - n0);
+        const float p3 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[3] - n1);
         m0 = n0;
         m1 = n1;
         l0 = l0 * al0 + p0 + p2;
         l1 = l1 * al1 + p1 + p3;
+        if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {  // a running max moved
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc[i][0] *= al0;
-          acc[i][2] *= al0;
-          acc[i][1] *= al1;
-          acc[i][3] *= al1;
+          for (int i = 0; i < 8; ++i) {
+            acc[i][0] *= al0;
+            acc[i][2] *= al0;
+            acc[i][1] *= al1;
+            acc[i][3] *= al1;
+          }
         }
-        // ---------------- P^T to the B-fragment layout via shared memory
+        // ---------------- P^T to the B-fragment layout via shared memory;
         // tokens beyond the request length are zeroed in V (stale cache bytes
         // could be NaN patterns; 0 * NaN would poison the sum)
-        const int nv = mt.n_valid;
         if constexpr (FP8) {
           __half* pb = reinterpret_cast<__half*>(pbuf);  // [8 rows][16 tokens]
           const float vsc = mt.vs[hw];
@@ -592,17 +598,24 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
           __syncwarp();
           const uint2 bq = lds64(pbuf + g * 32 + 8 * t);  // row g, tokens 4t..4t+3
           __syncwarp();
-          uint32_t vmask = 0xFFFFFFFFu;
-          if (nv < P) {
-            const int keep = min(max(nv - 4 * t, 0), 4);  // bytes of tokens 4t.. kept
-            vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
-          }
+          if (full_page) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t wl = lds32(Vt + (16 * i + g) * 16 + 4 * t) & vmask;
-            const uint32_t wh = lds32(Vt + (16 * i + g + 8) * 16 + 4 * t) & vmask;
-            mma16816<true>(acc[i], e4m3x2_to_f16x2(wl), e4m3x2_to_f16x2(wh),
-                           e4m3x2_to_f16x2(wl >> 16), e4m3x2_to_f16x2(wh >> 16), bq.x, bq.y);
+            for (int i = 0; i < 8; ++i) {
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16(lds32(Vt + (16 * i + g) * 16 + 4 * t), a0, a2);
+              e4m3x4_to_f16(lds32(Vt + (16 * i + g + 8) * 16 + 4 * t), a1, a3);
+              mma16816<true>(acc[i], a0, a1, a2, a3, bq.x, bq.y);
+            }
+          } else {
+            const int keep = min(max(nv - 4 * t, 0), 4);  // bytes of tokens 4t.. kept
+            const uint32_t vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16(lds32(Vt + (16 * i + g) * 16 + 4 * t) & vmask, a0, a2);
+              e4m3x4_to_f16(lds32(Vt + (16 * i + g + 8) * 16 + 4 * t) & vmask, a1, a3);
+              mma16816<true>(acc[i], a0, a1, a2, a3, bq.x, bq.y);
+            }
           }
         } else {
           float* pb = reinterpret_cast<float*>(pbuf);  // [8 rows][16 tokens] f32
@@ -622,7 +635,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
           const uint32_t l23 = f32x2_to_bf16x2(f2 - __uint_as_float(h23 << 16),
                                                f3 - __uint_as_float(h23 & 0xFFFF0000u));
           uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;  // tokens (4t,4t+1) and (4t+2,4t+3)
-          if (nv < P) {
+          if (!full_page) {
             const int keep = min(max(nv - 4 * t, 0), 4);
             mlo = keep >= 2 ? 0xFFFFFFFFu : (keep == 1 ? 0x0000FFFFu : 0u);
             mhi = keep >= 4 ? 0xFFFFFFFFu : (keep == 3 ? 0x0000FFFFu : 0u);
