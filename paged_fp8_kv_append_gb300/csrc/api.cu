@@ -36,9 +36,10 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
       return KV_ERR_UNSUPPORTED;
     cfg->kind = d.dtype == KV_DTYPE_E4M3 ? 0 : 1;
     // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
-    // tiles are twice as large) dividing Hkv; ring depth from the ring size
+    // tiles are twice as large) dividing Hkv and the consumer warp count;
+    // ring depth from the ring size
     int hs = cfg->kind == 0 ? 8 : 4;
-    while (d.num_kv_heads % hs != 0) hs >>= 1;
+    while (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % hs != 0) hs >>= 1;
     cfg->Hs = hs;
     const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 0 ? 1 : 2);
     cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;
@@ -46,7 +47,7 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     // A consumer warp serves every (consumers/Hs)-th unit; the ring depth must
     // be a multiple of that stride so each warp sees every phase of the stages
     // it uses (parity waits cannot tell phase n from phase n-2).
-    const int wph = gqa_consumer_warps() / hs;
+    const int wph = gqa_consumer_warps(cfg->kind) / hs;
     cfg->stages -= cfg->stages % wph;
     if (cfg->stages < 2 || cfg->stages < wph) return KV_ERR_UNSUPPORTED;
     const int sms = sm_count();

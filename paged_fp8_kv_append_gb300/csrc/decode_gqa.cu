@@ -211,17 +211,19 @@ __device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
 // group"; Hs = the largest power of two <= 8 that divides Hkv, <= 4 for
 // bf16).  The Hs K tiles of a page are contiguous in the cache, and so are
 // its Hs V tiles, so one unit is two bulk copies of Hs * P * D elements.
-// One CTA per SM: a producer warp and kConsumers consumer warps; consumer w
+// One CTA per SM: a producer warp and CONSUMERS consumer warps; consumer w
 // serves head w % Hs of every (w / Hs)-th unit, so each unit is consumed by
 // exactly Hs warps.  The ring holds kRingBytes of units in flight.
-#ifndef KV_GQA_CONSUMERS
-#define KV_GQA_CONSUMERS 8
+#ifndef KV_GQA_FP8_CONSUMERS
+#define KV_GQA_FP8_CONSUMERS 12
+#endif
+#ifndef KV_GQA_BF16_CONSUMERS
+#define KV_GQA_BF16_CONSUMERS 8
 #endif
 #ifndef KV_GQA_RING_KB
 #define KV_GQA_RING_KB 160
 #endif
 
-constexpr int kConsumers = KV_GQA_CONSUMERS;
 constexpr int kMaxStages = 40;
 
 template <bool FP8>
@@ -231,16 +233,19 @@ struct GqaCfg {
   static constexpr int ES = FP8 ? 1 : 2;            // cache element bytes
   static constexpr int TILE = P * D * ES;           // bytes of one head's K or V tile
   static constexpr int RING = KV_GQA_RING_KB * 1024;
-  static constexpr int THREADS = (kConsumers + 1) * 32;
+  // consumer warps: e4m3 pages carry half the bytes of bf16 ones, so each
+  // byte needs twice the consumer work; measured best at 12 (e4m3) and 8 (bf16)
+  static constexpr int CONSUMERS = FP8 ? KV_GQA_FP8_CONSUMERS : KV_GQA_BF16_CONSUMERS;
+  static constexpr int THREADS = (CONSUMERS + 1) * 32;
   static constexpr int R8 = 8;                      // query rows per kv head (padded)
   static constexpr int PFX_CACHE = 1024;            // pfx entries cached in smem
   static constexpr int PBUF = FP8 ? R8 * P * 2 : R8 * P * 4;  // per-warp P transpose
   // shared memory carve-up (byte offsets)
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_MERGE_O = OFF_RING + RING;                         // [W][R8][D] f32
-  static constexpr int OFF_MERGE_ML = OFF_MERGE_O + kConsumers * R8 * D * 4;  // [W][R8][2] f32
-  static constexpr int OFF_PBUF = OFF_MERGE_ML + kConsumers * R8 * 2 * 4;
-  static constexpr int OFF_META = OFF_PBUF + kConsumers * PBUF;               // [S] StageMeta
+  static constexpr int OFF_MERGE_ML = OFF_MERGE_O + CONSUMERS * R8 * D * 4;  // [W][R8][2] f32
+  static constexpr int OFF_PBUF = OFF_MERGE_ML + CONSUMERS * R8 * 2 * 4;
+  static constexpr int OFF_META = OFF_PBUF + CONSUMERS * PBUF;               // [S] StageMeta
   static constexpr int OFF_BAR = OFF_META + kMaxStages * 80;                  // full, empty
   static constexpr int OFF_PFX = OFF_BAR + 2 * kMaxStages * 8;
   static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;
@@ -281,7 +286,8 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const int Hs = a.Hs, HG = a.HG;              // heads per unit, head groups
   const int S = a.stages;                      // ring stages (<= kMaxStages)
   const int stage_bytes = 2 * Hs * C::TILE;
-  if (S < 2 || S > kMaxStages || S % (kConsumers / Hs) != 0 || stage_bytes * S > C::RING) {
+  if (Hs < 1 || C::CONSUMERS % Hs != 0 || S < 2 || S > kMaxStages ||
+      S % (C::CONSUMERS / Hs) != 0 || stage_bytes * S > C::RING) {
     if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad ring
     return;
   }
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const Cursor start = cursor_at(pfx, B, HG, x_begin);
   const int P = C::P, D = C::D;
 
-  if (warp == kConsumers) {
+  if (warp == C::CONSUMERS) {
     // ======================= producer warp =======================
     // Lane l owns unit x0 + l of each batch of 32 consecutive units.  Page
     // ids (and lengths) are loaded two batches ahead and scales one batch
@@ -441,7 +447,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const int g = lane >> 2, t = lane & 3;
   uint8_t* pbuf = pbuf_all + warp * C::PBUF;
   const int G = a.G, T = a.T, R = a.R;
-  const int WPH = kConsumers / Hs;          // warps per head
+  const int WPH = C::CONSUMERS / Hs;          // warps per head
   const int hw = warp % Hs, lg = warp / Hs;  // head within the group, page lane
   Cursor cur = start;
   long long x = x_begin;
@@ -675,12 +681,12 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
       ml[(2 * t + 1) * 2 + 0] = m1;
       ml[(2 * t + 1) * 2 + 1] = l1;
     }
-    named_bar_sync(1, kConsumers * 32);
+    named_bar_sync(1, C::CONSUMERS * 32);
     {
       // slot of this (CTA, segment) piece; rows (head in group, query row)
       const long long slot = (long long)r * HG + cur.h + blockIdx.x;
       const int tid = threadIdx.x;  // consumer thread index
-      for (int e = tid; e < Hs * C::R8 * D; e += kConsumers * 32) {
+      for (int e = tid; e < Hs * C::R8 * D; e += C::CONSUMERS * 32) {
         const int hh = e / (C::R8 * D), n = (e / D) % C::R8, dd = e % D;
         float M = -INFINITY;
         for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hs + hh) * C::R8 + n) * 2]);
@@ -702,7 +708,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
         }
       }
     }
-    named_bar_sync(1, kConsumers * 32);
+    named_bar_sync(1, C::CONSUMERS * 32);
 
     k_base += npages;
     x = piece_end;
@@ -793,7 +799,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
 
 int gqa_ring_bytes(int kind) { return kind == 0 ? GqaCfg<true>::RING : GqaCfg<false>::RING; }
 int gqa_max_stages() { return kMaxStages; }
-int gqa_consumer_warps() { return kConsumers; }
+int gqa_consumer_warps(int kind) {
+  return kind == 0 ? GqaCfg<true>::CONSUMERS : GqaCfg<false>::CONSUMERS;
+}
 
 int gqa_split_ctas_per_sm(int kind) {
   static int cache[2] = {-1, -1};

@@ -83,7 +83,7 @@ struct DecodeConfig {
 // choice of heads per unit and ring depth).
 int gqa_ring_bytes(int kind);
 int gqa_max_stages();
-int gqa_consumer_warps();
+int gqa_consumer_warps(int kind);
 
 kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig* cfg);
 size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
