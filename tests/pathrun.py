@@ -140,3 +140,157 @@ class Both:
         ref, written = oracle.attn(self.ref, wl.bits_u16(q), self.pt_h, self.sl_h, abort_h,
                                    w.sm_scale, w.num_q_heads, w.q_tokens)
         return out, ref, written
+
+
+class Bookkeeping:
+    """Host twin of a pool's integer state (tags, free list, free head) for
+    oracle.alloc / oracle.verify, without the cache arrays."""
+
+    def __init__(self, num_pages, page_size, tags, free_list):
+        self.num_pages, self.page_size = int(num_pages), int(page_size)
+        self.tags = np.array(tags, dtype=np.uint32)
+        self.free_list = np.array(free_list, dtype=np.int32)
+        self.free_head = np.zeros(1, np.int32)
+
+
+class FullSize:
+    """A full-size workload on the device, with the oracle twinning every
+    request's bookkeeping and, for sampled (request, kv head) pairs, the cache
+    contents and attention output (a one-kv-head oracle pool fed the same rows
+    in the same calls)."""
+
+    def __init__(self, w: wl.Workload, dtype: int, device="cuda", sample=(), heads=(0,)):
+        import paged_fp8_kv_append_gb300 as kv
+
+        self.kv, self.w, self.dtype, self.device = kv, w, dtype, device
+        tags, free = wl.initial_tags(w), wl.free_list(w)
+        self.dev = kv.KVPool(w.num_pages, w.page_size, w.num_kv_heads, w.head_dim_k,
+                             w.head_dim_v, dtype=dtype, layout=w.layout, device=device, tags=tags,
+                             free_list=free)
+        self.bk = Bookkeeping(w.num_pages, w.page_size, tags, free)
+        B, mp = w.B, w.max_pages
+        self.pt_d = torch.full((B, mp), -1, dtype=torch.int32, device=device)
+        self.et_d = torch.zeros((B, mp), dtype=torch.int32, device=device)
+        self.sl_d = torch.zeros(B, dtype=torch.int32, device=device)
+        self.pt_h = np.full((B, mp), -1, np.int32)
+        self.et_h = np.zeros((B, mp), np.uint32)
+        self.sl_h = np.zeros(B, np.int32)
+        # oracle twins: (r, h) -> (pool, page table, exp tags, seq len)
+        self.sample, self.heads = list(sample), list(heads)
+        self.twins = {}
+        for r in self.sample:
+            for h in self.heads:
+                npg = int(-(-(int(w.lens[r]) + w.steps) // w.page_size)) + 2
+                pool = oracle.Pool(npg, w.page_size, 1, w.head_dim_k, w.head_dim_v, dtype=dtype)
+                self.twins[(r, h)] = [pool, np.full((1, npg), -1, np.int32),
+                                      np.zeros((1, npg), np.uint32), np.zeros(1, np.int32)]
+
+    def _append(self, ks, vs, counts, max_new):
+        """One append call: ks/vs lists (per request, device bf16 [n][Hkv][D])."""
+        B = self.w.B
+        counts = np.asarray(counts, np.int64)
+        ind = np.zeros(B + 1, np.int32)
+        ind[1:] = np.cumsum(counts)
+        k = torch.cat([x for x in ks if x is not None and x.shape[0] > 0])
+        v = torch.cat([x for x in vs if x is not None and x.shape[0] > 0])
+        self.dev.append(B, k, v, torch.from_numpy(ind).to(self.device), int(max_new), self.pt_d,
+                        self.et_d, self.sl_d)
+        st, stop = oracle.alloc(self.bk, ind, int(max_new), self.pt_h, self.et_h, self.sl_h)
+        for (r, h), tw in self.twins.items():
+            if counts[r] == 0:
+                continue
+            pool, pt, et, sl = tw
+            kb = wl.bits_u16(ks[r][:, h:h + 1, :])
+            vb = wl.bits_u16(vs[r][:, h:h + 1, :])
+            s2, _ = oracle.append(pool, kb, vb, np.array([0, counts[r]], np.int32), int(counts[r]),
+                                  pt, et, sl)
+            assert s2 == 0
+        return st, stop
+
+    def fill(self, group=4):
+        """Every request's first L_r - 1 tokens, `group` requests per call."""
+        w = self.w
+        for r0 in range(0, w.B, group):
+            counts = np.zeros(w.B, np.int64)
+            ks, vs = [None] * w.B, [None] * w.B
+            for r in range(r0, min(w.B, r0 + group)):
+                counts[r] = int(w.lens[r]) - 1
+                ks[r], vs[r] = wl.kv_rows(w, r, 0, int(counts[r]), device=self.device)
+            st, stop = self._append(ks, vs, counts, int(counts.max()))
+            assert (st, stop) == (0, w.B)
+
+    def step_append(self, s):
+        k, v = wl.step_rows(self.w, s, device=self.device)
+        ks = [k[r:r + 1] for r in range(self.w.B)]
+        vs = [v[r:r + 1] for r in range(self.w.B)]
+        return self._append(ks, vs, np.ones(self.w.B, np.int64), 1)
+
+    def make_stale(self):
+        for r, j in wl.stale_slots(self.w):
+            self.et_h[r, j] = np.uint32(self.et_h[r, j]) - np.uint32(1)
+        self.et_d.copy_(torch.from_numpy(self.et_h.view(np.int32)))
+
+    def assert_bookkeeping(self):
+        d = self.dev
+        assert np.array_equal(d.tags.cpu().numpy().view(np.uint32), self.bk.tags), "tags"
+        assert np.array_equal(self.pt_d.cpu().numpy(), self.pt_h), "page_table"
+        assert np.array_equal(self.et_d.cpu().numpy().view(np.uint32), self.et_h), "exp_tags"
+        assert np.array_equal(self.sl_d.cpu().numpy(), self.sl_h), "seq_lens"
+        assert int(d.ctl[0].item()) == int(self.bk.free_head[0]), "free_head"
+
+    def assert_sampled_cache(self):
+        """Cache bytes and scales of every sampled (request, kv head), by logical page."""
+        P = self.w.page_size
+        for (r, h), (pool, pt, et, sl) in self.twins.items():
+            n = int(-(-int(sl[0]) // P))
+            assert int(sl[0]) == int(self.sl_h[r])
+            pages_d = torch.from_numpy(self.pt_h[r, :n].astype(np.int64)).to(self.device)
+            kc = self.dev.k_cache[pages_d, h].cpu()
+            vc = self.dev.v_cache[pages_d, h].cpu()
+            if self.dtype == 1:
+                kc, vc = kc.view(torch.int16), vc.view(torch.int16)
+            want_k = pool.k_cache[pt[0, :n], 0]
+            want_v = pool.v_cache[pt[0, :n], 0]
+            assert np.array_equal(kc.numpy().view(want_k.dtype), want_k), (r, h, "k")
+            assert np.array_equal(vc.numpy().view(want_v.dtype), want_v), (r, h, "v")
+            if self.dtype == 0:
+                ks = self.dev.k_scale[pages_d, h].cpu().numpy()
+                vs = self.dev.v_scale[pages_d, h].cpu().numpy()
+                assert np.array_equal(ks.view(np.uint32), pool.k_scale[pt[0, :n], 0].view(np.uint32))
+                assert np.array_equal(vs.view(np.uint32), pool.v_scale[pt[0, :n], 0].view(np.uint32))
+
+    def verify(self):
+        B = self.w.B
+        m_d = torch.zeros(B, dtype=torch.uint8, device=self.device)
+        self.dev.verify(B, self.pt_d, self.et_d, self.sl_d, m_d)
+        m_h = oracle.verify(self.bk.num_pages, self.w.page_size, self.bk.tags, self.pt_h,
+                            self.et_h, self.sl_h)
+        return m_d, m_h
+
+    def attn_check(self, q, abort_d, abort_h, sentinel=7.0):
+        """Attention on the device for the whole batch; oracle for the samples."""
+        w, B = self.w, self.w.B
+        out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), sentinel,
+                         dtype=torch.bfloat16, device=self.device)
+        ws = torch.empty(self.dev.workspace_size(B, w.num_q_heads, w.q_tokens), dtype=torch.uint8,
+                         device=self.device)
+        self.dev.attn(B, w.num_q_heads, w.q_tokens, q, self.pt_d, self.sl_d, abort_d, w.sm_scale,
+                      out, ws)
+        got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+        G = w.num_q_heads // w.num_kv_heads
+        qh = q.cpu()
+        checked = 0
+        for (r, h), (pool, pt, et, sl) in self.twins.items():
+            if abort_h is not None and abort_h[r]:
+                assert np.all(got[r] == sentinel), f"aborted request {r} written"
+                continue
+            qs = wl.bits_u16(qh[r:r + 1, :, h * G:(h + 1) * G, :])
+            ref, written = oracle.attn(pool, qs, pt, sl, None, w.sm_scale, G, w.q_tokens)
+            assert written[0] == 1
+            ok, mabs, mrel, _ = close(got[r, :, h * G:(h + 1) * G], ref[0])
+            assert ok, (r, h, mabs, mrel)
+            checked += 1
+        if abort_h is not None:
+            for r in np.nonzero(abort_h)[0]:
+                assert np.all(got[r] == sentinel), f"aborted request {r} written"
+        return checked

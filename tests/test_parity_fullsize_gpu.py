@@ -1,0 +1,71 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times.  Every request's bookkeeping (page tables, expected tags,
+tags, lengths, free head, abort masks) is compared bit-exactly with the
+oracle; cache bytes, scales and attention outputs are compared for sampled
+(request, kv head) pairs, the oracle running a one-kv-head pool fed the same
+rows in the same calls."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from pathrun import FullSize
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_gqa_batch_full_size_decode_steps(dtype):
+    w = wl.gqa_batch(steps=3)
+    rng = np.random.default_rng(1)
+    sample = sorted(rng.choice(w.B, 3, replace=False).tolist()) + [int(np.argmax(w.lens))]
+    fs = FullSize(w, dtype, sample=sample, heads=[0, 5])
+    fs.fill()
+    for s in range(2):
+        st, stop = fs.step_append(s)
+        assert (st, stop) == (0, w.B)
+    torch.cuda.synchronize()
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    m_d, m_h = fs.verify()
+    assert not m_h.any() and np.array_equal(m_d.cpu().numpy(), m_h)
+    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == len(sample) * 2
+    assert fs.dev.error() == 0
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_concurrency_128k_contexts(B):
+    w = wl.concurrency(B)
+    w.steps = 2
+    fs = FullSize(w, 0, sample=[0, B - 1] if B > 1 else [0], heads=[3])
+    fs.fill(group=2)
+    fs.step_append(0)
+    torch.cuda.synchronize()
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    assert fs.attn_check(wl.queries(w, device="cuda"), None, None) >= 1
+    assert fs.dev.error() == 0
+
+
+def test_skewed_stress_steps_with_stale_tags():
+    """256 requests, lognormal contexts up to 256k; every step appends one
+    token per request (pages come off a shuffled free list), then the tag
+    check and attention; the stale requests abort and are left untouched."""
+    w = wl.skewed(steps=4)
+    rng = np.random.default_rng(5)
+    live = [r for r in range(w.B) if r not in w.stale]
+    sample = sorted(rng.choice(live, 6, replace=False).tolist()) + [int(np.argmax(w.lens))] + list(w.stale)
+    fs = FullSize(w, 0, sample=sorted(set(sample)), heads=[1])
+    fs.fill(group=16)
+    fs.make_stale()
+    for s in range(3):
+        st, stop = fs.step_append(s)
+        assert (st, stop) == (0, w.B)
+        m_d, m_h = fs.verify()
+        assert np.array_equal(m_d.cpu().numpy(), m_h)
+        assert sorted(np.nonzero(m_h)[0].tolist()) == sorted(w.stale)
+    torch.cuda.synchronize()
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) >= 6
+    assert fs.dev.error() == 0
