@@ -55,27 +55,34 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
     cfg->grid = sms * per_sm;
     cfg->R8 = 8;
+    cfg->HG = d.num_kv_heads / hs;
+    cfg->unit_tokens = d.page_size;
     return KV_OK;
   }
-  // latent layout
-  if (d.head_dim_k != 576 || d.head_dim_v != 512 || d.page_size != 64 || T * Hq % 128 != 0)
+  // latent layout: query rows (T tokens x Hq heads) in blocks of 64
+  const int rb = latent_row_block();
+  if (d.head_dim_k != 576 || d.head_dim_v != 512 || d.page_size != 64 || (T * Hq) % rb != 0 ||
+      d.dtype != KV_DTYPE_E4M3)
     return KV_ERR_UNSUPPORTED;
   const int sms = sm_count();
   const int per_sm = sms > 0 ? latent_split_ctas_per_sm() : 0;
-  if (sms <= 0 || per_sm <= 0) return KV_ERR_UNSUPPORTED;
+  if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
   cfg->kind = 2;
   cfg->grid = sms * per_sm;
-  cfg->R8 = T * Hq;
+  cfg->R8 = rb;
   cfg->Hs = 1;
+  cfg->HG = T * Hq / rb;
   cfg->stages = 0;
+  cfg->unit_tokens = latent_unit_tokens();
   return KV_OK;
 }
 
 size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
                         void* base, DecodeWs* ws) {
   // one partial slot per (CTA, segment) piece; segments are (request, head
-  // group); each slot holds Hs heads x R8 rows
-  const long long slots = (long long)B * (Hkv / cfg.Hs) + cfg.grid;
+  // group) or (request, row block); each slot holds Hs heads x R8 rows
+  (void)Hkv;
+  const long long slots = (long long)B * cfg.HG + cfg.grid;
   size_t off = 0;
   const size_t o_pfx = off;
   off = align256(off + sizeof(int32_t) * (size_t)(B + 1));
@@ -140,8 +147,9 @@ kv_status decode_prepare(kv_pool* pool, int32_t B, int32_t Hq, int32_t T, const 
   x.grid = cfg.grid;
   x.R8 = cfg.R8;
   x.Hs = cfg.Hs;
-  x.HG = Hkv / cfg.Hs;
+  x.HG = cfg.HG;
   x.stages = cfg.stages;
+  x.unit_tokens = cfg.unit_tokens;
   const size_t need = decode_ws_layout(d, B, Hkv, cfg, workspace, &x.ws);
   if (B > 0 && workspace_bytes < need) return KV_ERR_INVALID_ARG;
   *kind = cfg.kind;

@@ -42,7 +42,8 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// pfx[r] = exclusive prefix of pages over requests that get output, rq_skip,
+// pfx[r] = exclusive prefix of units of work (pages, or half pages for the
+// latent layout) over requests that get output, rq_skip,
 // rq_bad cleared.  A request is skipped (no pages, no output) when aborted or
 // when its length is negative or needs more pages than its page table holds
 // (that also sets KV_ERR_INVALID_ARG).
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
       const bool bad_len = L < 0 || (long long)ceil_div(max(L, 0), P) > a.max_pages;
       if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
       const bool skip = aborted || bad_len;
-      np = skip ? 0 : ceil_div(L, P);
+      np = skip ? 0 : ceil_div(L, a.unit_tokens);
       a.ws.rq_skip[r] = skip ? 1 : 0;
       a.ws.rq_bad[r] = 0;
     }
@@ -127,7 +128,12 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* pfx, int B
     } while (c.r < B && pfx[c.r + 1] == pfx[c.r]);
     if (c.r < B) c.np = pfx[c.r + 1] - pfx[c.r];
   }
-  if (c.r < B) c.seg_start = (long long)groups * pfx[c.r] + (long long)c.h * c.np;
+  if (c.r < B) {
+    c.seg_start = (long long)groups * pfx[c.r] + (long long)c.h * c.np;
+  } else {  // past the last request (cannot happen inside a CTA range): end every loop
+    c.seg_start = (long long)groups * pfx[B];
+    c.np = 1;
+  }
 }
 
 // ------------------------------------------------- tensor-core helpers
@@ -734,7 +740,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
   const long long rh = item / a.R;
   const int r = (int)(rh / Hkv), h = (int)(rh % Hkv);
   const int Hs = a.Hs, HG = a.HG;
-  const int hg = h / Hs, hw = h % Hs;
+  // segment (request, head group | row block) and row inside its partials
+  const bool latent = a.d.layout == KV_LAYOUT_LATENT;
+  const int hg = latent ? n / a.R8 : h / Hs, hw = latent ? 0 : h % Hs;
+  const int nl = latent ? n % a.R8 : n;
   const long long seg = (long long)r * HG + hg;
   if (a.ws.rq_skip[r] || a.ws.rq_bad[r]) return;  // aborted: output left untouched
   const int Dv = a.d.head_dim_v;
@@ -756,7 +765,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     const int R8 = a.R8;
 #pragma unroll 2
     for (int c = 0; c <= c1 - c0; ++c) {
-      const long long rowi = ((slot0 + c) * Hs + hw) * R8 + n;
+      const long long rowi = ((slot0 + c) * Hs + hw) * R8 + nl;
       const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
       float4 o[4];
 #pragma unroll

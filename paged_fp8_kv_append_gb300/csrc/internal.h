@@ -65,18 +65,21 @@ struct DecodeArgs {
   int32_t grid;         // CTAs of the split kernel
   int32_t R8;           // rows per (partial slot, head) (R rounded up)
   int32_t Hs;           // kv heads per unit of work (a head group)
-  int32_t HG;           // head groups per request (Hkv / Hs)
+  int32_t HG;           // segments per request: head groups (GQA) or 64-row blocks (latent)
   int32_t stages;       // ring stages of the split kernel
+  int32_t unit_tokens;  // tokens per unit of work (GQA: a page; latent: half a page)
   DecodeWs ws;
 };
 
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {
-  int kind;    // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3
-  int grid;    // split-kernel CTAs
-  int R8;      // partial rows per (slot, head)
-  int Hs;      // kv heads per unit of work
-  int stages;  // ring stages
+  int kind;         // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3
+  int grid;         // split-kernel CTAs
+  int R8;           // partial rows per (slot, head)
+  int Hs;           // kv heads per unit of work
+  int HG;           // segments per request
+  int stages;       // ring stages
+  int unit_tokens;  // tokens per unit of work
 };
 
 // Ring bytes and stage limit of the GQA split kernel (for the host-side
@@ -98,5 +101,7 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* laun
 // Occupancy-derived CTAs per SM for the split kernels (cached per device).
 int gqa_split_ctas_per_sm(int kind);
 int latent_split_ctas_per_sm();
+int latent_unit_tokens();
+int latent_row_block();
 
 }  // namespace kvfp8
