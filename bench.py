@@ -319,6 +319,100 @@ class Arm:
         return t0.elapsed_time(t1), h2d, d2h
 
 
+# ------------------------------------------------------------ latent verify
+
+def latent_flops(w: wl.Workload, lens: np.ndarray) -> float:
+    """Algorithmic flops of one latent attention call: every query row t of
+    request r sees L_r - T + t + 1 positions, 2*(Dk + Dv) flops each."""
+    T = w.q_tokens
+    vis = sum(int(L) - T + t + 1 for L in lens for t in range(T))
+    return 2.0 * vis * w.num_q_heads * (w.head_dim_k + w.head_dim_v)
+
+
+def latent_bench(steps: int, warmup: int, device, peaks: dict) -> dict:
+    """One decode step of the latent speculative-verify workload (64 requests,
+    lognormal contexts 8k..64k, 128 heads x 4 draft tokens on one 576-wide
+    e4m3 row per token): append the 4 draft rows of every request, tag check,
+    attention (tcgen05 path) + combine."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    w = wl.latent_verify()
+    T, B = w.q_tokens, w.B
+    w.steps = T * (steps + warmup + 1)
+    import math as _m
+
+    need = int((-(-(w.lens.astype(np.int64) + w.steps) // 64)).sum())
+    w.num_pages = int(_m.ceil(need * 1.1)) + 8
+    pool = kv.KVPool(w.num_pages, 64, 1, 576, 512, dtype=0, layout=1, device=device,
+                     tags=wl.initial_tags(w), free_list=wl.free_list(w))
+    mp = w.max_pages
+    pt = torch.full((B, mp), -1, dtype=torch.int32, device=device)
+    et = torch.zeros((B, mp), dtype=torch.int32, device=device)
+    sl = torch.zeros(B, dtype=torch.int32, device=device)
+    lens0 = w.lens.astype(np.int64) - T
+    for r0 in range(0, B, 8):
+        counts = np.zeros(B, np.int64)
+        ks = []
+        for r in range(r0, min(B, r0 + 8)):
+            counts[r] = lens0[r]
+            ks.append(wl.kv_rows(w, r, 0, int(lens0[r]), device=device)[0])
+        ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+        pool.append(B, torch.cat(ks), None, ind.to(device), int(counts.max()), pt, et, sl)
+        del ks
+    mask = torch.zeros(B, dtype=torch.uint8, device=device)
+    out = torch.zeros((B, T, w.num_q_heads, 512), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(pool.workspace_size(B, w.num_q_heads, T), dtype=torch.uint8, device=device)
+    ind_t = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device=device)
+    g = torch.Generator(device=device)
+    drafts, qs = [], []
+    for s in range(steps + warmup):
+        g.manual_seed(w.seed * 17 + s)
+        drafts.append(torch.randn((B * T, 576), generator=g, device=device).to(torch.bfloat16))
+        qs.append(wl.queries(w, device=device, step=s))
+    lens = w.lens.astype(np.int64).copy()
+
+    def step(s, ev=None):
+        pool.append(B, drafts[s], None, ind_t, T, pt, et, sl)
+        pool.verify(B, pt, et, sl, mask)
+        if ev is not None:
+            ev[0].record()
+        pool.attn(B, w.num_q_heads, T, qs[s], pt, sl, mask, w.sm_scale, out, ws)
+        if ev is not None:
+            ev[1].record()
+
+    for s in range(warmup):
+        step(s)
+    torch.cuda.synchronize()
+    lens += T * warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    flops = []
+    for i in range(steps):
+        step(warmup + i, evs[i])
+        flops.append(latent_flops(w, lens + T * i))
+    t1.record()
+    torch.cuda.synchronize()
+    if pool.error() != 0:
+        raise RuntimeError(f"latent: device error {kv.kv_status_string(pool.error())}")
+    total = t0.elapsed_time(t1)
+    attn_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    tf = float(np.mean([f / (t * 1e-3) / 1e12 for f, t in zip(flops, attn_ms)]))
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    kv_bytes = float((lens + T * steps // 2).sum() * 576 + B * T * 128 * (576 + 512) * 2)
+    res = {"workload": "latent_verify: 64 requests, lognormal contexts (median 16k) in "
+                       "[8k, 64k], 128 heads x 4 draft tokens, one 576-wide e4m3 row per token "
+                       "(V = first 512), page 64",
+           "value": steps * B * T / (total / 1e3), "unit": "tokens/s",
+           "ms_per_step": total / steps, "attn_ms": float(attn_ms.mean()),
+           "attn_tflops": tf, "tensor_peak_tflops": peak, "tensor_frac": tf / peak,
+           "peak_source": "measured bf16 dense (f16 operands run at the same rate)",
+           "attn_gbs": kv_bytes / (attn_ms.mean() * 1e6)}
+    del pool
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w: wl.Workload, budget_s: float, device, start_req: int = 0,
@@ -366,6 +460,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-latent", action="store_true")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests of the GQA batch workload to use (32 = the full workload; "
                          "fewer only for small profiling captures)")
@@ -456,6 +551,11 @@ def main():
             "split_gbs": float(np.mean([b / (t * 1e6) for b, t in zip(b16, per16[:, 2])])),
         }
 
+    # ---- latent speculative-verify workload (tcgen05 path)
+    latent = None
+    if not args.no_latent:
+        latent = latent_bench(args.steps, args.warmup, device, peaks)
+
     # ---- CPU oracle baseline (rank 0, bounded sample)
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
@@ -491,6 +591,7 @@ def main():
                      "kernel": "paged_decode_attn_split (plan + gqa_split_kernel<e4m3>)",
                      "peak_source": peak_src},
         "bf16_kv": bf16,
+        "latent_verify": latent,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},

@@ -16,14 +16,15 @@
 // piece leaves a partial (o, running max, sum) for the combine kernel.
 //
 // Per unit:
-//   producer warp   bulk-copies the unit's 32 x 576 e4m3 bytes (one copy)
-//                   into a staging ring;
-//   converter warps convert them exactly to f16 into a 128B-swizzled K-major
-//                   tile (the same tile is the MN-major V^T operand);
+//   converter warps load the unit's 32 x 576 e4m3 bytes (the next unit's
+//                   loads in flight while this one converts) and convert them
+//                   exactly to f16 into one of three 128B-swizzled K-major
+//                   tiles (the same tile is the MN-major V^T operand);
 //   MMA warp        S = Q K^T   (tcgen05, M = 64 rows, N = 32 tokens, K = 576,
-//                   f16 x f16 -> f32 in tensor memory), later
-//                   O^T += V^T P^T (M = 128 dims x 4 blocks, N = 64 rows,
-//                   K = 32 tokens) accumulating in tensor memory;
+//                   f16 x f16 -> f32 into one of four tensor-memory buffers),
+//                   and two units later O^T += V^T P^T (M = 128 dims x 4
+//                   blocks, N = 64 rows, K = 32 tokens) accumulating in tensor
+//                   memory, so the tensor pipe never waits for the softmax;
 //   softmax warps   read S from tensor memory (one row per thread), apply the
 //                   page scale, the causal mask and the online softmax with a
 //                   lazily updated reference max (the output is rescaled only
@@ -42,35 +43,37 @@ constexpr int kUT = 32;        // tokens per unit
 constexpr int kPage = 64;      // tokens per page
 constexpr int kDK = 576, kDV = 512, kNKB = kDK / 64;  // K blocks of 64 dims
 constexpr int kRB = 64;        // query rows per segment
-constexpr int kNSTG = 3;       // e4m3 staging ring
+constexpr int kNKV = 3;        // f16 KV tiles (converted units)
+constexpr int kNS = 4;         // S buffers in tensor memory
+constexpr int kLag = 2;        // PV(u) is issued right after S(u + kLag)
 constexpr int kUnitBytes = kUT * kDK;  // 18432
 
-// warps: 0-3 softmax (tensor-memory lane quarters 0-3), 4-7 converters,
-// 8 producer, 9 MMA issuer
-constexpr int kThreads = 320;
+// warps: 0-3 softmax (tensor-memory lane quarters 0-3), 4-7 converters
+// (global e4m3 -> swizzled f16 tiles), 8 MMA issuer
+constexpr int kThreads = 288;
 constexpr int kSoftmaxWarps = 4, kConvWarps = 4;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kMmaWarp = 8;
 
 // shared memory (bytes); tiles 1024-byte aligned for the 128B swizzle
 constexpr int OFF_Q = 0;                                   // 9 x [64 rows][128 B]
-constexpr int OFF_KV = OFF_Q + kNKB * kRB * 128;           // 2 x 9 x [32 tokens][128 B]
+constexpr int OFF_KV = OFF_Q + kNKB * kRB * 128;           // 3 x 9 x [32 tokens][128 B]
 constexpr int KV_BYTES = kNKB * kUT * 128;                 // 36864
-constexpr int OFF_STG = OFF_KV + 2 * KV_BYTES;             // 3 x 18432
-constexpr int OFF_P = OFF_STG + kNSTG * kUnitBytes;        // 2 x [64 rows][128 B]
+constexpr int OFF_P = OFF_KV + kNKV * KV_BYTES;            // 2 x [64 rows][128 B]
 constexpr int P_BYTES = kRB * 128;
-constexpr int OFF_ALPHA = OFF_P + 2 * P_BYTES;             // 64 floats
-constexpr int OFF_META = OFF_ALPHA + kRB * 4;              // staging meta [3] + unit meta [2]
-constexpr int OFF_BAR = OFF_META + (kNSTG + 2) * 16;
-constexpr int NBAR = 2 * kNSTG + 2 + 2 + 2 + 2 + 2 + 4;
+constexpr int OFF_ALPHA = OFF_P + 2 * P_BYTES;             // 2 x 64 floats
+constexpr int OFF_FLAG = OFF_ALPHA + 2 * kRB * 4;          // 2 ints (+pad)
+constexpr int OFF_META = OFF_FLAG + 16;                    // unit meta [3]
+constexpr int OFF_BAR = OFF_META + kNKV * 16;
+constexpr int NBAR = 2 * kNKV + 2 * kNS + 2 + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_MISC + 64;
-static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && OFF_STG % 16 == 0, "alignment");
+static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks x 64 columns
-constexpr uint32_t kTmemS = 256;   // S: 2 buffers x 32 columns
+constexpr uint32_t kTmemS = 256;   // S: 4 buffers x 32 columns
 
 struct UnitMeta {
   int n_valid;  // valid tokens of the unit (0: skip)
@@ -225,26 +228,23 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_s = smem + OFF_Q;
   uint8_t* kv_s = smem + OFF_KV;
-  uint8_t* stg_s = smem + OFF_STG;
   uint8_t* p_s = smem + OFF_P;
-  float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
-  UnitMeta* stg_meta = reinterpret_cast<UnitMeta*>(smem + OFF_META);
-  UnitMeta* kv_meta = stg_meta + kNSTG;
+  float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);    // [2][64]
+  volatile int* flag_s = reinterpret_cast<volatile int*>(smem + OFF_FLAG);  // [2]
+  UnitMeta* kv_meta = reinterpret_cast<UnitMeta*>(smem + OFF_META);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* stg_full = bars;                    // [3] producer (+tx)
-  uint64_t* stg_empty = bars + kNSTG;           // [3] converters
-  uint64_t* kv_ready = bars + 2 * kNSTG;        // [2] converters
-  uint64_t* pv_done = kv_ready + 2;             // [2] MMA commit (frees KV and P buffers)
-  uint64_t* s_full = pv_done + 2;               // [2] MMA commit
-  uint64_t* s_free = s_full + 2;                // [2] softmax
-  uint64_t* p_ready = s_free + 2;               // [2] softmax
-  uint64_t* q_ready = p_ready + 2;              // converters
-  uint64_t* q_free = q_ready + 1;               // MMA commit
+  uint64_t* kv_ready = bars;                    // [3] converters
+  uint64_t* kv_free = kv_ready + kNKV;          // [3] MMA commit after PV
+  uint64_t* s_full = kv_free + kNKV;            // [4] MMA commit after S
+  uint64_t* s_free = s_full + kNS;              // [4] softmax
+  uint64_t* p_ready = s_free + kNS;             // [2] softmax
+  uint64_t* p_free = p_ready + 2;               // [2] MMA commit after PV
+  uint64_t* q_ready = p_free + 2;               // converters
+  uint64_t* q_free = q_ready + 1;               // MMA commit after a piece's last S
   uint64_t* epi_done = q_free + 1;              // softmax
   uint64_t* drain = epi_done + 1;               // MMA commit at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  volatile int* rescale_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, NRB = a.HG;  // row blocks per request
@@ -263,23 +263,24 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 32) {
-    for (int i = 0; i < kNSTG; ++i) {
-      mbar_init(&stg_full[i], 1);
-      mbar_init(&stg_empty[i], kConvWarps);
-    }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNKV; ++i) {
       mbar_init(&kv_ready[i], kConvWarps);
-      mbar_init(&pv_done[i], 1);
+      mbar_init(&kv_free[i], 1);
+    }
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], kSoftmaxWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_ready[i], kSoftmaxWarps);
+      mbar_init(&p_free[i], 1);
+      flag_s[i] = -1;
     }
     mbar_init(q_ready, kConvWarps);
     mbar_init(q_free, 1);
     mbar_init(epi_done, kSoftmaxWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
-    *rescale_flag = 0;
     fence_mbar_init();
   }
   tc_fence_before();
@@ -290,61 +291,38 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
   const Seg start = seg_at(pfx, B, NRB, x_begin);
   const uint8_t* cache = static_cast<const uint8_t*>(a.d.k_cache);
 
-  if (warp == kProducerWarp) {
-    // ============================ producer ============================
-    if (lane == 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      Seg s = start;
-      long long x = x_begin, u = 0;
-      bool go = true;
-      while (x < x_end && go) {
-        const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
-        const int L = a.seq_lens[s.r];
-        const int32_t* pt = a.page_table + (long long)s.r * a.max_pages;
-        for (long long xu = x; xu < piece_end; ++xu, ++u) {
-          const int j = (int)(xu - s.start);  // unit within the request
-          const int stage = (int)(u % kNSTG);
-          if (u >= kNSTG &&
-              !mbar_wait(&stg_empty[stage], (uint32_t)(((u / kNSTG) - 1) & 1), abort_flag, ctl,
-                         wait_info(warp, 1, stage))) {
-            go = false;
-            break;
-          }
-          const int p = pt[j >> 1];
-          const bool ok = p >= 0 && p < a.d.num_pages;
-          UnitMeta m;
-          m.n_valid = ok ? min(kUT, L - j * kUT) : 0;
-          m.pos0 = j * kUT;
-          m.scale = ok ? a.d.k_scale[p] : 1.0f;
-          m.unit = (int)u;
-          stg_meta[stage] = m;
-          if (ok) {
-            mbar_arrive_expect_tx(&stg_full[stage], kUnitBytes);
-            bulk_g2s(stg_s + stage * kUnitBytes,
-                     cache + (long long)p * kPage * kDK + (long long)(j & 1) * kUnitBytes,
-                     kUnitBytes, &stg_full[stage], policy);
-          } else {
-            a.ws.rq_bad[s.r] = 1;
-            set_error(ctl, KV_ERR_BAD_PAGE_ID);
-            mbar_arrive(&stg_full[stage]);
-          }
-        }
-        x = piece_end;
-        if (x == seg_end) seg_next(s, pfx, B, NRB);
-      }
-      // on abort, let copies already issued land before shared memory goes away
-      if (*abort_flag) {
-        for (long long q = max(0ll, u - kNSTG); q < u; ++q) {
-          const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&stg_full[q % kNSTG], (uint32_t)((q / kNSTG) & 1)) &&
-                 global_ns() - t0 < 100000000ull) {
-          }
-        }
-      }
-    }
-  } else if (warp >= kSoftmaxWarps && warp < kSoftmaxWarps + kConvWarps) {
+  if (warp >= kSoftmaxWarps && warp < kSoftmaxWarps + kConvWarps) {
     // ============================ converters ============================
-    const int ct = threadIdx.x - kSoftmaxWarps * 32;  // 0..127
+    // thread ct handles 16-byte pieces g = ct + 128 i (i < 9) of a unit's
+    // 32 x 576 e4m3 bytes: token g / 36, dims 16 (g % 36) .. +15
+    const int ct = threadIdx.x - kSoftmaxWarps * 32;
+    const int maxp = a.max_pages;
+    struct Pre {
+      uint4 d[9];
+      UnitMeta m;
+    };
+    auto fetch = [&](const Seg& sg, long long xu, long long uu, Pre& pr) {
+      const int j = (int)(xu - sg.start);
+      const int p = a.page_table[(long long)sg.r * maxp + (j >> 1)];
+      const bool ok = p >= 0 && p < a.d.num_pages;
+      const int L = a.seq_lens[sg.r];
+      pr.m.n_valid = ok ? min(kUT, L - j * kUT) : 0;
+      pr.m.pos0 = j * kUT;
+      pr.m.scale = ok ? a.d.k_scale[p] : 1.0f;
+      pr.m.unit = (int)uu;
+      if (!ok && ct == 0) {
+        a.ws.rq_bad[sg.r] = 1;
+        set_error(ctl, KV_ERR_BAD_PAGE_ID);
+      }
+      const uint8_t* src = cache + (long long)(ok ? p : 0) * kPage * kDK + (long long)(j & 1) * kUnitBytes;
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const int g = ct + 128 * i, t = g / 36;
+        pr.d[i] = (ok && t < pr.m.n_valid)
+                      ? __ldg(reinterpret_cast<const uint4*>(src + t * kDK + (g % 36) * 16))
+                      : make_uint4(0, 0, 0, 0);
+      }
+    };
     Seg s = start;
     long long x = x_begin, u = 0;
     int piece = 0;
@@ -358,7 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         break;
       }
       {
-        // row n -> (token t, head hq); 72 chunks of 8 dims per row
         const uint16_t* qbase = a.q + ((long long)s.r * a.T * a.Hq + (long long)s.rb * kRB) * kDK;
         for (int c = ct; c < kRB * (kDK / 8); c += kConvWarps * 32) {
           const int n = c / (kDK / 8), ck = c % (kDK / 8);
@@ -374,51 +351,35 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
       }
-      // ---- units
-      for (long long xu = x; xu < piece_end && go; ++xu, ++u) {
-        const int stage = (int)(u % kNSTG), kb = (int)(u & 1);
-        if (!mbar_wait(&stg_full[stage], (uint32_t)((u / kNSTG) & 1), abort_flag, ctl,
-                       wait_info(warp, 0, stage))) {
+      // ---- units, the next one's loads in flight while this one converts
+      Pre cur, nxt;
+      fetch(s, x, u, cur);
+      for (long long xu = x; xu < piece_end; ++xu, ++u) {
+        if (xu + 1 < piece_end) fetch(s, xu + 1, u + 1, nxt);
+        const int kb = (int)(u % kNKV);
+        if (u >= kNKV && !mbar_wait(&kv_free[kb], (uint32_t)(((u / kNKV) - 1) & 1), abort_flag,
+                                    ctl, wait_info(warp, 1, 32 + kb))) {
           go = false;
           break;
         }
-        if (u >= 2 && !mbar_wait(&pv_done[kb], (uint32_t)(((u >> 1) - 1) & 1), abort_flag, ctl,
-                                 wait_info(warp, 1, 32 + kb))) {
-          go = false;
-          break;
-        }
-        const UnitMeta m = stg_meta[stage];
-        const bool fresh = m.unit == (int)u;
-        if (!fresh && ct == 0) {
-          set_error(ctl, KV_ERR_INTERNAL);
-          *abort_flag = 1;
-        }
-        const int nv = fresh ? m.n_valid : 0;
-        const uint8_t* src = stg_s + stage * kUnitBytes;
         uint8_t* dst = kv_s + kb * KV_BYTES;
-        // 9 K blocks x 32 tokens x 8 chunks of 8 dims
-        for (int c = ct; c < kNKB * kUT * 8; c += kConvWarps * 32) {
-          const int blk = c >> 8, rem = c & 255, t = rem >> 3, ch = rem & 7;
-          uint4 o = make_uint4(0, 0, 0, 0);  // tokens past the length read as zero
-          if (t < nv) {
-            const uint2 w = *reinterpret_cast<const uint2*>(src + t * kDK + blk * 64 + ch * 8);
-            e4m3x4_to_f16(w.x, o.x, o.y);
-            e4m3x4_to_f16(w.y, o.z, o.w);
-          }
-          *reinterpret_cast<uint4*>(dst + blk * (kUT * 128) + swz(t, ch)) = o;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+          const int g = ct + 128 * i, t = g / 36, c16 = g % 36;
+          uint4 lo, hi;
+          e4m3x4_to_f16(cur.d[i].x, lo.x, lo.y);
+          e4m3x4_to_f16(cur.d[i].y, lo.z, lo.w);
+          e4m3x4_to_f16(cur.d[i].z, hi.x, hi.y);
+          e4m3x4_to_f16(cur.d[i].w, hi.z, hi.w);
+          uint8_t* blk = dst + (c16 >> 2) * (kUT * 128);
+          *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2)) = lo;
+          *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2 + 1)) = hi;
         }
-        if (ct == 0) {
-          UnitMeta km = m;
-          km.n_valid = nv;
-          km.unit = (int)u;
-          kv_meta[kb] = km;
-        }
+        if (ct == 0) kv_meta[kb] = cur.m;
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&kv_ready[kb]);
-          mbar_arrive(&stg_empty[stage]);
-        }
+        if (lane == 0) mbar_arrive(&kv_ready[kb]);
+        cur = nxt;
       }
       ++piece;
       x = piece_end;
@@ -431,78 +392,69 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     int piece = 0;
     bool go = true;
     const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s), p_base = smem_u32(p_s);
-    auto issue_pv = [&](long long uu, bool first) -> bool {
-      const int kb = (int)(uu & 1);
-      if (!mbar_wait(&p_ready[kb], (uint32_t)((uu >> 1) & 1), abort_flag, ctl,
-                     wait_info(warp, 0, 48 + kb)))
-        return false;
-      tc_fence_after();
-      if (lane == 0) {
-        for (int db = 0; db < kDV / 128; ++db) {
-          for (int st = 0; st < kUT / 16; ++st) {
-            // V^T: dims 128db.. (two 64-dim blocks, LBO apart), tokens 16st..
-            const uint64_t ad = sw128_desc(kv_base + kb * KV_BYTES + (2 * db) * (kUT * 128) +
-                                               st * 2048,
-                                           kUT * 128, 1024);
-            const uint64_t bd = sw128_desc(p_base + kb * P_BYTES + st * 32, 16, 1024);
-            mma_f16(tmem + kTmemO + 64 * db, ad, bd, kIdescPV, !(first && st == 0));
-          }
-        }
-        mma_commit(&pv_done[kb]);
-      }
-      __syncwarp();
-      return true;
-    };
     while (x < x_end && go) {
       const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
-      if (piece > 0 && !mbar_wait(epi_done, (uint32_t)((piece - 1) & 1), abort_flag, ctl,
-                                  wait_info(warp, 1, 61))) {
-        go = false;
-        break;
-      }
+      const long long u0 = u, n = piece_end - x;
       if (!mbar_wait(q_ready, (uint32_t)(piece & 1), abort_flag, ctl, wait_info(warp, 0, 62))) {
         go = false;
         break;
       }
-      tc_fence_after();
-      long long u0 = u;
-      for (long long xu = x; xu < piece_end; ++xu, ++u) {
-        const int kb = (int)(u & 1);
-        if (!mbar_wait(&kv_ready[kb], (uint32_t)((u >> 1) & 1), abort_flag, ctl,
-                       wait_info(warp, 0, 40 + kb))) {
-          go = false;
-          break;
-        }
-        if (u >= 2 && !mbar_wait(&s_free[kb], (uint32_t)(((u >> 1) - 1) & 1), abort_flag, ctl,
-                                 wait_info(warp, 1, 44 + kb))) {
-          go = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          for (int st = 0; st < kDK / 16; ++st) {
-            const uint64_t ad =
-                sw128_desc(q_base + (st >> 2) * (kRB * 128) + (st & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                sw128_desc(kv_base + kb * KV_BYTES + (st >> 2) * (kUT * 128) + (st & 3) * 32, 16,
-                           1024);
-            mma_f16(tmem + kTmemS + 32 * kb, ad, bd, kIdescS, st > 0);
+      for (long long i = 0; i < n + kLag && go; ++i) {
+        if (i < n) {  // ---- S(u0 + i) = Q K^T into S buffer (u0+i) % 4
+          const long long uu = u0 + i;
+          const int kb = (int)(uu % kNKV), sb = (int)(uu % kNS);
+          go = mbar_wait(&kv_ready[kb], (uint32_t)((uu / kNKV) & 1), abort_flag, ctl,
+                         wait_info(warp, 0, 40 + kb));
+          go = go && (uu < kNS || mbar_wait(&s_free[sb], (uint32_t)(((uu / kNS) - 1) & 1),
+                                            abort_flag, ctl, wait_info(warp, 1, 44 + sb)));
+          go = __all_sync(0xffffffffu, go);
+          if (!go) break;
+          tc_fence_after();
+          if (lane == 0) {
+            for (int st = 0; st < kDK / 16; ++st) {
+              const uint64_t ad =
+                  sw128_desc(q_base + (st >> 2) * (kRB * 128) + (st & 3) * 32, 16, 1024);
+              const uint64_t bd = sw128_desc(
+                  kv_base + kb * KV_BYTES + (st >> 2) * (kUT * 128) + (st & 3) * 32, 16, 1024);
+              mma_f16(tmem + kTmemS + 32 * sb, ad, bd, kIdescS, st > 0);
+            }
+            mma_commit(&s_full[sb]);
+            if (i == n - 1) mma_commit(q_free);  // every S of this piece is issued
           }
-          mma_commit(&s_full[kb]);
+          __syncwarp();
         }
-        __syncwarp();
-        if (u > u0 && !issue_pv(u - 1, u - 1 == u0)) {
-          go = false;
-          break;
+        if (i >= kLag) {  // ---- PV(u0 + i - kLag): O^T += V^T P^T
+          const long long v = u0 + i - kLag;
+          const int kb = (int)(v % kNKV), pb = (int)(v & 1);
+          // the first PV of a piece overwrites O: the previous piece's
+          // epilogue must have read it (its S products already ran ahead)
+          if (v == u0 && piece > 0) {
+            go = __all_sync(0xffffffffu, mbar_wait(epi_done, (uint32_t)((piece - 1) & 1),
+                                                   abort_flag, ctl, wait_info(warp, 1, 61)));
+            if (!go) break;
+          }
+          go = __all_sync(0xffffffffu, mbar_wait(&p_ready[pb], (uint32_t)((v >> 1) & 1),
+                                                 abort_flag, ctl, wait_info(warp, 0, 48 + pb)));
+          if (!go) break;
+          tc_fence_after();
+          if (lane == 0) {
+            for (int db = 0; db < kDV / 128; ++db) {
+              for (int st = 0; st < kUT / 16; ++st) {
+                // V^T: dims 128db.. (two 64-dim blocks, LBO apart), tokens 16st..
+                const uint64_t ad = sw128_desc(kv_base + kb * KV_BYTES +
+                                                   (2 * db) * (kUT * 128) + st * 2048,
+                                               kUT * 128, 1024);
+                const uint64_t bd = sw128_desc(p_base + pb * P_BYTES + st * 32, 16, 1024);
+                mma_f16(tmem + kTmemO + 64 * db, ad, bd, kIdescPV, !(v == u0 && st == 0));
+              }
+            }
+            mma_commit(&kv_free[kb]);
+            mma_commit(&p_free[pb]);
+          }
+          __syncwarp();
         }
       }
-      if (!go) break;
-      if (lane == 0) mma_commit(q_free);  // every S of this piece has been issued
-      __syncwarp();
-      if (u > u0 && !issue_pv(u - 1, u - 1 == u0)) {
-        go = false;
-        break;
-      }
+      u = u0 + n;
       ++piece;
       x = piece_end;
       if (x == seg_end) seg_next(s, pfx, B, NRB);
@@ -516,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSoftmaxWarps) {
     // ============================ softmax (warps 0-3) ============================
     const int q4 = warp;                 // tensor-memory lane quarter
     const bool owner = lane < 16;        // S rows live in lanes 0-15 of each quarter
@@ -525,7 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     const float ssl = a.sm_scale_log2;
     Seg s = start;
     long long x = x_begin, u = 0;
-    int piece = 0;
     bool go = true;
     while (x < x_end) {
       const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
@@ -538,32 +489,31 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       // every softmax warp runs every unit (and every named barrier), even
       // after a wait gave up, so the barrier sequence never diverges
       for (long long xu = x; xu < piece_end; ++xu, ++u) {
-        const int kb = (int)(u & 1);
-        go = go && mbar_wait(&s_full[kb], (uint32_t)((u >> 1) & 1), abort_flag, ctl,
-                             wait_info(warp, 0, 52 + kb));
-        go = go && mbar_wait(&kv_ready[kb], (uint32_t)((u >> 1) & 1), abort_flag, ctl,
+        const int sb = (int)(u % kNS), kb = (int)(u % kNKV), pb = (int)(u & 1);
+        go = go && mbar_wait(&s_full[sb], (uint32_t)((u / kNS) & 1), abort_flag, ctl,
+                             wait_info(warp, 0, 52 + sb));
+        go = go && mbar_wait(&kv_ready[kb], (uint32_t)((u / kNKV) & 1), abort_flag, ctl,
                              wait_info(warp, 0, 40 + kb));
         go = __all_sync(0xffffffffu, go);  // tensor-memory loads are warp-collective
         float v[32];
         if (go) {
           tc_fence_after();
-          tmem_ld32(tmem + kTmemS + 32 * kb + lane_off, v);
+          tmem_ld32(tmem + kTmemS + 32 * sb + lane_off, v);
           tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[kb]);
+        if (lane == 0) mbar_arrive(&s_free[sb]);
         const UnitMeta m = kv_meta[kb];
         if (go && m.unit != (int)u) {
           if (lane == 0) set_error(ctl, KV_ERR_INTERNAL);
           *abort_flag = 1;
           go = false;
         }
-        // P buffer kb is free once PV(u-2) has completed
-        go = go && (u < 2 || mbar_wait(&pv_done[kb], (uint32_t)(((u >> 1) - 1) & 1), abort_flag,
-                                       ctl, wait_info(warp, 1, 56 + kb)));
+        // P buffer pb is free once PV(u-2) has completed
+        go = go && (u < 2 || mbar_wait(&p_free[pb], (uint32_t)(((u >> 1) - 1) & 1), abort_flag,
+                                       ctl, wait_info(warp, 1, 56 + pb)));
         go = __all_sync(0xffffffffu, go);
         float alpha = 1.0f;
-        uint32_t pk[16];
         if (owner && go) {
           const float sc = m.scale * ssl;
           float mx = -INFINITY;
@@ -582,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
           }
           float sum = 0.0f;
           const float vs = m.scale;
+          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const float p0 = (v[i] == -INFINITY) ? 0.0f : ex2(v[i] - m_ref);
@@ -591,51 +542,44 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
           }
           l += sum;
           // P row n: tokens 0..31 = chunks 0..3 of a 128B-swizzled row
-          uint8_t* prow = p_s + kb * P_BYTES;
+          uint8_t* prow = p_s + pb * P_BYTES;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(prow + swz(n, c)) =
                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          if (alpha != 1.0f) *rescale_flag = 1;
+          if (alpha != 1.0f) flag_s[pb] = (int)u;  // unit number: never stale
         }
-        if (owner) alpha_s[n] = alpha;
+        if (owner) alpha_s[pb * kRB + n] = alpha;
         fence_async_smem();
         named_bar_sync(2, kSoftmaxWarps * 32);
-        const bool rescale = *rescale_flag != 0;
-        named_bar_sync(2, kSoftmaxWarps * 32);
-        if (rescale) {
+        if (flag_s[pb] == (int)u && u > u0) {
           // O^T columns are query rows: column n *= alpha[n], after PV(u-1)
-          if (u > u0) {
-            const long long pu = u - 1;
-            go = go && mbar_wait(&pv_done[pu & 1], (uint32_t)((pu >> 1) & 1), abort_flag, ctl,
-                                 wait_info(warp, 1, 58));
-            go = __all_sync(0xffffffffu, go);
-            if (go) {
-              tc_fence_after();
-              for (int db = 0; db < kDV / 128; ++db) {
-                for (int half = 0; half < 2; ++half) {
-                  float o[32];
-                  const uint32_t ta = tmem + kTmemO + 64 * db + 32 * half + lane_off;
-                  tmem_ld32(ta, o);
+          const long long pu = u - 1;
+          go = go && mbar_wait(&p_free[pu & 1], (uint32_t)((pu >> 1) & 1), abort_flag, ctl,
+                               wait_info(warp, 1, 58));
+          go = __all_sync(0xffffffffu, go);
+          if (go) {
+            tc_fence_after();
+            for (int db = 0; db < kDV / 128; ++db) {
+              for (int half = 0; half < 2; ++half) {
+                float o[32];
+                const uint32_t ta = tmem + kTmemO + 64 * db + 32 * half + lane_off;
+                tmem_ld32(ta, o);
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) o[i] *= alpha_s[32 * half + i];
-                  tmem_st32(ta, o);
-                }
+                for (int i = 0; i < 32; ++i) o[i] *= alpha_s[pb * kRB + 32 * half + i];
+                tmem_st32(ta, o);
               }
             }
           }
-          named_bar_sync(2, kSoftmaxWarps * 32);
-          if (threadIdx.x == 0) *rescale_flag = 0;
-          named_bar_sync(2, kSoftmaxWarps * 32);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_ready[kb]);
+        if (lane == 0) mbar_arrive(&p_ready[pb]);
       }
       // ---- epilogue: partial (o, m, l) of this piece
       if (u > u0) {
         const long long last = u - 1;
-        go = go && mbar_wait(&pv_done[last & 1], (uint32_t)((last >> 1) & 1), abort_flag, ctl,
+        go = go && mbar_wait(&p_free[last & 1], (uint32_t)((last >> 1) & 1), abort_flag, ctl,
                              wait_info(warp, 0, 59));
       }
       go = __all_sync(0xffffffffu, go);
@@ -648,10 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
           float o[32];
           tmem_ld32(tmem + kTmemO + 64 * db + 32 * half + lane_off, o);
           const int dv = 128 * db + 32 * q4 + lane;
-          for (int i = 0; i < 32; ++i) {
-            const long long row = slot * kRB + 32 * half + i;
-            a.ws.o_part[row * kDV + dv] = (u > u0) ? o[i] : 0.0f;
-          }
+          for (int i = 0; i < 32; ++i)
+            a.ws.o_part[(slot * kRB + 32 * half + i) * kDV + dv] = o[i];
         }
       }
       if (owner && go) {
@@ -661,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(epi_done);
-      ++piece;
       x = piece_end;
       if (x == seg_end) seg_next(s, pfx, B, NRB);
     }
