@@ -28,8 +28,8 @@
 // with mma.sync m16n8k16.  At 8 query rows per kv head the work is 16 flop per
 // cache byte, beyond what the fp32 CUDA cores sustain at HBM speed, so the
 // tensor pipe carries the dot products and the CUDA cores only convert and
-// run the softmax.  e4m3 codes convert exactly to f16; the per-page scales are
-// applied to the scores (K) and folded into P (V).
+// run the softmax.  e4m3 codes convert exactly to f16; the per-page K scale
+// multiplies the scores and the V scale enters P as an exponent bias.
 #include <float.h>
 
 #include "common.cuh"
@@ -576,18 +576,26 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
         }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        // e4m3: the page's V scale enters the weights as a bias log2(v_scale)
+        // on the exponent and the running max m tracks max(score + bias), so
+        // the f16 weights P = 2^(s + bias - m) stay <= 1 and a small scale
+        // cannot push them into f16's subnormal range; the row sum l takes
+        // the bias back out (bf16 KV has no scale: bias 0)
+        const float bias = FP8 ? __log2f(mt.vs[hw]) : 0.0f;
+        const float unbias = FP8 ? fast_exp2(-bias) : 1.0f;
+        const float n0 = fmaxf(m0, mx0 + bias), n1 = fmaxf(m1, mx1 + bias);
         // rows with nothing visible yet keep m = -inf and contribute nothing
         const float al0 = (n0 == -INFINITY) ? 1.0f : fast_exp2(m0 - n0);
         const float al1 = (n1 == -INFINITY) ? 1.0f : fast_exp2(m1 - n1);
-        const float p0 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[0] - n0);
-        const float p1 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[1] - n1);
-        const float p2 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[2] - n0);
-        const float p3 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[3] - n1);
+        const float c0 = bias - n0, c1 = bias - n1;
+        const float p0 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[0] + c0);
+        const float p1 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[1] + c1);
+        const float p2 = (n0 == -INFINITY) ? 0.0f : fast_exp2(s[2] + c0);
+        const float p3 = (n1 == -INFINITY) ? 0.0f : fast_exp2(s[3] + c1);
         m0 = n0;
         m1 = n1;
-        l0 = l0 * al0 + p0 + p2;
-        l1 = l1 * al1 + p1 + p3;
+        l0 = l0 * al0 + (p0 + p2) * unbias;
+        l1 = l1 * al1 + (p1 + p3) * unbias;
         if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {  // a running max moved
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -602,11 +610,10 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
         // could be NaN patterns; 0 * NaN would poison the sum)
         if constexpr (FP8) {
           __half* pb = reinterpret_cast<__half*>(pbuf);  // [8 rows][16 tokens]
-          const float vsc = mt.vs[hw];
-          pb[(2 * t) * 16 + g] = __float2half_rn(p0 * vsc);
-          pb[(2 * t + 1) * 16 + g] = __float2half_rn(p1 * vsc);
-          pb[(2 * t) * 16 + g + 8] = __float2half_rn(p2 * vsc);
-          pb[(2 * t + 1) * 16 + g + 8] = __float2half_rn(p3 * vsc);
+          pb[(2 * t) * 16 + g] = __float2half_rn(p0);
+          pb[(2 * t + 1) * 16 + g] = __float2half_rn(p1);
+          pb[(2 * t) * 16 + g + 8] = __float2half_rn(p2);
+          pb[(2 * t + 1) * 16 + g + 8] = __float2half_rn(p3);
           __syncwarp();
           const uint2 bq = lds64(pbuf + g * 32 + 8 * t);  // row g, tokens 4t..4t+3
           __syncwarp();

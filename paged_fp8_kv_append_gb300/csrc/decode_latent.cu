@@ -39,14 +39,13 @@
 namespace kvfp8 {
 namespace {
 
-constexpr int kUT = 32;        // tokens per unit
-constexpr int kPage = 64;      // tokens per page
+constexpr int kUT = 64;        // tokens per unit: one page
 constexpr int kDK = 576, kDV = 512, kNKB = kDK / 64;  // K blocks of 64 dims
 constexpr int kRB = 64;        // query rows per segment
-constexpr int kNKV = 3;        // f16 KV tiles (converted units)
-constexpr int kNS = 4;         // S buffers in tensor memory
-constexpr int kLag = 2;        // PV(u) is issued right after S(u + kLag)
-constexpr int kUnitBytes = kUT * kDK;  // 18432
+constexpr int kNKV = 2;        // f16 KV tiles (converted units)
+constexpr int kUnitBytes = kUT * kDK;            // 36864 e4m3 bytes per unit
+constexpr int kHalfPieces = kUnitBytes / 16 / 256;  // 16-byte pieces per thread per half unit
+static_assert(kHalfPieces == 9, "converter mapping");
 
 // warps: 0-3 softmax (tensor-memory lane quarters 0-3), 4-7 converters
 // (global e4m3 -> swizzled f16 tiles), 8 MMA issuer
@@ -54,26 +53,28 @@ constexpr int kThreads = 288;
 constexpr int kSoftmaxWarps = 4, kConvWarps = 4;
 constexpr int kMmaWarp = 8;
 
-// shared memory (bytes); tiles 1024-byte aligned for the 128B swizzle
+// shared memory (bytes); tiles 1024-byte aligned for the 128B swizzle.  A KV
+// tile is 9 blocks of [64 tokens][128 B]; once S has read it, its last block
+// (dims 512..575, not part of V) holds the unit's P tile [64 rows][128 B].
+constexpr int BLK = kUT * 128;                             // 8192
 constexpr int OFF_Q = 0;                                   // 9 x [64 rows][128 B]
-constexpr int OFF_KV = OFF_Q + kNKB * kRB * 128;           // 3 x 9 x [32 tokens][128 B]
-constexpr int KV_BYTES = kNKB * kUT * 128;                 // 36864
-constexpr int OFF_P = OFF_KV + kNKV * KV_BYTES;            // 2 x [64 rows][128 B]
-constexpr int P_BYTES = kRB * 128;
-constexpr int OFF_ALPHA = OFF_P + 2 * P_BYTES;             // 2 x 64 floats
+constexpr int OFF_KV = OFF_Q + kNKB * kRB * 128;
+constexpr int KV_BYTES = kNKB * BLK;                       // 73728
+constexpr int OFF_P_IN_KV = (kNKB - 1) * BLK;              // block 8
+constexpr int OFF_ALPHA = OFF_KV + kNKV * KV_BYTES;        // 2 x 64 floats
 constexpr int OFF_FLAG = OFF_ALPHA + 2 * kRB * 4;          // 2 ints (+pad)
-constexpr int OFF_META = OFF_FLAG + 16;                    // unit meta [3]
+constexpr int OFF_META = OFF_FLAG + 16;                    // unit meta [2]
 constexpr int OFF_BAR = OFF_META + kNKV * 16;
-constexpr int NBAR = 2 * kNKV + 2 * kNS + 2 + 2 + 4;
+constexpr int NBAR = 4 * kNKV + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_MISC + 64;
-static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(OFF_KV % 1024 == 0 && KV_BYTES % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks x 64 columns
-constexpr uint32_t kTmemS = 256;   // S: 4 buffers x 32 columns
+constexpr uint32_t kTmemS = 256;   // S: 2 buffers x 64 columns
 
 struct UnitMeta {
   int n_valid;  // valid tokens of the unit (0: skip)
@@ -98,16 +99,43 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, i
   return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescS = idesc_f16(64, kUT, 0, 0);   // S = Q K^T
+constexpr uint32_t kIdescS = idesc_f16(kRB, kUT, 0, 0);  // S = Q K^T
 constexpr uint32_t kIdescPV = idesc_f16(128, kRB, 1, 0); // O^T += V^T P^T
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        bool accumulate) {
+// issued by the elected lane of a converged warp (cheaper than a lone lane)
+__device__ __forceinline__ void mma_f16_if(uint32_t leader, uint32_t d_tmem, uint64_t a,
+                                           uint64_t b, uint32_t idesc, bool accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0)
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0), "r"(leader)
       : "memory");
+}
+
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred;
+}
+
+// non-blocking phase test
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// whole page into L2 ahead of the converters' loads (16-byte aligned, size a
+// multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -133,6 +161,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// M = 64 accumulator rows live in lanes 0..15 of each lane quarter: threads
+// 0..15 read lane t at columns c..c+31, threads 16..31 lane t-16 at c+32..c+63
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
@@ -228,21 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_s = smem + OFF_Q;
   uint8_t* kv_s = smem + OFF_KV;
-  uint8_t* p_s = smem + OFF_P;
   float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);    // [2][64]
   volatile int* flag_s = reinterpret_cast<volatile int*>(smem + OFF_FLAG);  // [2]
   UnitMeta* kv_meta = reinterpret_cast<UnitMeta*>(smem + OFF_META);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* kv_ready = bars;                    // [3] converters
-  uint64_t* kv_free = kv_ready + kNKV;          // [3] MMA commit after PV
-  uint64_t* s_full = kv_free + kNKV;            // [4] MMA commit after S
-  uint64_t* s_free = s_full + kNS;              // [4] softmax
-  uint64_t* p_ready = s_free + kNS;             // [2] softmax
-  uint64_t* p_free = p_ready + 2;               // [2] MMA commit after PV
-  uint64_t* q_ready = p_free + 2;               // converters
-  uint64_t* q_free = q_ready + 1;               // MMA commit after a piece's last S
-  uint64_t* epi_done = q_free + 1;              // softmax
-  uint64_t* drain = epi_done + 1;               // MMA commit at exit
+  uint64_t* kv_ready = bars;               // [2] converters (tile + meta written)
+  uint64_t* kv_free = kv_ready + kNKV;     // [2] MMA commit after PV: tile and P free
+  uint64_t* s_full = kv_free + kNKV;       // [2] MMA commit after S
+  uint64_t* p_ready = s_full + kNKV;       // [2] softmax: P written, O rescaled
+  uint64_t* q_ready = p_ready + kNKV;      // converters
+  uint64_t* q_free = q_ready + 1;          // MMA commit after a piece's last S
+  uint64_t* epi_done = q_free + 1;         // softmax: O of the piece read out
+  uint64_t* drain = epi_done + 1;          // MMA commit at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -266,14 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     for (int i = 0; i < kNKV; ++i) {
       mbar_init(&kv_ready[i], kConvWarps);
       mbar_init(&kv_free[i], 1);
-    }
-    for (int i = 0; i < kNS; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxWarps);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_ready[i], kSoftmaxWarps);
-      mbar_init(&p_free[i], 1);
       flag_s[i] = -1;
     }
     mbar_init(q_ready, kConvWarps);
@@ -293,42 +331,20 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
 
   if (warp >= kSoftmaxWarps && warp < kSoftmaxWarps + kConvWarps) {
     // ============================ converters ============================
-    // thread ct handles 16-byte pieces g = ct + 128 i (i < 9) of a unit's
-    // 32 x 576 e4m3 bytes: token g / 36, dims 16 (g % 36) .. +15
+    // Thread ct handles the 16-byte pieces g = ct + 128 i (i < 18) of a
+    // unit's 64 x 576 e4m3 bytes: token g / 36, dims 16 (g % 36) .. +15.
+    // Pieces i < 9 are tokens 0..31, the rest tokens 32..63; each half's loads
+    // are issued one half ahead, and the page two units ahead is pulled into L2.
     const int ct = threadIdx.x - kSoftmaxWarps * 32;
     const int maxp = a.max_pages;
-    struct Pre {
-      uint4 d[9];
-      UnitMeta m;
-    };
-    auto fetch = [&](const Seg& sg, long long xu, long long uu, Pre& pr) {
-      const int j = (int)(xu - sg.start);
-      const int p = a.page_table[(long long)sg.r * maxp + (j >> 1)];
-      const bool ok = p >= 0 && p < a.d.num_pages;
-      const int L = a.seq_lens[sg.r];
-      pr.m.n_valid = ok ? min(kUT, L - j * kUT) : 0;
-      pr.m.pos0 = j * kUT;
-      pr.m.scale = ok ? a.d.k_scale[p] : 1.0f;
-      pr.m.unit = (int)uu;
-      if (!ok && ct == 0) {
-        a.ws.rq_bad[sg.r] = 1;
-        set_error(ctl, KV_ERR_BAD_PAGE_ID);
-      }
-      const uint8_t* src = cache + (long long)(ok ? p : 0) * kPage * kDK + (long long)(j & 1) * kUnitBytes;
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const int g = ct + 128 * i, t = g / 36;
-        pr.d[i] = (ok && t < pr.m.n_valid)
-                      ? __ldg(reinterpret_cast<const uint4*>(src + t * kDK + (g % 36) * 16))
-                      : make_uint4(0, 0, 0, 0);
-      }
-    };
     Seg s = start;
     long long x = x_begin, u = 0;
     int piece = 0;
     bool go = true;
     while (x < x_end && go) {
       const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
+      const int32_t* prow = a.page_table + (long long)s.r * maxp;
+      const int L = a.seq_lens[s.r];
       // ---- Q block of this segment: rows rb*64 .. +63 of the request's T*Hq rows
       if (piece > 0 &&
           !mbar_wait(q_free, (uint32_t)((piece - 1) & 1), abort_flag, ctl, wait_info(warp, 1, 60))) {
@@ -351,35 +367,78 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
       }
-      // ---- units, the next one's loads in flight while this one converts
-      Pre cur, nxt;
-      fetch(s, x, u, cur);
-      for (long long xu = x; xu < piece_end; ++xu, ++u) {
-        if (xu + 1 < piece_end) fetch(s, xu + 1, u + 1, nxt);
-        const int kb = (int)(u % kNKV);
-        if (u >= kNKV && !mbar_wait(&kv_free[kb], (uint32_t)(((u / kNKV) - 1) & 1), abort_flag,
-                                    ctl, wait_info(warp, 1, 32 + kb))) {
-          go = false;
-          break;
-        }
-        uint8_t* dst = kv_s + kb * KV_BYTES;
+      // unit j of the request is page j
+      auto page_of = [&](long long xu) -> int {
+        return (xu < piece_end) ? prow[xu - s.start] : -1;
+      };
+      auto page_ok = [&](int pg) { return pg >= 0 && pg < a.d.num_pages; };
+      auto src_of = [&](int pg) -> const uint8_t* {
+        return cache + (long long)(page_ok(pg) ? pg : 0) * kUnitBytes;
+      };
+      auto load_half = [&](int pg, long long xu, int h, uint4 (&d)[kHalfPieces]) {
+        const int nv = page_ok(pg) ? min(kUT, L - (int)(xu - s.start) * kUT) : 0;
+        const uint8_t* src = src_of(pg);
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const int g = ct + 128 * i, t = g / 36, c16 = g % 36;
+        for (int i = 0; i < kHalfPieces; ++i) {
+          const int g = ct + 128 * (i + kHalfPieces * h), t = g / 36;
+          d[i] = (t < nv) ? __ldg(reinterpret_cast<const uint4*>(src + t * kDK + (g % 36) * 16))
+                          : make_uint4(0, 0, 0, 0);
+        }
+      };
+      auto convert_half = [&](uint8_t* dst, int h, const uint4 (&d)[kHalfPieces]) {
+#pragma unroll
+        for (int i = 0; i < kHalfPieces; ++i) {
+          const int g = ct + 128 * (i + kHalfPieces * h), t = g / 36, c16 = g % 36;
           uint4 lo, hi;
-          e4m3x4_to_f16(cur.d[i].x, lo.x, lo.y);
-          e4m3x4_to_f16(cur.d[i].y, lo.z, lo.w);
-          e4m3x4_to_f16(cur.d[i].z, hi.x, hi.y);
-          e4m3x4_to_f16(cur.d[i].w, hi.z, hi.w);
-          uint8_t* blk = dst + (c16 >> 2) * (kUT * 128);
+          e4m3x4_to_f16(d[i].x, lo.x, lo.y);
+          e4m3x4_to_f16(d[i].y, lo.z, lo.w);
+          e4m3x4_to_f16(d[i].z, hi.x, hi.y);
+          e4m3x4_to_f16(d[i].w, hi.z, hi.w);
+          uint8_t* blk = dst + (c16 >> 2) * BLK;
           *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2)) = lo;
           *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2 + 1)) = hi;
         }
-        if (ct == 0) kv_meta[kb] = cur.m;
+      };
+      int pg0 = page_of(x), pg1 = page_of(x + 1), pg2 = page_of(x + 2);
+      if (ct == 0) {
+        if (page_ok(pg0)) prefetch_l2(src_of(pg0), kUnitBytes);
+        if (page_ok(pg1)) prefetch_l2(src_of(pg1), kUnitBytes);
+      }
+      uint4 d0[kHalfPieces], d1[kHalfPieces];
+      load_half(pg0, x, 0, d0);
+      for (long long xu = x; xu < piece_end; ++xu, ++u) {
+        const int b = (int)(u & 1);
+        load_half(pg0, xu, 1, d1);
+        if (ct == 0 && page_ok(pg2)) prefetch_l2(src_of(pg2), kUnitBytes);
+        const int pg3 = page_of(xu + 3);
+        // meta of this unit (its scale load is the only dependent one)
+        UnitMeta m;
+        const bool ok = page_ok(pg0);
+        m.n_valid = ok ? min(kUT, L - (int)(xu - s.start) * kUT) : 0;
+        m.pos0 = (int)(xu - s.start) * kUT;
+        m.scale = ok ? a.d.k_scale[pg0] : 1.0f;
+        m.unit = (int)u;
+        if (!ok && ct == 0) {
+          a.ws.rq_bad[s.r] = 1;
+          set_error(ctl, KV_ERR_BAD_PAGE_ID);
+        }
+        // tile b is free once PV(u - 2) has completed
+        if (u >= kNKV && !mbar_wait(&kv_free[b], (uint32_t)(((u >> 1) - 1) & 1), abort_flag, ctl,
+                                    wait_info(warp, 1, 32 + b))) {
+          go = false;
+          break;
+        }
+        uint8_t* dst = kv_s + b * KV_BYTES;
+        convert_half(dst, 0, d0);
+        if (xu + 1 < piece_end) load_half(pg1, xu + 1, 0, d0);
+        convert_half(dst, 1, d1);
+        if (ct == 0) kv_meta[b] = m;
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_ready[kb]);
-        cur = nxt;
+        if (lane == 0) mbar_arrive(&kv_ready[b]);
+        pg0 = pg1;
+        pg1 = pg2;
+        pg2 = pg3;
       }
       ++piece;
       x = piece_end;
@@ -387,81 +446,102 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ============================
+    // Per piece, S(u) and PV(u) are issued as soon as their inputs are ready
+    // (PV first when both are): S(u) needs tile u converted and at most one
+    // unit ahead of PV; PV(u) needs P(u) (and, for the piece's first unit, the
+    // previous piece's output read out).
+    const uint32_t leader = elect_one();
     Seg s = start;
     long long x = x_begin, u = 0;
     int piece = 0;
     bool go = true;
-    const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s), p_base = smem_u32(p_s);
+    const uint32_t q_base = smem_u32(q_s), kv_base = smem_u32(kv_s);
+    const uint64_t dq0 = sw128_desc(q_base, 16, 1024);
+    const uint64_t dk0 = sw128_desc(kv_base, 16, 1024);
+    const uint64_t dv0 = sw128_desc(kv_base, BLK, 1024);
+    const uint64_t dp0 = sw128_desc(kv_base + OFF_P_IN_KV, 16, 1024);
     while (x < x_end && go) {
       const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
-      const long long u0 = u, n = piece_end - x;
-      if (!mbar_wait(q_ready, (uint32_t)(piece & 1), abort_flag, ctl, wait_info(warp, 0, 62))) {
-        go = false;
-        break;
-      }
-      for (long long i = 0; i < n + kLag && go; ++i) {
-        if (i < n) {  // ---- S(u0 + i) = Q K^T into S buffer (u0+i) % 4
-          const long long uu = u0 + i;
-          const int kb = (int)(uu % kNKV), sb = (int)(uu % kNS);
-          go = mbar_wait(&kv_ready[kb], (uint32_t)((uu / kNKV) & 1), abort_flag, ctl,
-                         wait_info(warp, 0, 40 + kb));
-          go = go && (uu < kNS || mbar_wait(&s_free[sb], (uint32_t)(((uu / kNS) - 1) & 1),
-                                            abort_flag, ctl, wait_info(warp, 1, 44 + sb)));
-          go = __all_sync(0xffffffffu, go);
-          if (!go) break;
-          tc_fence_after();
-          if (lane == 0) {
-            for (int st = 0; st < kDK / 16; ++st) {
-              const uint64_t ad =
-                  sw128_desc(q_base + (st >> 2) * (kRB * 128) + (st & 3) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(
-                  kv_base + kb * KV_BYTES + (st >> 2) * (kUT * 128) + (st & 3) * 32, 16, 1024);
-              mma_f16(tmem + kTmemS + 32 * sb, ad, bd, kIdescS, st > 0);
-            }
-            mma_commit(&s_full[sb]);
-            if (i == n - 1) mma_commit(q_free);  // every S of this piece is issued
-          }
-          __syncwarp();
-        }
-        if (i >= kLag) {  // ---- PV(u0 + i - kLag): O^T += V^T P^T
-          const long long v = u0 + i - kLag;
-          const int kb = (int)(v % kNKV), pb = (int)(v & 1);
-          // the first PV of a piece overwrites O: the previous piece's
-          // epilogue must have read it (its S products already ran ahead)
-          if (v == u0 && piece > 0) {
-            go = __all_sync(0xffffffffu, mbar_wait(epi_done, (uint32_t)((piece - 1) & 1),
-                                                   abort_flag, ctl, wait_info(warp, 1, 61)));
-            if (!go) break;
-          }
-          go = __all_sync(0xffffffffu, mbar_wait(&p_ready[pb], (uint32_t)((v >> 1) & 1),
-                                                 abort_flag, ctl, wait_info(warp, 0, 48 + pb)));
-          if (!go) break;
-          tc_fence_after();
-          if (lane == 0) {
-            for (int db = 0; db < kDV / 128; ++db) {
-              for (int st = 0; st < kUT / 16; ++st) {
-                // V^T: dims 128db.. (two 64-dim blocks, LBO apart), tokens 16st..
-                const uint64_t ad = sw128_desc(kv_base + kb * KV_BYTES +
-                                                   (2 * db) * (kUT * 128) + st * 2048,
-                                               kUT * 128, 1024);
-                const uint64_t bd = sw128_desc(p_base + pb * P_BYTES + st * 32, 16, 1024);
-                mma_f16(tmem + kTmemO + 64 * db, ad, bd, kIdescPV, !(v == u0 && st == 0));
+      const long long u0 = u, ue = u0 + (piece_end - x);
+      go = __all_sync(0xffffffffu, mbar_wait(q_ready, (uint32_t)(piece & 1), abort_flag, ctl,
+                                             wait_info(warp, 0, 62)));
+      if (!go) break;
+      long long ns = u0, np = u0;
+      bool epi_ok = piece == 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = global_ns();
+      while (np < ue) {
+        bool did = false;
+        if (np < ns) {  // ---- PV(np): O^T += V^T P^T
+          const int b = (int)(np & 1);
+          if (!epi_ok)
+            epi_ok = __all_sync(0xffffffffu, mbar_test(epi_done, (uint32_t)((piece - 1) & 1)));
+          if (epi_ok &&
+              __all_sync(0xffffffffu, mbar_test(&p_ready[b], (uint32_t)((np >> 1) & 1)))) {
+            tc_fence_after();
+            const uint32_t kvo = (uint32_t)(b * KV_BYTES) >> 4;
+#pragma unroll
+            for (int st = 0; st < kUT / 16; ++st) {
+#pragma unroll
+              for (int db = 0; db < kDV / 128; ++db) {
+                // V^T: dims 128db.. (two 64-dim blocks, BLK apart), tokens 16st..
+                const uint64_t ad = dv0 + kvo + ((uint32_t)(2 * db * BLK + st * 2048) >> 4);
+                const uint64_t bd = dp0 + kvo + (uint32_t)(st * 2);
+                mma_f16_if(leader, tmem + kTmemO + 64 * db, ad, bd, kIdescPV,
+                           !(np == u0 && st == 0));
               }
             }
-            mma_commit(&kv_free[kb]);
-            mma_commit(&p_free[pb]);
+            if (leader) mma_commit(&kv_free[b]);
+            __syncwarp();
+            ++np;
+            did = true;
           }
-          __syncwarp();
+        }
+        if (!did && ns < ue && ns - np < kNKV) {  // ---- S(ns) = Q K^T
+          const int b = (int)(ns & 1);
+          if (__all_sync(0xffffffffu, mbar_test(&kv_ready[b], (uint32_t)((ns >> 1) & 1)))) {
+            tc_fence_after();
+            const uint32_t kvo = (uint32_t)(b * KV_BYTES) >> 4;
+#pragma unroll
+            for (int st = 0; st < kDK / 16; ++st) {
+              const uint32_t off = (uint32_t)((st >> 2) * BLK + (st & 3) * 32) >> 4;
+              mma_f16_if(leader, tmem + kTmemS + 64 * b, dq0 + off, dk0 + kvo + off, kIdescS,
+                         st > 0);
+            }
+            if (leader) {
+              mma_commit(&s_full[b]);
+              if (ns == ue - 1) mma_commit(q_free);  // every S of this piece is issued
+            }
+            __syncwarp();
+            ++ns;
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if ((++idle & 63u) == 1u) {  // the clock is read only now and then
+          if (idle == 1u) t_idle = global_ns();
+          if (*abort_flag) {
+            go = false;
+          } else if (global_ns() - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            if (lane == 0 &&
+                atomicCAS(reinterpret_cast<int*>(ctl + KV_CTL_ERROR), 0, KV_ERR_TIMEOUT) == 0)
+              ctl[KV_CTL_WAIT_INFO] = wait_info(warp, 0, np < ns ? 48 : 40);
+            go = false;
+          }
+          go = __all_sync(0xffffffffu, go);
+          if (!go) break;
         }
       }
-      u = u0 + n;
+      u = ue;
       ++piece;
       x = piece_end;
       if (x == seg_end) seg_next(s, pfx, B, NRB);
     }
     // let every tensor-core operation issued here finish (bounded) before
     // tensor memory is freed: a commit tracks all earlier ones
-    if (lane == 0) {
+    if (leader) {
       mma_commit(drain);
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(drain, 0) && global_ns() - t0 < 100000000ull) {
@@ -470,9 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
     // ============================ softmax (warps 0-3) ============================
-    const int q4 = warp;                 // tensor-memory lane quarter
-    const bool owner = lane < 16;        // S rows live in lanes 0-15 of each quarter
-    const int n = 16 * q4 + lane;        // query row within the block (owners)
+    // Row r = 16 q4 + (lane & 15) of the block; lanes < 16 hold its tokens
+    // 0..31 of a unit, lanes >= 16 its tokens 32..63.  Logits are in log2
+    // units.  The page scale enters P as a bias log2(scale) on the exponent,
+    // and the reference max M tracks max(logit + bias) lazily (the output is
+    // rescaled only when it grows by more than 2^8), so P <= 2^8 and small
+    // scales do not push P into f16's subnormal range; the row sum l takes
+    // the bias back out.
+    const int q4 = warp;
+    const int r = 16 * q4 + (lane & 15), h = lane >> 4;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float ssl = a.sm_scale_log2;
     Seg s = start;
@@ -481,81 +567,83 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
     while (x < x_end) {
       const long long seg_end = s.start + s.np, piece_end = min(seg_end, x_end);
       const int L = a.seq_lens[s.r];
-      // row rb*64 + n of the request's (t, hq) rows: draft token t = row / Hq
-      const int tq = (s.rb * kRB + n) / a.Hq;
+      // row rb*64 + r of the request's (t, hq) rows: draft token t = row / Hq
+      const int tq = (s.rb * kRB + r) / a.Hq;
       const int lim = L - a.T + min(tq, a.T - 1);  // last visible position (inclusive)
-      float m_ref = -INFINITY, l = 0.0f;
+      float M = -INFINITY, l = 0.0f;
       const long long u0 = u;
       // every softmax warp runs every unit (and every named barrier), even
       // after a wait gave up, so the barrier sequence never diverges
       for (long long xu = x; xu < piece_end; ++xu, ++u) {
-        const int sb = (int)(u % kNS), kb = (int)(u % kNKV), pb = (int)(u & 1);
-        go = go && mbar_wait(&s_full[sb], (uint32_t)((u / kNS) & 1), abort_flag, ctl,
-                             wait_info(warp, 0, 52 + sb));
-        go = go && mbar_wait(&kv_ready[kb], (uint32_t)((u / kNKV) & 1), abort_flag, ctl,
-                             wait_info(warp, 0, 40 + kb));
+        const int b = (int)(u & 1);
+        go = go && mbar_wait(&s_full[b], (uint32_t)((u >> 1) & 1), abort_flag, ctl,
+                             wait_info(warp, 0, 52 + b));
+        go = go && mbar_wait(&kv_ready[b], (uint32_t)((u >> 1) & 1), abort_flag, ctl,
+                             wait_info(warp, 0, 44 + b));
         go = __all_sync(0xffffffffu, go);  // tensor-memory loads are warp-collective
         float v[32];
         if (go) {
           tc_fence_after();
-          tmem_ld32(tmem + kTmemS + 32 * sb + lane_off, v);
-          tc_fence_before();
+          tmem_ld16x2(tmem + kTmemS + 64 * b + lane_off, v);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-        const UnitMeta m = kv_meta[kb];
+        const UnitMeta m = kv_meta[b];
         if (go && m.unit != (int)u) {
           if (lane == 0) set_error(ctl, KV_ERR_INTERNAL);
           *abort_flag = 1;
           go = false;
         }
-        // P buffer pb is free once PV(u-2) has completed
-        go = go && (u < 2 || mbar_wait(&p_free[pb], (uint32_t)(((u >> 1) - 1) & 1), abort_flag,
-                                       ctl, wait_info(warp, 1, 56 + pb)));
         go = __all_sync(0xffffffffu, go);
         float alpha = 1.0f;
-        if (owner && go) {
-          const float sc = m.scale * ssl;
+        if (go) {
+          const float sc = m.scale * ssl, bias = __log2f(m.scale);
+          // tokens i <= thr of this thread's 32 are visible
+          const int thr = min(m.n_valid - 1, lim - m.pos0) - 32 * h;
           float mx = -INFINITY;
+          if (thr >= 31) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const bool vis = i < m.n_valid && m.pos0 + i <= lim;
-            v[i] = vis ? v[i] * sc : -INFINITY;
-            mx = fmaxf(mx, v[i]);
+            for (int i = 0; i < 32; ++i) {
+              v[i] *= sc;
+              mx = fmaxf(mx, v[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = (i <= thr) ? v[i] * sc : -INFINITY;
+              mx = fmaxf(mx, v[i]);
+            }
           }
-          // lazy reference max: only move it (and rescale O) when the tile's
-          // max exceeds it by more than 2^8
-          if (mx > m_ref + 8.0f) {
-            alpha = (m_ref == -INFINITY) ? 0.0f : ex2(m_ref - mx);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mb = mx + bias;
+          if (mb > M + 8.0f) {
+            alpha = (M == -INFINITY) ? 0.0f : ex2(M - mb);
             l *= alpha;
-            m_ref = mx;
+            M = mb;
           }
+          const float c = (M == -INFINITY) ? -INFINITY : bias - M;
           float sum = 0.0f;
-          const float vs = m.scale;
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = (v[i] == -INFINITY) ? 0.0f : ex2(v[i] - m_ref);
-            const float p1 = (v[i + 1] == -INFINITY) ? 0.0f : ex2(v[i + 1] - m_ref);
+            const float p0 = ex2(v[i] + c), p1 = ex2(v[i + 1] + c);
             sum += p0 + p1;
-            pk[i >> 1] = pack_f16(p0 * vs, p1 * vs);
+            pk[i >> 1] = pack_f16(p0, p1);
           }
-          l += sum;
-          // P row n: tokens 0..31 = chunks 0..3 of a 128B-swizzled row
-          uint8_t* prow = p_s + pb * P_BYTES;
+          l += sum * ex2(-bias);
+          // P row r, tokens 32h..32h+31 = chunks 4h..4h+3 of a 128B-swizzled row
+          uint8_t* prow = kv_s + b * KV_BYTES + OFF_P_IN_KV;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(prow + swz(n, c)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          if (alpha != 1.0f) flag_s[pb] = (int)u;  // unit number: never stale
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(prow + swz(r, 4 * h + c4)) =
+                make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+          if (alpha != 1.0f) flag_s[b] = (int)u;  // unit number: never stale
         }
-        if (owner) alpha_s[pb * kRB + n] = alpha;
+        if (h == 0) alpha_s[b * kRB + r] = alpha;
         fence_async_smem();
         named_bar_sync(2, kSoftmaxWarps * 32);
-        if (flag_s[pb] == (int)u && u > u0) {
+        if (flag_s[b] == (int)u && u > u0) {
           // O^T columns are query rows: column n *= alpha[n], after PV(u-1)
           const long long pu = u - 1;
-          go = go && mbar_wait(&p_free[pu & 1], (uint32_t)((pu >> 1) & 1), abort_flag, ctl,
+          go = go && mbar_wait(&kv_free[pu & 1], (uint32_t)((pu >> 1) & 1), abort_flag, ctl,
                                wait_info(warp, 1, 58));
           go = __all_sync(0xffffffffu, go);
           if (go) {
@@ -566,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
                 const uint32_t ta = tmem + kTmemO + 64 * db + 32 * half + lane_off;
                 tmem_ld32(ta, o);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= alpha_s[pb * kRB + 32 * half + i];
+                for (int i = 0; i < 32; ++i) o[i] *= alpha_s[b * kRB + 32 * half + i];
                 tmem_st32(ta, o);
               }
             }
@@ -574,12 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_ready[pb]);
+        if (lane == 0) mbar_arrive(&p_ready[b]);
       }
       // ---- epilogue: partial (o, m, l) of this piece
       if (u > u0) {
         const long long last = u - 1;
-        go = go && mbar_wait(&p_free[last & 1], (uint32_t)((last >> 1) & 1), abort_flag, ctl,
+        go = go && mbar_wait(&kv_free[last & 1], (uint32_t)((last >> 1) & 1), abort_flag, ctl,
                              wait_info(warp, 0, 59));
       }
       go = __all_sync(0xffffffffu, go);
@@ -596,9 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
             a.ws.o_part[(slot * kRB + 32 * half + i) * kDV + dv] = o[i];
         }
       }
-      if (owner && go) {
-        a.ws.ml_part[(slot * kRB + n) * 2 + 0] = m_ref;
-        a.ws.ml_part[(slot * kRB + n) * 2 + 1] = l;
+      const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      if (h == 0 && go) {
+        a.ws.ml_part[(slot * kRB + r) * 2 + 0] = M;
+        a.ws.ml_part[(slot * kRB + r) * 2 + 1] = l_row;
       }
       tc_fence_before();
       __syncwarp();

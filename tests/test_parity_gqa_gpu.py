@@ -99,6 +99,28 @@ def test_multi_token_causal_and_group_sizes(T, Hq, Hkv):
     _check_out(out, ref, written, None)
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("mag", [1e-4, 3e3])
+def test_kv_magnitude_extremes(dtype, mag):
+    """K/V drawn at 1e-4 and 3e3: page scales far from 1 (about 1e-6 and 30)
+    must not push the attention weights out of f16's normal range.  Outputs
+    are compared relative to the magnitude (the absolute term of the bound
+    would otherwise hide a tiny-scale error)."""
+    lens = np.array([37, 300, 1000, 5], np.int32)
+    w = wl.Workload("magnitude", 123, lens, 16, 4, 128, 128, 16, 2, 0, 256,
+                    float(np.float32(1 / np.sqrt(128))), magnitude=mag)
+    b = Both(w, dtype)
+    assert b.fill()[0] == 0
+    torch.cuda.synchronize()
+    b.assert_state_equal()
+    out, ref, written = b.attn(_q(w), None, None)
+    assert written.all() and b.dev.error() == 0
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    for r in range(w.B):
+        ok, mabs, mrel, _ = close(got[r] / mag, ref[r] / mag)
+        assert ok, f"request {r}: max abs {mabs:.3g}, max rel {mrel:.3g} (relative to {mag})"
+
+
 def test_bad_page_id_is_not_read():
     """A request whose page table holds an out-of-range id, with the no-op
     tracker: no output, KV_ERR_BAD_PAGE_ID, other requests unaffected."""

@@ -12,11 +12,11 @@ from pathrun import Both, FullSize, bf16_to_f64, close
 pytestmark = pytest.mark.gpu
 
 
-def _lat(lens, T, Hq, seed=3):
+def _lat(lens, T, Hq, seed=3, magnitude=1.0):
     lens = np.array(lens, np.int32)
     npg = int((-(-lens.astype(np.int64) // 64)).sum()) + 8
     return wl.Workload("latent", seed, lens, Hq, 1, 576, 512, 64, T, 1, npg,
-                       float(np.float32(1 / np.sqrt(576))))
+                       float(np.float32(1 / np.sqrt(576))), magnitude=magnitude)
 
 
 def _check(out, ref, written, sentinel=7.0):
@@ -44,6 +44,24 @@ def test_latent_small(T, Hq, lens):
     out, ref, written = b.attn(wl.queries(w, device="cuda"), None, None)
     assert b.dev.error() == 0, b.kv.kv_status_string(b.dev.error())
     _check(out, ref, written)
+
+
+@pytest.mark.parametrize("mag", [1e-4, 3e3])
+def test_latent_magnitude_extremes(mag):
+    """Cache rows drawn at 1e-4 and 3e3 (page scales about 1e-6 and 30): the
+    attention weights must stay in f16's normal range.  Compared relative to
+    the magnitude."""
+    w = _lat([300, 1000, 65, 7], 4, 16, seed=21, magnitude=mag)
+    b = Both(w, 0)
+    assert b.fill()[0] == 0
+    torch.cuda.synchronize()
+    b.assert_state_equal()
+    out, ref, written = b.attn(wl.queries(w, device="cuda"), None, None)
+    assert written.all() and b.dev.error() == 0
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    for r in range(w.B):
+        ok, mabs, mrel, _ = close(got[r] / mag, ref[r] / mag)
+        assert ok, f"request {r}: max abs {mabs:.3g} max rel {mrel:.3g} (relative to {mag})"
 
 
 def test_latent_ring_wraps_and_abort():

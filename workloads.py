@@ -38,6 +38,7 @@ class Workload:
     stale: list = field(default_factory=list)  # requests given one stale expected tag
     channel_std: bool = False    # per-(K|V, head, dim) std ~ U(0.5, 4)
     steps: int = 0               # decode steps the pool must have room for
+    magnitude: float = 1.0       # K/V rows are drawn at this overall scale
 
     @property
     def B(self) -> int:
@@ -170,13 +171,13 @@ def kv_rows(w: Workload, r: int, row0: int, nrows: int, device="cpu", tag: int =
         pos = blk * 4096 + hi
     k = torch.cat(outs_k)
     if w.layout == 1:
-        return k.to(torch.bfloat16), None
+        return (k * w.magnitude).to(torch.bfloat16), None
     v = torch.cat(outs_v)
     sk, sv = channel_std(w, 0), channel_std(w, 1)
     if sk is not None:
         k = k * torch.as_tensor(sk, dtype=torch.float32, device=device)
         v = v * torch.as_tensor(sv, dtype=torch.float32, device=device)
-    return k.to(torch.bfloat16), v.to(torch.bfloat16)
+    return (k * w.magnitude).to(torch.bfloat16), (v * w.magnitude).to(torch.bfloat16)
 
 
 def queries(w: Workload, device="cpu", step: int = 0) -> torch.Tensor:
