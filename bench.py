@@ -319,6 +319,79 @@ class Arm:
         return t0.elapsed_time(t1), h2d, d2h
 
 
+# ------------------------------------------------------------ verify overhead
+
+def graph_overhead(arm: "Arm", replays: int) -> dict:
+    """Cost of the page-tag check inside a whole step: two CUDA graphs of the
+    same step structure, append -> verify -> split -> combine and append ->
+    split -> combine with no abort mask, replayed alternately; overhead =
+    median(with) / median(without) - 1.  All tags are valid, so both attend
+    exactly the same requests.  Each replay is a real decode step (one more
+    token per request)."""
+    kv, w, B, h = arm.kv, arm.w, arm.w.B, arm.pool.handle
+    k0, v0, q0 = arm.k_steps[0], arm.v_steps[0], arm.q_steps[0]
+
+    def body(check: bool):
+        arm.pool.append(B, k0, v0, arm.ones, 1, arm.pt, arm.et, arm.sl)
+        mask = None
+        if check:
+            arm.pool.verify(B, arm.pt, arm.et, arm.sl, arm.mask)
+            mask = arm.mask
+        kv.paged_decode_attn_split(h, B, w.num_q_heads, w.q_tokens, q0, arm.pt, arm.sl, mask,
+                                   w.sm_scale, arm.ws)
+        kv.paged_decode_attn_combine(h, B, w.num_q_heads, w.q_tokens, mask, arm.out, arm.ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body(True)
+        body(False)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_with, g_without = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_with):
+        body(True)
+    with torch.cuda.graph(g_without):
+        body(False)
+    for _ in range(3):
+        g_with.replay()
+        g_without.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(replays)]
+    for i in range(replays):
+        ev[i][0].record()
+        g_with.replay()
+        ev[i][1].record()
+        g_without.replay()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    if arm.pool.error() != 0:
+        raise RuntimeError(f"verify overhead: device error {kv.kv_status_string(arm.pool.error())}")
+    t_with = [e[0].elapsed_time(e[1]) for e in ev]
+    t_without = [e[1].elapsed_time(e[2]) for e in ev]
+    mw, mo = statistics.median(t_with), statistics.median(t_without)
+    del g_with, g_without
+    return {"workload": w.name, "replays": replays, "ms_with_verify": mw,
+            "ms_without_verify": mo, "verify_overhead_pct": 100.0 * (mw / mo - 1.0),
+            "mean_overhead_pct": 100.0 * (sum(t_with) / sum(t_without) - 1.0)}
+
+
+def skewed_overhead(device, replays: int) -> dict:
+    """Verify overhead on the skewed long-context stress workload: 256
+    requests, lognormal contexts (median 16k, up to 256k), 32 q / 4 kv heads,
+    e4m3, page 16 (about 427k pages checked per step)."""
+    w = wl.skewed(steps=2 * (replays + 8))
+    w.stale = []  # every tag valid: both graphs attend the same requests
+    arm = Arm(w, 0, device, 1)
+    res = graph_overhead(arm, replays)
+    res["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
+                       "32 q / 4 kv heads, head dim 128, page 16, e4m3; all tags valid")
+    res["pages_checked_per_step"] = int((-(-(w.lens.astype(np.int64)) // 16)).sum())
+    del arm
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ latent verify
 
 def latent_flops(w: wl.Workload, lens: np.ndarray) -> float:
@@ -461,6 +534,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-latent", action="store_true")
+    ap.add_argument("--no-overhead", action="store_true",
+                    help="skip the CUDA-graph verify-overhead measurement")
+    ap.add_argument("--overhead-replays", type=int, default=20)
     ap.add_argument("--batch", type=int, default=32,
                     help="requests of the GQA batch workload to use (32 = the full workload; "
                          "fewer only for small profiling captures)")
@@ -506,7 +582,8 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     total_steps = 2 * (args.steps + args.warmup)
-    w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + 2)
+    graph_steps = 0 if args.no_overhead else 2 * (args.overhead_replays + 8)
+    w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + graph_steps + 2)
     if args.batch != w.B:
         w = wl.subset(w, args.batch)
 
@@ -516,6 +593,9 @@ def main():
     total_ms, per, lens_timed, launches = arm.run(args.steps, args.warmup)
     clocks = sampler.stop()
     e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup)
+    overhead = None
+    if not args.no_overhead:
+        overhead = {"gqa_batch": graph_overhead(arm, args.overhead_replays)}
     del arm
     torch.cuda.empty_cache()
 
@@ -556,6 +636,10 @@ def main():
     if not args.no_latent:
         latent = latent_bench(args.steps, args.warmup, device, peaks)
 
+    # ---- verify overhead on the skewed stress workload (the step it is defined on)
+    if overhead is not None:
+        overhead["skewed"] = skewed_overhead(device, args.overhead_replays)
+
     # ---- CPU oracle baseline (rank 0, bounded sample)
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
@@ -586,6 +670,7 @@ def main():
                       "split": float(per[:, 2].mean() * 1e3),
                       "combine": float(per[:, 3].mean() * 1e3)},
         "verify_share_pct": float(100.0 * per[:, 1].mean() / step_ms),
+        "verify_overhead": overhead,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "kernel": "paged_decode_attn_split (plan + gqa_split_kernel<e4m3>)",
