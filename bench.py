@@ -402,14 +402,14 @@ def latent_flops(w: wl.Workload, lens: np.ndarray) -> float:
     return 2.0 * vis * w.num_q_heads * (w.head_dim_k + w.head_dim_v)
 
 
-def latent_bench(steps: int, warmup: int, device, peaks: dict) -> dict:
+def latent_bench(steps: int, warmup: int, device, peaks: dict, B: int = 64) -> dict:
     """One decode step of the latent speculative-verify workload (64 requests,
     lognormal contexts 8k..64k, 128 heads x 4 draft tokens on one 576-wide
     e4m3 row per token): append the 4 draft rows of every request, tag check,
     attention (tcgen05 path) + combine."""
     import paged_fp8_kv_append_gb300 as kv
 
-    w = wl.latent_verify()
+    w = wl.latent_verify(B=B)
     T, B = w.q_tokens, w.B
     w.steps = T * (steps + warmup + 1)
     import math as _m
@@ -473,7 +473,7 @@ def latent_bench(steps: int, warmup: int, device, peaks: dict) -> dict:
     tf = float(np.mean([f / (t * 1e-3) / 1e12 for f, t in zip(flops, attn_ms)]))
     peak = float(peaks.get("bf16_tflops", 1900.0))
     kv_bytes = float((lens + T * steps // 2).sum() * 576 + B * T * 128 * (576 + 512) * 2)
-    res = {"workload": "latent_verify: 64 requests, lognormal contexts (median 16k) in "
+    res = {"workload": f"latent_verify: {B} requests, lognormal contexts (median 16k) in "
                        "[8k, 64k], 128 heads x 4 draft tokens, one 576-wide e4m3 row per token "
                        "(V = first 512), page 64",
            "value": steps * B * T / (total / 1e3), "unit": "tokens/s",
@@ -537,6 +537,9 @@ def main():
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the CUDA-graph verify-overhead measurement")
     ap.add_argument("--overhead-replays", type=int, default=20)
+    ap.add_argument("--latent-only", type=int, default=0, metavar="B",
+                    help="run only the latent verify workload with B requests and print its "
+                         "line (small profiling captures)")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests of the GQA batch workload to use (32 = the full workload; "
                          "fewer only for small profiling captures)")
@@ -573,6 +576,17 @@ def main():
                     "d2h_bytes_per_step": 0},
         }
         print(json.dumps(line))
+        return
+
+    if args.latent_only > 0:
+        device = torch.device("cuda", local)
+        peaks = {}
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except Exception:
+            pass
+        print(json.dumps(latent_bench(args.steps, args.warmup, device, peaks,
+                                      B=args.latent_only)))
         return
 
     if ws > 1:

@@ -331,10 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
 
   if (warp >= kSoftmaxWarps && warp < kSoftmaxWarps + kConvWarps) {
     // ============================ converters ============================
-    // Thread ct handles the 16-byte pieces g = ct + 128 i (i < 18) of a
-    // unit's 64 x 576 e4m3 bytes: token g / 36, dims 16 (g % 36) .. +15.
-    // Pieces i < 9 are tokens 0..31, the rest tokens 32..63; each half's loads
-    // are issued one half ahead, and the page two units ahead is pulled into L2.
+    // A unit's 64 x 576 e4m3 bytes are converted in two halves of 32 tokens,
+    // 9 16-byte pieces per thread each; each half's loads are issued one half
+    // ahead, and the page two units ahead is pulled into L2.
     const int ct = threadIdx.x - kSoftmaxWarps * 32;
     const int maxp = a.max_pages;
     Seg s = start;
@@ -375,28 +374,31 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       auto src_of = [&](int pg) -> const uint8_t* {
         return cache + (long long)(page_ok(pg) ? pg : 0) * kUnitBytes;
       };
+      // half h = tokens 32h..32h+31; piece k of this thread is token
+      // 32h + ct / 4, dims 64k + 16 (ct % 4) .. +15 (dim block k), so a warp
+      // stores 8 rows of one block and the 128B swizzle spreads its 16-byte
+      // stores over all banks
       auto load_half = [&](int pg, long long xu, int h, uint4 (&d)[kHalfPieces]) {
         const int nv = page_ok(pg) ? min(kUT, L - (int)(xu - s.start) * kUT) : 0;
-        const uint8_t* src = src_of(pg);
+        const int t = 32 * h + (ct >> 2);
+        const uint8_t* src = src_of(pg) + t * kDK + (ct & 3) * 16;
 #pragma unroll
-        for (int i = 0; i < kHalfPieces; ++i) {
-          const int g = ct + 128 * (i + kHalfPieces * h), t = g / 36;
-          d[i] = (t < nv) ? __ldg(reinterpret_cast<const uint4*>(src + t * kDK + (g % 36) * 16))
+        for (int k = 0; k < kHalfPieces; ++k)
+          d[k] = (t < nv) ? __ldg(reinterpret_cast<const uint4*>(src + k * 64))
                           : make_uint4(0, 0, 0, 0);
-        }
       };
       auto convert_half = [&](uint8_t* dst, int h, const uint4 (&d)[kHalfPieces]) {
+        const int t = 32 * h + (ct >> 2), j = ct & 3;
+        const uint32_t o_lo = swz(t, 2 * j), o_hi = swz(t, 2 * j + 1);
 #pragma unroll
-        for (int i = 0; i < kHalfPieces; ++i) {
-          const int g = ct + 128 * (i + kHalfPieces * h), t = g / 36, c16 = g % 36;
+        for (int k = 0; k < kHalfPieces; ++k) {
           uint4 lo, hi;
-          e4m3x4_to_f16(d[i].x, lo.x, lo.y);
-          e4m3x4_to_f16(d[i].y, lo.z, lo.w);
-          e4m3x4_to_f16(d[i].z, hi.x, hi.y);
-          e4m3x4_to_f16(d[i].w, hi.z, hi.w);
-          uint8_t* blk = dst + (c16 >> 2) * BLK;
-          *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2)) = lo;
-          *reinterpret_cast<uint4*>(blk + swz(t, (c16 & 3) * 2 + 1)) = hi;
+          e4m3x4_to_f16(d[k].x, lo.x, lo.y);
+          e4m3x4_to_f16(d[k].y, lo.z, lo.w);
+          e4m3x4_to_f16(d[k].z, hi.x, hi.y);
+          e4m3x4_to_f16(d[k].w, hi.z, hi.w);
+          *reinterpret_cast<uint4*>(dst + k * BLK + o_lo) = lo;
+          *reinterpret_cast<uint4*>(dst + k * BLK + o_hi) = hi;
         }
       };
       int pg0 = page_of(x), pg1 = page_of(x + 1), pg2 = page_of(x + 2);
