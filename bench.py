@@ -35,6 +35,15 @@ import workloads as wl  # noqa: E402
 METRIC = ("decode attn tokens/s & achieved HBM GB/s vs ~8 TB/s, FP8 vs BF16 KV, 1×GB300")
 NOMINAL_HBM_GBS = 8000.0
 
+# DRAM counters of gqa_split_kernel<e4m3> from one ncu capture of a small case
+# (the first 8 requests of the GQA batch workload; profiles/
+# gqa_split_e4m3_small_full.md): reads per algorithmic byte, and the partial
+# (o, m, l) writes of its 8 * 2 + 152 pieces.  Re-take them whenever the
+# kernel changes.
+SPLIT_NCU = {"read_per_alg_byte": 377.356288 / 377.100912, "write_bytes": 3428096.0,
+             "pieces": 8 * 2 + 152, "heads_per_unit": 4,
+             "profile": "profiles/gqa_split_e4m3_small_full.md"}
+
 
 # ------------------------------------------------------------ distributed
 
@@ -621,6 +630,11 @@ def main():
     attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_timed]
     split_bytes = [algorithmic_bytes(w, L, 0, include_out=False) for L in lens_timed]
     achieved = float(np.mean([b / (t * 1e6) for b, t in zip(split_bytes, split_ms)]))
+    # DRAM traffic per split launch, scaled from the small-case capture: reads
+    # in proportion to the algorithmic bytes, partial writes to the pieces
+    pieces = w.B * (w.num_kv_heads // SPLIT_NCU["heads_per_unit"]) + 152
+    traffic = (SPLIT_NCU["read_per_alg_byte"] * float(np.mean(split_bytes))
+               + SPLIT_NCU["write_bytes"] * pieces / SPLIT_NCU["pieces"])
     attn_gbs = float(np.mean([b / ((p[2] + p[3]) * 1e6) for b, p in zip(attn_bytes, per)]))
     peaks = {}
     try:
@@ -686,7 +700,10 @@ def main():
         "verify_share_pct": float(100.0 * per[:, 1].mean() / step_ms),
         "verify_overhead": overhead,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "traffic_note": "bytes per launch, ncu dram read+write of a small-case "
+                                     "capture scaled to this launch (" + SPLIT_NCU["profile"] + ")",
+                     "algorithmic_bytes": float(np.mean(split_bytes)),
                      "kernel": "paged_decode_attn_split (plan + gqa_split_kernel<e4m3>)",
                      "peak_source": peak_src},
         "bf16_kv": bf16,

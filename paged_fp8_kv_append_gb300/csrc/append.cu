@@ -54,6 +54,8 @@ __device__ long long block_incl_scan(long long v, long long* warp_sums) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ long long warp_sums[32];
   __shared__ int s_stop, s_code;
   __shared__ long long s_consumed_at_stop, s_chunk_total;
@@ -276,6 +278,8 @@ __device__ void append_block(const uint16_t* src, long long src_stride, int nrow
 // {0: K, 1: V}; latent pools use z = 0 only), so a decode-step append of one
 // row per request is a short chain of memory round trips.
 __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[9];
   extern __shared__ __align__(16) uint8_t tile[];
   const kv_pool_desc& d = a.d;
@@ -325,8 +329,7 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
-  append_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(append_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   ++*launches;
   // pages a request can touch in one call: ceil((max_new + P - 1) / P)
@@ -345,8 +348,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   }
   const unsigned items = a.d.layout == KV_LAYOUT_GQA ? 2u * (unsigned)a.d.num_kv_heads : 1u;
   dim3 grid((unsigned)a.B, (unsigned)pieces, items);
-  append_data_kernel<<<grid, kDataThreads, tile_bytes, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(append_data_kernel, grid, dim3(kDataThreads), tile_bytes, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }

@@ -104,6 +104,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation and waits for the grids before it (with
+// their memory visible) before its first global-memory access, so the order
+// of the stream is kept exactly while a kernel's launch overlaps the tail of
+// the previous one.  `trigger` lets the next kernel launch early (its CTAs
+// then sit in its own wait); the persistent split kernels do not trigger, so
+// nothing waits resident beside them.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Diagnostic word of a wait (see KV_CTL_WAIT_INFO).
 __device__ __forceinline__ int wait_info(int warp, int which, int stage) {
   return (int)((blockIdx.x << 12) | ((warp & 31) << 7) | ((which & 1) << 6) | (stage & 63));

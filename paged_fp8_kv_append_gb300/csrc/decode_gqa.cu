@@ -48,6 +48,8 @@ constexpr int kPlanThreads = 1024;
 // when its length is negative or needs more pages than its page table holds
 // (that also sets KV_ERR_INVALID_ARG).
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int P = a.d.page_size;
@@ -275,6 +277,7 @@ static_assert(sizeof(StageMeta) == 80, "StageMeta layout");
 template <bool FP8>
 __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
     gqa_split_kernel(const DecodeArgs a) {
+  pdl_wait();
   using C = GqaCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem + C::OFF_RING;
@@ -738,6 +741,8 @@ constexpr int kCombineWarps = 8;
 // single pass over the pieces suffices; lane l owns dims [4l, 4l+4) of every
 // 128-dim group.  Written as bf16 (RNE).
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const int Hkv = a.d.num_kv_heads;
@@ -841,18 +846,17 @@ int gqa_split_ctas_per_sm(int kind) {
 }
 
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s, int* launches) {
-  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
 
 cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches) {
-  if (kind == 0)
-    gqa_split_kernel<true><<<a.grid, GqaCfg<true>::THREADS, GqaCfg<true>::SMEM, s>>>(a);
-  else
-    gqa_split_kernel<false><<<a.grid, GqaCfg<false>::THREADS, GqaCfg<false>::SMEM, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      kind == 0 ? launch_pdl(gqa_split_kernel<true>, dim3(a.grid),
+                             dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)
+                : launch_pdl(gqa_split_kernel<false>, dim3(a.grid),
+                             dim3(GqaCfg<false>::THREADS), GqaCfg<false>::SMEM, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
@@ -861,8 +865,8 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* laun
   const long long items = (long long)a.B * a.d.num_kv_heads * a.R;
   if (items <= 0) return cudaSuccess;
   const long long blocks = (items + kCombineWarps - 1) / kCombineWarps;
-  combine_kernel<<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }

@@ -272,6 +272,7 @@ __device__ void seg_next(Seg& s, const int32_t* pfx, int B, int groups) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeArgs a) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_s = smem + OFF_Q;
   uint8_t* kv_s = smem + OFF_KV;
@@ -727,8 +728,7 @@ int latent_unit_tokens() { return kUT; }
 int latent_row_block() { return kRB; }
 
 cudaError_t launch_latent_split(const DecodeArgs& a, cudaStream_t s, int* launches) {
-  latent_split_kernel<<<a.grid, kThreads, SMEM, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(latent_split_kernel, dim3(a.grid), dim3(kThreads), SMEM, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }

@@ -28,6 +28,8 @@ constexpr int kUnroll = 16;
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     verify_kernel(VerifyArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int cta_bad;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -82,8 +84,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int* launches) {
   if (a.B <= 0) return cudaSuccess;
-  verify_kernel<<<(unsigned)a.B * kCluster, kThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(verify_kernel, dim3((unsigned)a.B * kCluster), dim3(kThreads), 0, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
