@@ -235,9 +235,12 @@ class Arm:
             self.q_steps.append(wl.queries(w, device=device, step=s))
         self.step_no = 0
 
-    def step(self, ev=None, launches=None):
-        """append 1 token/request -> verify -> split -> combine, on the current stream."""
-        kv, w, B, s = self.kv, self.w, self.w.B, self.step_no
+    def step(self, ev=None, launches=None, B=None):
+        """append 1 token/request -> verify -> split -> combine, on the current
+        stream, for the first B requests (all by default: the C ABI reads only
+        the first B rows of every per-request array)."""
+        kv, w, s = self.kv, self.w, self.step_no
+        B = w.B if B is None else B
         h = self.pool.handle
         if ev is not None:
             ev[0].record()
@@ -262,14 +265,16 @@ class Arm:
         if launches is not None:
             launches.append(n)
         self.step_no += 1
-        self.lens += 1
+        self.lens[:B] += 1
 
-    def run(self, steps: int, warmup: int):
+    def run(self, steps: int, warmup: int, B=None, sync_ranks=True):
+        B = self.w.B if B is None else B
         for _ in range(warmup):
-            self.step()
+            self.step(B=B)
         torch.cuda.synchronize()
-        barrier()
-        lens_timed = [self.lens + i for i in range(steps)]
+        if sync_ranks:
+            barrier()
+        lens_timed = [self.lens[:B] + i for i in range(steps)]
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
         launches = []
         t0 = torch.cuda.Event(enable_timing=True)
@@ -277,7 +282,7 @@ class Arm:
         torch.cuda.synchronize()
         t0.record()
         for i in range(steps):
-            self.step(evs[i], launches)
+            self.step(evs[i], launches, B=B)
         t1.record()
         torch.cuda.synchronize()
         total_ms = t0.elapsed_time(t1)
@@ -385,20 +390,88 @@ def graph_overhead(arm: "Arm", replays: int) -> dict:
             "mean_overhead_pct": 100.0 * (sum(t_with) / sum(t_without) - 1.0)}
 
 
-def skewed_overhead(device, replays: int) -> dict:
-    """Verify overhead on the skewed long-context stress workload: 256
-    requests, lognormal contexts (median 16k, up to 256k), 32 q / 4 kv heads,
-    e4m3, page 16 (about 427k pages checked per step)."""
-    w = wl.skewed(steps=2 * (replays + 8))
+def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B=None,
+              aborted=()) -> dict:
+    """tokens/s of the whole step (non-aborted requests / summed kernel time)
+    and GB/s of split + combine over the algorithmic bytes of the requests
+    attended, for the first B requests of an Arm."""
+    B = w.B if B is None else B
+    total_ms, per, lens_timed, _ = arm.run(steps, warmup, B=B, sync_ranks=False)
+    keep = np.array([r not in set(aborted) for r in range(B)])
+    sub = wl.subset(w, B)
+    byt = []
+    for L in lens_timed:
+        Lk = np.where(keep, L, 0)
+        b = algorithmic_bytes(sub, Lk, dtype)
+        # Q and O only for the requests attended
+        b -= (B - int(keep.sum())) * sub.q_tokens * sub.num_q_heads * (sub.head_dim_k +
+                                                                       sub.head_dim_v) * 2
+        byt.append(b)
+    attn_ms = per[:, 2] + per[:, 3]
+    gbs = float(np.mean([b / (t * 1e6) for b, t in zip(byt, attn_ms)]))
+    return {"requests": B, "attended": int(keep.sum()),
+            "tokens_per_s": int(keep.sum()) * w.q_tokens * steps / (total_ms / 1e3),
+            "ms_per_step": total_ms / steps, "attn_us": float(attn_ms.mean() * 1e3),
+            "attn_gbs": gbs, "pct_of_8000": 100.0 * gbs / NOMINAL_HBM_GBS,
+            "kernel_us": {k: float(per[:, i].mean() * 1e3)
+                          for i, k in enumerate(("append", "verify", "split", "combine"))}}
+
+
+def concurrency_sweep(device, steps: int, warmup: int, peak: float,
+                      points=(1, 8, 16, 32, 64)) -> dict:
+    """The concurrency sweep: 1..64 requests of 131,072 tokens (64 q / 8 kv
+    heads, D 128, P 16), e4m3 and bf16.  One pool per dtype is filled with 64
+    requests; each point steps the first B of them."""
+    out = {}
+    n_steps = len(points) * (steps + warmup) + 2
+    for dtype, name in ((0, "e4m3"), (1, "bf16")):
+        w = wl.concurrency(max(points))
+        w.steps = n_steps
+        w.num_pages = int(w.B * (-(-(131072 + n_steps) // 16))) + 64
+        arm = Arm(w, dtype, device, n_steps)
+        pts = []
+        for B in points:
+            line = step_line(w, arm, dtype, steps, warmup, B=B)
+            line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
+            pts.append(line)
+        out[name] = pts
+        del arm
+        torch.cuda.empty_cache()
+    out["workload"] = ("concurrency: B requests of 131,072 tokens, 64 q / 8 kv heads, head dim "
+                       "128, page 16; step = append 1 token/request + tag check + attention")
+    return out
+
+
+def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float):
+    """The skewed long-context stress workload (256 requests, lognormal
+    contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
+    428k pages checked per step): the verify overhead with every tag valid,
+    then the full step with its seeded stale tags (those requests abort)."""
+    w = wl.skewed(steps=2 * (replays + 8) + steps + warmup + 8)
+    stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
-    arm = Arm(w, 0, device, 1)
-    res = graph_overhead(arm, replays)
-    res["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
-                       "32 q / 4 kv heads, head dim 128, page 16, e4m3; all tags valid")
-    res["pages_checked_per_step"] = int((-(-(w.lens.astype(np.int64)) // 16)).sum())
+    arm = Arm(w, 0, device, steps + warmup)
+    over = graph_overhead(arm, replays)
+    over["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
+                        "32 q / 4 kv heads, head dim 128, page 16, e4m3; all tags valid")
+    over["pages_checked_per_step"] = int((-(-(w.lens.astype(np.int64)) // 16)).sum())
+    # the step as the workload defines it: one seeded stale tag in 1% of requests
+    w.stale = stale
+    et = arm.et.cpu().numpy().view(np.uint32).copy()
+    for r, j in wl.stale_slots(w):
+        et[r, j] = np.uint32(et[r, j]) - np.uint32(1)
+    arm.et.copy_(torch.from_numpy(et.view(np.int32)))
+    arm.step_no = 0
+    line = step_line(w, arm, 0, steps, warmup, aborted=stale)
+    if not np.array_equal(np.flatnonzero(arm.mask.cpu().numpy()), np.array(sorted(stale))):
+        raise RuntimeError("skewed step: abort mask differs from the stale requests")
+    line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
+    line["aborted"] = sorted(stale)
+    line["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
+                        "32 q / 4 kv heads, head dim 128, page 16, e4m3; 3 stale requests abort")
     del arm
     torch.cuda.empty_cache()
-    return res
+    return over, line
 
 
 # ------------------------------------------------------------ latent verify
@@ -546,6 +619,8 @@ def main():
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the CUDA-graph verify-overhead measurement")
     ap.add_argument("--overhead-replays", type=int, default=20)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the 1..64-request concurrency sweep at 128k")
     ap.add_argument("--latent-only", type=int, default=0, metavar="B",
                     help="run only the latent verify workload with B requests and print its "
                          "line (small profiling captures)")
@@ -664,9 +739,17 @@ def main():
     if not args.no_latent:
         latent = latent_bench(args.steps, args.warmup, device, peaks)
 
-    # ---- verify overhead on the skewed stress workload (the step it is defined on)
+    # ---- skewed stress workload: verify overhead (the step it is defined on)
+    # and the full step with its stale tags
+    skewed = None
     if overhead is not None:
-        overhead["skewed"] = skewed_overhead(device, args.overhead_replays)
+        overhead["skewed"], skewed = skewed_lines(device, args.overhead_replays, args.steps,
+                                                  args.warmup, peak)
+
+    # ---- concurrency sweep (1..64 requests at 128k), e4m3 and bf16
+    conc = None
+    if not args.no_sweep:
+        conc = concurrency_sweep(device, args.steps, args.warmup, peak)
 
     # ---- CPU oracle baseline (rank 0, bounded sample)
     cpu = None
@@ -699,6 +782,8 @@ def main():
                       "combine": float(per[:, 3].mean() * 1e3)},
         "verify_share_pct": float(100.0 * per[:, 1].mean() / step_ms),
         "verify_overhead": overhead,
+        "skewed_step": skewed,
+        "concurrency": conc,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "traffic_note": "bytes per launch, ncu dram read+write of a small-case "

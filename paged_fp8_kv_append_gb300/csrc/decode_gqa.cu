@@ -740,66 +740,113 @@ constexpr int kCombineWarps = 8;
 // O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c, with a running max so a
 // single pass over the pieces suffices; lane l owns dims [4l, 4l+4) of every
 // 128-dim group.  Written as bf16 (RNE).
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a) {
+// S warps per output row (S = 1, 2, 4 or 8): warp k of a row merges the row's
+// partials k, k + S, ..., then the S running states are merged through
+// shared memory.  S > 1 when a segment has many partials (few long requests),
+// so the merge of one row is no long serial chain.
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a, int S) {
+  __shared__ float st_o[kCombineWarps][512];
+  __shared__ float st_ml[kCombineWarps][2];
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const long long item = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = warp % S;
+  const long long item = (long long)blockIdx.x * (kCombineWarps / S) + warp / S;
   const int Hkv = a.d.num_kv_heads;
   const long long nitems = (long long)a.B * Hkv * a.R;
-  if (item >= nitems) return;
-  const int n = (int)(item % a.R);
-  const long long rh = item / a.R;
-  const int r = (int)(rh / Hkv), h = (int)(rh % Hkv);
-  const int Hs = a.Hs, HG = a.HG;
-  // segment (request, head group | row block) and row inside its partials
-  const bool latent = a.d.layout == KV_LAYOUT_LATENT;
-  const int hg = latent ? n / a.R8 : h / Hs, hw = latent ? 0 : h % Hs;
-  const int nl = latent ? n % a.R8 : n;
-  const long long seg = (long long)r * HG + hg;
-  if (a.ws.rq_skip[r] || a.ws.rq_bad[r]) return;  // aborted: output left untouched
   const int Dv = a.d.head_dim_v;
-  const int tq = n / a.G, hq = h * a.G + n % a.G;
-  uint16_t* out = a.out + (((long long)r * a.T + tq) * a.Hq + hq) * Dv;
-  const int32_t* pfx = a.ws.pfx;
-  const int np = pfx[r + 1] - pfx[r];
   const int ngroups = Dv / 128;  // Dv is 128 or 512
   float acc[4][4];
   float M = -INFINITY, L = 0.0f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
-  if (np > 0) {
-    const long long total = (long long)pfx[a.B] * HG;
-    const long long per = (total + a.grid - 1) / a.grid;
-    const long long start = (long long)HG * pfx[r] + (long long)hg * np;
-    const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
-    const long long slot0 = seg + c0;
-    const int R8 = a.R8;
+  // every warp reaches the block barrier below, so no early return
+  bool skip = item >= nitems;
+  int r = 0, h = 0, n = 0;
+  if (!skip) {
+    n = (int)(item % a.R);
+    const long long rh = item / a.R;
+    r = (int)(rh / Hkv);
+    h = (int)(rh % Hkv);
+    skip = a.ws.rq_skip[r] || a.ws.rq_bad[r];  // aborted: output left untouched
+  }
+  if (!skip) {
+    const int Hs = a.Hs, HG = a.HG;
+    // segment (request, head group | row block) and row inside its partials
+    const bool latent = a.d.layout == KV_LAYOUT_LATENT;
+    const int hg = latent ? n / a.R8 : h / Hs, hw = latent ? 0 : h % Hs;
+    const int nl = latent ? n % a.R8 : n;
+    const long long seg = (long long)r * HG + hg;
+    const int32_t* pfx = a.ws.pfx;
+    const int np = pfx[r + 1] - pfx[r];
+    if (np > 0) {
+      const long long total = (long long)pfx[a.B] * HG;
+      const long long per = (total + a.grid - 1) / a.grid;
+      const long long start = (long long)HG * pfx[r] + (long long)hg * np;
+      const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
+      const long long slot0 = seg + c0;
+      const int R8 = a.R8;
 #pragma unroll 2
-    for (int c = 0; c <= c1 - c0; ++c) {
-      const long long rowi = ((slot0 + c) * Hs + hw) * R8 + nl;
-      const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
-      float4 o[4];
+      for (int c = sub; c <= c1 - c0; c += S) {
+        const long long rowi = ((slot0 + c) * Hs + hw) * R8 + nl;
+        const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
+        float4 o[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < ngroups)
-          o[q] = *reinterpret_cast<const float4*>(a.ws.o_part + rowi * Dv + 128 * q + 4 * lane);
-      if (ml.x == -INFINITY) continue;  // piece saw nothing visible
-      const float Mn = fmaxf(M, ml.x);
-      const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
-      L = L * sa + ml.y * sb;
+        for (int q = 0; q < 4; ++q)
+          if (q < ngroups)
+            o[q] = *reinterpret_cast<const float4*>(a.ws.o_part + rowi * Dv + 128 * q + 4 * lane);
+        if (ml.x == -INFINITY) continue;  // piece saw nothing visible
+        const float Mn = fmaxf(M, ml.x);
+        const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
+        L = L * sa + ml.y * sb;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < ngroups) {
-          acc[q][0] = acc[q][0] * sa + o[q].x * sb;
-          acc[q][1] = acc[q][1] * sa + o[q].y * sb;
-          acc[q][2] = acc[q][2] * sa + o[q].z * sb;
-          acc[q][3] = acc[q][3] * sa + o[q].w * sb;
+        for (int q = 0; q < 4; ++q) {
+          if (q < ngroups) {
+            acc[q][0] = acc[q][0] * sa + o[q].x * sb;
+            acc[q][1] = acc[q][1] * sa + o[q].y * sb;
+            acc[q][2] = acc[q][2] * sa + o[q].z * sb;
+            acc[q][3] = acc[q][3] * sa + o[q].w * sb;
+          }
         }
+        M = Mn;
       }
-      M = Mn;
     }
   }
+  if (S > 1) {
+    if (lane == 0) {
+      st_ml[warp][0] = M;
+      st_ml[warp][1] = L;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q < ngroups)
+        *reinterpret_cast<float4*>(&st_o[warp][128 * q + 4 * lane]) =
+            make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+    __syncthreads();
+    if (sub == 0 && !skip) {
+      for (int k = 1; k < S; ++k) {
+        const float Mk = st_ml[warp + k][0], Lk = st_ml[warp + k][1];
+        if (Mk == -INFINITY) continue;
+        const float Mn = fmaxf(M, Mk);
+        const float sa = exp2f(M - Mn), sb = exp2f(Mk - Mn);
+        L = L * sa + Lk * sb;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q < ngroups) {
+            const float4 ok = *reinterpret_cast<const float4*>(&st_o[warp + k][128 * q + 4 * lane]);
+            acc[q][0] = acc[q][0] * sa + ok.x * sb;
+            acc[q][1] = acc[q][1] * sa + ok.y * sb;
+            acc[q][2] = acc[q][2] * sa + ok.z * sb;
+            acc[q][3] = acc[q][3] * sa + ok.w * sb;
+          }
+        }
+        M = Mn;
+      }
+    }
+  }
+  if (sub != 0 || skip) return;
+  const int tq = n / a.G, hq = h * a.G + n % a.G;
+  uint16_t* out = a.out + (((long long)r * a.T + tq) * a.Hq + hq) * Dv;
   const float inv = (M == -INFINITY) ? 0.0f : 1.0f / L;  // nothing visible: zeros
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -813,6 +860,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     }
   }
 }
+
 
 }  // namespace
 
@@ -864,9 +912,15 @@ cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int*
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* launches) {
   const long long items = (long long)a.B * a.d.num_kv_heads * a.R;
   if (items <= 0) return cudaSuccess;
-  const long long blocks = (items + kCombineWarps - 1) / kCombineWarps;
+  // partials of one segment: about 1 + grid / segments; give each merging
+  // warp at least two of them
+  const double pieces = 1.0 + (double)a.grid / ((double)a.B * a.HG);
+  int S = 1;
+  while (S < kCombineWarps && 4.0 * S <= pieces) S *= 2;
+  const long long per_cta = kCombineWarps / S;
+  const long long blocks = (items + per_cta - 1) / per_cta;
   const cudaError_t e =
-      launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, a);
+      launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, a, S);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
