@@ -25,7 +25,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-OK, ERR_INVALID_ARG, ERR_OUT_OF_PAGES, ERR_BAD_PAGE_ID = 0, 1, 4, 5
+OK, ERR_INVALID_ARG, ERR_OUT_OF_PAGES, ERR_BAD_PAGE_ID, ERR_TAG_MISMATCH = 0, 1, 4, 5, 8
 
 
 def build(force: bool = False) -> str:
@@ -74,6 +74,8 @@ def _load():
             )
             lib.or_append_latent.restype = i32
             lib.or_verify.argtypes = [i32, i32, vp, i32, vp, vp, i32, vp, vp]
+            lib.or_release.argtypes = [i32, vp, vp, i32, vp, vp, i32, vp, vp]
+            lib.or_release.restype = i32
             lib.or_attn_gqa.argtypes = (
                 [i32] * 6 + [vp] * 4 + [i32, i32, i32, vp, i32, vp, vp, vp, f32, vp, vp]
             )
@@ -187,6 +189,16 @@ def append(pool: Pool, k_new, v_new, new_indptr, max_new, page_table, exp_tags, 
             _p(np.ascontiguousarray(k_new, np.uint16)), _p(new_indptr), int(max_new),
             _p(page_table), _p(exp_tags), page_table.shape[1], _p(seq_lens), _p(stop))
     return int(st), int(stop[0])
+
+
+def release(pool: Pool, page_table, exp_tags, seq_lens, mask=None):
+    """Return the pages of the masked requests (all when mask is None) to the
+    free list.  Arrays are updated in place; returns the status."""
+    B = len(seq_lens)
+    m = None if mask is None else np.ascontiguousarray(mask, np.uint8)
+    return int(_load().or_release(pool.page_size, _p(pool.free_list), _p(pool.free_head), B,
+                                  _p(page_table), _p(exp_tags), page_table.shape[1],
+                                  _p(seq_lens), _p(m)))
 
 
 def verify(pool_num_pages, page_size, tags, page_table, exp_tags, seq_lens):

@@ -47,6 +47,7 @@
 #define OR_ERR_INVALID_ARG 1
 #define OR_ERR_OUT_OF_PAGES 4
 #define OR_ERR_BAD_PAGE_ID 5
+#define OR_ERR_TAG_MISMATCH 8
 
 /* ------------------------------------------------------------------------ */
 /* OFP8 E4M3 codec                                                           */
@@ -165,9 +166,17 @@ static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
  * order from free_list[free_head ...].  Each popped page p gets
  * tags[p] += 1 (mod 2^32); page_table[r][j] = p; exp_tags[r][j] = tags[p].
  *
+ * Before a request's rows go into its partly filled last page (n > 0 and
+ * L not a multiple of P), that page's recorded mapping is checked like a
+ * read: page_table[r][L/P] must be a page id in [0, num_pages) whose tag is
+ * still exp_tags[r][L/P]; a page reallocated since (its tag changed) is not
+ * written.
+ *
  * The call stops at the first request that cannot be served, and leaves
  * that request and every later one untouched:
  *   - n < 0, L < 0, n > max_new or L + n > max_pages * P  -> INVALID_ARG
+ *   - the partly filled page's id is out of range         -> BAD_PAGE_ID
+ *   - the partly filled page's tag differs                -> TAG_MISMATCH
  *   - not enough entries left in the free list             -> OUT_OF_PAGES
  *   - a popped entry is not a page id in [0, num_pages)    -> BAD_PAGE_ID
  * *stop_req receives the index of that request (B if every request was
@@ -189,6 +198,18 @@ int or_alloc(int num_pages, int page_size, uint32_t* tags,
     if (n < 0 || L < 0 || n > max_new || L + n > (int64_t)max_pages * P) {
       *stop_req = r;
       return OR_ERR_INVALID_ARG;
+    }
+    if (n > 0 && L % P != 0) {
+      int64_t jl = L / P;
+      int32_t p = page_table[(int64_t)r * max_pages + jl];
+      if (p < 0 || p >= num_pages) {
+        *stop_req = r;
+        return OR_ERR_BAD_PAGE_ID;
+      }
+      if (tags[p] != exp_tags[(int64_t)r * max_pages + jl]) {
+        *stop_req = r;
+        return OR_ERR_TAG_MISMATCH;
+      }
     }
     first = ceil_div64(L, P);
     need = ceil_div64(L + n, P) - first;
@@ -212,6 +233,55 @@ int or_alloc(int num_pages, int page_size, uint32_t* tags,
     }
     *free_head += (int32_t)need;
     seq_lens[r] = (int32_t)(L + n);
+  }
+  return OR_OK;
+}
+
+/*
+ * Release: the pages of finished requests go back to the pool (SFS,
+ * "Protecting a shared KV cache": a page's tag changes whenever it is
+ * reallocated, so once a released page is handed out again every mapping
+ * still recorded for it is stale).
+ *
+ * Requests r < B with mask[r] != 0 (every request when mask is NULL) are
+ * released, in request order.  Request r owns its first n_r = ceil(L_r / P)
+ * page-table entries, L_r = seq_lens[r].  Nothing changes when
+ *   - a released request has L_r < 0 or n_r > max_pages     -> INVALID_ARG
+ *   - the total T = sum of n_r exceeds *free_head (more pages
+ *     than the free list has handed out)                      -> INVALID_ARG.
+ * Otherwise *free_head -= T and the pages, in (request, page) order, are
+ * written to free_list[*free_head ...], so the next allocations pop them in
+ * that order (the free list is used as a stack).  Their page-table entries
+ * become -1, their expected tags 0, and seq_lens[r] = 0.  Page ids are
+ * returned as recorded: an id outside [0, num_pages) is refused when an
+ * append pops it.  Tags are not touched here; each page's tag changes when
+ * it is popped again.
+ */
+int or_release(int page_size, int32_t* free_list, int32_t* free_head, int B,
+               int32_t* page_table, uint32_t* exp_tags, int max_pages,
+               int32_t* seq_lens, const uint8_t* mask) {
+  int64_t P = page_size, total = 0, k = 0, j;
+  int r;
+  for (r = 0; r < B; ++r) {
+    int64_t L = seq_lens[r], n;
+    if (mask && !mask[r]) continue;
+    if (L < 0) return OR_ERR_INVALID_ARG;
+    n = ceil_div64(L, P);
+    if (n > max_pages) return OR_ERR_INVALID_ARG;
+    total += n;
+  }
+  if (total > *free_head) return OR_ERR_INVALID_ARG;
+  *free_head -= (int32_t)total;
+  for (r = 0; r < B; ++r) {
+    int64_t n;
+    if (mask && !mask[r]) continue;
+    n = ceil_div64(seq_lens[r], P);
+    for (j = 0; j < n; ++j) {
+      free_list[*free_head + k++] = page_table[(int64_t)r * max_pages + j];
+      page_table[(int64_t)r * max_pages + j] = -1;
+      exp_tags[(int64_t)r * max_pages + j] = 0;
+    }
+    seq_lens[r] = 0;
   }
   return OR_OK;
 }
