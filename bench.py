@@ -335,14 +335,15 @@ class Arm:
 
 # ------------------------------------------------------------ verify overhead
 
-def graph_overhead(arm: "Arm", replays: int) -> dict:
+def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
     """Cost of the page-tag check inside a whole step: two CUDA graphs of the
     same step structure, append -> verify -> split -> combine and append ->
     split -> combine with no abort mask, replayed alternately; overhead =
     median(with) / median(without) - 1.  All tags are valid, so both attend
     exactly the same requests.  Each replay is a real decode step (one more
     token per request)."""
-    kv, w, B, h = arm.kv, arm.w, arm.w.B, arm.pool.handle
+    kv, w, h = arm.kv, arm.w, arm.pool.handle
+    B = w.B if B is None else B
     k0, v0, q0 = arm.k_steps[0], arm.v_steps[0], arm.q_steps[0]
 
     def body(check: bool):
@@ -381,11 +382,12 @@ def graph_overhead(arm: "Arm", replays: int) -> dict:
     torch.cuda.synchronize()
     if arm.pool.error() != 0:
         raise RuntimeError(f"verify overhead: device error {kv.kv_status_string(arm.pool.error())}")
+    arm.lens[:B] += 2 + 2 * 3 + 2 * replays  # every run of the body appended one token
     t_with = [e[0].elapsed_time(e[1]) for e in ev]
     t_without = [e[1].elapsed_time(e[2]) for e in ev]
     mw, mo = statistics.median(t_with), statistics.median(t_without)
     del g_with, g_without
-    return {"workload": w.name, "replays": replays, "ms_with_verify": mw,
+    return {"workload": w.name, "requests": B, "replays": replays, "ms_with_verify": mw,
             "ms_without_verify": mo, "verify_overhead_pct": 100.0 * (mw / mo - 1.0),
             "mean_overhead_pct": 100.0 * (sum(t_with) / sum(t_without) - 1.0)}
 
@@ -417,13 +419,14 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
                           for i, k in enumerate(("append", "verify", "split", "combine"))}}
 
 
-def concurrency_sweep(device, steps: int, warmup: int, peak: float,
+def concurrency_sweep(device, steps: int, warmup: int, peak: float, replays: int,
                       points=(1, 8, 16, 32, 64)) -> dict:
     """The concurrency sweep: 1..64 requests of 131,072 tokens (64 q / 8 kv
     heads, D 128, P 16), e4m3 and bf16.  One pool per dtype is filled with 64
     requests; each point steps the first B of them."""
     out = {}
-    n_steps = len(points) * (steps + warmup) + 2
+    graph_points = (1, 8)
+    n_steps = len(points) * (steps + warmup) + 2 * len(graph_points) * (replays + 8) + 2
     for dtype, name in ((0, "e4m3"), (1, "bf16")):
         w = wl.concurrency(max(points))
         w.steps = n_steps
@@ -435,10 +438,46 @@ def concurrency_sweep(device, steps: int, warmup: int, peak: float,
             line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
             pts.append(line)
         out[name] = pts
+        if dtype == 0:  # the tag check at small batch, as CUDA graphs
+            out["verify_overhead_e4m3"] = [graph_overhead(arm, replays, B=b) for b in graph_points]
         del arm
         torch.cuda.empty_cache()
     out["workload"] = ("concurrency: B requests of 131,072 tokens, 64 q / 8 kv heads, head dim "
                        "128, page 16; step = append 1 token/request + tag check + attention")
+    return out
+
+
+def release_lines(arm: "Arm") -> list:
+    """kv_release_pages on a filled pool: a seeded 10% of the requests, then
+    all the others.  Algorithmic bytes: 16 per page (its id read, written to
+    the free list, its page-table entry and expected tag cleared)."""
+    w, B = arm.w, arm.w.B
+    P = w.page_size
+    sel = np.zeros(B, np.uint8)
+    sel[np.random.default_rng(w.seed + 7).choice(B, max(1, B // 10), replace=False)] = 1
+    ws = torch.empty(arm.kv.kv_release_workspace_size(B), dtype=torch.uint8, device=arm.device)
+    # an empty release first: loads the kernels, changes nothing
+    arm.pool.release(B, arm.pt, arm.et, arm.sl, torch.zeros(B, dtype=torch.uint8,
+                                                            device=arm.device), ws)
+    out = []
+    for name, mask in (("10% of requests", sel), ("the other 90%", 1 - sel)):
+        L = arm.sl.cpu().numpy().astype(np.int64)
+        pages = int((-(-L // P) * mask).sum())
+        m_d = torch.from_numpy(mask).to(arm.device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        # keep the GPU busy while the host enqueues, so the events time the
+        # kernels and not the launch calls
+        torch.cuda._sleep(1_000_000)
+        e0.record()
+        arm.pool.release(B, arm.pt, arm.et, arm.sl, m_d, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if arm.pool.error() != 0:
+            raise RuntimeError(f"release: {arm.kv.kv_status_string(arm.pool.error())}")
+        us = e0.elapsed_time(e1) * 1e3
+        out.append({"released": name, "requests": int(mask.sum()), "pages": pages, "us": us,
+                    "gbs": 16.0 * pages / (us * 1e3)})
     return out
 
 
@@ -469,6 +508,7 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float):
     line["aborted"] = sorted(stale)
     line["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
                         "32 q / 4 kv heads, head dim 128, page 16, e4m3; 3 stale requests abort")
+    line["release"] = release_lines(arm)
     del arm
     torch.cuda.empty_cache()
     return over, line
@@ -749,7 +789,7 @@ def main():
     # ---- concurrency sweep (1..64 requests at 128k), e4m3 and bf16
     conc = None
     if not args.no_sweep:
-        conc = concurrency_sweep(device, args.steps, args.warmup, peak)
+        conc = concurrency_sweep(device, args.steps, args.warmup, peak, args.overhead_replays)
 
     # ---- CPU oracle baseline (rank 0, bounded sample)
     cpu = None

@@ -55,7 +55,8 @@ typedef enum {
   KV_ERR_OUT_OF_PAGES = 4,  /* device: free list exhausted during an append */
   KV_ERR_BAD_PAGE_ID = 5,   /* device: a page id outside [0, num_pages) was met */
   KV_ERR_TIMEOUT = 6,       /* device: a bounded wait inside a kernel gave up */
-  KV_ERR_INTERNAL = 7       /* device: an internal consistency check failed (a library bug) */
+  KV_ERR_INTERNAL = 7,      /* device: an internal consistency check failed (a library bug) */
+  KV_ERR_TAG_MISMATCH = 8   /* device: append met a partly filled page whose tag changed */
 } kv_status;
 
 typedef enum { KV_DTYPE_E4M3 = 0, KV_DTYPE_BF16 = 1 } kv_dtype;
@@ -150,11 +151,16 @@ kv_status kv_pool_destroy(kv_pool* pool);
  * scale = amax/448 (IEEE fp32; 1.0 if that is 0) from the rows this call
  * writes into it, separately for K and V; a partly filled page keeps its
  * scale; each element becomes e4m3_rne_satfinite(x / scale).  bf16: the bits
- * are copied.  The first request that cannot be served (free list exhausted:
- * KV_ERR_OUT_OF_PAGES; bad free-list entry: KV_ERR_BAD_PAGE_ID; too many rows
- * for max_new_per_req or for its page table: KV_ERR_INVALID_ARG) and every
- * later request are left untouched; its index goes to ctl[KV_CTL_APPEND_STOP]
- * and the code to ctl[KV_CTL_ERROR].  Two kernel launches.
+ * are copied.  Before rows go into a request's partly filled last page (n > 0
+ * and L not a multiple of P) that mapping is checked like a read: the page
+ * id must be in range and its tag must still be the expected one, so a page
+ * reallocated since is never written.  The first request that cannot be
+ * served (free list exhausted: KV_ERR_OUT_OF_PAGES; bad free-list entry or
+ * out-of-range partly filled page: KV_ERR_BAD_PAGE_ID; partly filled page
+ * with a changed tag: KV_ERR_TAG_MISMATCH; too many rows for max_new_per_req
+ * or for its page table: KV_ERR_INVALID_ARG) and every later request are left
+ * untouched; its index goes to ctl[KV_CTL_APPEND_STOP] and the code to
+ * ctl[KV_CTL_ERROR].  Two kernel launches.
  */
 kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B,
                              const void* k_new, const void* v_new,
@@ -177,6 +183,41 @@ kv_status kv_verify_tags(kv_pool* pool, void* stream, int32_t B,
                          const int32_t* page_table, const uint32_t* exp_tags,
                          int32_t max_pages_per_req, const int32_t* seq_lens,
                          uint8_t* abort_mask);
+
+/* Bytes of device workspace kv_release_pages needs for B requests (the
+ * per-request offsets of the released pages). */
+size_t kv_release_workspace_size(int32_t B);
+
+/*
+ * Return the pages of finished requests to the pool (SFS "Protecting a
+ * shared KV cache": a page's tag changes whenever it is reallocated, so once
+ * a released page is handed out again every mapping still recorded for it
+ * fails the tag check).  No counterpart in the pages beyond that lifecycle;
+ * the free list is used as a stack.
+ *
+ *   page_table, exp_tags  [B][max_pages_per_req] (device, in/out)
+ *   seq_lens              int32 [B] (device, in/out)
+ *   release_mask          uint8 [B] (device): release request r iff nonzero;
+ *                         NULL releases every request.
+ *   workspace             device, >= kv_release_workspace_size(B) bytes,
+ *                         16-byte aligned, caller-owned scratch.
+ *
+ * Request r owns its first ceil(seq_lens[r]/P) page-table entries.  With T
+ * the total over the released requests, the free head moves down by T and
+ * the released pages, in (request, page) order, are written to
+ * free_list[head ...], so the next appends pop them in that order and bump
+ * their tags.  Their page-table entries become -1, their expected tags 0 and
+ * their seq_lens 0.  Page ids are returned as recorded; an id outside
+ * [0, num_pages) is refused later, when an append pops it.  Nothing changes,
+ * and ctl[KV_CTL_ERROR] gets KV_ERR_INVALID_ARG, when a released request has
+ * a negative length or one needing more than max_pages_per_req pages, or T
+ * exceeds the free head (more pages than the pool has handed out).  Tags are
+ * not touched.  Two kernel launches.
+ */
+kv_status kv_release_pages(kv_pool* pool, void* stream, int32_t B, int32_t* page_table,
+                           uint32_t* exp_tags, int32_t max_pages_per_req, int32_t* seq_lens,
+                           const uint8_t* release_mask, void* workspace,
+                           size_t workspace_bytes);
 
 /* Bytes of device workspace paged_decode_attn needs for this batch shape on
  * the current device (0 for invalid arguments or when no device is

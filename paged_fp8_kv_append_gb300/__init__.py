@@ -29,6 +29,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 # status codes
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA = 0, 1, 2, 3
 KV_ERR_OUT_OF_PAGES, KV_ERR_BAD_PAGE_ID, KV_ERR_TIMEOUT, KV_ERR_INTERNAL = 4, 5, 6, 7
+KV_ERR_TAG_MISMATCH = 8
 KV_DTYPE_E4M3, KV_DTYPE_BF16 = 0, 1
 KV_LAYOUT_GQA, KV_LAYOUT_LATENT = 0, 1
 KV_CTL_FREE_HEAD, KV_CTL_ERROR, KV_CTL_APPEND_STOP, KV_CTL_WAIT_INFO, KV_CTL_WORDS = 0, 1, 2, 3, 4
@@ -54,6 +55,10 @@ _lib.kv_append_quantize.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _v
 _lib.kv_append_quantize.restype = _i32
 _lib.kv_verify_tags.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp]
 _lib.kv_verify_tags.restype = _i32
+_lib.kv_release_workspace_size.argtypes = [_i32]
+_lib.kv_release_workspace_size.restype = _sz
+_lib.kv_release_pages.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _sz]
+_lib.kv_release_pages.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_vp, _i32, _i32, _i32]
 _lib.paged_decode_workspace_size.restype = _sz
 _lib.paged_decode_attn.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _f32,
@@ -155,6 +160,20 @@ def kv_verify_tags(handle, B, page_table, exp_tags, seq_lens, abort_mask, stream
         _ptr(exp_tags, _U32, "exp_tags"), int(page_table.shape[-1]),
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(abort_mask, torch.uint8, "abort_mask"))
     _check(st, "kv_verify_tags")
+
+
+def kv_release_workspace_size(B) -> int:
+    return int(_lib.kv_release_workspace_size(int(B)))
+
+
+def kv_release_pages(handle, B, page_table, exp_tags, seq_lens, release_mask, workspace,
+                     stream=None):
+    st = _lib.kv_release_pages(
+        handle, _stream(stream), int(B), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(exp_tags, _U32, "exp_tags"), int(page_table.shape[-1]),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(release_mask, torch.uint8, "release_mask"),
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()))
+    _check(st, "kv_release_pages")
 
 
 def paged_decode_workspace_size(handle, B, num_q_heads, q_tokens) -> int:
@@ -279,6 +298,10 @@ class KVPool:
 
     def verify(self, B, page_table, exp_tags, seq_lens, abort_mask, stream=None):
         kv_verify_tags(self.handle, B, page_table, exp_tags, seq_lens, abort_mask, stream)
+
+    def release(self, B, page_table, exp_tags, seq_lens, release_mask, workspace, stream=None):
+        kv_release_pages(self.handle, B, page_table, exp_tags, seq_lens, release_mask, workspace,
+                         stream)
 
     def workspace_size(self, B, num_q_heads, q_tokens) -> int:
         n = paged_decode_workspace_size(self.handle, B, num_q_heads, q_tokens)

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvfp8.so")
-SOURCES = ["api.cu", "append.cu", "verify.cu", "decode_gqa.cu", "decode_latent.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "append.cu", "verify.cu", "release.cu", "decode_gqa.cu", "decode_latent.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

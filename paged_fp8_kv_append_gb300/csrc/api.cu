@@ -254,6 +254,33 @@ kv_status kv_verify_tags(kv_pool* pool, void* stream, int32_t B, const int32_t* 
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
+size_t kv_release_workspace_size(int32_t B) { return B < 0 ? 0 : release_ws_bytes(B); }
+
+kv_status kv_release_pages(kv_pool* pool, void* stream, int32_t B, int32_t* page_table,
+                           uint32_t* exp_tags, int32_t max_pages_per_req, int32_t* seq_lens,
+                           const uint8_t* release_mask, void* workspace,
+                           size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  if (B < 0 || max_pages_per_req <= 0) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!page_table || !exp_tags || !seq_lens || !workspace) return KV_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || workspace_bytes < release_ws_bytes(B)) return KV_ERR_INVALID_ARG;
+  ReleaseArgs a;
+  a.d = pool->d;
+  a.B = B;
+  a.max_pages = max_pages_per_req;
+  a.page_table = page_table;
+  a.exp_tags = exp_tags;
+  a.seq_lens = seq_lens;
+  a.mask = release_mask;
+  a.offsets = static_cast<long long*>(workspace);
+  int n = 0;
+  const cudaError_t e = launch_release(a, static_cast<cudaStream_t>(stream), &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 size_t paged_decode_workspace_size(const kv_pool* pool, int32_t B, int32_t num_q_heads,
                                    int32_t q_tokens) {
   if (!pool || B < 0) return 0;
@@ -329,6 +356,7 @@ const char* kv_status_string(kv_status s) {
     case KV_ERR_BAD_PAGE_ID: return "KV_ERR_BAD_PAGE_ID";
     case KV_ERR_TIMEOUT: return "KV_ERR_TIMEOUT";
     case KV_ERR_INTERNAL: return "KV_ERR_INTERNAL";
+    case KV_ERR_TAG_MISMATCH: return "KV_ERR_TAG_MISMATCH";
   }
   return "KV_ERR_UNKNOWN";
 }

@@ -82,6 +82,16 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
       if (n < 0 || L < 0 || n > a.max_new || L + n > (long long)a.max_pages * P) {
         code = KV_ERR_INVALID_ARG;
       } else {
+        if (n > 0 && L % P != 0) {
+          // rows go into the partly filled last page: check its mapping like
+          // a read, so a page reallocated since is never written
+          const long long jl = L / P;
+          const int p = a.page_table[(long long)r * a.max_pages + jl];
+          if (p < 0 || p >= d.num_pages)
+            code = KV_ERR_BAD_PAGE_ID;
+          else if (d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jl])
+            code = KV_ERR_TAG_MISMATCH;
+        }
         first = (L + P - 1) / P;
         need = (L + n + P - 1) / P - first;
       }

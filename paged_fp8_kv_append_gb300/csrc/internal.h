@@ -41,6 +41,19 @@ struct VerifyArgs {
 };
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s, int* launches);
 
+// ---- release ------------------------------------------------------------
+struct ReleaseArgs {
+  kv_pool_desc d;
+  int32_t B, max_pages;
+  int32_t* page_table;
+  uint32_t* exp_tags;
+  int32_t* seq_lens;
+  const uint8_t* mask;   // NULL: every request
+  long long* offsets;    // workspace: [B+1] released-page prefix, then [1] base, [1] ok
+};
+size_t release_ws_bytes(int B);
+cudaError_t launch_release(const ReleaseArgs& a, cudaStream_t s, int* launches);
+
 // ---- decode -------------------------------------------------------------
 // Workspace carve-up (all offsets 256-byte aligned).
 struct DecodeWs {

@@ -91,6 +91,17 @@ class Both:
             self.et_h[r, j] = np.uint32(self.et_h[r, j]) - np.uint32(1)
         self.et_d.copy_(torch.from_numpy(self.et_h.view(np.int32)))
 
+    def release(self, mask=None):
+        """Release the masked requests' pages (all when mask is None) on both
+        sides; returns the oracle's status (the device's goes to ctl)."""
+        B = self.w.B
+        ws = torch.empty(self.kv.kv_release_workspace_size(B), dtype=torch.uint8,
+                         device=self.device)
+        m = None if mask is None else np.asarray(mask, np.uint8)
+        m_d = None if m is None else torch.from_numpy(m).to(self.device)
+        self.dev.release(B, self.pt_d, self.et_d, self.sl_d, m_d, ws)
+        return oracle.release(self.ref, self.pt_h, self.et_h, self.sl_h, m)
+
     # ---- state comparison (bit-exact)
     def assert_state_equal(self):
         d, r = self.dev, self.ref
@@ -114,6 +125,7 @@ class Both:
         assert np.array_equal(self.et_d.cpu().numpy().view(np.uint32), self.et_h), "exp_tags"
         assert np.array_equal(self.sl_d.cpu().numpy(), self.sl_h), "seq_lens"
         assert int(d.ctl[0].item()) == int(r.free_head[0]), "free_head"
+        assert np.array_equal(d.free_list.cpu().numpy(), r.free_list), "free_list"
 
     def verify(self):
         B = self.w.B

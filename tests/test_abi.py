@@ -81,3 +81,25 @@ def test_entry_points_reject_bad_arguments(kv):
         assert lib.kv_last_launch_count(h) == 0
     finally:
         kv.kv_pool_destroy(h)
+
+
+def test_release_argument_checks(kv):
+    """kv_release_pages refuses bad arguments before enqueuing anything."""
+    h = kv.kv_pool_create(_desc(kv))
+    lib = kv._lib
+    fake, ws = 0x10000, 0x20000
+    need = kv.kv_release_workspace_size(4)
+    assert need >= 8 * 5 and kv.kv_release_workspace_size(-1) == 0
+    try:
+        rel = lib.kv_release_pages
+        assert rel(None, None, 4, fake, fake, 8, fake, None, ws, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, -1, fake, fake, 8, fake, None, ws, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 4, fake, fake, 0, fake, None, ws, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 4, None, fake, 8, fake, None, ws, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 4, fake, fake, 8, fake, None, None, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 4, fake, fake, 8, fake, None, ws + 4, need) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 4, fake, fake, 8, fake, None, ws, need - 8) == kv.KV_ERR_INVALID_ARG
+        assert rel(h, None, 0, None, None, 8, None, None, None, 0) == kv.KV_OK  # nothing to do
+        assert kv.kv_status_string(kv.KV_ERR_TAG_MISMATCH) == "KV_ERR_TAG_MISMATCH"
+    finally:
+        kv.kv_pool_destroy(h)

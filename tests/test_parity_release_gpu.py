@@ -1,0 +1,123 @@
+"""GPU parity of the page lifecycle: kv_release_pages, reallocation of the
+released pages (tags bumped on re-pop), the stale mappings that then fail the
+tag check, and append's tag check on a partly filled page ("Smaller, faster,
+safer: running Kimi and GLM at scale", section "Protecting a shared KV
+cache").  Pool state is compared bit-exactly with the oracle, free list and
+free head included; attention after reuse within the usual tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from pathrun import Both, bf16_to_f64, close
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(lens, layout=0, seed=41):
+    lens = np.array(lens, np.int32)
+    if layout == 0:
+        npg = int((-(-lens.astype(np.int64) // 16)).sum()) + 40
+        return wl.Workload("lifecycle", seed, lens, 16, 4, 128, 128, 16, 1, 0, npg,
+                           float(np.float32(1 / np.sqrt(128))), steps=1200)
+    npg = int((-(-lens.astype(np.int64) // 64)).sum()) + 16
+    return wl.Workload("lifecycle_latent", seed, lens, 16, 1, 576, 512, 64, 4, 1, npg,
+                       float(np.float32(1 / np.sqrt(576))), steps=1200)
+
+
+def _check_attn(b, q):
+    out, ref, written = b.attn(q, None, None)
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    for r in range(b.w.B):
+        if written[r]:
+            ok, mabs, mrel, _ = close(got[r], ref[r])
+            assert ok, f"request {r}: max abs {mabs:.3g} max rel {mrel:.3g}"
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_release_reuse_and_stale_mappings(dtype):
+    w = _w([37, 300, 64, 1000, 5, 129], seed=41 + dtype)
+    b = Both(w, dtype)
+    assert b.fill()[0] == 0
+    old = (b.pt_h.copy(), b.et_h.copy(), b.sl_h.copy())
+    mask = np.array([1, 0, 1, 0, 0, 1], np.uint8)
+    assert b.release(mask) == 0
+    torch.cuda.synchronize()
+    assert b.dev.error() == 0
+    b.assert_state_equal()
+    assert b.sl_h.tolist() == [0, 300, 0, 1000, 5, 0]
+    # the released requests start again; together they re-pop every released page
+    news = np.array([200, 0, 90, 0, 0, 70], np.int64)
+    ks, vs = [], []
+    for r in range(w.B):
+        k, v = wl.kv_rows(w, r, 0, int(news[r]), device="cuda", tag=7)
+        ks.append(k)
+        vs.append(v)
+    assert b.append(ks, vs, news) == (0, w.B)
+    torch.cuda.synchronize()
+    assert b.dev.error() == 0
+    b.assert_state_equal()
+    # the mappings recorded before the release are stale now: tag check aborts them
+    pt_o, et_o, sl_o = (torch.from_numpy(old[0]).cuda(), torch.from_numpy(old[1].view(np.int32))
+                        .cuda(), torch.from_numpy(old[2]).cuda())
+    m_d = torch.zeros(w.B, dtype=torch.uint8, device="cuda")
+    b.dev.verify(w.B, pt_o, et_o, sl_o, m_d)
+    import oracle
+    m_h = oracle.verify(b.ref.num_pages, w.page_size, b.ref.tags, old[0], old[1], old[2])
+    assert np.array_equal(m_d.cpu().numpy(), m_h)
+    assert m_h.tolist() == mask.tolist()
+    # the live mappings pass, and attention over the reused pages matches
+    m_d, m_h = b.verify()
+    assert not m_h.any() and np.array_equal(m_d.cpu().numpy(), m_h)
+    _check_attn(b, wl.queries(w, device="cuda"))
+
+
+def test_release_all_and_refill_latent():
+    w = _w([700, 64, 130, 2], layout=1)
+    b = Both(w, 0)
+    assert b.fill()[0] == 0
+    assert b.release(None) == 0
+    torch.cuda.synchronize()
+    b.assert_state_equal()
+    assert int(b.dev.ctl[0].item()) == 0
+    assert b.fill(lens=np.array([65, 500, 1, 64], np.int32), tag=3)[0] == 0
+    torch.cuda.synchronize()
+    b.assert_state_equal()
+    _check_attn(b, wl.queries(w, device="cuda"))
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_append_stops_at_a_reallocated_partial_page(dtype):
+    w = _w([37, 300, 64, 1000, 5, 129], seed=43)
+    b = Both(w, dtype)
+    b.fill()
+    torch.cuda.synchronize()
+    # request 3's partly filled page (1000 = 62 * 16 + 8) changed hands
+    p = int(b.pt_h[3, 1000 // 16])
+    b.ref.tags[p] += np.uint32(1)
+    b.dev.tags[p] += 1
+    ks, vs = [], []
+    for r in range(w.B):
+        k, v = wl.kv_rows(w, r, int(b.sl_h[r]), 1, device="cuda", tag=9)
+        ks.append(k)
+        vs.append(v)
+    st, stop = b.append(ks, vs, np.ones(w.B, np.int64))
+    torch.cuda.synchronize()
+    assert (st, stop) == (b.kv.KV_ERR_TAG_MISMATCH, 3)
+    assert b.dev.error() == b.kv.KV_ERR_TAG_MISMATCH
+    assert int(b.dev.ctl[2].item()) == 3
+    b.assert_state_equal()  # requests 0..2 appended, 3..5 untouched
+
+
+def test_release_refused_when_more_than_handed_out():
+    w = _w([37, 300, 64], seed=44)
+    b = Both(w, 0)
+    b.fill()
+    torch.cuda.synchronize()
+    head = int(b.ref.free_head[0])
+    b.ref.free_head[0] = head - 2  # both sides believe fewer pages were handed out
+    b.dev.ctl[0] = head - 2
+    assert b.release(None) == b.kv.KV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert b.dev.error() == b.kv.KV_ERR_INVALID_ARG
+    b.assert_state_equal()  # nothing changed
