@@ -333,6 +333,56 @@ class Arm:
         return t0.elapsed_time(t1), h2d, d2h
 
 
+# ------------------------------------------------------------ bulk append
+
+def bulk_append_line(w: wl.Workload, dtype: int, device, peak: float) -> dict:
+    """One kv_append_quantize call that fills every request of a workload
+    from empty (the prefill-to-decode handoff: bf16 rows in, e4m3 or bf16
+    pages out).  Algorithmic bytes: the bf16 rows read, the cache bytes
+    written, and for e4m3 one fp32 scale per (page, kv head, K|V) written."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    B, P = w.B, w.page_size
+    pool = kv.KVPool(w.num_pages, P, w.num_kv_heads, w.head_dim_k, w.head_dim_v, dtype=dtype,
+                     layout=w.layout, device=device, tags=wl.initial_tags(w),
+                     free_list=wl.free_list(w))
+    mp = w.max_pages
+    pt = torch.full((B, mp), -1, dtype=torch.int32, device=device)
+    et = torch.zeros((B, mp), dtype=torch.int32, device=device)
+    sl = torch.zeros(B, dtype=torch.int32, device=device)
+    lens = w.lens.astype(np.int64)
+    ks, vs = [], []
+    for r in range(B):
+        k, v = wl.kv_rows(w, r, 0, int(lens[r]), device=device)
+        ks.append(k)
+        vs.append(v)
+    k_all = torch.cat(ks)
+    v_all = torch.cat(vs) if w.layout == 0 else None
+    del ks, vs
+    ind = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(1_000_000)
+    e0.record()
+    pool.append(B, k_all, v_all, ind, int(lens.max()), pt, et, sl)
+    e1.record()
+    torch.cuda.synchronize()
+    if pool.error() != 0:
+        raise RuntimeError(f"bulk append: {kv.kv_status_string(pool.error())}")
+    ms = e0.elapsed_time(e1)
+    rows = int(lens.sum())
+    width = w.num_kv_heads * (w.head_dim_k + (w.head_dim_v if w.layout == 0 else 0))
+    pages = int((-(-lens // P)).sum())
+    out_b = rows * width * (1 if dtype == 0 else 2)
+    scales = pages * (w.num_kv_heads * 2 if w.layout == 0 else 1) * 4 if dtype == 0 else 0
+    byt = rows * width * 2 + out_b + scales
+    del pool, k_all, v_all
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "cache": "e4m3" if dtype == 0 else "bf16", "rows": rows,
+            "ms": ms, "rows_per_s": rows / (ms / 1e3), "gbs": byt / (ms * 1e6),
+            "pct_of_measured": 100.0 * byt / (ms * 1e6) / peak, "bytes": byt}
+
+
 # ------------------------------------------------------------ verify overhead
 
 def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
@@ -659,6 +709,8 @@ def main():
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the CUDA-graph verify-overhead measurement")
     ap.add_argument("--overhead-replays", type=int, default=20)
+    ap.add_argument("--no-bulk", action="store_true",
+                    help="skip the bulk-append (prefill handoff) lines")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the 1..64-request concurrency sweep at 128k")
     ap.add_argument("--latent-only", type=int, default=0, metavar="B",
@@ -786,6 +838,12 @@ def main():
         overhead["skewed"], skewed = skewed_lines(device, args.overhead_replays, args.steps,
                                                   args.warmup, peak)
 
+    # ---- bulk append (prefill handoff): the whole GQA batch and latent workloads
+    bulk = None
+    if not args.no_bulk:
+        bulk = [bulk_append_line(w, 0, device, peak), bulk_append_line(w, 1, device, peak),
+                bulk_append_line(wl.latent_verify(), 0, device, peak)]
+
     # ---- concurrency sweep (1..64 requests at 128k), e4m3 and bf16
     conc = None
     if not args.no_sweep:
@@ -823,6 +881,7 @@ def main():
         "verify_share_pct": float(100.0 * per[:, 1].mean() / step_ms),
         "verify_overhead": overhead,
         "skewed_step": skewed,
+        "bulk_append": bulk,
         "concurrency": conc,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

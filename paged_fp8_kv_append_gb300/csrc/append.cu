@@ -19,6 +19,8 @@
 //     (K and V separately), scale = amax/448 (IEEE division; 1 when 0), and stores
 //     e4m3(x / scale) with round-to-nearest-even and saturation; a page that
 //     already held rows keeps its scale.  bf16 pools copy the bits.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,12 +55,25 @@ __device__ long long block_incl_scan(long long v, long long* warp_sums) {
   return r;
 }
 
+// Index of the request whose popped-page range [incl[r] - need[r], incl[r])
+// holds flattened page g of the chunk: the first r with incl[r] > g.
+__device__ __forceinline__ int owner_of(const long long* incl, int n, long long g) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (incl[mid] > g) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
   __shared__ long long warp_sums[32];
+  __shared__ long long s_incl[kPlanThreads];  // inclusive prefix of pages popped in the chunk
+  __shared__ long long s_first[kPlanThreads]; // first new logical page of each request
   __shared__ int s_stop, s_code;
-  __shared__ long long s_consumed_at_stop, s_chunk_total;
+  __shared__ long long s_badg;
   const kv_pool_desc& d = a.d;
   const long long P = d.page_size;
   const long long head0 = a.d.ctl[KV_CTL_FREE_HEAD];
@@ -74,6 +89,7 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
 
   for (int base = 0; base < a.B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
+    const int nreq = min(kPlanThreads, a.B - base);
     long long need = 0, L = 0, n = 0, first = 0;
     int code = 0;
     if (r < a.B) {
@@ -98,51 +114,53 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     }
     const long long incl = block_incl_scan(need, warp_sums);
     const long long excl = incl - need;
-    const long long pos0 = head0 + consumed + excl;  // this request's free-list slice
-    if (r < a.B && code == 0) {
-      if (pos0 + need > d.num_pages) {
-        code = KV_ERR_OUT_OF_PAGES;
-      } else {
-        for (long long j = 0; j < need; ++j) {
-          const int p = d.free_list[pos0 + j];
-          if (p < 0 || p >= d.num_pages) {
-            code = KV_ERR_BAD_PAGE_ID;
-            break;
-          }
-        }
-      }
-    }
+    const long long pool0 = head0 + consumed;  // free-list position of the chunk's first pop
+    if (r < a.B && code == 0 && pool0 + incl > d.num_pages) code = KV_ERR_OUT_OF_PAGES;
+    s_incl[threadIdx.x] = incl;
+    s_first[threadIdx.x] = first;
     if (threadIdx.x == 0) {
       s_stop = a.B;
       s_code = 0;
+      s_badg = LLONG_MAX;
     }
     __syncthreads();
+    const long long chunk_total = s_incl[nreq - 1];
+    // every entry the chunk would pop, all threads at once: the first one
+    // that is not a page id marks its request
+    for (long long g = threadIdx.x; g < chunk_total && pool0 + g < d.num_pages; g += kPlanThreads) {
+      const int p = d.free_list[pool0 + g];
+      if (p < 0 || p >= d.num_pages) atomicMin(reinterpret_cast<unsigned long long*>(&s_badg),
+                                               (unsigned long long)g);
+    }
+    __syncthreads();
+    if (s_badg != LLONG_MAX && r < a.B && code == 0 &&
+        threadIdx.x == owner_of(s_incl, nreq, s_badg))
+      code = KV_ERR_BAD_PAGE_ID;
     if (code != 0) atomicMin(&s_stop, r);
     __syncthreads();
     const int chunk_stop = s_stop;
-    if (r == chunk_stop) {
-      s_code = code;
-      s_consumed_at_stop = excl;
-    }
-    if (threadIdx.x == kPlanThreads - 1) s_chunk_total = incl;
+    if (r == chunk_stop) s_code = code;
     __syncthreads();
-    if (r < a.B && r < chunk_stop) {
-      for (long long j = 0; j < need; ++j) {
-        const int p = d.free_list[pos0 + j];
-        const uint32_t t = d.tags[p] + 1u;  // wraps mod 2^32
-        d.tags[p] = t;
-        a.page_table[(long long)r * a.max_pages + first + j] = p;
-        a.exp_tags[(long long)r * a.max_pages + first + j] = t;
-      }
-      a.seq_lens[r] = (int32_t)(L + n);
+    // pages popped by the requests before the stopping one
+    const int si = chunk_stop - base;
+    const long long served =
+        chunk_stop < a.B ? (si > 0 ? s_incl[si - 1] : 0) : chunk_total;
+    for (long long g = threadIdx.x; g < served; g += kPlanThreads) {
+      const int i = owner_of(s_incl, nreq, g);
+      const long long j = s_first[i] + g - (i > 0 ? s_incl[i - 1] : 0);
+      const int p = d.free_list[pool0 + g];
+      const uint32_t t = d.tags[p] + 1u;  // wraps mod 2^32
+      d.tags[p] = t;
+      a.page_table[(long long)(base + i) * a.max_pages + j] = p;
+      a.exp_tags[(long long)(base + i) * a.max_pages + j] = t;
     }
+    if (r < a.B && r < chunk_stop) a.seq_lens[r] = (int32_t)(L + n);
+    consumed += served;
     if (chunk_stop < a.B) {
-      consumed += s_consumed_at_stop;
       stop = chunk_stop;
       stop_code = s_code;
       break;
     }
-    consumed += s_chunk_total;
     __syncthreads();
   }
   if (threadIdx.x == 0) {
@@ -336,6 +354,205 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
   }
 }
 
+// ---- register-resident paths (the common shapes) ----------------------------
+//
+// Bulk appends (a prefill handed to the decode cache) touch every page of a
+// request; these paths read each source byte once.  A GQA (page, kv head,
+// K|V) tile of up to 4096 values sits in one warp's registers: amax by a warp
+// reduction, then quantise and store from the registers.  One CTA takes 8
+// tiles of a page (one per warp).  A latent page (up to 64 rows of up to 576 values)
+// is split over the CTA's 8 warps by row, with a block-wide amax.
+
+constexpr int kTileWarps = 8;
+constexpr int kTileChunks = 16;  // 16-byte source chunks per lane (P * D <= 4096)
+constexpr int kLatChunks = 18;   // per lane: ceil(8 rows * 72 chunks / 32)
+
+__device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, int D, bool fp8,
+                          bool fresh, float* scale_slot, uint8_t* dst, bool dim_major, int P,
+                          int slot0, uint8_t* wtile) {
+  const int lane = threadIdx.x & 31;
+  const int cpr = D / 8, total = nrows * cpr;
+  uint4 v[kTileChunks];
+#pragma unroll
+  for (int t = 0; t < kTileChunks; ++t) {
+    const int q = lane + 32 * t;
+    v[t] = q < total ? *reinterpret_cast<const uint4*>(src + (q / cpr) * src_stride + 8 * (q % cpr))
+                     : make_uint4(0, 0, 0, 0);
+  }
+  float s = 1.0f;
+  if (fp8) {
+    if (fresh) {
+      float m = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kTileChunks; ++t) m = fmaxf(m, amax8(v[t]));
+      s = scale_from_amax(warp_max(m));
+      if (lane == 0) *scale_slot = s;
+    } else {
+      s = *scale_slot;
+    }
+  }
+  if (!dim_major) {
+#pragma unroll
+    for (int t = 0; t < kTileChunks; ++t) {
+      const int q = lane + 32 * t;
+      if (q < total) {
+        const long long o = (long long)(slot0 + q / cpr) * D + 8 * (q % cpr);
+        if (fp8)
+          *reinterpret_cast<uint2*>(dst + o) = quant8(v[t], s);
+        else
+          *reinterpret_cast<uint4*>(dst + 2 * o) = v[t];
+      }
+    }
+    return;
+  }
+  // dim-major destination: element (row i, dim dd) at (dd * P + slot0 + i),
+  // assembled in this warp's shared tile
+#pragma unroll
+  for (int t = 0; t < kTileChunks; ++t) {
+    const int q = lane + 32 * t;
+    if (q < total) {
+      const int i = q / cpr, c = q % cpr;
+      const int o = 8 * c * P + slot0 + i;
+      if (fp8) {
+        const uint2 c8 = quant8(v[t], s);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          wtile[o + k * P] = (uint8_t)(((k < 4 ? c8.x : c8.y) >> (8 * (k & 3))) & 0xFFu);
+      } else {
+        const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+        uint16_t* t16 = reinterpret_cast<uint16_t*>(wtile);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t16[o + k * P] = (uint16_t)(w[k >> 1] >> (16 * (k & 1)));
+      }
+    }
+  }
+  __syncwarp();
+  const int es = fp8 ? 1 : 2;
+  if (nrows == P && (D * P * es) % 16 == 0) {
+    for (int k = lane; k < D * P * es / 16; k += 32)
+      reinterpret_cast<uint4*>(dst)[k] = reinterpret_cast<const uint4*>(wtile)[k];
+  } else {
+    for (int e = lane; e < D * nrows; e += 32) {
+      const int o = (e / nrows) * P + slot0 + e % nrows;
+      if (fp8)
+        dst[o] = wtile[o];
+      else
+        reinterpret_cast<uint16_t*>(dst)[o] = reinterpret_cast<const uint16_t*>(wtile)[o];
+    }
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t wtiles[];
+  const kv_pool_desc& d = a.d;
+  const int r = blockIdx.x;
+  if (r >= d.ctl[KV_CTL_APPEND_STOP]) return;
+  const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+  if (n <= 0) return;
+  const long long P = d.page_size;
+  const long long Lnew = a.seq_lens[r];
+  const long long L0 = Lnew - n;
+  const bool fp8 = d.dtype == KV_DTYPE_E4M3;
+  const int es = fp8 ? 1 : 2;
+  const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* wtile = wtiles + (size_t)warp * Dv * P * es;
+  for (long long jp = L0 / P + blockIdx.y; jp * P < Lnew; jp += gridDim.y) {
+    const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
+    const int nrows = (int)(pos_hi - pos_lo);
+    const int slot0 = (int)(pos_lo - jp * P);
+    const long long row0 = a.new_indptr[r] + (pos_lo - L0);
+    const int p = a.page_table[(long long)r * a.max_pages + jp];
+    if (p < 0 || p >= d.num_pages) {
+      if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+      return;  // uniform across the block
+    }
+    const bool fresh = jp * P >= L0;  // popped by this call
+    // CTA z takes tiles 8z .. 8z+7 of the page (tile 2h = K of head h, 2h+1 = V)
+    for (int t = blockIdx.z * kTileWarps + warp; t < 2 * H; t += kTileWarps * gridDim.z) {
+      const int h = t >> 1;
+      if ((t & 1) == 0) {
+        tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
+                  fp8 ? d.k_scale + (long long)p * H + h : nullptr,
+                  static_cast<uint8_t*>(d.k_cache) + (((long long)p * H + h) * P * Dk) * es,
+                  false, (int)P, slot0, wtile);
+      } else {
+        tile_warp(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
+                  fp8 ? d.v_scale + (long long)p * H + h : nullptr,
+                  static_cast<uint8_t*>(d.v_cache) + (((long long)p * H + h) * Dv * P) * es,
+                  true, (int)P, slot0, wtile);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[kTileWarps];
+  const kv_pool_desc& d = a.d;
+  const int r = blockIdx.x;
+  if (r >= d.ctl[KV_CTL_APPEND_STOP]) return;
+  const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+  if (n <= 0) return;
+  const long long P = d.page_size;
+  const long long Lnew = a.seq_lens[r];
+  const long long L0 = Lnew - n;
+  const int Dk = d.head_dim_k, cpr = Dk / 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (long long jp = L0 / P + blockIdx.y; jp * P < Lnew; jp += gridDim.y) {
+    const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
+    const int nrows = (int)(pos_hi - pos_lo);
+    const int slot0 = (int)(pos_lo - jp * P);
+    const long long row0 = a.new_indptr[r] + (pos_lo - L0);
+    const int p = a.page_table[(long long)r * a.max_pages + jp];
+    if (p < 0 || p >= d.num_pages) {
+      if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+      return;  // uniform across the block
+    }
+    const bool fresh = jp * P >= L0;
+    // warp w takes rows w, w + 8, ... of this call's rows in the page
+    const int my_rows = nrows > warp ? (nrows - warp + kTileWarps - 1) / kTileWarps : 0;
+    const int total = my_rows * cpr;
+    uint4 v[kLatChunks];
+#pragma unroll
+    for (int t = 0; t < kLatChunks; ++t) {
+      const int q = lane + 32 * t;
+      const int i = warp + kTileWarps * (q / cpr);
+      v[t] = q < total ? *reinterpret_cast<const uint4*>(a.k_new + (row0 + i) * Dk + 8 * (q % cpr))
+                       : make_uint4(0, 0, 0, 0);
+    }
+    float s;
+    if (fresh) {
+      float m = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kLatChunks; ++t) m = fmaxf(m, amax8(v[t]));
+      m = warp_max(m);
+      if (lane == 0) red[warp] = m;
+      __syncthreads();
+      m = lane < kTileWarps ? red[lane] : 0.0f;
+      s = scale_from_amax(warp_max(m));
+      if (threadIdx.x == 0) d.k_scale[p] = s;
+      __syncthreads();  // red is reused by the next page
+    } else {
+      s = d.k_scale[p];
+    }
+    uint8_t* dst = static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk;
+#pragma unroll
+    for (int t = 0; t < kLatChunks; ++t) {
+      const int q = lane + 32 * t;
+      if (q < total) {
+        const int i = warp + kTileWarps * (q / cpr);
+        *reinterpret_cast<uint2*>(dst + (long long)(slot0 + i) * Dk + 8 * (q % cpr)) =
+            quant8(v[t], s);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
@@ -347,6 +564,33 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   long long pieces = (a.max_new + 2 * P - 2) / P;
   if (pieces <= 0 || a.B <= 0) return cudaSuccess;
   if (pieces > 65535) pieces = 65535;  // the kernel strides over the rest
+  const long long Pl = a.d.page_size;
+  const int es = a.d.dtype == KV_DTYPE_E4M3 ? 1 : 2;
+  // The register-resident kernels are large: a decode-size append (a few
+  // rows per request, a handful of CTAs) spends its time fetching their
+  // instructions, so it takes the compact per-tile kernel below.
+  const bool bulk = a.max_new >= 2 * Pl;
+  if (bulk && a.d.layout == KV_LAYOUT_GQA && Pl * a.d.head_dim_k <= 32 * 8 * kTileChunks &&
+      Pl * a.d.head_dim_v <= 32 * 8 * kTileChunks) {
+    const size_t smem = (size_t)kTileWarps * a.d.head_dim_v * Pl * es;
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(append_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    const unsigned groups = (unsigned)((2 * a.d.num_kv_heads + kTileWarps - 1) / kTileWarps);
+    e = launch_pdl(append_gqa_kernel, dim3((unsigned)a.B, (unsigned)pieces, groups),
+                   dim3(kTileWarps * 32), smem, s, a);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+  }
+  if (bulk && a.d.layout == KV_LAYOUT_LATENT && Pl <= 8 * kTileWarps &&
+      (long long)((Pl + kTileWarps - 1) / kTileWarps) * (a.d.head_dim_k / 8) <= 32 * kLatChunks) {
+    e = launch_pdl(append_latent_kernel, dim3((unsigned)a.B, (unsigned)pieces),
+                   dim3(kTileWarps * 32), 0, s, a);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+  }
   const size_t tile_bytes = a.d.layout == KV_LAYOUT_GQA
                                 ? (size_t)a.d.head_dim_v * a.d.page_size *
                                       (a.d.dtype == KV_DTYPE_E4M3 ? 1 : 2)

@@ -177,3 +177,29 @@ def test_bf16_inputs_exhaustive_codes_scale_one():
     torch.cuda.synchronize()
     assert np.all(b.ref.k_scale[b.pt_h[0, : rows.shape[0] // P], 0] == 1.0)
     b.assert_state_equal()
+
+
+@pytest.mark.parametrize("bad_at", [None, 0.7])
+def test_append_many_requests_and_a_bad_free_list_entry(bad_at):
+    """1500 requests (two chunks of the planner), short ragged lengths; with
+    bad_at, a free-list entry 70% of the way in is not a page id: the call
+    stops at the request that would pop it, earlier ones are served, and the
+    pool state matches the oracle bit for bit."""
+    rng = np.random.default_rng(17)
+    lens = rng.integers(0, 41, 1500).astype(np.int32)
+    need = int((-(-lens.astype(np.int64) // 16)).sum())
+    w = wl.Workload("many", 123, lens, 4, 2, 128, 128, 16, 1, 0, need + 50,
+                    float(np.float32(0.088)))
+    free = wl.free_list(w).copy()
+    if bad_at is not None:
+        free[int(bad_at * need)] = -7
+    b = Both(w, 0, free=free)
+    st, stop = b.fill()
+    torch.cuda.synchronize()
+    if bad_at is None:
+        assert (st, stop) == (0, w.B) and b.dev.error() == 0
+    else:
+        assert st == b.kv.KV_ERR_BAD_PAGE_ID and 0 < stop < w.B
+        assert b.dev.error() == b.kv.KV_ERR_BAD_PAGE_ID
+        assert int(b.dev.ctl[2].item()) == stop
+    b.assert_state_equal()
