@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "quant.cuh"
 
 namespace kvfp8 {
 
@@ -172,10 +173,6 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
 
 constexpr int kDataThreads = 256;
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) {
-  return __uint_as_float((b & 0xFFFFu) << 16);
-}
-
 __device__ float block_max(float v, float* red) {
   v = warp_max(v);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -190,39 +187,6 @@ __device__ float block_max(float v, float* red) {
   float r = red[8];
   __syncthreads();
   return r;
-}
-
-// e4m3 codes of x / scale for two values (x0 -> low byte): IEEE fp32
-// division, then the hardware round-to-nearest-even saturating conversion.
-__device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale) {
-  const float2 q = make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3)) & 0xFFFFu;
-}
-
-// Scale of a fresh block: amax / 448 in fp32; 1 when that is 0.
-__device__ __forceinline__ float scale_from_amax(float amax) {
-  const float s = __fdiv_rn(amax, 448.0f);
-  return s > 0.0f ? s : 1.0f;
-}
-
-__device__ __forceinline__ float amax8(uint4 v) {
-  float m = 0.0f;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[k])));
-    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[k] >> 16)));
-  }
-  return m;
-}
-
-// 8 bf16 values -> 8 e4m3 codes (byte k = element k)
-__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) c[k] = quant2(bf16_bits_to_f32(w[k]), bf16_bits_to_f32(w[k] >> 16), s);
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 // One block of rows for one (page, kv head, K-or-V): `nrows` source rows of
@@ -254,6 +218,7 @@ __device__ void append_block(const uint16_t* src, long long src_stride, int nrow
       s = *scale_slot;
     }
   }
+  const float rs = __frcp_rn(s);
   for (int i0 = 0; i0 < nrows; i0 += rpp) {
     const int i = i0 + i_off;
     if (!(active && i < nrows)) continue;
@@ -261,13 +226,13 @@ __device__ void append_block(const uint16_t* src, long long src_stride, int nrow
     if (!dim_major) {
       if (fp8)
         *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + (long long)(slot0 + i) * D + 8 * c) =
-            quant8(v, s);
+            quant8_rs(v, s, rs);
       else
         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst) + (long long)(slot0 + i) * D + 8 * c) = v;
     } else {
       const int slot = slot0 + i;
       if (fp8) {
-        const uint2 q = quant8(v, s);
+        const uint2 q = quant8_rs(v, s, rs);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           tile[(8 * c + k) * P + slot] = (uint8_t)(((k < 4 ? q.x : q.y) >> (8 * (k & 3))) & 0xFFu);
@@ -358,19 +323,97 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
 //
 // Bulk appends (a prefill handed to the decode cache) touch every page of a
 // request; these paths read each source byte once.  A GQA (page, kv head,
-// K|V) tile of up to 4096 values sits in one warp's registers: amax by a warp
+// K|V) tile of up to 2048 values sits in one warp's registers: amax by a warp
 // reduction, then quantise and store from the registers.  One CTA takes 8
 // tiles of a page (one per warp).  A latent page (up to 64 rows of up to 576 values)
 // is split over the CTA's 8 warps by row, with a block-wide amax.
 
 constexpr int kTileWarps = 8;
-constexpr int kTileChunks = 16;  // 16-byte source chunks per lane (P * D <= 4096)
+constexpr int kTileChunks = 8;   // 16-byte source chunks per lane (P * D <= 2048)
 constexpr int kLatChunks = 18;   // per lane: ceil(8 rows * 72 chunks / 32)
+
+// A whole 16-token page of a 128-dim V tile, transposed in registers: lane l
+// loads dims 4l..4l+3 of every row and writes those 4 dim rows of 16 slots.
+__device__ void v_page_16x128(const uint16_t* src, long long src_stride, bool fp8,
+                              float* scale_slot, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+  uint2 x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    x[i] = *reinterpret_cast<const uint2*>(src + i * src_stride + 4 * lane);
+  if (!fp8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a = k < 2 ? x[2 * j].x : x[2 * j].y, b = k < 2 ? x[2 * j + 1].x
+                                                                      : x[2 * j + 1].y;
+        w[j] = (k & 1) ? __byte_perm(a, b, 0x7632) : __byte_perm(a, b, 0x5410);
+      }
+      uint4* o = reinterpret_cast<uint4*>(dst + (4 * lane + k) * 32);
+      o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    return;
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(amax2(x[i].x), amax2(x[i].y)));
+  const float s = scale_from_amax(warp_max(m)), rs = __frcp_rn(s);
+  if (lane == 0) *scale_slot = s;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = k < 2 ? x[2 * j].x : x[2 * j].y, b = k < 2 ? x[2 * j + 1].x
+                                                                    : x[2 * j + 1].y;
+      c[j] = (k & 1) ? quant2_rs(bf16_hi(a), bf16_hi(b), s, rs)
+                     : quant2_rs(bf16_lo(a), bf16_lo(b), s, rs);
+    }
+    *reinterpret_cast<uint4*>(dst + (4 * lane + k) * 16) =
+        make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
+                   c[6] | (c[7] << 16));
+  }
+}
+
+// A whole 16-token page of a 128-dim K tile (token-major): lane l holds
+// dims 8 (l % 16) .. +7 of rows l / 16, l / 16 + 2, ...
+__device__ void k_page_16x128(const uint16_t* src, long long src_stride, bool fp8,
+                              float* scale_slot, uint8_t* dst) {
+  const int lane = threadIdx.x & 31, c = lane & 15, i0 = lane >> 4;
+  uint4 x[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    x[t] = *reinterpret_cast<const uint4*>(src + (2 * t + i0) * src_stride + 8 * c);
+  if (!fp8) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      *reinterpret_cast<uint4*>(dst + ((2 * t + i0) * 128 + 8 * c) * 2) = x[t];
+    return;
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) m = fmaxf(m, amax8(x[t]));
+  const float s = scale_from_amax(warp_max(m)), rs = __frcp_rn(s);
+  if (lane == 0) *scale_slot = s;
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    *reinterpret_cast<uint2*>(dst + (2 * t + i0) * 128 + 8 * c) = quant8_rs(x[t], s, rs);
+}
 
 __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, int D, bool fp8,
                           bool fresh, float* scale_slot, uint8_t* dst, bool dim_major, int P,
                           int slot0, uint8_t* wtile) {
   const int lane = threadIdx.x & 31;
+  if (nrows == 16 && P == 16 && D == 128) {  // a whole page (fresh by construction)
+    if (dim_major)
+      v_page_16x128(src, src_stride, fp8, scale_slot, dst);
+    else
+      k_page_16x128(src, src_stride, fp8, scale_slot, dst);
+    return;
+  }
   const int cpr = D / 8, total = nrows * cpr;
   uint4 v[kTileChunks];
 #pragma unroll
@@ -391,6 +434,7 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
       s = *scale_slot;
     }
   }
+  const float rs = __frcp_rn(s);
   if (!dim_major) {
 #pragma unroll
     for (int t = 0; t < kTileChunks; ++t) {
@@ -398,7 +442,7 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
       if (q < total) {
         const long long o = (long long)(slot0 + q / cpr) * D + 8 * (q % cpr);
         if (fp8)
-          *reinterpret_cast<uint2*>(dst + o) = quant8(v[t], s);
+          *reinterpret_cast<uint2*>(dst + o) = quant8_rs(v[t], s, rs);
         else
           *reinterpret_cast<uint4*>(dst + 2 * o) = v[t];
       }
@@ -414,7 +458,7 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
       const int i = q / cpr, c = q % cpr;
       const int o = 8 * c * P + slot0 + i;
       if (fp8) {
-        const uint2 c8 = quant8(v[t], s);
+        const uint2 c8 = quant8_rs(v[t], s, rs);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           wtile[o + k * P] = (uint8_t)(((k < 4 ? c8.x : c8.y) >> (8 * (k & 3))) & 0xFFu);
@@ -540,6 +584,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
     } else {
       s = d.k_scale[p];
     }
+    const float rs = __frcp_rn(s);
     uint8_t* dst = static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk;
 #pragma unroll
     for (int t = 0; t < kLatChunks; ++t) {
@@ -547,7 +592,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
       if (q < total) {
         const int i = warp + kTileWarps * (q / cpr);
         *reinterpret_cast<uint2*>(dst + (long long)(slot0 + i) * Dk + 8 * (q % cpr)) =
-            quant8(v[t], s);
+            quant8_rs(v[t], s, rs);
       }
     }
   }
