@@ -295,6 +295,47 @@ class Arm:
                                f"barrier={(info >> 6) & 1} stage={info & 63}; dtype={self.dtype})")
         return total_ms, per, lens_timed, int(sum(launches))
 
+    def run_graphs(self, steps: int, warmup: int):
+        """The next warmup + steps steps as CUDA graphs, one per step's inputs
+        (a serving loop replays its decode step the same way), replayed in
+        order; each replay is a real decode step.  Returns the timed steps'
+        total ms."""
+        kv, w, h, B = self.kv, self.w, self.pool.handle, self.w.B
+
+        def body(s):
+            self.pool.append(B, self.k_steps[s], self.v_steps[s], self.ones, 1, self.pt,
+                             self.et, self.sl)
+            self.pool.verify(B, self.pt, self.et, self.sl, self.mask)
+            kv.paged_decode_attn_split(h, B, w.num_q_heads, w.q_tokens, self.q_steps[s],
+                                       self.pt, self.sl, self.mask, w.sm_scale, self.ws)
+            kv.paged_decode_attn_combine(h, B, w.num_q_heads, w.q_tokens, self.mask, self.out,
+                                         self.ws)
+
+        s0, n = self.step_no, steps + warmup
+        torch.cuda.synchronize()
+        graphs = []
+        for i in range(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(s0 + i)
+            graphs.append(g)
+        for i in range(warmup):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(warmup, n):
+            graphs[i].replay()
+        t1.record()
+        torch.cuda.synchronize()
+        if self.pool.error() != 0:
+            raise RuntimeError(f"graph steps: {self.kv.kv_status_string(self.pool.error())}")
+        self.step_no += n
+        self.lens += n
+        del graphs
+        return t0.elapsed_time(t1)
+
     def run_e2e(self, steps: int, warmup: int):
         """Same steps through host buffers: H2D of the new rows and the queries
         from pinned memory, D2H of the outputs and abort mask, all timed."""
@@ -771,7 +812,7 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    total_steps = 2 * (args.steps + args.warmup)
+    total_steps = 3 * (args.steps + args.warmup)
     graph_steps = 0 if args.no_overhead else 2 * (args.overhead_replays + 8)
     w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + graph_steps + 2)
     if args.batch != w.B:
@@ -781,6 +822,7 @@ def main():
     arm = Arm(w, 0, device, total_steps)
     sampler = ClockSampler(smi_index(local))
     total_ms, per, lens_timed, launches = arm.run(args.steps, args.warmup)
+    graph_ms = arm.run_graphs(args.steps, args.warmup)
     clocks = sampler.stop()
     e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup)
     overhead = None
@@ -789,9 +831,11 @@ def main():
     del arm
     torch.cuda.empty_cache()
 
-    max_ms = reduce_max(total_ms)
+    eager_ms = reduce_max(total_ms)
+    max_ms = reduce_max(graph_ms)
     tokens = reduce_sum(args.steps * w.B * w.q_tokens)
     value = tokens / (max_ms / 1e3)
+    eager_value = tokens / (eager_ms / 1e3)
     e2e_value = tokens / (reduce_max(e2e_ms) / 1e3)
     split_ms = per[:, 2]
     attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_timed]
@@ -872,6 +916,9 @@ def main():
             "batch": w.B, "mean_context": float(w.lens.mean()), "kv_bytes_per_step":
                 int(np.mean(attn_bytes)), "l2": "inputs larger than L2 (>1.2 GB of KV per step)",
             "parallelism": f"dp{ws} replicas" if ws > 1 else "1 GPU"},
+        "step_mode": "each step replayed as a CUDA graph (one per step's inputs); eager_value: "
+                     "the same steps launched one call at a time",
+        "eager_value": eager_value, "eager_ms_per_step": eager_ms / args.steps,
         "attn_gbs": attn_gbs,
         "attn_pct_of_8000": 100.0 * attn_gbs / NOMINAL_HBM_GBS,
         "kernel_us": {"append": float(per[:, 0].mean() * 1e3),
