@@ -754,6 +754,9 @@ def main():
                     help="skip the bulk-append (prefill handoff) lines")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the 1..64-request concurrency sweep at 128k")
+    ap.add_argument("--conc-only", type=int, default=0, metavar="B",
+                    help="run only the e4m3 step on B requests of 131,072 tokens and print its "
+                         "line (small profiling captures)")
     ap.add_argument("--latent-only", type=int, default=0, metavar="B",
                     help="run only the latent verify workload with B requests and print its "
                          "line (small profiling captures)")
@@ -793,6 +796,15 @@ def main():
                     "d2h_bytes_per_step": 0},
         }
         print(json.dumps(line))
+        return
+
+    if args.conc_only > 0:
+        device = torch.device("cuda", local)
+        w = wl.concurrency(args.conc_only)
+        w.steps = args.steps + args.warmup + 2
+        w.num_pages = int(w.B * (-(-(131072 + w.steps) // 16))) + 64
+        arm = Arm(w, 0, device, args.steps + args.warmup)
+        print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
         return
 
     if args.latent_only > 0:
