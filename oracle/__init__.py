@@ -66,11 +66,11 @@ def _load():
             lib.or_alloc.argtypes = [i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp, vp]
             lib.or_alloc.restype = i32
             lib.or_append_gqa.argtypes = (
-                [i32] * 6 + [vp] * 7 + [i32] + [vp, vp, vp, i32, vp, vp, i32, vp, vp]
+                [i32] * 6 + [vp] * 7 + [i32] + [vp, vp, vp, i32, vp, vp, i32, vp, vp, i32]
             )
             lib.or_append_gqa.restype = i32
             lib.or_append_latent.argtypes = (
-                [i32, i32, i32] + [vp] * 5 + [i32, vp, vp, i32, vp, vp, i32, vp, vp]
+                [i32, i32, i32] + [vp] * 5 + [i32, vp, vp, i32, vp, vp, i32, vp, vp, i32]
             )
             lib.or_append_latent.restype = i32
             lib.or_verify.argtypes = [i32, i32, vp, i32, vp, vp, i32, vp, vp]
@@ -131,8 +131,9 @@ class Pool:
     """
 
     def __init__(self, num_pages, page_size, num_kv_heads, dk, dv, dtype=0,
-                 layout=0, tags=None, free_list=None):
+                 layout=0, tags=None, free_list=None, scale_mode=0):
         self.num_pages, self.page_size = int(num_pages), int(page_size)
+        self.scale_mode = int(scale_mode)  # 0: frozen scales; 1: re-quantise
         self.num_kv_heads, self.dk, self.dv = int(num_kv_heads), int(dk), int(dv)
         self.dtype, self.layout = int(dtype), int(layout)
         edt = np.uint8 if dtype == 0 else np.uint16
@@ -181,13 +182,14 @@ def append(pool: Pool, k_new, v_new, new_indptr, max_new, page_table, exp_tags, 
             _p(pool.tags), _p(pool.free_list), _p(pool.free_head), B,
             _p(np.ascontiguousarray(k_new, np.uint16)), _p(np.ascontiguousarray(v_new, np.uint16)),
             _p(new_indptr), int(max_new), _p(page_table), _p(exp_tags), page_table.shape[1],
-            _p(seq_lens), _p(stop))
+            _p(seq_lens), _p(stop), pool.scale_mode)
     else:
         st = lib.or_append_latent(
             pool.num_pages, pool.page_size, pool.dk, _p(pool.k_cache), _p(pool.k_scale),
             _p(pool.tags), _p(pool.free_list), _p(pool.free_head), B,
             _p(np.ascontiguousarray(k_new, np.uint16)), _p(new_indptr), int(max_new),
-            _p(page_table), _p(exp_tags), page_table.shape[1], _p(seq_lens), _p(stop))
+            _p(page_table), _p(exp_tags), page_table.shape[1], _p(seq_lens), _p(stop),
+            pool.scale_mode)
     return int(st), int(stop[0])
 
 

@@ -290,6 +290,25 @@ int or_release(int page_size, int32_t* free_list, int32_t* free_head, int B,
 /* Append with quantise-on-write                                             */
 /* ------------------------------------------------------------------------ */
 
+/*
+ * scale_mode 1 (re-quantise; the default mode 0 keeps a block's scale frozen
+ * at its first write, and later rows saturate at +-448 * scale).  When the
+ * rows an append writes into a partly filled (page, kv head, K|V) block need
+ * a larger scale, s_new = or_scale_from_amax(amax of those rows) > s_old,
+ * the block takes s_new and each code c already in it is re-encoded:
+ * v = fp32(decode(c) * s_old), c' = encode(v / s_new) (fp32 division, e4m3
+ * RNE with saturation), so those values are rounded a second time.  This
+ * re-encodes n codes at codes[i * stride].
+ */
+static void requant_codes(uint8_t* codes, int64_t n, int64_t stride, float s_old,
+                          float s_new) {
+  int64_t i;
+  for (i = 0; i < n; ++i) {
+    float v = (float)or_e4m3_decode(codes[i * stride]) * s_old;
+    codes[i * stride] = (uint8_t)or_quantize(v, s_new);
+  }
+}
+
 /* byte offset of element (p, h, slot, d) in the GQA K cache / V cache */
 static int64_t k_off(int64_t p, int64_t h, int64_t slot, int64_t d, int64_t H,
                      int64_t P, int64_t D) {
@@ -324,7 +343,7 @@ int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
                   const uint16_t* k_new, const uint16_t* v_new,
                   const int32_t* new_indptr, int max_new, int32_t* page_table,
                   uint32_t* exp_tags, int max_pages, int32_t* seq_lens,
-                  int32_t* stop_req) {
+                  int32_t* stop_req, int scale_mode) {
   int64_t P = page_size, H = num_kv_heads;
   int32_t* old_len = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
   uint8_t* fresh = (uint8_t*)calloc((size_t)num_pages, 1);
@@ -363,6 +382,33 @@ int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
             }
             k_scale[p * H + h] = or_scale_from_amax(ka);
             v_scale[p * H + h] = or_scale_from_amax(va);
+          } else if (scale_mode == 1) {
+            int64_t n_old = pos_lo - jp * P;  /* slots already written */
+            float ka = 0.0f, va = 0.0f, kn, vn;
+            for (pos = pos_lo; pos < pos_hi; ++pos) {
+              int64_t row = row0 + (pos - L0);
+              for (d = 0; d < Dk; ++d) {
+                float x = fabsf(bf16_to_f32(k_new[(row * H + h) * Dk + d]));
+                if (x > ka) ka = x;
+              }
+              for (d = 0; d < Dv; ++d) {
+                float x = fabsf(bf16_to_f32(v_new[(row * H + h) * Dv + d]));
+                if (x > va) va = x;
+              }
+            }
+            kn = or_scale_from_amax(ka);
+            vn = or_scale_from_amax(va);
+            if (kn > k_scale[p * H + h]) {  /* K rows: Dk codes per slot */
+              requant_codes(k_cache + k_off(p, h, 0, 0, H, P, Dk), n_old * Dk, 1,
+                            k_scale[p * H + h], kn);
+              k_scale[p * H + h] = kn;
+            }
+            if (vn > v_scale[p * H + h]) {  /* V: per dim, its slots are contiguous */
+              for (d = 0; d < Dv; ++d)
+                requant_codes(v_cache + v_off(p, h, 0, d, H, P, Dv), n_old, 1,
+                              v_scale[p * H + h], vn);
+              v_scale[p * H + h] = vn;
+            }
           }
           ks = k_scale[p * H + h];
           vs = v_scale[p * H + h];
@@ -406,7 +452,7 @@ int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
                      int32_t* free_head, int B, const uint16_t* kv_new,
                      const int32_t* new_indptr, int max_new,
                      int32_t* page_table, uint32_t* exp_tags, int max_pages,
-                     int32_t* seq_lens, int32_t* stop_req) {
+                     int32_t* seq_lens, int32_t* stop_req, int scale_mode) {
   int64_t P = page_size;
   int32_t* old_len = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
   uint8_t* fresh = (uint8_t*)calloc((size_t)num_pages, 1);
@@ -437,6 +483,20 @@ int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
           }
         }
         scale[p] = or_scale_from_amax(a);
+      } else if (scale_mode == 1) {
+        float a = 0.0f;
+        for (pos = pos_lo; pos < pos_hi; ++pos) {
+          int64_t row = row0 + (pos - L0);
+          for (d = 0; d < Dk; ++d) {
+            float x = fabsf(bf16_to_f32(kv_new[row * Dk + d]));
+            if (x > a) a = x;
+          }
+        }
+        if (or_scale_from_amax(a) > scale[p]) {  /* the rows already written */
+          requant_codes(cache + p * P * Dk, (pos_lo - jp * P) * Dk, 1, scale[p],
+                        or_scale_from_amax(a));
+          scale[p] = or_scale_from_amax(a);
+        }
       }
       s = scale[p];
       for (pos = pos_lo; pos < pos_hi; ++pos) {

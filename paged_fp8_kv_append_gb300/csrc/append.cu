@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
       }
     }
     const long long incl = block_incl_scan(need, warp_sums);
-    const long long excl = incl - need;
     const long long pool0 = head0 + consumed;  // free-list position of the chunk's first pop
     if (r < a.B && code == 0 && pool0 + incl > d.num_pages) code = KV_ERR_OUT_OF_PAGES;
     s_incl[threadIdx.x] = incl;
