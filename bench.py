@@ -191,13 +191,14 @@ class ClockSampler:
 class Arm:
     """One pool (e4m3 or bf16) filled with the workload, ready to step."""
 
-    def __init__(self, w: wl.Workload, dtype: int, device, total_steps: int):
+    def __init__(self, w: wl.Workload, dtype: int, device, total_steps: int, scale_mode=0):
         import paged_fp8_kv_append_gb300 as kv
 
         self.kv, self.w, self.dtype, self.device = kv, w, dtype, device
         self.pool = kv.KVPool(w.num_pages, w.page_size, w.num_kv_heads, w.head_dim_k,
                               w.head_dim_v, dtype=dtype, layout=w.layout, device=device,
-                              tags=wl.initial_tags(w), free_list=wl.free_list(w))
+                              tags=wl.initial_tags(w), free_list=wl.free_list(w),
+                              scale_mode=scale_mode)
         B, mp = w.B, w.max_pages
         self.pt = torch.full((B, mp), -1, dtype=torch.int32, device=device)
         self.et = torch.zeros((B, mp), dtype=torch.int32, device=device)
@@ -422,6 +423,67 @@ def bulk_append_line(w: wl.Workload, dtype: int, device, peak: float) -> dict:
     return {"workload": w.name, "cache": "e4m3" if dtype == 0 else "bf16", "rows": rows,
             "ms": ms, "rows_per_s": rows / (ms / 1e3), "gbs": byt / (ms * 1e6),
             "pct_of_measured": 100.0 * byt / (ms * 1e6) / peak, "bytes": byt}
+
+
+# ------------------------------------------------------------ re-quantising scale mode
+
+def dequant_rel_error(pool, pt, lens, src_k, P: int) -> float:
+    """Worst per-row relative error of the dequantised K rows of the last
+    appended token of every request against the bf16 rows appended:
+    max |deq - x| / max |x| over each (request, kv head) row."""
+    import paged_fp8_kv_append_gb300 as kv  # noqa: F401
+
+    worst = 0.0
+    for r in range(len(lens)):
+        pos = int(lens[r]) - 1
+        p = int(pt[r, pos // P].item())
+        codes = pool.k_cache[p, :, pos % P, :]                       # [Hkv][D] uint8
+        deq = codes.view(torch.float8_e4m3fn).float() * pool.k_scale[p][:, None]
+        x = src_k[r].float()                                          # [Hkv][D]
+        err = (deq - x).abs().amax(dim=1) / x.abs().amax(dim=1).clamp_min(1e-30)
+        worst = max(worst, float(err.max()))
+    return worst
+
+
+def requant_lines(device, steps: int, warmup: int, w: wl.Workload) -> dict:
+    """KV_SCALE_REQUANTIZE: the decode step's append with it on the GQA batch,
+    and its effect on a stream whose single-token rows grow 1.35x per step
+    (frozen scales saturate the larger rows; re-quantised ones keep them)."""
+    arm = Arm(w, 0, device, steps + warmup, scale_mode=1)
+    _, per, _, _ = arm.run(steps, warmup, sync_ranks=False)
+    out = {"append_us_requantize": float(per[:, 0].mean() * 1e3)}
+    del arm
+    torch.cuda.empty_cache()
+    # accuracy on a growing stream: 32 requests of 20 rows, then 16 growing steps
+    import paged_fp8_kv_append_gb300 as kv
+
+    lens = np.full(32, 20, np.int32)
+    sw = wl.Workload("growth", 20267, lens, 64, 8, 128, 128, 16, 1, 0, 32 * 4 + 64,
+                     float(np.float32(1 / np.sqrt(128))), steps=20)
+    for mode in (0, 1):
+        pool = kv.KVPool(sw.num_pages, 16, 8, 128, 128, dtype=0, layout=0, device=device,
+                         tags=wl.initial_tags(sw), free_list=wl.free_list(sw), scale_mode=mode)
+        B, mp = sw.B, sw.max_pages
+        pt = torch.full((B, mp), -1, dtype=torch.int32, device=device)
+        et = torch.zeros((B, mp), dtype=torch.int32, device=device)
+        sl = torch.zeros(B, dtype=torch.int32, device=device)
+        k0 = torch.cat([wl.kv_rows(sw, r, 0, 20, device=device)[0] for r in range(B)])
+        v0 = torch.cat([wl.kv_rows(sw, r, 0, 20, device=device)[1] for r in range(B)])
+        ind = torch.arange(0, 21 * B, 20, dtype=torch.int32, device=device)[:B + 1]
+        pool.append(B, k0, v0, ind, 20, pt, et, sl)
+        ones = torch.arange(B + 1, dtype=torch.int32, device=device)
+        worst = 0.0
+        for st in range(16):
+            k, v = wl.step_rows(sw, st, device=device)
+            g = 1.35 ** (st + 1)
+            k, v = (k.float() * g).to(torch.bfloat16), (v.float() * g).to(torch.bfloat16)
+            pool.append(B, k, v, ones, 1, pt, et, sl)
+            worst = max(worst, dequant_rel_error(pool, pt, sl.cpu().numpy(), k, 16))
+        out[f"stream_max_rel_error_{'requantize' if mode else 'frozen'}"] = worst
+        del pool
+    out["stream"] = ("32 requests of 20 rows, then 16 single-token steps whose rows grow 1.35x "
+                     "per step; worst per-row relative error of the newest K row, dequantised")
+    return out
 
 
 # ------------------------------------------------------------ verify overhead
@@ -750,6 +812,8 @@ def main():
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the CUDA-graph verify-overhead measurement")
     ap.add_argument("--overhead-replays", type=int, default=20)
+    ap.add_argument("--no-requant", action="store_true",
+                    help="skip the re-quantising scale mode lines")
     ap.add_argument("--no-bulk", action="store_true",
                     help="skip the bulk-append (prefill handoff) lines")
     ap.add_argument("--no-sweep", action="store_true",
@@ -894,6 +958,12 @@ def main():
         overhead["skewed"], skewed = skewed_lines(device, args.overhead_replays, args.steps,
                                                   args.warmup, peak)
 
+    # ---- re-quantising scale mode (decode-step append cost, accuracy effect)
+    requant = None
+    if not args.no_requant:
+        requant = requant_lines(device, args.steps, args.warmup, w)
+        requant["append_us_frozen"] = float(per[:, 0].mean() * 1e3)
+
     # ---- bulk append (prefill handoff): the whole GQA batch and latent workloads
     bulk = None
     if not args.no_bulk:
@@ -941,6 +1011,7 @@ def main():
         "verify_overhead": overhead,
         "skewed_step": skewed,
         "bulk_append": bulk,
+        "requantize": requant,
         "concurrency": conc,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -70,6 +70,18 @@ typedef enum {
   KV_LAYOUT_LATENT = 1
 } kv_layout;
 
+/* How an append treats a partly filled e4m3 block (page, kv head, K|V; a
+ * whole page for the latent layout) whose new rows need a larger scale. */
+typedef enum {
+  /* the scale stays as its first write set it; larger rows saturate at
+   * +-448 * scale (the default) */
+  KV_SCALE_FROZEN = 0,
+  /* the block takes scale = amax/448 of the new rows and its codes already
+   * written are re-encoded: code' = e4m3(fp32(decode(code) * old) / new),
+   * rounding those values a second time */
+  KV_SCALE_REQUANTIZE = 1
+} kv_scale_mode;
+
 /* Slots of the pool's int32 control block (device memory, KV_CTL_WORDS
  * ints, caller-owned; zero it when creating a pool). */
 enum {
@@ -114,6 +126,7 @@ typedef struct {
   uint32_t* tags;
   int32_t* free_list;
   int32_t* ctl;
+  int32_t scale_mode;  /* kv_scale_mode (e4m3 pools; ignored for bf16) */
 } kv_pool_desc;
 
 typedef struct kv_pool kv_pool; /* opaque host handle */

@@ -32,6 +32,7 @@ KV_ERR_OUT_OF_PAGES, KV_ERR_BAD_PAGE_ID, KV_ERR_TIMEOUT, KV_ERR_INTERNAL = 4, 5,
 KV_ERR_TAG_MISMATCH = 8
 KV_DTYPE_E4M3, KV_DTYPE_BF16 = 0, 1
 KV_LAYOUT_GQA, KV_LAYOUT_LATENT = 0, 1
+KV_SCALE_FROZEN, KV_SCALE_REQUANTIZE = 0, 1
 KV_CTL_FREE_HEAD, KV_CTL_ERROR, KV_CTL_APPEND_STOP, KV_CTL_WAIT_INFO, KV_CTL_WORDS = 0, 1, 2, 3, 4
 
 
@@ -43,6 +44,7 @@ class kv_pool_desc(ctypes.Structure):
         ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
         ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
         ("tags", ctypes.c_void_p), ("free_list", ctypes.c_void_p), ("ctl", ctypes.c_void_p),
+        ("scale_mode", ctypes.c_int32),
     ]
 
 
@@ -238,8 +240,9 @@ class KVPool:
 
     def __init__(self, num_pages, page_size, num_kv_heads, head_dim_k, head_dim_v,
                  dtype=KV_DTYPE_E4M3, layout=KV_LAYOUT_GQA, device="cuda", tags=None,
-                 free_list=None):
+                 free_list=None, scale_mode=KV_SCALE_FROZEN):
         dev = torch.device(device)
+        self.scale_mode = int(scale_mode)
         self.num_pages, self.page_size = int(num_pages), int(page_size)
         self.num_kv_heads, self.head_dim_k, self.head_dim_v = (
             int(num_kv_heads), int(head_dim_k), int(head_dim_v))
@@ -276,6 +279,7 @@ class KVPool:
         d.v_scale = self.v_scale.data_ptr() if self.v_scale is not None else None
         d.tags, d.free_list, d.ctl = (self.tags.data_ptr(), self.free_list.data_ptr(),
                                       self.ctl.data_ptr())
+        d.scale_mode = self.scale_mode
         self.desc = d
         self.handle = kv_pool_create(d)
 

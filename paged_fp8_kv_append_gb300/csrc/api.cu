@@ -170,6 +170,8 @@ kv_status kv_pool_create(const kv_pool_desc* desc, kv_pool** out) {
     return KV_ERR_INVALID_ARG;
   if (d.dtype != KV_DTYPE_E4M3 && d.dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
   if (d.layout != KV_LAYOUT_GQA && d.layout != KV_LAYOUT_LATENT) return KV_ERR_INVALID_ARG;
+  if (d.scale_mode != KV_SCALE_FROZEN && d.scale_mode != KV_SCALE_REQUANTIZE)
+    return KV_ERR_INVALID_ARG;
   if (!d.k_cache || !d.tags || !d.free_list || !d.ctl) return KV_ERR_INVALID_ARG;
   if (!aligned16(d.k_cache) || !aligned16(d.tags) || !aligned16(d.free_list) ||
       !aligned16(d.ctl))

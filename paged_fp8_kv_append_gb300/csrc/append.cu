@@ -188,6 +188,23 @@ __device__ float block_max(float v, float* red) {
   return r;
 }
 
+// KV_SCALE_REQUANTIZE: the code c of a block whose scale grows from s_old
+// to s_new becomes e4m3(fp32(decode(c) * s_old) / s_new) (IEEE divide).
+__device__ __forceinline__ uint8_t requant_code(uint8_t c, float s_old, float s_new) {
+  const float v = __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3))), s_old);
+  return (uint8_t)(e4m3x2(__fdiv_rn(v, s_new), 0.0f) & 0xFFu);
+}
+
+// Re-encode the n_old slots already written in a block (token-major: rows of
+// D codes; dim-major: D rows of P slots), threads tid, tid + nthreads, ...
+__device__ void requant_block(uint8_t* dst, int n_old, int D, bool dim_major, int P, float s_old,
+                              float s_new, int tid, int nthreads) {
+  for (int e = tid; e < n_old * D; e += nthreads) {
+    const int o = dim_major ? (e / n_old) * P + e % n_old : e;
+    dst[o] = requant_code(dst[o], s_old, s_new);
+  }
+}
+
 // One block of rows for one (page, kv head, K-or-V): `nrows` source rows of
 // D bf16 values, row i at src + i * src_stride (elements).  Pass 1 finds the
 // amax (fresh e4m3 blocks only), pass 2 quantises (or copies) and stores.
@@ -196,7 +213,8 @@ __device__ float block_max(float v, float* red) {
 // assembled in shared memory and written one dim row at a time.
 __device__ void append_block(const uint16_t* src, long long src_stride, int nrows, int D,
                              bool fp8, bool fresh, float* scale_slot, void* dst,
-                             bool dim_major, int P, int slot0, uint8_t* tile, float* red) {
+                             bool dim_major, int P, int slot0, uint8_t* tile, float* red,
+                             bool requant) {
   const int tpr = D / 8;                       // threads per row (16-byte loads)
   const int rpp = kDataThreads / tpr;          // rows per pass
   const int c = threadIdx.x % tpr, i_off = threadIdx.x / tpr;
@@ -215,6 +233,22 @@ __device__ void append_block(const uint16_t* src, long long src_stride, int nrow
       if (threadIdx.x == 0) *scale_slot = s;
     } else {
       s = *scale_slot;
+      if (requant) {  // a larger scale for the new rows: re-encode the old ones
+        float m = 0.0f;
+        for (int i0 = 0; i0 < nrows; i0 += rpp) {
+          const int i = i0 + i_off;
+          if (active && i < nrows)
+            m = fmaxf(m, amax8(*reinterpret_cast<const uint4*>(src + i * src_stride + 8 * c)));
+        }
+        const float s_new = scale_from_amax(block_max(m, red));
+        if (s_new > s) {
+          requant_block(static_cast<uint8_t*>(dst), slot0, D, dim_major, P, s, s_new,
+                        threadIdx.x, kDataThreads);
+          __syncthreads();  // every thread has read the old scale
+          if (threadIdx.x == 0) *scale_slot = s_new;
+          s = s_new;
+        }
+      }
     }
   }
   const float rs = __frcp_rn(s);
@@ -283,6 +317,7 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
   const long long Lnew = a.seq_lens[r];
   const long long L0 = Lnew - n;
   const bool fp8 = d.dtype == KV_DTYPE_E4M3;
+  const bool requant = fp8 && d.scale_mode == KV_SCALE_REQUANTIZE;
   const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
   const int h = blockIdx.z >> 1;
   const bool is_v = (blockIdx.z & 1) != 0;
@@ -300,7 +335,7 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
     if (d.layout == KV_LAYOUT_LATENT) {
       append_block(a.k_new + row0 * Dk, Dk, nrows, Dk, true, fresh, d.k_scale + p,
                    static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, false, (int)P,
-                   slot0, tile, red);
+                   slot0, tile, red, requant);
       continue;
     }
     const int es = fp8 ? 1 : 2;
@@ -308,12 +343,14 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
       const long long kp = (((long long)p * H + h) * P) * Dk;
       append_block(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
                    fp8 ? d.k_scale + (long long)p * H + h : nullptr,
-                   static_cast<uint8_t*>(d.k_cache) + kp * es, false, (int)P, slot0, tile, red);
+                   static_cast<uint8_t*>(d.k_cache) + kp * es, false, (int)P, slot0, tile, red,
+                   requant);
     } else {
       const long long vp = ((long long)p * H + h) * (long long)Dv * P;
       append_block(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
                    fp8 ? d.v_scale + (long long)p * H + h : nullptr,
-                   static_cast<uint8_t*>(d.v_cache) + vp * es, true, (int)P, slot0, tile, red);
+                   static_cast<uint8_t*>(d.v_cache) + vp * es, true, (int)P, slot0, tile, red,
+                   requant);
     }
   }
 }
@@ -404,7 +441,7 @@ __device__ void k_page_16x128(const uint16_t* src, long long src_stride, bool fp
 
 __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, int D, bool fp8,
                           bool fresh, float* scale_slot, uint8_t* dst, bool dim_major, int P,
-                          int slot0, uint8_t* wtile) {
+                          int slot0, uint8_t* wtile, bool requant) {
   const int lane = threadIdx.x & 31;
   if (nrows == 16 && P == 16 && D == 128) {  // a whole page (fresh by construction)
     if (dim_major)
@@ -431,6 +468,18 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
       if (lane == 0) *scale_slot = s;
     } else {
       s = *scale_slot;
+      if (requant) {  // a larger scale for the new rows: re-encode the old ones
+        float m = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kTileChunks; ++t) m = fmaxf(m, amax8(v[t]));
+        const float s_new = scale_from_amax(warp_max(m));
+        if (s_new > s) {
+          requant_block(dst, slot0, D, dim_major, P, s, s_new, lane, 32);
+          __syncwarp();
+          if (lane == 0) *scale_slot = s_new;
+          s = s_new;
+        }
+      }
     }
   }
   const float rs = __frcp_rn(s);
@@ -499,6 +548,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
   const long long Lnew = a.seq_lens[r];
   const long long L0 = Lnew - n;
   const bool fp8 = d.dtype == KV_DTYPE_E4M3;
+  const bool requant = fp8 && d.scale_mode == KV_SCALE_REQUANTIZE;
   const int es = fp8 ? 1 : 2;
   const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
   const int warp = threadIdx.x >> 5;
@@ -521,12 +571,12 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
         tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
                   fp8 ? d.k_scale + (long long)p * H + h : nullptr,
                   static_cast<uint8_t*>(d.k_cache) + (((long long)p * H + h) * P * Dk) * es,
-                  false, (int)P, slot0, wtile);
+                  false, (int)P, slot0, wtile, requant);
       } else {
         tile_warp(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
                   fp8 ? d.v_scale + (long long)p * H + h : nullptr,
                   static_cast<uint8_t*>(d.v_cache) + (((long long)p * H + h) * Dv * P) * es,
-                  true, (int)P, slot0, wtile);
+                  true, (int)P, slot0, wtile, requant);
       }
     }
   }
@@ -582,6 +632,23 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
       __syncthreads();  // red is reused by the next page
     } else {
       s = d.k_scale[p];
+      if (d.scale_mode == KV_SCALE_REQUANTIZE) {  // re-encode the rows already written
+        float m = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kLatChunks; ++t) m = fmaxf(m, amax8(v[t]));
+        m = warp_max(m);
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = lane < kTileWarps ? red[lane] : 0.0f;
+        const float s_new = scale_from_amax(warp_max(m));
+        if (s_new > s) {
+          requant_block(static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, slot0, Dk,
+                        false, (int)P, s, s_new, threadIdx.x, kTileWarps * 32);
+          s = s_new;
+        }
+        __syncthreads();  // old scale read and red consumed by every thread
+        if (threadIdx.x == 0 && s_new > d.k_scale[p]) d.k_scale[p] = s_new;
+      }
     }
     const float rs = __frcp_rn(s);
     uint8_t* dst = static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk;

@@ -30,7 +30,7 @@ class Both:
     """A pool on the device (library) and its host twin (oracle)."""
 
     def __init__(self, w: wl.Workload, dtype: int, device="cuda", num_pages=None, free=None,
-                 tags=None):
+                 tags=None, scale_mode=0):
         import paged_fp8_kv_append_gb300 as kv
 
         self.kv, self.w, self.dtype = kv, w, dtype
@@ -39,9 +39,10 @@ class Both:
         tags = wl.initial_tags(w) if tags is None else tags
         self.dev = kv.KVPool(npg, w.page_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v,
                              dtype=dtype, layout=w.layout, device=device, tags=tags,
-                             free_list=free)
+                             free_list=free, scale_mode=scale_mode)
         self.ref = oracle.Pool(npg, w.page_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v,
-                               dtype=dtype, layout=w.layout, tags=tags, free_list=free)
+                               dtype=dtype, layout=w.layout, tags=tags, free_list=free,
+                               scale_mode=scale_mode)
         B, mp = w.B, w.max_pages
         self.pt_d = torch.full((B, mp), -1, dtype=torch.int32, device=device)
         self.et_d = torch.zeros((B, mp), dtype=torch.int32, device=device)
