@@ -11,25 +11,28 @@
 // 0 .. L - T + i.
 //
 // Work decomposition: a segment is (request, block of 64 query rows); a unit
-// is 32 tokens (half a 64-token page).  Units are laid out segment-major and
-// cut into equal ranges, one per CTA (one CTA per SM); each (CTA, segment)
-// piece leaves a partial (o, running max, sum) for the combine kernel.
+// is one 64-token page.  Units are laid out segment-major and cut into equal
+// ranges, one per CTA (one CTA per SM); each (CTA, segment) piece leaves a
+// partial (o, running max, sum) for the combine kernel.
 //
 // Per unit:
-//   converter warps load the unit's 32 x 576 e4m3 bytes (the next unit's
-//                   loads in flight while this one converts) and convert them
-//                   exactly to f16 into one of three 128B-swizzled K-major
-//                   tiles (the same tile is the MN-major V^T operand);
-//   MMA warp        S = Q K^T   (tcgen05, M = 64 rows, N = 32 tokens, K = 576,
-//                   f16 x f16 -> f32 into one of four tensor-memory buffers),
-//                   and two units later O^T += V^T P^T (M = 128 dims x 4
-//                   blocks, N = 64 rows, K = 32 tokens) accumulating in tensor
-//                   memory, so the tensor pipe never waits for the softmax;
-//   softmax warps   read S from tensor memory (one row per thread), apply the
-//                   page scale, the causal mask and the online softmax with a
-//                   lazily updated reference max (the output is rescaled only
-//                   when a row's max grows by more than 2^8), and write P (f16,
-//                   V scale folded in) as the swizzled B operand.
+//   converter warps load the page's 64 x 576 e4m3 bytes (each half's loads a
+//                   half ahead; the page two units ahead is prefetched into
+//                   L2) and convert them exactly to f16 into one of two
+//                   128B-swizzled K-major tiles (the same tile is the
+//                   MN-major V^T operand);
+//   MMA warp        S = Q K^T   (tcgen05, M = 64 rows, N = 64 tokens, K = 576,
+//                   f16 x f16 -> f32 into one of two tensor-memory buffers)
+//                   and O^T += V^T P^T (M = 128 dims x 4 blocks, N = 64 rows,
+//                   K = 64 tokens) accumulating in tensor memory, each issued
+//                   as soon as its inputs are ready, S up to one unit ahead;
+//   softmax warps   read S from tensor memory (all 32 lanes: two threads per
+//                   row), apply the page scale, the causal mask and the online
+//                   softmax with a lazily updated reference max (the output is
+//                   rescaled only when a row's max grows by more than 2^8),
+//                   and write P (f16; the page's scale enters as an exponent
+//                   bias) into the tile's last 64-dim block, which V does not
+//                   use, as the swizzled B operand.
 // Every wait is bounded; on timeout the kernel records KV_ERR_TIMEOUT, lets
 // the asynchronous work it issued finish (bounded) and frees its tensor
 // memory before returning.

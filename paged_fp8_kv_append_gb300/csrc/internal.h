@@ -80,7 +80,7 @@ struct DecodeArgs {
   int32_t Hs;           // kv heads per unit of work (a head group)
   int32_t HG;           // segments per request: head groups (GQA) or 64-row blocks (latent)
   int32_t stages;       // ring stages of the split kernel
-  int32_t unit_tokens;  // tokens per unit of work (GQA: a page; latent: half a page)
+  int32_t unit_tokens;  // tokens per unit of work (a page)
   DecodeWs ws;
 };
 
