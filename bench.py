@@ -486,6 +486,75 @@ def requant_lines(device, steps: int, warmup: int, w: wl.Workload) -> dict:
     return out
 
 
+# ------------------------------------------------------------ continuous batching
+
+def churn_line(device, steps: int, warmup: int) -> dict:
+    """Continuous batching over 128 request slots (64 q / 8 kv heads, head dim
+    128, page 16, e4m3; prompts lognormal, median 4k tokens, in [512, 32k]).
+    Every step, 3 requests finish and release their pages, 3 new ones join
+    the freed slots with a bulk append of their prompts, then every slot
+    takes a decode step (append -> verify -> attention).  Reports the time
+    of each phase and the decode tokens/s including the churn."""
+    import math as _m
+
+    rng = np.random.default_rng(20268)
+    S = 128
+
+    def prompt_lens(n):
+        return np.clip(np.round(rng.lognormal(_m.log(4096), 1.0, n)), 512, 32768).astype(np.int32)
+
+    lens = prompt_lens(S)
+    n_steps = steps + warmup
+    w = wl.Workload("churn", 20268, lens, 64, 8, 128, 128, 16, 1, 0,
+                    int((-(-lens.astype(np.int64) // 16)).sum() * 2) + 4096,
+                    float(np.float32(1 / np.sqrt(128))), steps=32768 + n_steps)
+    arm = Arm(w, 0, device, n_steps)
+    kv, h = arm.kv, arm.pool.handle
+    rel_ws = torch.empty(kv.kv_release_workspace_size(S), dtype=torch.uint8, device=device)
+    phase = {"release": [], "join": [], "step": []}
+    tokens, t_total = 0, 0.0
+    for it in range(n_steps):
+        leave = rng.choice(S, 3, replace=False)
+        mask = np.zeros(S, np.uint8)
+        mask[leave] = 1
+        new = prompt_lens(3)
+        counts = np.zeros(S, np.int64)
+        counts[leave] = new
+        ks, vs = [], []
+        for r, n in zip(leave, new):
+            k, v = wl.kv_rows(w, int(r), 0, int(n), device=device, tag=1000 + it)
+            ks.append(k)
+            vs.append(v)
+        k_new, v_new = torch.cat(ks), torch.cat(vs)
+        ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).to(device)
+        m_d = torch.from_numpy(mask).to(device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1_000_000)
+        ev[0].record()
+        arm.pool.release(S, arm.pt, arm.et, arm.sl, m_d, rel_ws)
+        ev[1].record()
+        arm.pool.append(S, k_new, v_new, ind, int(new.max()), arm.pt, arm.et, arm.sl)
+        ev[2].record()
+        arm.step()
+        ev[3].record()
+        torch.cuda.synchronize()
+        if arm.pool.error() != 0:
+            raise RuntimeError(f"churn: {kv.kv_status_string(arm.pool.error())}")
+        if it >= warmup:
+            for k_, (a, b) in zip(("release", "join", "step"), ((0, 1), (1, 2), (2, 3))):
+                phase[k_].append(ev[a].elapsed_time(ev[b]))
+            t_total += ev[0].elapsed_time(ev[3])
+            tokens += S
+    del arm
+    torch.cuda.empty_cache()
+    return {"workload": "churn: 128 request slots, 64 q / 8 kv heads, head dim 128, page 16, "
+                        "e4m3; prompts lognormal (median 4k) in [512, 32k]; per step 3 leave "
+                        "(release) and 3 join (bulk prompt append), then a decode step",
+            "decode_tokens_per_s": tokens / (t_total / 1e3),
+            "us": {k_: float(np.mean(v) * 1e3) for k_, v in phase.items()}}
+
+
 # ------------------------------------------------------------ verify overhead
 
 def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
@@ -814,6 +883,8 @@ def main():
     ap.add_argument("--overhead-replays", type=int, default=20)
     ap.add_argument("--no-requant", action="store_true",
                     help="skip the re-quantising scale mode lines")
+    ap.add_argument("--no-churn", action="store_true",
+                    help="skip the continuous-batching line")
     ap.add_argument("--no-bulk", action="store_true",
                     help="skip the bulk-append (prefill handoff) lines")
     ap.add_argument("--no-sweep", action="store_true",
@@ -970,6 +1041,11 @@ def main():
         bulk = [bulk_append_line(w, 0, device, peak), bulk_append_line(w, 1, device, peak),
                 bulk_append_line(wl.latent_verify(), 0, device, peak)]
 
+    # ---- continuous batching: requests leave and join between decode steps
+    churn = None
+    if not args.no_churn:
+        churn = churn_line(device, args.steps, args.warmup)
+
     # ---- concurrency sweep (1..64 requests at 128k), e4m3 and bf16
     conc = None
     if not args.no_sweep:
@@ -1012,6 +1088,7 @@ def main():
         "skewed_step": skewed,
         "bulk_append": bulk,
         "requantize": requant,
+        "churn": churn,
         "concurrency": conc,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
 // Bulk appends (a prefill handed to the decode cache) touch every page of a
 // request; these paths read each source byte once.  A GQA (page, kv head,
 // K|V) tile of up to 2048 values sits in one warp's registers: amax by a warp
-// reduction, then quantise and store from the registers.  One CTA takes 8
-// tiles of a page (one per warp).  A latent page (up to 64 rows of up to 576 values)
-// is split over the CTA's 8 warps by row, with a block-wide amax.
+// reduction, then quantise and store from the registers.  A latent page (up
+// to 64 rows of up to 576 values) is split over a CTA's 8 warps by row, with
+// a block-wide amax.  Both kernels are persistent (two CTAs per SM).
 
 constexpr int kTileWarps = 8;
 constexpr int kTileChunks = 8;   // 16-byte source chunks per lane (P * D <= 2048)
@@ -535,88 +535,143 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
   __syncwarp();
 }
 
+// Work items of a bulk append: every (request, page this call touches),
+// times per_page (tiles per page for GQA, 1 for latent), in request order.
+// The CTA's threads build the inclusive prefix pre[0..B] in shared memory, so
+// a persistent grid visits only real work however few requests have rows.
+constexpr int kMaxPersistB = 16384;
+
+__device__ int bulk_items_prefix(const AppendArgs& a, int B, int per_page, int* pre, int* wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const long long P = a.d.page_size;
+  int carry = 0;
+  if (threadIdx.x == 0) pre[0] = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    int v = 0;
+    if (r < B) {
+      const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+      if (n > 0) {
+        const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
+        v = (int)((Lnew - 1) / P - L0 / P + 1) * per_page;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[wid] = v;
+    __syncthreads();
+    int before = carry;
+    for (int k = 0; k < wid; ++k) before += wsum[k];
+    if (r < B) pre[r + 1] = before + v;
+    int chunk = 0;
+    for (int k = 0; k < nw; ++k) chunk += wsum[k];
+    carry += chunk;
+    __syncthreads();
+  }
+  return carry;
+}
+
+// request owning item i: the r with pre[r] <= i < pre[r + 1]
+__device__ __forceinline__ int item_owner(const int* pre, int B, int i) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// GQA: persistent CTAs; each warp takes (request, page, tile) items in turn.
 __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ __align__(16) uint8_t wtiles[];
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int wsum[kTileWarps];
   const kv_pool_desc& d = a.d;
-  const int r = blockIdx.x;
-  if (r >= d.ctl[KV_CTL_APPEND_STOP]) return;
-  const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
-  if (n <= 0) return;
   const long long P = d.page_size;
-  const long long Lnew = a.seq_lens[r];
-  const long long L0 = Lnew - n;
   const bool fp8 = d.dtype == KV_DTYPE_E4M3;
   const bool requant = fp8 && d.scale_mode == KV_SCALE_REQUANTIZE;
   const int es = fp8 ? 1 : 2;
   const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
   const int warp = threadIdx.x >> 5;
-  uint8_t* wtile = wtiles + (size_t)warp * Dv * P * es;
-  for (long long jp = L0 / P + blockIdx.y; jp * P < Lnew; jp += gridDim.y) {
+  const int B = min(a.B, (int)d.ctl[KV_CTL_APPEND_STOP]);
+  uint8_t* wtile = smem + (size_t)warp * Dv * P * es;
+  int* pre = reinterpret_cast<int*>(smem + (size_t)kTileWarps * Dv * P * es);
+  const int tiles = 2 * H;
+  const int total = B > 0 ? bulk_items_prefix(a, B, tiles, pre, wsum) : 0;
+  for (int it = blockIdx.x * kTileWarps + warp; it < total; it += gridDim.x * kTileWarps) {
+    const int r = item_owner(pre, B, it);
+    const int local = it - pre[r], t = local % tiles;
+    const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+    const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
+    const long long jp = L0 / P + local / tiles;
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
     const int nrows = (int)(pos_hi - pos_lo);
     const int slot0 = (int)(pos_lo - jp * P);
     const long long row0 = a.new_indptr[r] + (pos_lo - L0);
     const int p = a.page_table[(long long)r * a.max_pages + jp];
-    if (p < 0 || p >= d.num_pages) {
-      if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
-      return;  // uniform across the block
+    if (p < 0 || p >= d.num_pages) {  // uniform across the warp
+      if ((threadIdx.x & 31) == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+      continue;
     }
     const bool fresh = jp * P >= L0;  // popped by this call
-    // CTA z takes tiles 8z .. 8z+7 of the page (tile 2h = K of head h, 2h+1 = V)
-    for (int t = blockIdx.z * kTileWarps + warp; t < 2 * H; t += kTileWarps * gridDim.z) {
-      const int h = t >> 1;
-      if ((t & 1) == 0) {
-        tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
-                  fp8 ? d.k_scale + (long long)p * H + h : nullptr,
-                  static_cast<uint8_t*>(d.k_cache) + (((long long)p * H + h) * P * Dk) * es,
-                  false, (int)P, slot0, wtile, requant);
-      } else {
-        tile_warp(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
-                  fp8 ? d.v_scale + (long long)p * H + h : nullptr,
-                  static_cast<uint8_t*>(d.v_cache) + (((long long)p * H + h) * Dv * P) * es,
-                  true, (int)P, slot0, wtile, requant);
-      }
+    const int h = t >> 1;
+    if ((t & 1) == 0) {
+      tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
+                fp8 ? d.k_scale + (long long)p * H + h : nullptr,
+                static_cast<uint8_t*>(d.k_cache) + (((long long)p * H + h) * P * Dk) * es, false,
+                (int)P, slot0, wtile, requant);
+    } else {
+      tile_warp(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
+                fp8 ? d.v_scale + (long long)p * H + h : nullptr,
+                static_cast<uint8_t*>(d.v_cache) + (((long long)p * H + h) * Dv * P) * es, true,
+                (int)P, slot0, wtile, requant);
     }
   }
 }
 
+// Latent: persistent CTAs; each CTA takes (request, page) items in turn.
 __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[kTileWarps];
+  __shared__ int wsum[kTileWarps];
   const kv_pool_desc& d = a.d;
-  const int r = blockIdx.x;
-  if (r >= d.ctl[KV_CTL_APPEND_STOP]) return;
-  const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
-  if (n <= 0) return;
   const long long P = d.page_size;
-  const long long Lnew = a.seq_lens[r];
-  const long long L0 = Lnew - n;
   const int Dk = d.head_dim_k, cpr = Dk / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (long long jp = L0 / P + blockIdx.y; jp * P < Lnew; jp += gridDim.y) {
+  const int B = min(a.B, (int)d.ctl[KV_CTL_APPEND_STOP]);
+  int* pre = reinterpret_cast<int*>(smem);
+  const int total = B > 0 ? bulk_items_prefix(a, B, 1, pre, wsum) : 0;
+  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    const int r = item_owner(pre, B, it);
+    const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+    const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
+    const long long jp = L0 / P + (it - pre[r]);
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
     const int nrows = (int)(pos_hi - pos_lo);
     const int slot0 = (int)(pos_lo - jp * P);
     const long long row0 = a.new_indptr[r] + (pos_lo - L0);
     const int p = a.page_table[(long long)r * a.max_pages + jp];
-    if (p < 0 || p >= d.num_pages) {
+    if (p < 0 || p >= d.num_pages) {  // uniform across the block
       if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
-      return;  // uniform across the block
+      continue;
     }
     const bool fresh = jp * P >= L0;
     // warp w takes rows w, w + 8, ... of this call's rows in the page
     const int my_rows = nrows > warp ? (nrows - warp + kTileWarps - 1) / kTileWarps : 0;
-    const int total = my_rows * cpr;
+    const int tot = my_rows * cpr;
     uint4 v[kLatChunks];
 #pragma unroll
     for (int t = 0; t < kLatChunks; ++t) {
       const int q = lane + 32 * t;
       const int i = warp + kTileWarps * (q / cpr);
-      v[t] = q < total ? *reinterpret_cast<const uint4*>(a.k_new + (row0 + i) * Dk + 8 * (q % cpr))
-                       : make_uint4(0, 0, 0, 0);
+      v[t] = q < tot ? *reinterpret_cast<const uint4*>(a.k_new + (row0 + i) * Dk + 8 * (q % cpr))
+                     : make_uint4(0, 0, 0, 0);
     }
     float s;
     if (fresh) {
@@ -655,7 +710,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
 #pragma unroll
     for (int t = 0; t < kLatChunks; ++t) {
       const int q = lane + 32 * t;
-      if (q < total) {
+      if (q < tot) {
         const int i = warp + kTileWarps * (q / cpr);
         *reinterpret_cast<uint2*>(dst + (long long)(slot0 + i) * Dk + 8 * (q % cpr)) =
             quant8_rs(v[t], s, rs);
@@ -681,24 +736,37 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   // rows per request, a handful of CTAs) spends its time fetching their
   // instructions, so it takes the compact per-tile kernel below.
   const bool bulk = a.max_new >= 2 * Pl;
-  if (bulk && a.d.layout == KV_LAYOUT_GQA && Pl * a.d.head_dim_k <= 32 * 8 * kTileChunks &&
-      Pl * a.d.head_dim_v <= 32 * 8 * kTileChunks) {
-    const size_t smem = (size_t)kTileWarps * a.d.head_dim_v * Pl * es;
+  static int sms = 0;
+  if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess)
+    sms = 0;
+  const size_t pre_bytes = sizeof(int) * ((size_t)a.B + 1);
+  // the work-item count is held in an int
+  const long long per_page = a.d.layout == KV_LAYOUT_GQA ? 2LL * a.d.num_kv_heads : 1LL;
+  const bool persist = bulk && sms > 0 && a.B <= kMaxPersistB &&
+                       (long long)a.B * ((a.max_new + 2 * P - 2) / P) * per_page <= INT_MAX;
+  if (persist && a.d.layout == KV_LAYOUT_GQA &&
+      Pl * a.d.head_dim_k <= 32 * 8 * kTileChunks && Pl * a.d.head_dim_v <= 32 * 8 * kTileChunks) {
+    const size_t smem = (size_t)kTileWarps * a.d.head_dim_v * Pl * es + pre_bytes;
     if (smem > 48 * 1024) {
       e = cudaFuncSetAttribute(append_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
     }
-    const unsigned groups = (unsigned)((2 * a.d.num_kv_heads + kTileWarps - 1) / kTileWarps);
-    e = launch_pdl(append_gqa_kernel, dim3((unsigned)a.B, (unsigned)pieces, groups),
-                   dim3(kTileWarps * 32), smem, s, a);
+    e = launch_pdl(append_gqa_kernel, dim3((unsigned)(2 * sms)), dim3(kTileWarps * 32), smem, s,
+                   a);
     if (e == cudaSuccess) ++*launches;
     return e;
   }
-  if (bulk && a.d.layout == KV_LAYOUT_LATENT && Pl <= 8 * kTileWarps &&
+  if (persist && a.d.layout == KV_LAYOUT_LATENT &&
+      Pl <= 8 * kTileWarps &&
       (long long)((Pl + kTileWarps - 1) / kTileWarps) * (a.d.head_dim_k / 8) <= 32 * kLatChunks) {
-    e = launch_pdl(append_latent_kernel, dim3((unsigned)a.B, (unsigned)pieces),
-                   dim3(kTileWarps * 32), 0, s, a);
+    if (pre_bytes > 48 * 1024) {
+      e = cudaFuncSetAttribute(append_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)pre_bytes);
+      if (e != cudaSuccess) return e;
+    }
+    e = launch_pdl(append_latent_kernel, dim3((unsigned)(2 * sms)), dim3(kTileWarps * 32),
+                   pre_bytes, s, a);
     if (e == cudaSuccess) ++*launches;
     return e;
   }
