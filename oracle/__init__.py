@@ -26,6 +26,8 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_INVALID_ARG, ERR_OUT_OF_PAGES, ERR_BAD_PAGE_ID, ERR_TAG_MISMATCH = 0, 1, 4, 5, 8
+# abort-mask bits of a step: the page-tag check failed / the append stopped first
+ABORT_TAG, ABORT_UNSERVED = 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -242,3 +244,56 @@ def attn(pool: Pool, q_bits, page_table, seq_lens, abort_mask, sm_scale, num_q_h
                            _p(sl), _p(am), _p(q_bits), float(np.float32(sm_scale)), _p(out),
                            _p(written))
     return out, written
+
+
+def step(pool: Pool, leave_mask, k_new, v_new, new_indptr, max_new, page_table, exp_tags,
+         seq_lens, q_bits, sm_scale, num_q_heads, q_tokens, remove_aborted=True):
+    """One continuous-batching decode step over B request slots ("Smaller,
+    faster, safer: running Kimi and GLM at scale", section "Protecting a
+    shared KV cache": the tag check runs on every step, before attention, and
+    a request that fails it is aborted and returns no data).  A slot with
+    length 0 is empty.  In order:
+
+    1. requests with leave_mask[r] != 0 release their pages (release());
+    2. the tag check over every mapping that exists now: abort bit ABORT_TAG;
+    3. the append, in which a request with ABORT_TAG appends nothing (its
+       rows are dropped); every request at or after the append's stop index
+       gets ABORT_UNSERVED;
+    4. attention for every request whose abort mask is 0;
+    5. with remove_aborted, requests with ABORT_TAG release their pages.
+
+    The mappings the append creates are pages it has just popped, with the
+    tag it has just stamped, and the rows it puts into a partly filled page
+    go there only after step 2 found that page's tag unchanged; so every
+    page attention reads has passed the check.  Arrays are updated in place.
+    Returns (status, abort_mask, out, written); status is the first nonzero
+    status of the phases."""
+    status = OK
+    if leave_mask is not None:
+        status = release(pool, page_table, exp_tags, seq_lens, leave_mask)
+    mask = verify(pool.num_pages, pool.page_size, pool.tags, page_table, exp_tags, seq_lens)
+    ind = np.asarray(new_indptr, np.int64)
+    B = len(seq_lens)
+    keep = [r for r in range(B) if not mask[r]]
+    counts = np.zeros(B, np.int64)
+    counts[keep] = ind[1:][keep] - ind[:-1][keep]
+    ind_eff = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    k_new = np.asarray(k_new)
+    ks = [k_new[ind[r]:ind[r + 1]] for r in keep]
+    k_eff = np.concatenate(ks) if ks else k_new[:0]
+    v_eff = None
+    if v_new is not None:
+        v_new = np.asarray(v_new)
+        vs = [v_new[ind[r]:ind[r + 1]] for r in keep]
+        v_eff = np.concatenate(vs) if vs else v_new[:0]
+    st, stop = append(pool, k_eff, v_eff if v_eff is not None else k_eff, ind_eff, max_new,
+                      page_table, exp_tags, seq_lens)
+    status = status or st
+    mask[stop:] |= ABORT_UNSERVED
+    out, written = attn(pool, q_bits, page_table, seq_lens, mask, sm_scale, num_q_heads,
+                        q_tokens)
+    if remove_aborted:
+        stale = (mask & ABORT_TAG).astype(np.uint8)
+        if stale.any():
+            status = status or release(pool, page_table, exp_tags, seq_lens, stale)
+    return status, mask, out, written
