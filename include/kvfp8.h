@@ -82,6 +82,14 @@ typedef enum {
   KV_SCALE_REQUANTIZE = 1
 } kv_scale_mode;
 
+/* kv_decode_step: abort-mask bits it writes, and its flags. */
+enum {
+  KV_ABORT_TAG = 1,          /* failed the page-tag check (stale or out-of-range mapping,
+                                or a length its page table cannot hold) */
+  KV_ABORT_UNSERVED = 2,     /* the step's append stopped at or before this request */
+  KV_STEP_REMOVE_ABORTED = 1 /* flag: release the pages of KV_ABORT_TAG requests */
+};
+
 /* Slots of the pool's int32 control block (device memory, KV_CTL_WORDS
  * ints, caller-owned; zero it when creating a pool). */
 enum {
@@ -321,6 +329,53 @@ const char* kv_status_string(kv_status status);
 /* Number of kernel launches the last call on this pool enqueued (for
  * launch accounting by benchmarks). */
 int32_t kv_last_launch_count(const kv_pool* pool);
+
+/* Bytes of device workspace kv_decode_step needs (0 for invalid arguments
+ * or when no device is visible). */
+size_t kv_decode_step_workspace_size(const kv_pool* pool, int32_t B,
+                                     int32_t num_q_heads, int32_t q_tokens);
+
+/*
+ * One continuous-batching decode step over B request slots, in one call
+ * with no host synchronisation (SFS "Protecting a shared KV cache": the
+ * page-tag check stays on for every step while requests join and leave, and
+ * a request whose pages were reallocated is aborted and returns no data).
+ * A slot whose seq_lens entry is 0 is empty.  The call runs, on `stream`:
+ *
+ *   1. leave_mask (uint8 [B], device, or NULL): requests with a nonzero
+ *      entry release their pages, as kv_release_pages does;
+ *   2. the tag check of kv_verify_tags over the mappings that exist now,
+ *      writing abort_mask (uint8 [B], device, out): KV_ABORT_TAG or 0;
+ *   3. the append of kv_append_quantize (k_new, v_new, new_indptr,
+ *      max_new_per_req: a joining request's prompt rows, a decoding one's
+ *      new rows), in which a request with KV_ABORT_TAG appends nothing (its
+ *      rows are skipped; the request is still checked for a negative length
+ *      or rows beyond its page table); every request at or after the index
+ *      at which the append stopped gets KV_ABORT_UNSERVED;
+ *   4. paged_decode_attn over q, for every request whose abort_mask is 0;
+ *      the others' output rows are left untouched;
+ *   5. with flags & KV_STEP_REMOVE_ABORTED, requests with KV_ABORT_TAG
+ *      release their pages (seq_lens 0: the slot is empty again).
+ *      KV_ABORT_UNSERVED requests keep their state.
+ *
+ * The check runs before the append: every mapping the append adds is a page
+ * it has just popped and stamped, and rows go into a partly filled page only
+ * after that page passed the check, so attention reads only checked pages
+ * and a stale request costs no other request its step.  Arguments are those
+ * of the calls above (same meaning, layout and ownership); workspace is
+ * device scratch of at least kv_decode_step_workspace_size bytes, 256-byte
+ * aligned.  Every argument is checked before anything is launched
+ * (KV_ERR_INVALID_ARG / KV_ERR_UNSUPPORTED, nothing launched); device-found
+ * errors go to ctl[KV_CTL_ERROR], first error wins.  Six kernel launches,
+ * plus two for each release phase that runs.
+ */
+kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                         int32_t q_tokens, const uint8_t* leave_mask, const void* k_new,
+                         const void* v_new, const int32_t* new_indptr,
+                         int32_t max_new_per_req, int32_t* page_table, uint32_t* exp_tags,
+                         int32_t max_pages_per_req, int32_t* seq_lens, const void* q,
+                         float sm_scale, void* out, uint8_t* abort_mask, int32_t flags,
+                         void* workspace, size_t workspace_bytes);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,7 @@ KV_ERR_TAG_MISMATCH = 8
 KV_DTYPE_E4M3, KV_DTYPE_BF16 = 0, 1
 KV_LAYOUT_GQA, KV_LAYOUT_LATENT = 0, 1
 KV_SCALE_FROZEN, KV_SCALE_REQUANTIZE = 0, 1
+KV_ABORT_TAG, KV_ABORT_UNSERVED, KV_STEP_REMOVE_ABORTED = 1, 2, 1
 KV_CTL_FREE_HEAD, KV_CTL_ERROR, KV_CTL_APPEND_STOP, KV_CTL_WAIT_INFO, KV_CTL_WORDS = 0, 1, 2, 3, 4
 
 
@@ -74,6 +75,11 @@ _lib.paged_decode_attn_combine.restype = _i32
 _lib.paged_decode_attn_noalloc.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp,
                                            _vp, _f32, _vp]
 _lib.paged_decode_attn_noalloc.restype = _i32
+_lib.kv_decode_step_workspace_size.argtypes = [_vp, _i32, _i32, _i32]
+_lib.kv_decode_step_workspace_size.restype = _sz
+_lib.kv_decode_step.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                _i32, _vp, _vp, _f32, _vp, _vp, _i32, _vp, _sz]
+_lib.kv_decode_step.restype = _i32
 _lib.kv_status_string.argtypes = [_i32]
 _lib.kv_status_string.restype = ctypes.c_char_p
 _lib.kv_last_launch_count.argtypes = [_vp]
@@ -227,6 +233,26 @@ def paged_decode_attn_combine(handle, B, num_q_heads, q_tokens, abort_mask, out,
     _check(st, "paged_decode_attn_combine")
 
 
+def kv_decode_step_workspace_size(handle, B, num_q_heads, q_tokens) -> int:
+    return int(_lib.kv_decode_step_workspace_size(handle, int(B), int(num_q_heads),
+                                                  int(q_tokens)))
+
+
+def kv_decode_step(handle, B, num_q_heads, q_tokens, leave_mask, k_new, v_new, new_indptr,
+                   max_new_per_req, page_table, exp_tags, seq_lens, q, sm_scale, out, abort_mask,
+                   flags, workspace, stream=None):
+    st = _lib.kv_decode_step(
+        handle, _stream(stream), int(B), int(num_q_heads), int(q_tokens),
+        _ptr(leave_mask, torch.uint8, "leave_mask"), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(new_indptr, torch.int32, "new_indptr"),
+        int(max_new_per_req), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(exp_tags, _U32, "exp_tags"), int(page_table.shape[-1]),
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(q, torch.bfloat16, "q"), float(sm_scale),
+        _ptr(out, torch.bfloat16, "out"), _ptr(abort_mask, torch.uint8, "abort_mask"),
+        int(flags), _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()))
+    _check(st, "kv_decode_step")
+
+
 # ---------------------------------------------------------------- pool helper
 
 class KVPool:
@@ -317,6 +343,19 @@ class KVPool:
              workspace, stream=None):
         paged_decode_attn(self.handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,
                           abort_mask, sm_scale, out, workspace, stream)
+
+    def step_workspace_size(self, B, num_q_heads, q_tokens) -> int:
+        n = kv_decode_step_workspace_size(self.handle, B, num_q_heads, q_tokens)
+        if n == 0 and B > 0:
+            raise KVError(KV_ERR_UNSUPPORTED, "kv_decode_step_workspace_size")
+        return n
+
+    def step(self, B, num_q_heads, q_tokens, leave_mask, k_new, v_new, new_indptr,
+             max_new_per_req, page_table, exp_tags, seq_lens, q, sm_scale, out, abort_mask,
+             flags, workspace, stream=None):
+        kv_decode_step(self.handle, B, num_q_heads, q_tokens, leave_mask, k_new, v_new,
+                       new_indptr, max_new_per_req, page_table, exp_tags, seq_lens, q, sm_scale,
+                       out, abort_mask, flags, workspace, stream)
 
     def error(self) -> int:
         """Device error word (synchronises)."""

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/kvfp8.h: argument validation,
 // launch configuration and workspace carve-up.  All compute is in the
-// kernels of append.cu, verify.cu, decode_gqa.cu and decode_latent.cu.
+// kernels of append.cu, verify.cu, release.cu, decode_gqa.cu and
+// decode_latent.cu; kv_decode_step chains them on one stream.
 #include <math.h>
 
 #include <new>
@@ -226,6 +227,7 @@ kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B, const void*
   a.exp_tags = exp_tags;
   a.max_pages = max_pages_per_req;
   a.seq_lens = seq_lens;
+  a.step_mask = nullptr;
   int n = 0;
   const cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), &n);
   pool->last_launches = n;
@@ -276,6 +278,7 @@ kv_status kv_release_pages(kv_pool* pool, void* stream, int32_t B, int32_t* page
   a.exp_tags = exp_tags;
   a.seq_lens = seq_lens;
   a.mask = release_mask;
+  a.mask_bits = 0xFF;
   a.offsets = static_cast<long long*>(workspace);
   int n = 0;
   const cudaError_t e = launch_release(a, static_cast<cudaStream_t>(stream), &n);
@@ -346,6 +349,99 @@ kv_status paged_decode_attn(kv_pool* pool, void* stream, int32_t B, int32_t num_
                                  workspace, workspace_bytes);
   pool->last_launches += n;
   return st;
+}
+
+size_t kv_decode_step_workspace_size(const kv_pool* pool, int32_t B, int32_t num_q_heads,
+                                     int32_t q_tokens) {
+  if (!pool || B < 0) return 0;
+  DecodeConfig cfg;
+  if (decode_config(pool, B, num_q_heads, q_tokens, &cfg) != KV_OK) return 0;
+  const size_t dec = decode_ws_layout(pool->d, B, pool->d.num_kv_heads, cfg, nullptr, nullptr);
+  return align256(dec) + release_ws_bytes(B);
+}
+
+kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                         int32_t q_tokens, const uint8_t* leave_mask, const void* k_new,
+                         const void* v_new, const int32_t* new_indptr, int32_t max_new_per_req,
+                         int32_t* page_table, uint32_t* exp_tags, int32_t max_pages_per_req,
+                         int32_t* seq_lens, const void* q, float sm_scale, void* out,
+                         uint8_t* abort_mask, int32_t flags, void* workspace,
+                         size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  const kv_pool_desc& d = pool->d;
+  if (B < 0 || (flags & ~KV_STEP_REMOVE_ABORTED) != 0) return KV_ERR_INVALID_ARG;
+  if (max_new_per_req < 0 || max_pages_per_req <= 0) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!new_indptr || !page_table || !exp_tags || !seq_lens || !abort_mask)
+    return KV_ERR_INVALID_ARG;
+  if (max_new_per_req > 0) {
+    if (!k_new || !aligned16(k_new)) return KV_ERR_INVALID_ARG;
+    if (d.layout == KV_LAYOUT_GQA && (!v_new || !aligned16(v_new))) return KV_ERR_INVALID_ARG;
+  }
+  // attention arguments and the workspace, before anything is launched
+  DecodeArgs da;
+  int kind = 0;
+  kv_status st = decode_prepare(pool, B, num_q_heads, q_tokens, q, page_table, max_pages_per_req,
+                                seq_lens, abort_mask, sm_scale, out, workspace, workspace_bytes,
+                                true, true, &da, &kind);
+  if (st != KV_OK) return st;
+  const size_t need = kv_decode_step_workspace_size(pool, B, num_q_heads, q_tokens);
+  if (need == 0 || workspace_bytes < need) return KV_ERR_INVALID_ARG;
+  const size_t dec = need - release_ws_bytes(B);
+  long long* rel_ws = reinterpret_cast<long long*>(static_cast<uint8_t*>(workspace) + dec);
+
+  ReleaseArgs ra;
+  ra.d = d;
+  ra.B = B;
+  ra.max_pages = max_pages_per_req;
+  ra.page_table = page_table;
+  ra.exp_tags = exp_tags;
+  ra.seq_lens = seq_lens;
+  ra.offsets = rel_ws;
+  VerifyArgs va;
+  va.num_pages = d.num_pages;
+  va.page_size = d.page_size;
+  va.B = B;
+  va.max_pages = max_pages_per_req;
+  va.tags = d.tags;
+  va.page_table = page_table;
+  va.exp_tags = exp_tags;
+  va.seq_lens = seq_lens;
+  va.abort_mask = abort_mask;
+  AppendArgs aa;
+  aa.d = d;
+  aa.B = B;
+  aa.k_new = static_cast<const uint16_t*>(k_new);
+  aa.v_new = static_cast<const uint16_t*>(v_new);
+  aa.new_indptr = new_indptr;
+  aa.max_new = max_new_per_req;
+  aa.page_table = page_table;
+  aa.exp_tags = exp_tags;
+  aa.max_pages = max_pages_per_req;
+  aa.seq_lens = seq_lens;
+  aa.step_mask = abort_mask;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int n = 0;
+  cudaError_t e = cudaSuccess;
+  if (leave_mask != nullptr) {
+    ra.mask = leave_mask;
+    ra.mask_bits = 0xFF;
+    e = launch_release(ra, s, &n);
+  }
+  if (e == cudaSuccess) e = launch_verify(va, s, &n);
+  if (e == cudaSuccess) e = launch_append(aa, s, &n);
+  if (e == cudaSuccess) e = launch_decode_plan(da, s, &n);
+  if (e == cudaSuccess) e = launch_decode_split(da, kind, s, &n);
+  if (e == cudaSuccess) e = launch_decode_combine(da, s, &n);
+  if (e == cudaSuccess && (flags & KV_STEP_REMOVE_ABORTED) != 0) {
+    ra.mask = abort_mask;
+    ra.mask_bits = KV_ABORT_TAG;
+    e = launch_release(ra, s, &n);
+  }
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 const char* kv_status_string(kv_status s) {

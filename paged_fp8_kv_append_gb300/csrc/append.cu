@@ -67,6 +67,18 @@ __device__ __forceinline__ int owner_of(const long long* incl, int n, long long 
   return lo;
 }
 
+// Rows request r appends in this call (none when the step mask drops it).
+__device__ __forceinline__ long long req_rows(const AppendArgs& a, int r) {
+  if (a.step_mask != nullptr && a.step_mask[r] != 0) return 0;
+  return (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+}
+
+// With a step mask, every request at or after `stop` is marked unserved.
+__device__ void mark_unserved(const AppendArgs& a, int stop) {
+  if (a.step_mask == nullptr) return;
+  for (int r = stop + threadIdx.x; r < a.B; r += blockDim.x) a.step_mask[r] |= KV_ABORT_UNSERVED;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -85,6 +97,7 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
       d.ctl[KV_CTL_APPEND_STOP] = 0;
       set_error(d.ctl, KV_ERR_INVALID_ARG);
     }
+    mark_unserved(a, 0);
     return;
   }
 
@@ -95,7 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     int code = 0;
     if (r < a.B) {
       L = a.seq_lens[r];
-      n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+      n = req_rows(a, r);
       if (n < 0 || L < 0 || n > a.max_new || L + n > (long long)a.max_pages * P) {
         code = KV_ERR_INVALID_ARG;
       } else {
@@ -168,6 +181,8 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     d.ctl[KV_CTL_APPEND_STOP] = stop;
     if (stop_code != 0) set_error(d.ctl, stop_code);
   }
+  __syncthreads();  // every thread has read its own mask entry
+  mark_unserved(a, stop);
 }
 
 constexpr int kDataThreads = 256;
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
   const kv_pool_desc& d = a.d;
   const int r = blockIdx.x;
   if (r >= d.ctl[KV_CTL_APPEND_STOP]) return;
-  const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+  const long long n = req_rows(a, r);
   if (n <= 0) return;
   const long long P = d.page_size;
   const long long Lnew = a.seq_lens[r];
@@ -550,7 +565,7 @@ __device__ int bulk_items_prefix(const AppendArgs& a, int B, int per_page, int* 
     const int r = base + threadIdx.x;
     int v = 0;
     if (r < B) {
-      const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+      const long long n = req_rows(a, r);
       if (n > 0) {
         const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
         v = (int)((Lnew - 1) / P - L0 / P + 1) * per_page;
@@ -605,7 +620,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
   for (int it = blockIdx.x * kTileWarps + warp; it < total; it += gridDim.x * kTileWarps) {
     const int r = item_owner(pre, B, it);
     const int local = it - pre[r], t = local % tiles;
-    const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+    const long long n = req_rows(a, r);
     const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
     const long long jp = L0 / P + local / tiles;
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
@@ -649,7 +664,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
   const int total = B > 0 ? bulk_items_prefix(a, B, 1, pre, wsum) : 0;
   for (int it = blockIdx.x; it < total; it += gridDim.x) {
     const int r = item_owner(pre, B, it);
-    const long long n = (long long)a.new_indptr[r + 1] - a.new_indptr[r];
+    const long long n = req_rows(a, r);
     const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
     const long long jp = L0 / P + (it - pre[r]);
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);

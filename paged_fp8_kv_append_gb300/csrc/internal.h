@@ -27,6 +27,10 @@ struct AppendArgs {
   uint32_t* exp_tags;
   int32_t max_pages;
   int32_t* seq_lens;
+  // NULL, or [B] (the step driver's abort mask): a request with a nonzero
+  // entry appends no rows; the plan then sets KV_ABORT_UNSERVED on every
+  // request at or after its stop index.
+  uint8_t* step_mask;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
 
@@ -49,6 +53,7 @@ struct ReleaseArgs {
   uint32_t* exp_tags;
   int32_t* seq_lens;
   const uint8_t* mask;   // NULL: every request
+  uint8_t mask_bits;     // with a mask: release r iff mask[r] & mask_bits
   long long* offsets;    // workspace: [B+1] released-page prefix, then [1] base, [1] ok
 };
 size_t release_ws_bytes(int B);

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kPlanThreads) release_plan_kernel(ReleaseArgs 
   for (int base = 0; base < a.B; base += kPlanThreads) {
     const int r = base + threadIdx.x;
     long long n = 0;
-    if (r < a.B && (a.mask == nullptr || a.mask[r] != 0)) {
+    if (r < a.B && (a.mask == nullptr || (a.mask[r] & a.mask_bits) != 0)) {
       const long long L = a.seq_lens[r];
       n = (L + P - 1) / P;
       if (L < 0 || n > a.max_pages) {
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kScatterThreads) release_scatter_kernel(Releas
   const int r = blockIdx.x;
   const long long* off = a.offsets;
   if (off[a.B + 2] == 0) return;  // the plan refused the call
-  if (a.mask != nullptr && a.mask[r] == 0) return;
+  if (a.mask != nullptr && (a.mask[r] & a.mask_bits) == 0) return;
   const long long o = off[r], n = off[r + 1] - o;
   const long long j0 = (long long)blockIdx.y * kScatterChunk;
   if (j0 >= n) {

@@ -136,6 +136,42 @@ class Both:
                             self.et_h, self.sl_h)
         return m_d, m_h
 
+    def step(self, leave, rows_k, rows_v, counts, q, remove=True, max_new=None, sentinel=7.0):
+        """One kv_decode_step on the device and oracle.step on the host, on
+        the same rows (lists of per-request bf16 device tensors) and queries.
+        Returns (oracle status, device abort mask, oracle abort mask, device
+        out, oracle out, oracle written)."""
+        w, B = self.w, self.w.B
+        counts = np.asarray(counts, np.int64)
+        ind = np.zeros(B + 1, np.int32)
+        ind[1:] = np.cumsum(counts)
+        ks = [x for x in rows_k if x is not None and x.shape[0] > 0]
+        vs = [x for x in rows_v if x is not None and x.shape[0] > 0] if w.layout == 0 else []
+        if ks:
+            k = torch.cat(ks).contiguous()
+            v = torch.cat(vs).contiguous() if w.layout == 0 else None
+        else:  # nothing to append: still a valid call
+            k = torch.zeros((1, w.num_kv_heads, w.head_dim_k), dtype=torch.bfloat16,
+                            device=self.device)
+            v = torch.zeros((1, w.num_kv_heads, w.head_dim_v), dtype=torch.bfloat16,
+                            device=self.device) if w.layout == 0 else None
+        mx = int(counts.max()) if max_new is None else max_new
+        lv = None if leave is None else np.asarray(leave, np.uint8)
+        lv_d = None if lv is None else torch.from_numpy(lv).to(self.device)
+        out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), sentinel,
+                         dtype=torch.bfloat16, device=self.device)
+        m_d = torch.full((B,), 0xEE, dtype=torch.uint8, device=self.device)
+        ws = torch.empty(self.dev.step_workspace_size(B, w.num_q_heads, w.q_tokens),
+                         dtype=torch.uint8, device=self.device)
+        flags = self.kv.KV_STEP_REMOVE_ABORTED if remove else 0
+        self.dev.step(B, w.num_q_heads, w.q_tokens, lv_d, k, v, torch.from_numpy(ind).to(self.device),
+                      mx, self.pt_d, self.et_d, self.sl_d, q, w.sm_scale, out, m_d, flags, ws)
+        st, m_h, ref, written = oracle.step(
+            self.ref, lv, wl.bits_u16(k), None if v is None else wl.bits_u16(v), ind, mx,
+            self.pt_h, self.et_h, self.sl_h, wl.bits_u16(q), w.sm_scale, w.num_q_heads,
+            w.q_tokens, remove_aborted=remove)
+        return st, m_d, m_h, out, ref, written
+
     def attn(self, q, abort_d, abort_h, sentinel=7.0, phases=False):
         w, B = self.w, self.w.B
         out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), sentinel,

@@ -103,3 +103,34 @@ def test_release_argument_checks(kv):
         assert kv.kv_status_string(kv.KV_ERR_TAG_MISMATCH) == "KV_ERR_TAG_MISMATCH"
     finally:
         kv.kv_pool_destroy(h)
+
+
+def test_step_argument_checks(kv):
+    """kv_decode_step refuses bad arguments before enqueuing anything (the
+    checks below all come before any device query)."""
+    h = kv.kv_pool_create(_desc(kv))
+    lib = kv._lib
+    f, ws = 0x10000, 0x20000
+    assert kv.kv_decode_step_workspace_size(None, 4, 16, 1) == 0
+    assert kv.kv_decode_step_workspace_size(h, -1, 16, 1) == 0
+    try:
+        def step(pool=h, B=4, flags=0, k=f, v=f, ind=f, max_new=1, pt=f, mp=8, sl=f, mask=f):
+            return lib.kv_decode_step(pool, None, B, 16, 1, None, k, v, ind, max_new, pt, f, mp,
+                                      sl, f, 1.0, f, mask, flags, ws, 1 << 20)
+        bad = kv.KV_ERR_INVALID_ARG
+        assert step(pool=None) == bad
+        assert step(B=-1) == bad
+        assert step(flags=2) == bad               # unknown flag bit
+        assert step(max_new=-1) == bad
+        assert step(mp=0) == bad
+        assert step(mask=None) == bad             # the abort mask is always written
+        assert step(ind=None) == bad
+        assert step(pt=None) == bad
+        assert step(sl=None) == bad
+        assert step(k=None) == bad
+        assert step(k=f + 2) == bad               # rows must be 16-byte aligned
+        assert step(v=None) == bad                # GQA needs V rows
+        assert step(B=0, mask=None, ind=None, pt=None, sl=None) == kv.KV_OK
+        assert lib.kv_last_launch_count(h) == 0
+    finally:
+        kv.kv_pool_destroy(h)
