@@ -488,13 +488,12 @@ def requant_lines(device, steps: int, warmup: int, w: wl.Workload) -> dict:
 
 # ------------------------------------------------------------ continuous batching
 
-def churn_line(device, steps: int, warmup: int) -> dict:
-    """Continuous batching over 128 request slots (64 q / 8 kv heads, head dim
-    128, page 16, e4m3; prompts lognormal, median 4k tokens, in [512, 32k]).
-    Every step, 3 requests finish and release their pages, 3 new ones join
-    the freed slots with a bulk append of their prompts, then every slot
-    takes a decode step (append -> verify -> attention).  Reports the time
-    of each phase and the decode tokens/s including the churn."""
+def _churn(device, steps: int, warmup: int, driver: bool) -> dict:
+    """One churn run (see churn_line).  driver: every step is one
+    kv_decode_step call (leavers released, joiners' prompts and everyone
+    else's new row appended together, tag check, attention, aborted requests
+    removed); otherwise the same work as separate calls (release, the
+    joiners' bulk append, then a decode step: append, verify, attention)."""
     import math as _m
 
     rng = np.random.default_rng(20268)
@@ -509,50 +508,94 @@ def churn_line(device, steps: int, warmup: int) -> dict:
                     int((-(-lens.astype(np.int64) // 16)).sum() * 2) + 4096,
                     float(np.float32(1 / np.sqrt(128))), steps=32768 + n_steps)
     arm = Arm(w, 0, device, n_steps)
-    kv, h = arm.kv, arm.pool.handle
+    kv = arm.kv
     rel_ws = torch.empty(kv.kv_release_workspace_size(S), dtype=torch.uint8, device=device)
+    step_ws = torch.empty(arm.pool.step_workspace_size(S, w.num_q_heads, w.q_tokens),
+                          dtype=torch.uint8, device=device)
     phase = {"release": [], "join": [], "step": []}
-    tokens, t_total = 0, 0.0
+    totals, rows_per_step = [], []
     for it in range(n_steps):
         leave = rng.choice(S, 3, replace=False)
         mask = np.zeros(S, np.uint8)
         mask[leave] = 1
         new = prompt_lens(3)
-        counts = np.zeros(S, np.int64)
-        counts[leave] = new
-        ks, vs = [], []
-        for r, n in zip(leave, new):
-            k, v = wl.kv_rows(w, int(r), 0, int(n), device=device, tag=1000 + it)
-            ks.append(k)
-            vs.append(v)
-        k_new, v_new = torch.cat(ks), torch.cat(vs)
-        ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).to(device)
         m_d = torch.from_numpy(mask).to(device)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        torch.cuda.synchronize()
-        torch.cuda._sleep(1_000_000)
-        ev[0].record()
-        arm.pool.release(S, arm.pt, arm.et, arm.sl, m_d, rel_ws)
-        ev[1].record()
-        arm.pool.append(S, k_new, v_new, ind, int(new.max()), arm.pt, arm.et, arm.sl)
-        ev[2].record()
-        arm.step()
-        ev[3].record()
-        torch.cuda.synchronize()
+        prompts = {}
+        for r, n in zip(leave, new):
+            prompts[int(r)] = wl.kv_rows(w, int(r), 0, int(n), device=device, tag=1000 + it)
+        if driver:
+            counts = np.ones(S, np.int64)
+            ks, vs = [], []
+            for r in range(S):
+                if r in prompts:  # the prompt, then its first decode row
+                    counts[r] = prompts[r][0].shape[0] + 1
+                    ks.append(prompts[r][0])
+                    vs.append(prompts[r][1])
+                ks.append(arm.k_steps[it][r:r + 1])
+                vs.append(arm.v_steps[it][r:r + 1])
+            k_new, v_new = torch.cat(ks), torch.cat(vs)
+            ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).to(device)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda.synchronize()
+            torch.cuda._sleep(1_000_000)
+            ev[0].record()
+            arm.pool.step(S, w.num_q_heads, w.q_tokens, m_d, k_new, v_new, ind,
+                          int(counts.max()), arm.pt, arm.et, arm.sl, arm.q_steps[it], w.sm_scale,
+                          arm.out, arm.mask, kv.KV_STEP_REMOVE_ABORTED, step_ws)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if it >= warmup:
+                totals.append(ev[0].elapsed_time(ev[1]))
+                rows_per_step.append(int(counts.sum()))
+        else:
+            counts = np.zeros(S, np.int64)
+            counts[leave] = new
+            k_new = torch.cat([prompts[int(r)][0] for r in leave])
+            v_new = torch.cat([prompts[int(r)][1] for r in leave])
+            ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).to(device)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            torch.cuda.synchronize()
+            torch.cuda._sleep(1_000_000)
+            ev[0].record()
+            arm.pool.release(S, arm.pt, arm.et, arm.sl, m_d, rel_ws)
+            ev[1].record()
+            arm.pool.append(S, k_new, v_new, ind, int(new.max()), arm.pt, arm.et, arm.sl)
+            ev[2].record()
+            arm.step()
+            ev[3].record()
+            torch.cuda.synchronize()
+            if it >= warmup:
+                for k_, (a, b) in zip(("release", "join", "step"), ((0, 1), (1, 2), (2, 3))):
+                    phase[k_].append(ev[a].elapsed_time(ev[b]))
+                totals.append(ev[0].elapsed_time(ev[3]))
         if arm.pool.error() != 0:
             raise RuntimeError(f"churn: {kv.kv_status_string(arm.pool.error())}")
-        if it >= warmup:
-            for k_, (a, b) in zip(("release", "join", "step"), ((0, 1), (1, 2), (2, 3))):
-                phase[k_].append(ev[a].elapsed_time(ev[b]))
-            t_total += ev[0].elapsed_time(ev[3])
-            tokens += S
+        if driver and int(arm.mask.sum().item()) != 0:
+            raise RuntimeError("churn: a request was aborted with every tag valid")
     del arm
     torch.cuda.empty_cache()
+    t = float(np.sum(totals))
+    res = {"decode_tokens_per_s": S * len(totals) / (t / 1e3),
+           "us_per_step": float(np.mean(totals) * 1e3)}
+    if driver:
+        res["rows_appended_per_step"] = float(np.mean(rows_per_step))
+    else:
+        res["us"] = {k_: float(np.mean(v) * 1e3) for k_, v in phase.items()}
+    return res
+
+
+def churn_line(device, steps: int, warmup: int) -> dict:
+    """Continuous batching over 128 request slots (64 q / 8 kv heads, head dim
+    128, page 16, e4m3; prompts lognormal, median 4k tokens, in [512, 32k]).
+    Every step, 3 requests finish and release their pages, 3 new ones join
+    the freed slots with their prompts, and every slot takes a decode step.
+    Measured two ways on the same seeded workload: one kv_decode_step call
+    per step, and the same work as separate calls (with its phase times)."""
     return {"workload": "churn: 128 request slots, 64 q / 8 kv heads, head dim 128, page 16, "
                         "e4m3; prompts lognormal (median 4k) in [512, 32k]; per step 3 leave "
-                        "(release) and 3 join (bulk prompt append), then a decode step",
-            "decode_tokens_per_s": tokens / (t_total / 1e3),
-            "us": {k_: float(np.mean(v) * 1e3) for k_, v in phase.items()}}
+                        "and 3 join with their prompts, then every slot decodes one token",
+            "step_driver": _churn(device, steps, warmup, True),
+            "separate_calls": _churn(device, steps, warmup, False)}
 
 
 # ------------------------------------------------------------ verify overhead
