@@ -337,41 +337,76 @@ class Arm:
         del graphs
         return t0.elapsed_time(t1)
 
-    def run_e2e(self, steps: int, warmup: int):
-        """Same steps through host buffers: H2D of the new rows and the queries
-        from pinned memory, D2H of the outputs and abort mask, all timed."""
-        w, B = self.w, self.w.B
-        kh = [self.k_steps[self.step_no + i].cpu().pin_memory() for i in range(steps + warmup)]
-        vh = [self.v_steps[self.step_no + i].cpu().pin_memory() for i in range(steps + warmup)]
-        qh = [self.q_steps[self.step_no + i].cpu().pin_memory() for i in range(steps + warmup)]
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        mask_h = torch.empty(self.mask.shape, dtype=self.mask.dtype).pin_memory()
-        kd, vd, qd = (torch.empty_like(self.k_steps[0]), torch.empty_like(self.v_steps[0]),
-                      torch.empty_like(self.q_steps[0]))
+    def run_e2e(self, steps: int, warmup: int, graph: bool = True):
+        """The next steps through host buffers and the one-call step API: per
+        step, H2D copies of its new rows and queries from pinned host memory,
+        kv_decode_step (tag check, append, attention), and D2H copies of the
+        output and the abort mask into pinned memory, all inside the timed
+        region.  graph: each step (copies included) is captured as a CUDA
+        graph and the graphs are replayed in order, as a serving loop replays
+        its step; otherwise every call is launched eagerly."""
+        kv, w, B = self.kv, self.w, self.w.B
+        n = steps + warmup
+        s0 = self.step_no
+        # one pinned staging buffer per step holding its K rows, V rows and
+        # queries back to back (one H2D copy), and one device buffer holding
+        # the output then the abort mask (one D2H copy)
+        parts = [self.k_steps[0], self.v_steps[0], self.q_steps[0]]
+        sizes = [t.numel() * 2 for t in parts]
+        offs = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+        stage_h = []
+        for i in range(n):
+            buf = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+            for t, o, sz in zip((self.k_steps[s0 + i], self.v_steps[s0 + i],
+                                 self.q_steps[s0 + i]), offs, sizes):
+                buf[o:o + sz].copy_(t.cpu().contiguous().view(torch.uint8).reshape(-1))
+            stage_h.append(buf)
+        stage_d = torch.empty(offs[-1], dtype=torch.uint8, device=self.device)
+        kd, vd, qd = (stage_d[o:o + sz].view(torch.bfloat16).view(t.shape)
+                      for t, o, sz in zip(parts, offs, sizes))
+        out_bytes = self.out.numel() * 2
+        res_d = torch.empty(out_bytes + B, dtype=torch.uint8, device=self.device)
+        out_d = res_d[:out_bytes].view(torch.bfloat16).view(self.out.shape)
+        mask_d = res_d[out_bytes:]
+        res_h = torch.empty(out_bytes + B, dtype=torch.uint8).pin_memory()
+        ws = torch.empty(self.pool.step_workspace_size(B, w.num_q_heads, w.q_tokens),
+                         dtype=torch.uint8, device=self.device)
 
         def one(i):
-            kd.copy_(kh[i], non_blocking=True)
-            vd.copy_(vh[i], non_blocking=True)
-            qd.copy_(qh[i], non_blocking=True)
-            s = self.step_no
-            self.k_steps[s], self.v_steps[s], self.q_steps[s] = kd, vd, qd
-            self.step()
-            out_h.copy_(self.out, non_blocking=True)
-            mask_h.copy_(self.mask, non_blocking=True)
+            stage_d.copy_(stage_h[i], non_blocking=True)
+            self.pool.step(B, w.num_q_heads, w.q_tokens, None, kd, vd, self.ones, 1, self.pt,
+                           self.et, self.sl, qd, w.sm_scale, out_d, mask_d, 0, ws)
+            res_h.copy_(res_d, non_blocking=True)
 
+        torch.cuda.synchronize()
+        if graph:
+            graphs = []
+            for i in range(n):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    one(i)
+                graphs.append(g)
+            run = lambda i: graphs[i].replay()  # noqa: E731
+        else:
+            run = one
         for i in range(warmup):
-            one(i)
+            run(i)
         torch.cuda.synchronize()
         barrier()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for i in range(steps):
-            one(warmup + i)
+            run(warmup + i)
         t1.record()
         torch.cuda.synchronize()
-        h2d = kd.numel() * 2 + vd.numel() * 2 + qd.numel() * 2
-        d2h = out_h.numel() * 2 + mask_h.numel()
+        if self.pool.error() != 0:
+            raise RuntimeError(f"e2e steps: {kv.kv_status_string(self.pool.error())}")
+        if int(res_h[out_bytes:].sum()) != 0:
+            raise RuntimeError("e2e steps: a request was aborted with every tag valid")
+        self.step_no += n
+        self.lens += n
+        h2d, d2h = stage_d.numel(), res_d.numel()
         return t0.elapsed_time(t1), h2d, d2h
 
 
@@ -1002,7 +1037,7 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    total_steps = 3 * (args.steps + args.warmup)
+    total_steps = 4 * (args.steps + args.warmup)
     graph_steps = 0 if args.no_overhead else 2 * (args.overhead_replays + 8)
     w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + graph_steps + 2)
     if args.batch != w.B:
@@ -1014,7 +1049,8 @@ def main():
     total_ms, per, lens_timed, launches = arm.run(args.steps, args.warmup)
     graph_ms = arm.run_graphs(args.steps, args.warmup)
     clocks = sampler.stop()
-    e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup)
+    e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup, graph=True)
+    e2e_eager_ms, _, _ = arm.run_e2e(args.steps, args.warmup, graph=False)
     overhead = None
     if not args.no_overhead:
         overhead = {"gqa_batch": graph_overhead(arm, args.overhead_replays)}
@@ -1027,6 +1063,7 @@ def main():
     value = tokens / (max_ms / 1e3)
     eager_value = tokens / (eager_ms / 1e3)
     e2e_value = tokens / (reduce_max(e2e_ms) / 1e3)
+    e2e_eager_value = tokens / (reduce_max(e2e_eager_ms) / 1e3)
     split_ms = per[:, 2]
     attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_timed]
     split_bytes = [algorithmic_bytes(w, L, 0, include_out=False) for L in lens_timed]
@@ -1144,7 +1181,11 @@ def main():
         "latent_verify": latent,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "mode": "per step: one H2D copy of its rows and queries from pinned memory, "
+                        "one kv_decode_step call, one D2H copy of output and abort mask; each "
+                        "step captured as a CUDA graph and replayed in order",
+                "eager_value": e2e_eager_value},
         "gpu_launches": launches,
         "clocks": clocks,
     }
