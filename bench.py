@@ -973,6 +973,10 @@ def main():
     ap.add_argument("--latent-only", type=int, default=0, metavar="B",
                     help="run only the latent verify workload with B requests and print its "
                          "line (small profiling captures)")
+    ap.add_argument("--bulk-only", type=int, default=0, metavar="B",
+                    help="run only the bulk (prefill handoff) append of B requests of the GQA "
+                         "batch workload into an e4m3 pool and print its line (small "
+                         "profiling captures)")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests of the GQA batch workload to use (32 = the full workload; "
                          "fewer only for small profiling captures)")
@@ -1018,6 +1022,19 @@ def main():
         w.num_pages = int(w.B * (-(-(131072 + w.steps) // 16))) + 64
         arm = Arm(w, 0, device, args.steps + args.warmup)
         print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
+        return
+
+    if args.bulk_only > 0:
+        device = torch.device("cuda", local)
+        peak = 6681.5
+        try:
+            peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+        except Exception:
+            pass
+        w = wl.subset(wl.gqa_batch(), args.bulk_only)
+        for _ in range(args.warmup):
+            bulk_append_line(w, 0, device, peak)
+        print(json.dumps([bulk_append_line(w, 0, device, peak) for _ in range(args.steps)]))
         return
 
     if args.latent_only > 0:

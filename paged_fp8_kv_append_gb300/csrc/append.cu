@@ -383,6 +383,19 @@ constexpr int kTileWarps = 8;
 constexpr int kTileChunks = 8;   // 16-byte source chunks per lane (P * D <= 2048)
 constexpr int kLatChunks = 18;   // per lane: ceil(8 rows * 72 chunks / 32)
 
+// A whole 16 x 128 page whose scale is below 2^-90, element by element with
+// the IEEE divide (kept out of line: it is rare and its code is long).
+__device__ __noinline__ void page_ieee(const uint16_t* src, long long src_stride, bool dim_major,
+                                       float s, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < 16 * 128; e += 32) {
+    const int i = e >> 7, dd = e & 127;
+    const float x = bf16_bits_to_f32(src[i * src_stride + dd]);
+    dst[dim_major ? dd * 16 + i : i * 128 + dd] =
+        (uint8_t)(e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xFFu);
+  }
+}
+
 // A whole 16-token page of a 128-dim V tile, transposed in registers: lane l
 // loads dims 4l..4l+3 of every row and writes those 4 dim rows of 16 slots.
 __device__ void v_page_16x128(const uint16_t* src, long long src_stride, bool fp8,
@@ -408,11 +421,23 @@ __device__ void v_page_16x128(const uint16_t* src, long long src_stride, bool fp
     }
     return;
   }
-  float m = 0.0f;
+  uint32_t mb = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(amax2(x[i].x), amax2(x[i].y)));
-  const float s = scale_from_amax(warp_max(m)), rs = __frcp_rn(s);
+  for (int i = 0; i < 16; ++i) mb = absbits_max2(absbits_max2(mb, x[i].x), x[i].y);
+  mb = absbits_warp_max(mb);
+  float amax = __uint_as_float(mb << 16);
+  if (mb > 0x7F80u) {  // a NaN: the float maximum skips it
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(amax2(x[i].x), amax2(x[i].y)));
+    amax = warp_max(m);
+  }
+  const float s = scale_from_amax(amax), rs = __frcp_rn(s);
   if (lane == 0) *scale_slot = s;
+  if (!scale_fast_ok(s)) {
+    page_ieee(src, src_stride, true, s, dst);
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     uint32_t c[8];
@@ -420,8 +445,8 @@ __device__ void v_page_16x128(const uint16_t* src, long long src_stride, bool fp
     for (int j = 0; j < 8; ++j) {
       const uint32_t a = k < 2 ? x[2 * j].x : x[2 * j].y, b = k < 2 ? x[2 * j + 1].x
                                                                     : x[2 * j + 1].y;
-      c[j] = (k & 1) ? quant2_rs(bf16_hi(a), bf16_hi(b), s, rs)
-                     : quant2_rs(bf16_lo(a), bf16_lo(b), s, rs);
+      c[j] = (k & 1) ? e4m3x2(div_fresh(bf16_hi(a), s, rs), div_fresh(bf16_hi(b), s, rs))
+                     : e4m3x2(div_fresh(bf16_lo(a), s, rs), div_fresh(bf16_lo(b), s, rs));
     }
     *reinterpret_cast<uint4*>(dst + (4 * lane + k) * 16) =
         make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
@@ -444,27 +469,37 @@ __device__ void k_page_16x128(const uint16_t* src, long long src_stride, bool fp
       *reinterpret_cast<uint4*>(dst + ((2 * t + i0) * 128 + 8 * c) * 2) = x[t];
     return;
   }
-  float m = 0.0f;
+  uint32_t mb = 0;
 #pragma unroll
-  for (int t = 0; t < 8; ++t) m = fmaxf(m, amax8(x[t]));
-  const float s = scale_from_amax(warp_max(m)), rs = __frcp_rn(s);
+  for (int t = 0; t < 8; ++t) mb = absbits_max8(mb, x[t]);
+  mb = absbits_warp_max(mb);
+  float amax = __uint_as_float(mb << 16);
+  if (mb > 0x7F80u) {  // a NaN: the float maximum skips it
+    float m = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m = fmaxf(m, amax8(x[t]));
+    amax = warp_max(m);
+  }
+  const float s = scale_from_amax(amax), rs = __frcp_rn(s);
   if (lane == 0) *scale_slot = s;
-#pragma unroll
-  for (int t = 0; t < 8; ++t)
-    *reinterpret_cast<uint2*>(dst + (2 * t + i0) * 128 + 8 * c) = quant8_rs(x[t], s, rs);
-}
-
-__device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, int D, bool fp8,
-                          bool fresh, float* scale_slot, uint8_t* dst, bool dim_major, int P,
-                          int slot0, uint8_t* wtile, bool requant) {
-  const int lane = threadIdx.x & 31;
-  if (nrows == 16 && P == 16 && D == 128) {  // a whole page (fresh by construction)
-    if (dim_major)
-      v_page_16x128(src, src_stride, fp8, scale_slot, dst);
-    else
-      k_page_16x128(src, src_stride, fp8, scale_slot, dst);
+  if (!scale_fast_ok(s)) {
+    page_ieee(src, src_stride, false, s, dst);
     return;
   }
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    *reinterpret_cast<uint2*>(dst + (2 * t + i0) * 128 + 8 * c) =
+        make_uint2(quant_word_fresh(x[t].x, s, rs) | (quant_word_fresh(x[t].y, s, rs) << 16),
+                   quant_word_fresh(x[t].z, s, rs) | (quant_word_fresh(x[t].w, s, rs) << 16));
+}
+
+// Any other tile: part of a page, another page shape, or the re-quantising
+// mode's re-encoding (kept out of line so the whole-page code stays small).
+__device__ __noinline__ void tile_warp_generic(const uint16_t* src, long long src_stride,
+                                               int nrows, int D, bool fp8, bool fresh,
+                                               float* scale_slot, uint8_t* dst, bool dim_major,
+                                               int P, int slot0, uint8_t* wtile, bool requant) {
+  const int lane = threadIdx.x & 31;
   const int cpr = D / 8, total = nrows * cpr;
   uint4 v[kTileChunks];
 #pragma unroll
@@ -548,6 +583,21 @@ __device__ void tile_warp(const uint16_t* src, long long src_stride, int nrows, 
     }
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void tile_warp(const uint16_t* src, long long src_stride, int nrows,
+                                          int D, bool fp8, bool fresh, float* scale_slot,
+                                          uint8_t* dst, bool dim_major, int P, int slot0,
+                                          uint8_t* wtile, bool requant) {
+  if (nrows == 16 && P == 16 && D == 128) {  // a whole page (fresh by construction)
+    if (dim_major)
+      v_page_16x128(src, src_stride, fp8, scale_slot, dst);
+    else
+      k_page_16x128(src, src_stride, fp8, scale_slot, dst);
+    return;
+  }
+  tile_warp_generic(src, src_stride, nrows, D, fp8, fresh, scale_slot, dst, dim_major, P, slot0,
+                    wtile, requant);
 }
 
 // Work items of a bulk append: every (request, page this call touches),

@@ -78,6 +78,35 @@ __device__ __forceinline__ float div_fast(float x, float s, float rs) {
   return copysignf(fabsf(q0) < 1024.0f ? q1 : q0, x);
 }
 
+// x / s where |x| <= amax and s = scale_from_amax(amax) >= 2^-90: the rows of
+// a block whose scale they set.  There |x * rs| <= 448 (1 + 2^-22) < 1024, so
+// div_fast's guard always takes the corrected quotient and can be left out.
+__device__ __forceinline__ float div_fresh(float x, float s, float rs) {
+  const float q0 = x * rs;
+  return copysignf(__fmaf_rn(__fmaf_rn(-q0, s, x), rs, q0), x);
+}
+
+// e4m3 codes of the two bf16 values of w, under div_fresh's conditions
+__device__ __forceinline__ uint32_t quant_word_fresh(uint32_t w, float s, float rs) {
+  return e4m3x2(div_fresh(bf16_lo(w), s, rs), div_fresh(bf16_hi(w), s, rs));
+}
+
+// Largest magnitude among bf16 values, on their bit patterns: with the sign
+// bits cleared, finite and infinite magnitudes order like unsigned integers
+// (NaN patterns order above infinity: a result above 0x7F80 means a NaN was
+// present, which the caller handles with the float maximum, which skips it).
+__device__ __forceinline__ uint32_t absbits_max2(uint32_t m, uint32_t w) {
+  return __vmaxu2(m, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ uint32_t absbits_max8(uint32_t m, uint4 v) {
+  return absbits_max2(absbits_max2(m, v.x), absbits_max2(v.y & 0x7FFF7FFFu,
+                      __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+}
+// the two halves of a packed maximum, reduced over the warp
+__device__ __forceinline__ uint32_t absbits_warp_max(uint32_t m) {
+  return __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
+}
+
 // the division as the append kernels perform it, element by element
 __device__ __forceinline__ float div_by_scale(float x, float s, float rs) {
   return scale_fast_ok(s) ? div_fast(x, s, rs) : __fdiv_rn(x, s);

@@ -1,5 +1,5 @@
-// Exhaustive check of div_by_scale (quant.cuh) against CUDA's correctly
-// rounded division: for every bf16 bit pattern x and every scale the append
+// Exhaustive check of div_by_scale and div_fresh (quant.cuh) against CUDA's
+// correctly rounded division: for every bf16 bit pattern x and every scale the append
 // kernels can produce (amax / 448 of a positive finite bf16 amax, and 1.0),
 // the e4m3 code of the quotient must be the same.  Test infrastructure:
 // built and run by tests/test_quant_exhaustive_gpu.py.  Prints the number of
@@ -24,7 +24,12 @@ __global__ void check(const float* scales, long long nscales, unsigned long long
     const float rs = __frcp_rn(s);
     const uint32_t ref = kvfp8::e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xFFu;
     const uint32_t got = kvfp8::e4m3x2(kvfp8::div_by_scale(x, s, rs), 0.0f) & 0xFFu;
-    if (ref != got) {
+    // div_fresh serves a block's own rows (|x| <= its amax, so |x * rs| <=
+    // 448 (1 + 2^-22)); checked here on the wider |x * rs| < 1024
+    bool fresh_bad = false;
+    if (kvfp8::scale_fast_ok(s) && fabsf(x * rs) < 1024.0f)
+      fresh_bad = (kvfp8::e4m3x2(kvfp8::div_fresh(x, s, rs), 0.0f) & 0xFFu) != ref;
+    if (ref != got || fresh_bad) {
       atomicAdd(bad, 1ull);
       atomicMin(first, (unsigned long long)i);
     }
