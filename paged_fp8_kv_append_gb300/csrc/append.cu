@@ -698,16 +698,59 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
   }
 }
 
+// Block-wide largest magnitude of the latent rows a CTA holds (bit-pattern
+// maximum; a NaN falls back to the float maximum, which skips it).
+__device__ float latent_block_amax(const uint4 (&v)[kLatChunks], uint32_t* redu) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t mb = 0;
+#pragma unroll
+  for (int t = 0; t < kLatChunks; ++t) mb = absbits_max8(mb, v[t]);
+  mb = absbits_warp_max(mb);
+  if (lane == 0) redu[warp] = mb;
+  __syncthreads();
+  mb = __reduce_max_sync(0xffffffffu, lane < kTileWarps ? redu[lane] : 0u);
+  float amax = __uint_as_float(mb << 16);
+  if (mb > 0x7F80u) {  // uniform across the block
+    float m = 0.0f;
+#pragma unroll
+    for (int t = 0; t < kLatChunks; ++t) m = fmaxf(m, amax8(v[t]));
+    m = warp_max(m);
+    __syncthreads();
+    if (lane == 0) reinterpret_cast<float*>(redu)[warp] = m;
+    __syncthreads();
+    amax = warp_max(lane < kTileWarps ? reinterpret_cast<float*>(redu)[lane] : 0.0f);
+  }
+  __syncthreads();  // redu is reused by the next page
+  return amax;
+}
+
+// Rows of a latent page quantised against a scale they did not set (a partly
+// filled page) or a scale below 2^-90: the guarded division (out of line).
+__device__ __noinline__ void latent_rows_slow(const uint4 (&v)[kLatChunks], int my_rows, int cpr,
+                                              int Dk, float s, float rs, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < kLatChunks; ++t) {
+    const int q = lane + 32 * t, qd = q / cpr, qm = q - qd * cpr;
+    if (qd < my_rows)
+      *reinterpret_cast<uint2*>(dst + (long long)qd * kTileWarps * Dk + 8 * qm) =
+          quant8_rs(v[t], s, rs);
+  }
+}
+
 // Latent: persistent CTAs; each CTA takes (request, page) items in turn.
+// kCpr: 16-byte chunks per row when known at compile time (72 for 576-wide
+// rows), 0 to take it from the pool.
+template <int kCpr>
 __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float red[kTileWarps];
+  __shared__ uint32_t redu[kTileWarps];
   __shared__ int wsum[kTileWarps];
   const kv_pool_desc& d = a.d;
   const long long P = d.page_size;
-  const int Dk = d.head_dim_k, cpr = Dk / 8;
+  const int Dk = kCpr > 0 ? 8 * kCpr : d.head_dim_k, cpr = kCpr > 0 ? kCpr : Dk / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = min(a.B, (int)d.ctl[KV_CTL_APPEND_STOP]);
   int* pre = reinterpret_cast<int*>(smem);
@@ -729,57 +772,49 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
     const bool fresh = jp * P >= L0;
     // warp w takes rows w, w + 8, ... of this call's rows in the page
     const int my_rows = nrows > warp ? (nrows - warp + kTileWarps - 1) / kTileWarps : 0;
-    const int tot = my_rows * cpr;
+    const uint16_t* src = a.k_new + (row0 + warp) * Dk;
+    // chunk t of this lane: q = lane + 32 t, row q / cpr of the warp's rows
     uint4 v[kLatChunks];
 #pragma unroll
     for (int t = 0; t < kLatChunks; ++t) {
-      const int q = lane + 32 * t;
-      const int i = warp + kTileWarps * (q / cpr);
-      v[t] = q < tot ? *reinterpret_cast<const uint4*>(a.k_new + (row0 + i) * Dk + 8 * (q % cpr))
-                     : make_uint4(0, 0, 0, 0);
+      const int q = lane + 32 * t, qd = q / cpr, qm = q - qd * cpr;
+      v[t] = qd < my_rows
+                 ? *reinterpret_cast<const uint4*>(src + (long long)qd * kTileWarps * Dk + 8 * qm)
+                 : make_uint4(0, 0, 0, 0);
     }
     float s;
+    bool own_rows = false;  // every row of the page's block is in this call
     if (fresh) {
-      float m = 0.0f;
-#pragma unroll
-      for (int t = 0; t < kLatChunks; ++t) m = fmaxf(m, amax8(v[t]));
-      m = warp_max(m);
-      if (lane == 0) red[warp] = m;
-      __syncthreads();
-      m = lane < kTileWarps ? red[lane] : 0.0f;
-      s = scale_from_amax(warp_max(m));
+      s = scale_from_amax(latent_block_amax(v, redu));
       if (threadIdx.x == 0) d.k_scale[p] = s;
-      __syncthreads();  // red is reused by the next page
+      own_rows = true;
     } else {
       s = d.k_scale[p];
       if (d.scale_mode == KV_SCALE_REQUANTIZE) {  // re-encode the rows already written
-        float m = 0.0f;
-#pragma unroll
-        for (int t = 0; t < kLatChunks; ++t) m = fmaxf(m, amax8(v[t]));
-        m = warp_max(m);
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        m = lane < kTileWarps ? red[lane] : 0.0f;
-        const float s_new = scale_from_amax(warp_max(m));
+        const float s_new = scale_from_amax(latent_block_amax(v, redu));
         if (s_new > s) {
           requant_block(static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, slot0, Dk,
                         false, (int)P, s, s_new, threadIdx.x, kTileWarps * 32);
           s = s_new;
+          own_rows = true;  // the new scale is the amax of exactly these rows
         }
-        __syncthreads();  // old scale read and red consumed by every thread
+        __syncthreads();  // the old scale is read by every thread
         if (threadIdx.x == 0 && s_new > d.k_scale[p]) d.k_scale[p] = s_new;
       }
     }
     const float rs = __frcp_rn(s);
-    uint8_t* dst = static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk;
+    uint8_t* dst = static_cast<uint8_t*>(d.k_cache) + (long long)(p * P + slot0 + warp) * Dk;
+    if (own_rows && scale_fast_ok(s)) {  // uniform across the block
 #pragma unroll
-    for (int t = 0; t < kLatChunks; ++t) {
-      const int q = lane + 32 * t;
-      if (q < tot) {
-        const int i = warp + kTileWarps * (q / cpr);
-        *reinterpret_cast<uint2*>(dst + (long long)(slot0 + i) * Dk + 8 * (q % cpr)) =
-            quant8_rs(v[t], s, rs);
+      for (int t = 0; t < kLatChunks; ++t) {
+        const int q = lane + 32 * t, qd = q / cpr, qm = q - qd * cpr;
+        if (qd < my_rows)
+          *reinterpret_cast<uint2*>(dst + (long long)qd * kTileWarps * Dk + 8 * qm) = make_uint2(
+              quant_word_fresh(v[t].x, s, rs) | (quant_word_fresh(v[t].y, s, rs) << 16),
+              quant_word_fresh(v[t].z, s, rs) | (quant_word_fresh(v[t].w, s, rs) << 16));
       }
+    } else {
+      latent_rows_slow(v, my_rows, cpr, Dk, s, rs, dst);
     }
   }
 }
@@ -825,13 +860,18 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   if (persist && a.d.layout == KV_LAYOUT_LATENT &&
       Pl <= 8 * kTileWarps &&
       (long long)((Pl + kTileWarps - 1) / kTileWarps) * (a.d.head_dim_k / 8) <= 32 * kLatChunks) {
+    const bool k72 = a.d.head_dim_k == 576;
     if (pre_bytes > 48 * 1024) {
-      e = cudaFuncSetAttribute(append_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)pre_bytes);
+      e = k72 ? cudaFuncSetAttribute(append_latent_kernel<72>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pre_bytes)
+              : cudaFuncSetAttribute(append_latent_kernel<0>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pre_bytes);
       if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(append_latent_kernel, dim3((unsigned)(2 * sms)), dim3(kTileWarps * 32),
-                   pre_bytes, s, a);
+    e = k72 ? launch_pdl(append_latent_kernel<72>, dim3((unsigned)(2 * sms)),
+                         dim3(kTileWarps * 32), pre_bytes, s, a)
+            : launch_pdl(append_latent_kernel<0>, dim3((unsigned)(2 * sms)),
+                         dim3(kTileWarps * 32), pre_bytes, s, a);
     if (e == cudaSuccess) ++*launches;
     return e;
   }
