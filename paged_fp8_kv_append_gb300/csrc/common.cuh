@@ -109,8 +109,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // their memory visible) before its first global-memory access, so the order
 // of the stream is kept exactly while a kernel's launch overlaps the tail of
 // the previous one.  `trigger` lets the next kernel launch early (its CTAs
-// then sit in its own wait); the persistent split kernels do not trigger, so
-// nothing waits resident beside them.
+// then sit in its own wait).  Every kernel triggers right after its own wait,
+// so a kernel's dependents launch only once the kernel before it has
+// completed: at most two grids of the stream are resident at a time.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -164,6 +165,12 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 

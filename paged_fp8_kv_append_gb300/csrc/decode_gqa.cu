@@ -278,6 +278,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
     gqa_split_kernel(const DecodeArgs a) {
   pdl_wait();
+  pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
   using C = GqaCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem + C::OFF_RING;
@@ -744,7 +745,10 @@ constexpr int kCombineWarps = 8;
 // partials k, k + S, ..., then the S running states are merged through
 // shared memory.  S > 1 when a segment has many partials (few long requests),
 // so the merge of one row is no long serial chain.
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a, int S) {
+// NG: 128-dim groups of a row (Dv / 128: 1 or 4).
+template <int NG>
+__global__ void __launch_bounds__(kCombineWarps * 32, 2)
+    combine_kernel(const DecodeArgs a, int S) {
   __shared__ float st_o[kCombineWarps][512];
   __shared__ float st_ml[kCombineWarps][2];
   pdl_wait();
@@ -754,8 +758,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
   const long long item = (long long)blockIdx.x * (kCombineWarps / S) + warp / S;
   const int Hkv = a.d.num_kv_heads;
   const long long nitems = (long long)a.B * Hkv * a.R;
-  const int Dv = a.d.head_dim_v;
-  const int ngroups = Dv / 128;  // Dv is 128 or 512
+  const int Dv = 128 * NG;
+  constexpr int ngroups = NG;
   float acc[4][4];
   float M = -INFINITY, L = 0.0f;
 #pragma unroll
@@ -786,26 +790,59 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
       const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
       const long long slot0 = seg + c0;
       const int R8 = a.R8;
-#pragma unroll 2
-      for (int c = sub; c <= c1 - c0; c += S) {
-        const long long rowi = ((slot0 + c) * Hs + hw) * R8 + nl;
-        const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowi * 2);
-        float4 o[4];
+      // this warp's pieces c = sub + S j, j < cnt, merged 32 at a time: each
+      // lane reads one piece's (max, sum), the chunk's max and weights come
+      // from warp reductions, then the weighted outputs are summed with
+      // independent loads (no chain through a running max)
+      const int cnt = (c1 - c0 + 1 - sub + S - 1) / S;
+      for (int j0 = 0; j0 < cnt; j0 += 32) {
+        const int j = j0 + lane;
+        float mj = -INFINITY, lj = 0.0f;
+        long long rowj = 0;
+        if (j < cnt) {
+          rowj = ((slot0 + sub + (long long)S * j) * Hs + hw) * R8 + nl;
+          const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowj * 2);
+          mj = ml.x;
+          lj = ml.y;
+        }
+        const float Mc = warp_max(mj);
+        if (Mc == -INFINITY) continue;  // no piece of the chunk saw anything visible
+        const float Mn = fmaxf(M, Mc);
+        const float sa = exp2f(M - Mn);  // 0 while nothing is accumulated (M = -inf)
+        const float wj = (mj == -INFINITY) ? 0.0f : exp2f(mj - Mn);
+        L = L * sa + warp_sum(lj * wj);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q < ngroups)
-            o[q] = *reinterpret_cast<const float4*>(a.ws.o_part + rowi * Dv + 128 * q + 4 * lane);
-        if (ml.x == -INFINITY) continue;  // piece saw nothing visible
-        const float Mn = fmaxf(M, ml.x);
-        const float sa = exp2f(M - Mn), sb = exp2f(ml.x - Mn);
-        L = L * sa + ml.y * sb;
+          acc[q][0] *= sa, acc[q][1] *= sa, acc[q][2] *= sa, acc[q][3] *= sa;
+        const int nj = min(32, cnt - j0);
+        // kU pieces' loads are issued before their products are summed
+        constexpr int kU = 8 / NG;
+        for (int k0 = 0; k0 < nj; k0 += kU) {
+          float4 o[kU][NG];
+          float wk[kU];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q < ngroups) {
-            acc[q][0] = acc[q][0] * sa + o[q].x * sb;
-            acc[q][1] = acc[q][1] * sa + o[q].y * sb;
-            acc[q][2] = acc[q][2] * sa + o[q].z * sb;
-            acc[q][3] = acc[q][3] * sa + o[q].w * sb;
+          for (int u = 0; u < kU; ++u) {
+            const bool ok = k0 + u < nj;  // uniform across the warp
+            wk[u] = __shfl_sync(0xffffffffu, wj, ok ? k0 + u : 0);
+            const long long rk = __shfl_sync(0xffffffffu, rowj, ok ? k0 + u : 0);
+#pragma unroll
+            for (int q = 0; q < NG; ++q)
+              o[u][q] = ok ? *reinterpret_cast<const float4*>(a.ws.o_part + rk * Dv + 128 * q +
+                                                              4 * lane)
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (!ok) wk[u] = 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            // a piece that saw nothing has weight 0 and adds nothing
+            const bool use = wk[u] != 0.0f;
+#pragma unroll
+            for (int q = 0; q < NG; ++q) {
+              acc[q][0] = use ? __fmaf_rn(o[u][q].x, wk[u], acc[q][0]) : acc[q][0];
+              acc[q][1] = use ? __fmaf_rn(o[u][q].y, wk[u], acc[q][1]) : acc[q][1];
+              acc[q][2] = use ? __fmaf_rn(o[u][q].z, wk[u], acc[q][2]) : acc[q][2];
+              acc[q][3] = use ? __fmaf_rn(o[u][q].w, wk[u], acc[q][3]) : acc[q][3];
+            }
           }
         }
         M = Mn;
@@ -920,7 +957,11 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s, int* laun
   const long long per_cta = kCombineWarps / S;
   const long long blocks = (items + per_cta - 1) / per_cta;
   const cudaError_t e =
-      launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, a, S);
+      a.d.head_dim_v == 128
+          ? launch_pdl(combine_kernel<1>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+                       a, S)
+          : launch_pdl(combine_kernel<4>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+                       a, S);
   if (e == cudaSuccess) ++*launches;
   return e;
 }

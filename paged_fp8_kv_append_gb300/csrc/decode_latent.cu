@@ -276,6 +276,7 @@ __device__ void seg_next(Seg& s, const int32_t* pfx, int B, int groups) {
 
 __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeArgs a) {
   pdl_wait();
+  pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* q_s = smem + OFF_Q;
   uint8_t* kv_s = smem + OFF_KV;
