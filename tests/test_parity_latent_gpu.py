@@ -87,8 +87,9 @@ def test_latent_ring_wraps_and_abort():
 
 def test_latent_verify_full_size_sampled():
     """The 64-request latent verify workload (lognormal contexts 8k..64k, 128
-    heads x 4 draft tokens) at full size; the oracle checks a sample of
-    requests on a subset of heads (heads are independent given the cache)."""
+    heads x 4 draft tokens) at full size; the oracle checks a sample: a few
+    heads of three requests (heads are independent given the cache) and all
+    heads and draft tokens of the four shortest requests."""
     w = wl.latent_verify()
     kvp = __import__("paged_fp8_kv_append_gb300")
     dev = kvp.KVPool(w.num_pages, 64, 1, 576, 512, dtype=0, layout=1, device="cuda",
@@ -114,9 +115,13 @@ def test_latent_verify_full_size_sampled():
     import oracle
 
     rng = np.random.default_rng(2)
-    heads = [0, 37, 127]
     got_all = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
-    for r in sorted(rng.choice(B, 2, replace=False).tolist()) + [int(np.argmax(w.lens))]:
+    # three heads of two seeded requests and of the longest; every head and
+    # draft token of the four shortest requests
+    cases = [(r, [0, 37, 127]) for r in sorted(rng.choice(B, 2, replace=False).tolist())]
+    cases.append((int(np.argmax(w.lens)), [0, 37, 127]))
+    cases += [(int(r), list(range(128))) for r in np.argsort(w.lens, kind="stable")[:4]]
+    for r, heads in cases:
         L = int(w.lens[r])
         npg = -(-L // 64) + 1
         pool = oracle.Pool(npg, 64, 1, 576, 512, dtype=0, layout=1)
