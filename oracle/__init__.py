@@ -295,5 +295,7 @@ def step(pool: Pool, leave_mask, k_new, v_new, new_indptr, max_new, page_table, 
     if remove_aborted:
         stale = (mask & ABORT_TAG).astype(np.uint8)
         if stale.any():
-            status = status or release(pool, page_table, exp_tags, seq_lens, stale)
+            # runs whatever an earlier phase reported; the first error is kept
+            st = release(pool, page_table, exp_tags, seq_lens, stale)
+            status = status or st
     return status, mask, out, written

@@ -178,3 +178,76 @@ def test_step_latent_two_draft_tokens():
     for x, y in zip(*res):
         assert np.array_equal(x, y)
     assert res[0][5].tolist() == [1, 1, 1]
+
+
+def _check_invariants(pool, pt, et, sl):
+    """Page conservation and consistency after a step: the free list's tail
+    and the live mappings together hold every page exactly once, every live
+    mapping carries its page's current tag, and each request maps exactly
+    its first ceil(L / P) entries."""
+    head = int(pool.free_head[0])
+    free = pool.free_list[head:].tolist()
+    mapped = []
+    for r in range(len(sl)):
+        n = -(-int(sl[r]) // P)
+        assert all(p >= 0 for p in pt[r, :n]) and all(p == -1 for p in pt[r, n:]), r
+        mapped += pt[r, :n].tolist()
+        for j in range(n):
+            assert et[r, j] == pool.tags[pt[r, j]], (r, j)
+    assert sorted(free + mapped) == list(range(pool.num_pages))
+
+
+def test_step_random_sequence_invariants():
+    """Forty random steps (leaves, joins, decode rows, injected stale tags,
+    runs out of pages now and then): after every step the pool is
+    consistent, the aborted set is exactly the injected stale requests and
+    the unserved ones are exactly those at or after the append's stop."""
+    rng = np.random.default_rng(7)
+    B, mp = 6, 12
+    pool = _pool(24)
+    pt, et, sl = np.full((B, mp), -1, np.int32), np.zeros((B, mp), np.uint32), np.zeros(B, np.int32)
+    saw = {"oop": 0, "stale": 0, "join": 0}
+    for step in range(40):
+        live = [r for r in range(B) if sl[r] > 0]
+        leave = np.zeros(B, np.uint8)
+        for r in live:
+            if rng.random() < 0.15:
+                leave[r] = 1
+        counts = np.zeros(B, np.int64)
+        for r in range(B):
+            if sl[r] > 0 and not leave[r]:
+                counts[r] = 1
+            elif rng.random() < 0.5:
+                counts[r] = int(rng.integers(1, 30))  # a new request's prompt
+                saw["join"] += 1
+        counts = np.minimum(counts, mp * P - np.where(leave == 1, 0, sl))
+        stale = []
+        cand = [r for r in live if not leave[r]]
+        if cand and rng.random() < 0.3:
+            r = int(rng.choice(cand))
+            j = int(rng.integers(0, -(-int(sl[r]) // P)))
+            et[r, j] -= np.uint32(1)
+            stale.append(r)
+            saw["stale"] += 1
+        k, v = _rows(rng, int(counts.sum()) or 1)
+        q = bf16_bits(rng.standard_normal((B, 1, 1, 16)))
+        st, mask, out, written = oracle.step(pool, leave if leave.any() else None, k, v,
+                                             _ind(counts), int(max(counts.max(), 1)), pt, et, sl,
+                                             q, 0.25, 1, 1)
+        assert st in (oracle.OK, oracle.ERR_OUT_OF_PAGES)
+        assert set(np.flatnonzero(mask & oracle.ABORT_TAG).tolist()) == set(stale)
+        unserved = np.flatnonzero(mask & oracle.ABORT_UNSERVED).tolist()
+        if st == oracle.ERR_OUT_OF_PAGES:
+            saw["oop"] += 1
+            assert unserved and unserved == list(range(unserved[0], B))
+        else:
+            assert not unserved
+        assert [r for r in range(B) if written[r]] == [r for r in range(B) if mask[r] == 0]
+        for r in stale:
+            assert sl[r] == 0  # removed in the same step
+        _check_invariants(pool, pt, et, sl)
+        if st == oracle.ERR_OUT_OF_PAGES:  # make room: the longest request leaves
+            r = int(np.argmax(sl))
+            assert oracle.release(pool, pt, et, sl, np.eye(B, dtype=np.uint8)[r]) == 0
+            _check_invariants(pool, pt, et, sl)
+    assert saw["oop"] > 0 and saw["stale"] > 0 and saw["join"] > 0, saw
