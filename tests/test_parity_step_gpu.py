@@ -207,3 +207,60 @@ def test_step_in_a_cuda_graph():
         _check_step(b, (st, m_d, m_h, out, ref, written), rnd)
         if rnd == 2:
             assert m_h.tolist() == [0, 0, 0, 0, 1, 0, 0, 0] and b.sl_h[4] == 0
+
+
+@pytest.mark.parametrize("dtype,scale_mode", [(0, 0), (1, 0), (0, 1)])
+def test_step_random_rounds(dtype, scale_mode):
+    """Thirty random steps on a small pool: leaves, joins with prompts of up
+    to a few pages, decode rows, injected stale tags, and steps that run out
+    of pages (the longest request then leaves to make room).  Pool state,
+    abort mask and outputs match the oracle's step after every step."""
+    rng = np.random.default_rng(100 + 10 * dtype + scale_mode)
+    S = 10
+    w = wl.Workload("step_rand", 301 + dtype + 7 * scale_mode, np.zeros(S, np.int32), 16, 4, 128,
+                    128, 16, 1, 0, 40, float(np.float32(1 / np.sqrt(128))), steps=400,
+                    magnitude=1.0)
+    b = Both(w, dtype, scale_mode=scale_mode)
+    rows = _Rows(b)
+    mp = b.pt_h.shape[1]
+    seen = {"oop": 0, "stale": 0}
+    for rnd in range(30):
+        live = [r for r in range(S) if b.sl_h[r] > 0]
+        leave = np.zeros(S, np.uint8)
+        for r in live:
+            if rng.random() < 0.15:
+                leave[r] = 1
+        counts = np.zeros(S, np.int64)
+        for r in range(S):
+            if b.sl_h[r] > 0 and not leave[r]:
+                counts[r] = 1
+            elif rng.random() < 0.4:
+                counts[r] = int(rng.integers(1, 200))
+        counts = np.minimum(counts, mp * 16 - np.where(leave == 1, 0, b.sl_h))
+        stale = []
+        cand = [r for r in live if not leave[r]]
+        if cand and rng.random() < 0.3:
+            r = int(rng.choice(cand))
+            j = int(rng.integers(0, -(-int(b.sl_h[r]) // 16)))
+            b.et_h[r, j] = np.uint32(b.et_h[r, j]) - np.uint32(1)
+            b.et_d.copy_(torch.from_numpy(b.et_h.view(np.int32)))
+            stale.append(r)
+            seen["stale"] += 1
+        ks, vs = rows(counts)
+        res = b.step(leave if leave.any() else None, ks, vs, counts,
+                     wl.queries(w, device="cuda", step=rnd))
+        st = res[0]
+        _check_step(b, res, rnd, expect_status=st)
+        assert st in (0, b.kv.KV_ERR_OUT_OF_PAGES)
+        assert set(np.flatnonzero(res[2] & 1).tolist()) == set(stale)
+        if st != 0:
+            seen["oop"] += 1
+            b.dev.ctl[b.kv.KV_CTL_ERROR] = 0
+            r = int(np.argmax(b.sl_h))
+            mask = np.zeros(S, np.uint8)
+            mask[r] = 1
+            assert b.release(mask) == 0
+            torch.cuda.synchronize()
+            assert b.dev.error() == 0
+            b.assert_state_equal()
+    assert seen["oop"] > 0 and seen["stale"] > 0, seen
