@@ -366,8 +366,9 @@ size_t kv_decode_step_workspace_size(const kv_pool* pool, int32_t B,
  * device scratch of at least kv_decode_step_workspace_size bytes, 256-byte
  * aligned.  Every argument is checked before anything is launched
  * (KV_ERR_INVALID_ARG / KV_ERR_UNSUPPORTED, nothing launched); device-found
- * errors go to ctl[KV_CTL_ERROR], first error wins.  Six kernel launches,
- * plus two for each release phase that runs.
+ * errors go to ctl[KV_CTL_ERROR], first error wins.  Five kernel launches
+ * (the append's plan kernel also writes the attention plan), plus two for
+ * each release phase that runs.
  */
 kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
                          int32_t q_tokens, const uint8_t* leave_mask, const void* k_new,

@@ -228,6 +228,7 @@ kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B, const void*
   a.max_pages = max_pages_per_req;
   a.seq_lens = seq_lens;
   a.step_mask = nullptr;
+  a.fuse_plan = false;
   int n = 0;
   const cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), &n);
   pool->last_launches = n;
@@ -421,6 +422,8 @@ kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_h
   aa.max_pages = max_pages_per_req;
   aa.seq_lens = seq_lens;
   aa.step_mask = abort_mask;
+  aa.fuse_plan = true;  // the append's plan kernel also writes the attention plan
+  aa.plan = da;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int n = 0;
@@ -432,7 +435,6 @@ kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_h
   }
   if (e == cudaSuccess) e = launch_verify(va, s, &n);
   if (e == cudaSuccess) e = launch_append(aa, s, &n);
-  if (e == cudaSuccess) e = launch_decode_plan(da, s, &n);
   if (e == cudaSuccess) e = launch_decode_split(da, kind, s, &n);
   if (e == cudaSuccess) e = launch_decode_combine(da, s, &n);
   if (e == cudaSuccess && (flags & KV_STEP_REMOVE_ABORTED) != 0) {

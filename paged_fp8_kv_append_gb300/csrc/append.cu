@@ -22,6 +22,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "decode_plan.cuh"
 #include "internal.h"
 #include "quant.cuh"
 
@@ -30,6 +31,7 @@ namespace kvfp8 {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+static_assert(kPlanThreads == kDecodePlanThreads, "the fused attention plan runs on this block");
 
 // Inclusive block scan of a 64-bit value over kPlanThreads threads.
 __device__ long long block_incl_scan(long long v, long long* warp_sums) {
@@ -98,6 +100,10 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
       set_error(d.ctl, KV_ERR_INVALID_ARG);
     }
     mark_unserved(a, 0);
+    if (a.fuse_plan) {
+      __syncthreads();  // every abort bit is set
+      decode_plan_block(a.plan);
+    }
     return;
   }
 
@@ -183,6 +189,10 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
   }
   __syncthreads();  // every thread has read its own mask entry
   mark_unserved(a, stop);
+  if (a.fuse_plan) {
+    __syncthreads();  // final lengths and abort bits are written
+    decode_plan_block(a.plan);
+  }
 }
 
 constexpr int kDataThreads = 256;

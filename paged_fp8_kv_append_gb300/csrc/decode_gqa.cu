@@ -33,6 +33,7 @@
 #include <float.h>
 
 #include "common.cuh"
+#include "decode_plan.cuh"
 #include "internal.h"
 
 namespace kvfp8 {
@@ -40,57 +41,12 @@ namespace {
 
 // ----------------------------------------------------------- batch plan
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = kDecodePlanThreads;
 
-// pfx[r] = exclusive prefix of units of work (pages, or half pages for the
-// latent layout) over requests that get output, rq_skip,
-// rq_bad cleared.  A request is skipped (no pages, no output) when aborted or
-// when its length is negative or needs more pages than its page table holds
-// (that also sets KV_ERR_INVALID_ARG).
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int warp_sums[32];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int P = a.d.page_size;
-  int carry = 0;
-  for (int base = 0; base < a.B; base += kPlanThreads) {
-    const int r = base + threadIdx.x;
-    int np = 0;
-    if (r < a.B) {
-      const int L = a.seq_lens[r];
-      const bool aborted = a.abort_mask != nullptr && a.abort_mask[r] != 0;
-      const bool bad_len = L < 0 || (long long)ceil_div(max(L, 0), P) > a.max_pages;
-      if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
-      const bool skip = aborted || bad_len;
-      np = skip ? 0 : ceil_div(L, a.unit_tokens);
-      a.ws.rq_skip[r] = skip ? 1 : 0;
-      a.ws.rq_bad[r] = 0;
-    }
-    int v = np;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_sums[wid] = v;
-    __syncthreads();
-    if (wid == 0) {
-      int w = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += n;
-      }
-      warp_sums[lane] = w;
-    }
-    __syncthreads();
-    const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
-    if (r < a.B) a.ws.pfx[r] = carry + incl - np;
-    carry += warp_sums[31];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) a.ws.pfx[a.B] = carry;
+  decode_plan_block(a);
 }
 
 // ------------------------------------------------- segment cursor

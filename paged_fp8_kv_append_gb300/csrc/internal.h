@@ -15,25 +15,6 @@ struct kv_pool {
 
 namespace kvfp8 {
 
-// ---- append -------------------------------------------------------------
-struct AppendArgs {
-  kv_pool_desc d;
-  int32_t B;
-  const uint16_t* k_new;  // bf16 bits
-  const uint16_t* v_new;
-  const int32_t* new_indptr;
-  int32_t max_new;
-  int32_t* page_table;
-  uint32_t* exp_tags;
-  int32_t max_pages;
-  int32_t* seq_lens;
-  // NULL, or [B] (the step driver's abort mask): a request with a nonzero
-  // entry appends no rows; the plan then sets KV_ABORT_UNSERVED on every
-  // request at or after its stop index.
-  uint8_t* step_mask;
-};
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
-
 // ---- verify -------------------------------------------------------------
 struct VerifyArgs {
   int32_t num_pages, page_size, B, max_pages;
@@ -88,6 +69,29 @@ struct DecodeArgs {
   int32_t unit_tokens;  // tokens per unit of work (a page)
   DecodeWs ws;
 };
+
+// ---- append -------------------------------------------------------------
+struct AppendArgs {
+  kv_pool_desc d;
+  int32_t B;
+  const uint16_t* k_new;  // bf16 bits
+  const uint16_t* v_new;
+  const int32_t* new_indptr;
+  int32_t max_new;
+  int32_t* page_table;
+  uint32_t* exp_tags;
+  int32_t max_pages;
+  int32_t* seq_lens;
+  // NULL, or [B] (the step driver's abort mask): a request with a nonzero
+  // entry appends no rows; the plan then sets KV_ABORT_UNSERVED on every
+  // request at or after its stop index.
+  uint8_t* step_mask;
+  // with fuse_plan the plan kernel also writes the attention plan of `plan`
+  // (the one-call step: the lengths and abort bits it leaves are final)
+  bool fuse_plan;
+  DecodeArgs plan;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
 
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {
