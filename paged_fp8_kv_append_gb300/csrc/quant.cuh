@@ -117,10 +117,6 @@ __device__ __forceinline__ uint32_t quant_word(uint32_t w, float s, float rs) {
   return e4m3x2(div_fast(bf16_lo(w), s, rs), div_fast(bf16_hi(w), s, rs));
 }
 
-__device__ __forceinline__ uint32_t quant2_rs(float x0, float x1, float s, float rs) {
-  return e4m3x2(div_by_scale(x0, s, rs), div_by_scale(x1, s, rs));
-}
-
 // 8 bf16 values -> 8 e4m3 codes with the faster division
 __device__ __forceinline__ uint2 quant8_rs(uint4 v, float s, float rs) {
   if (!scale_fast_ok(s)) return quant8(v, s);
