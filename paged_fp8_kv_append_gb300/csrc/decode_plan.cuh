@@ -5,6 +5,8 @@
 // the step needs no separate plan launch.
 #pragma once
 
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,19 +21,25 @@ constexpr int kDecodePlanThreads = 1024;
 // (that also sets KV_ERR_INVALID_ARG).
 __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
   __shared__ int warp_sums[32];
+  __shared__ int s_overflow;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int P = a.d.page_size;
-  int carry = 0;
+  // the prefix is held in int32: a batch of more than 2^28 units (so that
+  // units times head groups stay clear of 2^31; only possible with lengths no
+  // pool can back) is refused as a whole
+  long long carry = 0;
+  if (threadIdx.x == 0) s_overflow = 0;
   for (int base = 0; base < a.B; base += kDecodePlanThreads) {
     const int r = base + threadIdx.x;
     int np = 0;
     if (r < a.B) {
-      const int L = a.seq_lens[r];
+      const long long L = a.seq_lens[r];  // 64-bit: L + P - 1 may pass 2^31
       const bool aborted = a.abort_mask != nullptr && a.abort_mask[r] != 0;
-      const bool bad_len = L < 0 || (long long)ceil_div(max(L, 0), P) > a.max_pages;
+      const bool bad_len = L < 0 || (L + P - 1) / P > a.max_pages;
       if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
       const bool skip = aborted || bad_len;
-      np = skip ? 0 : ceil_div(L, a.unit_tokens);
+      // at most ceil(2^31 / P) units: an int
+      np = skip ? 0 : (int)((L + a.unit_tokens - 1) / a.unit_tokens);
       a.ws.rq_skip[r] = skip ? 1 : 0;
       a.ws.rq_bad[r] = 0;
     }
@@ -54,11 +62,22 @@ __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
     }
     __syncthreads();
     const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
-    if (r < a.B) a.ws.pfx[r] = carry + incl - np;
+    const long long excl = carry + incl - np;
+    if (r < a.B) a.ws.pfx[r] = excl > INT_MAX ? INT_MAX : (int)excl;
     carry += warp_sums[31];
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.ws.pfx[a.B] = carry;
+  if (carry > INT_MAX / 8) s_overflow = 1;  // same value in every thread
+  __syncthreads();
+  if (s_overflow) {  // nothing is attended; the call reports the batch
+    for (int r = threadIdx.x; r <= a.B; r += kDecodePlanThreads) {
+      a.ws.pfx[r] = 0;
+      if (r < a.B) a.ws.rq_skip[r] = 1;
+    }
+    if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+    return;
+  }
+  if (threadIdx.x == 0) a.ws.pfx[a.B] = (int)carry;
 }
 
 }  // namespace kvfp8

@@ -1,10 +1,11 @@
-"""Bulk appends at the batch-size boundary of the persistent append kernels:
+"""Limits.  Bulk appends at the batch-size boundary of the persistent append kernels:
 up to 16,384 requests a call, every CTA holds the per-request work prefix in
 shared memory (64 KB at the limit); above it the call takes the compact
 per-(request, page, head) kernel.  Both sides of the boundary must leave the
 pool bit-identical to the oracle's append ("Smaller, faster, safer: running
 Kimi and GLM at scale", section "Quantizing the KV cache": rows are
-quantised to e4m3 as they are written into the paged cache)."""
+quantised to e4m3 as they are written into the paged cache).  And an
+attention batch too large for the plan's 32-bit prefix is refused."""
 import numpy as np
 import pytest
 import torch
@@ -60,3 +61,28 @@ def test_bulk_append_batch_limit(B, dtype):
     assert st == oracle.ERR_OUT_OF_PAGES and b.dev.error() == st
     assert 0 < stop < B and stop == int(b.dev.ctl[b.kv.KV_CTL_APPEND_STOP].item())
     b.assert_state_equal()
+
+
+def test_attention_refuses_a_batch_too_large_to_plan():
+    """Lengths no pool can back -- two requests of 2^31 - 1 tokens, 2^28 page
+    units in all -- would overflow the plan's 32-bit prefix: the plan refuses
+    the batch with KV_ERR_INVALID_ARG, reads no page and writes no output.
+    (Called through the C ABI directly, which takes the page-table width as
+    an argument; the refused batch reads none of it.)"""
+    import paged_fp8_kv_append_gb300 as kv
+
+    pool = kv.KVPool(64, 16, 2, 128, 128, dtype=0, device="cuda")
+    B, Hq = 2, 8
+    mp = (2 ** 31 - 1 + 15) // 16
+    sl = torch.full((B,), 2 ** 31 - 1, dtype=torch.int32, device="cuda")
+    pt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
+    q = torch.zeros((B, 1, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((B, 1, Hq, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(pool.workspace_size(B, Hq, 1), dtype=torch.uint8, device="cuda")
+    st = kv._lib.paged_decode_attn(pool.handle, torch.cuda.current_stream().cuda_stream, B, Hq,
+                                   1, q.data_ptr(), pt.data_ptr(), mp, sl.data_ptr(), None,
+                                   0.088, out.data_ptr(), ws.data_ptr(), ws.numel())
+    assert st == kv.KV_OK
+    torch.cuda.synchronize()
+    assert pool.error() == kv.KV_ERR_INVALID_ARG
+    assert torch.all(out == 7.0)
