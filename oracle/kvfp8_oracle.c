@@ -195,7 +195,9 @@ int or_alloc(int num_pages, int page_size, uint32_t* tags,
     int64_t L = seq_lens[r];
     int64_t n = (int64_t)new_indptr[r + 1] - new_indptr[r];
     int64_t first, need, j;
-    if (n < 0 || L < 0 || n > max_new || L + n > (int64_t)max_pages * P) {
+    /* the new length must fit its page table and stay an int32 length */
+    if (n < 0 || L < 0 || n > max_new || L + n > (int64_t)max_pages * P ||
+        L + n > INT32_MAX) {
       *stop_req = r;
       return OR_ERR_INVALID_ARG;
     }

@@ -196,3 +196,28 @@ def test_fp8_pool_holds_twice_the_tokens():
     b16 = (bf.k_cache.nbytes + bf.v_cache.nbytes) / tok
     assert b8 == 2052 and b16 == 4096
     assert abs(b16 / b8 - 1.996) < 1e-3
+
+
+def test_append_refuses_a_length_past_int32():
+    """seq_lens are int32: an append that would take a request past 2^31 - 1
+    tokens is refused (INVALID_ARG) even when the declared page-table width
+    could hold it, and nothing changes.  (A page-aligned length and an
+    exhausted free list, so no entry of the small page table is touched
+    whichever check fires.)"""
+    import ctypes
+
+    lib = oracle._load()
+    P, mp = 16, 2 ** 27 + 1                       # mp * P > 2^31
+    tags = np.zeros(8, np.uint32)
+    free = np.arange(8, dtype=np.int32)
+    head = np.full(1, 8, np.int32)                # every page handed out: nothing is popped
+    pt = np.full(4, -1, np.int32)                 # only the declared width is large
+    et = np.zeros(4, np.uint32)
+    sl = np.array([2 ** 31 - 16], np.int32)       # page-aligned, one page short of 2^31
+    stop = np.zeros(1, np.int32)
+    ind = np.array([0, 16], np.int32)             # 16 more rows would reach 2^31
+    p = oracle._p
+    st = lib.or_alloc(8, P, p(tags), p(free), p(head), 1, p(ind), 16, p(pt), p(et), mp, p(sl),
+                      p(stop), None)
+    assert st == oracle.ERR_INVALID_ARG and int(stop[0]) == 0
+    assert int(head[0]) == 8 and sl.tolist() == [2 ** 31 - 16] and not tags.any()
