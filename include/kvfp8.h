@@ -179,7 +179,7 @@ kv_status kv_pool_destroy(kv_pool* pool);
  * served (free list exhausted: KV_ERR_OUT_OF_PAGES; bad free-list entry or
  * out-of-range partly filled page: KV_ERR_BAD_PAGE_ID; partly filled page
  * with a changed tag: KV_ERR_TAG_MISMATCH; too many rows for max_new_per_req
- * or for its page table: KV_ERR_INVALID_ARG) and every later request are left
+ * or for its page table, or a new length past 2^31 - 1: KV_ERR_INVALID_ARG) and every later request are left
  * untouched; its index goes to ctl[KV_CTL_APPEND_STOP] and the code to
  * ctl[KV_CTL_ERROR].  Two kernel launches.
  */

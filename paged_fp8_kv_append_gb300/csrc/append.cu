@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     if (r < a.B) {
       L = a.seq_lens[r];
       n = req_rows(a, r);
-      if (n < 0 || L < 0 || n > a.max_new || L + n > (long long)a.max_pages * P) {
+      // the new length must fit the page table and stay an int32 length
+      if (n < 0 || L < 0 || n > a.max_new || L + n > (long long)a.max_pages * P ||
+          L + n > INT_MAX) {
         code = KV_ERR_INVALID_ARG;
       } else {
         if (n > 0 && L % P != 0) {

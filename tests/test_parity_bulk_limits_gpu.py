@@ -86,3 +86,30 @@ def test_attention_refuses_a_batch_too_large_to_plan():
     torch.cuda.synchronize()
     assert pool.error() == kv.KV_ERR_INVALID_ARG
     assert torch.all(out == 7.0)
+
+
+def test_append_refuses_a_length_past_int32():
+    """An append that would take a request past 2^31 - 1 tokens is refused
+    with KV_ERR_INVALID_ARG although the declared page-table width could hold
+    it, as the oracle does; nothing changes.  (A page-aligned length and an
+    exhausted free list: no page-table entry is touched whichever check
+    fires.  Called through the C ABI, which takes the width as an argument.)"""
+    import paged_fp8_kv_append_gb300 as kv
+
+    pool = kv.KVPool(8, 16, 1, 128, 128, dtype=0, device="cuda")
+    pool.ctl[kv.KV_CTL_FREE_HEAD] = 8  # every page handed out
+    mp = 2 ** 27 + 1
+    sl = torch.tensor([2 ** 31 - 16], dtype=torch.int32, device="cuda")
+    pt = torch.full((1, 4), -1, dtype=torch.int32, device="cuda")
+    et = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    k = torch.zeros((16, 1, 128), dtype=torch.bfloat16, device="cuda")
+    ind = torch.tensor([0, 16], dtype=torch.int32, device="cuda")
+    st = kv._lib.kv_append_quantize(pool.handle, torch.cuda.current_stream().cuda_stream, 1,
+                                    k.data_ptr(), k.data_ptr(), ind.data_ptr(), 16, pt.data_ptr(),
+                                    et.data_ptr(), mp, sl.data_ptr())
+    assert st == kv.KV_OK
+    torch.cuda.synchronize()
+    assert pool.error() == kv.KV_ERR_INVALID_ARG
+    assert int(pool.ctl[kv.KV_CTL_APPEND_STOP].item()) == 0
+    assert int(pool.ctl[kv.KV_CTL_FREE_HEAD].item()) == 8
+    assert sl.tolist() == [2 ** 31 - 16] and torch.all(pt == -1)
