@@ -642,6 +642,26 @@ def churn_line(device, steps: int, warmup: int) -> dict:
             "separate_calls": _churn(device, steps, warmup, False)}
 
 
+# ------------------------------------------------------------ wider query groups
+
+def wide_group_line(device, steps: int, warmup: int, peak: float) -> dict:
+    """The GQA batch's requests with 96 query heads on its 8 kv heads (the
+    GLM-class group of 12): 12 query rows per kv head, served as two blocks
+    of 8 by separate consumer warps over the same K/V tiles.  e4m3; the step
+    is append -> verify -> split -> combine as in the headline."""
+    import dataclasses
+
+    w = dataclasses.replace(wl.gqa_batch(steps=steps + warmup + 2), num_q_heads=96)
+    arm = Arm(w, 0, device, steps + warmup)
+    line = step_line(w, arm, 0, steps, warmup)
+    line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
+    line["workload"] = ("gqa_batch with 96 q / 8 kv heads (12 query rows per kv head): 32 "
+                        "requests, contexts U[4096, 32768], head dim 128, page 16, e4m3")
+    del arm
+    torch.cuda.empty_cache()
+    return line
+
+
 # ------------------------------------------------------------ verify overhead
 
 def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
@@ -970,6 +990,8 @@ def main():
     ap.add_argument("--overhead-replays", type=int, default=20)
     ap.add_argument("--no-requant", action="store_true",
                     help="skip the re-quantising scale mode lines")
+    ap.add_argument("--no-wide", action="store_true",
+                    help="skip the 96 q / 8 kv head (12 rows per kv head) step line")
     ap.add_argument("--no-churn", action="store_true",
                     help="skip the continuous-batching line")
     ap.add_argument("--no-bulk", action="store_true",
@@ -1147,6 +1169,11 @@ def main():
         bulk = [bulk_append_line(w, 0, device, peak), bulk_append_line(w, 1, device, peak),
                 bulk_append_line(wl.latent_verify(), 0, device, peak)]
 
+    # ---- a wider query group (12 rows per kv head)
+    wide = None
+    if not args.no_wide:
+        wide = wide_group_line(device, args.steps, args.warmup, peak)
+
     # ---- continuous batching: requests leave and join between decode steps
     churn = None
     if not args.no_churn:
@@ -1195,6 +1222,7 @@ def main():
         "bulk_append": bulk,
         "requantize": requant,
         "churn": churn,
+        "wide_group": wide,
         "concurrency": conc,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

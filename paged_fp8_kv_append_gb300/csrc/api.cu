@@ -33,14 +33,20 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
   if (d.layout == KV_LAYOUT_GQA) {
     if (Hq % d.num_kv_heads != 0) return KV_ERR_INVALID_ARG;
     const int G = Hq / d.num_kv_heads;
-    if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || T * G > 8)
+    // query rows per kv head, in blocks of 8 (one consumer warp each)
+    const long long R = (long long)T * G;
+    if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 32)
       return KV_ERR_UNSUPPORTED;
+    const int rb = (int)((R + 7) / 8);
     cfg->kind = d.dtype == KV_DTYPE_E4M3 ? 0 : 1;
     // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
-    // tiles are twice as large) dividing Hkv and the consumer warp count;
-    // ring depth from the ring size
+    // tiles are twice as large) dividing Hkv, with heads x row blocks dividing
+    // the consumer warp count; ring depth from the ring size
     int hs = cfg->kind == 0 ? 8 : 4;
-    while (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % hs != 0) hs >>= 1;
+    while (hs > 0 &&
+           (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rb) != 0))
+      hs >>= 1;
+    if (hs == 0) return KV_ERR_UNSUPPORTED;  // no split of the consumers fits
     cfg->Hs = hs;
     const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 0 ? 1 : 2);
     cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;
@@ -48,14 +54,14 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     // A consumer warp serves every (consumers/Hs)-th unit; the ring depth must
     // be a multiple of that stride so each warp sees every phase of the stages
     // it uses (parity waits cannot tell phase n from phase n-2).
-    const int wph = gqa_consumer_warps(cfg->kind) / hs;
+    const int wph = gqa_consumer_warps(cfg->kind) / (hs * rb);
     cfg->stages -= cfg->stages % wph;
     if (cfg->stages < 2 || cfg->stages < wph) return KV_ERR_UNSUPPORTED;
     const int sms = sm_count();
     const int per_sm = sms > 0 ? gqa_split_ctas_per_sm(cfg->kind) : 0;
     if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
     cfg->grid = sms * per_sm;
-    cfg->R8 = 8;
+    cfg->R8 = 8 * rb;
     cfg->HG = d.num_kv_heads / hs;
     cfg->unit_tokens = d.page_size;
     return KV_OK;

@@ -175,9 +175,12 @@ __device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
 // group"; Hs = the largest power of two <= 8 that divides Hkv, <= 4 for
 // bf16).  The Hs K tiles of a page are contiguous in the cache, and so are
 // its Hs V tiles, so one unit is two bulk copies of Hs * P * D elements.
-// One CTA per SM: a producer warp and CONSUMERS consumer warps; consumer w
-// serves head w % Hs of every (w / Hs)-th unit, so each unit is consumed by
-// exactly Hs warps.  The ring holds kRingBytes of units in flight.
+// One CTA per SM: a producer warp and CONSUMERS consumer warps.  A kv head's
+// R = T * G query rows come in RB = ceil(R / 8) blocks of 8 (one mma N tile);
+// a (kv head, row block) pair is a "virtual head", Hv = Hs * RB of them per
+// unit.  Consumer w serves virtual head w % Hv of every (w / Hv)-th unit, so
+// each unit is consumed by exactly Hv warps, which share its K and V tiles.
+// The ring holds kRingBytes of units in flight.
 #ifndef KV_GQA_FP8_CONSUMERS
 #define KV_GQA_FP8_CONSUMERS 12
 #endif
@@ -250,10 +253,15 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, Hkv = a.d.num_kv_heads;
   const int Hs = a.Hs, HG = a.HG;              // heads per unit, head groups
+  // query rows of a kv head come in blocks of 8, one block per consumer warp:
+  // a unit is consumed by Hv = Hs * RB warps ("virtual heads")
+  const int RB = a.R8 / C::R8, Hv = Hs * RB;
+  const int rb_mul = (256 + RB - 1) / RB;  // v / RB == (v * rb_mul) >> 8 for v < 12
   const int S = a.stages;                      // ring stages (<= kMaxStages)
   const int stage_bytes = 2 * Hs * C::TILE;
-  if (Hs < 1 || C::CONSUMERS % Hs != 0 || S < 2 || S > kMaxStages ||
-      S % (C::CONSUMERS / Hs) != 0 || stage_bytes * S > C::RING) {
+  if (Hs < 1 || RB < 1 || RB > 4 || RB * C::R8 != a.R8 || (a.R + C::R8 - 1) / C::R8 != RB ||
+      C::CONSUMERS % Hv != 0 || S < 2 || S > kMaxStages || S % (C::CONSUMERS / Hv) != 0 ||
+      stage_bytes * S > C::RING) {
     if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad ring
     return;
   }
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], Hs);
+      mbar_init(&empty[s], Hv);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -413,8 +421,10 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const int g = lane >> 2, t = lane & 3;
   uint8_t* pbuf = pbuf_all + warp * C::PBUF;
   const int G = a.G, T = a.T, R = a.R;
-  const int WPH = C::CONSUMERS / Hs;          // warps per head
-  const int hw = warp % Hs, lg = warp / Hs;  // head within the group, page lane
+  const int WPH = C::CONSUMERS / Hv;          // warps per virtual head
+  const int vh = warp % Hv, lg = warp / Hv;  // virtual head, page lane
+  const int hw = vh / RB;                    // kv head within the group
+  const int n0 = (vh % RB) * C::R8;          // this warp's first query row of the head
   Cursor cur = start;
   long long x = x_begin;
   long long k_base = 0;
@@ -432,8 +442,9 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
     // or chunk c = t + 4*(j/2) (bf16) -- 8 dims per chunk.
     uint32_t qf[8][2];
     {
-      const bool live = g < R;
-      const int tq = live ? g / G : 0, hq = live ? h * G + g % G : 0;
+      const int row = n0 + g;
+      const bool live = row < R;
+      const int tq = live ? row / G : 0, hq = live ? h * G + row % G : 0;
       const uint16_t* qrow = a.q + (((long long)r * T + tq) * a.Hq + hq) * D;
       if constexpr (FP8) {
 #pragma unroll
@@ -464,8 +475,8 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
       }
     }
     // visibility limit (inclusive) of rows 2t and 2t+1
-    const int lim0 = L - T + min((2 * t) / G, T - 1);
-    const int lim1 = L - T + min((2 * t + 1) / G, T - 1);
+    const int lim0 = L - T + min((n0 + 2 * t) / G, T - 1);
+    const int lim1 = L - T + min((n0 + 2 * t + 1) / G, T - 1);
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     float acc[8][4];
@@ -659,21 +670,27 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
       // slot of this (CTA, segment) piece; rows (head in group, query row)
       const long long slot = (long long)r * HG + cur.h + blockIdx.x;
       const int tid = threadIdx.x;  // consumer thread index
-      for (int e = tid; e < Hs * C::R8 * D; e += C::CONSUMERS * 32) {
-        const int hh = e / (C::R8 * D), n = (e / D) % C::R8, dd = e % D;
+      // element e is dim dd of row nw of virtual head v (shifts only: this
+      // loop is on every piece's critical path); v is kv head hh's row block
+      // j, so the row of the kv head is 8 j + nw.  v < Hv <= 12, where
+      // (v * ceil(256 / RB)) >> 8 is exactly v / RB for RB <= 4.
+      static_assert(C::R8 == 8 && D == 128, "epilogue index shifts");
+      for (int e = tid; e < Hv * C::R8 * D; e += C::CONSUMERS * 32) {
+        const int dd = e & (D - 1), nw = (e >> 7) & (C::R8 - 1), v = e >> 10;
+        const int hh = (v * rb_mul) >> 8, n = (v - hh * RB) * C::R8 + nw;
         float M = -INFINITY;
-        for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hs + hh) * C::R8 + n) * 2]);
+        for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * C::R8 + nw) * 2]);
         float o = 0.0f, lsum = 0.0f;
         if (M != -INFINITY) {
           for (int q = 0; q < WPH; ++q) {
-            const int w = q * Hs + hh;
-            const float mw = merge_ml[(w * C::R8 + n) * 2];
+            const int w = q * Hv + v;
+            const float mw = merge_ml[(w * C::R8 + nw) * 2];
             const float sc = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-            o += merge_o[(w * C::R8 + n) * D + dd] * sc;
-            lsum += merge_ml[(w * C::R8 + n) * 2 + 1] * sc;
+            o += merge_o[(w * C::R8 + nw) * D + dd] * sc;
+            lsum += merge_ml[(w * C::R8 + nw) * 2 + 1] * sc;
           }
         }
-        const long long row = (slot * Hs + hh) * C::R8 + n;
+        const long long row = (slot * Hs + hh) * a.R8 + n;
         a.ws.o_part[row * D + dd] = o;
         if (dd == 0) {
           a.ws.ml_part[row * 2 + 0] = M;

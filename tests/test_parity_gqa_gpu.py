@@ -203,3 +203,29 @@ def test_append_many_requests_and_a_bad_free_list_entry(bad_at):
         assert b.dev.error() == b.kv.KV_ERR_BAD_PAGE_ID
         assert int(b.dev.ctl[2].item()) == stop
     b.assert_state_equal()
+
+
+# (T, Hq, Hkv): query rows per kv head R = T * Hq / Hkv beyond one block of 8 --
+# GLM-class groups (96 q / 8 kv heads), speculative tokens on G = 8 models,
+# and a ragged last block
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("T,Hq,Hkv", [(1, 96, 8), (2, 16, 2), (4, 16, 2), (3, 24, 4),
+                                      (1, 32, 1), (5, 10, 2)])
+def test_more_than_eight_rows_per_kv_head(dtype, T, Hq, Hkv):
+    """More than 8 query rows per kv head: each (kv head, block of 8 rows)
+    pair is served by its own consumer warps over the same K/V tiles.  bf16
+    pools have no split of their consumer warps for 17-24 rows and say so."""
+    R = T * Hq // Hkv
+    lens = np.array([3, 9, 40, 129, 2, 1, 300], np.int32)
+    w = wl.Workload("rows", 917 + T + Hq, lens, Hq, Hkv, 128, 128, 16, T, 0, 320,
+                    float(np.float32(1 / np.sqrt(128))))
+    b = Both(w, dtype)
+    assert b.fill()[0] == 0
+    if dtype == 1 and 16 < R <= 24:
+        with pytest.raises(b.kv.KVError) as e:
+            b.dev.workspace_size(w.B, Hq, T)
+        assert e.value.status == b.kv.KV_ERR_UNSUPPORTED
+        return
+    out, ref, written = b.attn(_q(w), None, None)
+    assert b.dev.error() == 0
+    _check_out(out, ref, written, None)
