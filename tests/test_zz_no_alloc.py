@@ -52,6 +52,31 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype):
     assert b.dev.error() == 0
 
 
+def test_noalloc_latent_layout():
+    """The same for the latent (tensor-core) path: 4 draft tokens x 16 heads on
+    one 576-wide row per token."""
+    lens = np.array([37, 300, 64, 1000], np.int32)
+    w = wl.Workload("noalloc_lat", 4343, lens, 16, 1, 576, 512, 64, 4, 1, 64,
+                    float(np.float32(1 / np.sqrt(576))))
+    b = Both(w, 0)
+    assert b.fill()[0] == 0
+    q = wl.queries(w, device="cuda")
+    kv = b.kv
+    shape = (w.B, 4, 16, 512)
+    ref = torch.full(shape, 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(b.dev.workspace_size(w.B, 16, 4), dtype=torch.uint8, device="cuda")
+    kv.paged_decode_attn(b.dev.handle, w.B, 16, 4, q, b.pt_d, b.sl_d, None, w.sm_scale, ref, ws)
+    want = _bits(ref)
+    out = torch.full(shape, 7.0, dtype=torch.bfloat16, device="cuda")
+    kv.paged_decode_attn_noalloc(b.dev.handle, w.B, 16, 4, q, b.pt_d, b.sl_d, None, w.sm_scale,
+                                 out)
+    got = _bits(out)
+    for r in range(w.B):
+        ok, mabs, mrel, _ = close(got[r], want[r])
+        assert ok, (r, mabs, mrel)
+    assert b.dev.error() == 0
+
+
 def test_noalloc_refuses_batches_beyond_its_scratch():
     import paged_fp8_kv_append_gb300 as kv
 
