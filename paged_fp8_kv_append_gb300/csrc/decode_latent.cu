@@ -78,6 +78,12 @@ static_assert(SMEM <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O^T: 4 blocks x 64 columns
 constexpr uint32_t kTmemS = 256;   // S: 2 buffers x 64 columns
+// Q dims 0..255 as the A operand of S (f16, two dims per column; row r of the
+// M = 64 block in lane 32 (r / 16) + r % 16, as the M = 64 accumulator): the
+// first kQTmemSlices of S's 16-dim K slices read A from here instead of
+// shared memory, so shared memory serves only their B (K) operand.
+constexpr uint32_t kTmemQ = 384;
+constexpr int kQTmemDims = 256, kQTmemSlices = kQTmemDims / 16;
 
 struct UnitMeta {
   int n_valid;  // valid tokens of the unit (0: skip)
@@ -112,6 +118,16 @@ __device__ __forceinline__ void mma_f16_if(uint32_t leader, uint32_t d_tmem, uin
       "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
       " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0), "r"(leader)
+      : "memory");
+}
+
+// the same with the A operand read from tensor memory at column address a_tmem
+__device__ __forceinline__ void mma_f16_ts_if(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                              uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0), "r"(leader)
       : "memory");
 }
 
@@ -193,6 +209,19 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -355,10 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         go = false;
         break;
       }
+      tc_fence_after();  // the previous piece's S MMAs have read Q's tensor memory
       {
         const uint16_t* qbase = a.q + ((long long)s.r * a.T * a.Hq + (long long)s.rb * kRB) * kDK;
-        for (int c = ct; c < kRB * (kDK / 8); c += kConvWarps * 32) {
-          const int n = c / (kDK / 8), ck = c % (kDK / 8);
+        // dims kQTmemDims.. to shared memory, 128B-swizzled (the A operand
+        // of S's remaining slices; the blocks below them stay unused)
+        constexpr int kCk0 = kQTmemDims / 8, kCkN = kDK / 8 - kCk0;
+        for (int c = ct; c < kRB * kCkN; c += kConvWarps * 32) {
+          const int n = c / kCkN, ck = kCk0 + c % kCkN;
           const uint4 v = *reinterpret_cast<const uint4*>(qbase + (long long)n * kDK + ck * 8);
           uint4 o;
           o.x = bf16x2_to_f16x2(v.x);
@@ -367,6 +400,31 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
           o.w = bf16x2_to_f16x2(v.w);
           *reinterpret_cast<uint4*>(q_s + (ck >> 3) * (kRB * 128) + swz(n, ck & 7)) = o;
         }
+        // dims 0..kQTmemDims-1 to tensor memory: converter warp w writes lane
+        // quarter w % 4; its lane i < 16 holds row 16 (w % 4) + i of the block
+        // (lanes 16..31 write zeros to columns nothing else uses)
+        {
+          const int qq = warp & 3, row = 16 * qq + (lane & 15);
+          const uint16_t* qrow = qbase + (long long)row * kDK;
+          const uint32_t q_lanes = (uint32_t)(32 * qq) << 16;
+#pragma unroll 1
+          for (int k = 0; k < kQTmemDims / 64; ++k) {  // 64 dims = 32 columns per store
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 v = lane < 16
+                                  ? *reinterpret_cast<const uint4*>(qrow + 64 * k + 8 * j)
+                                  : make_uint4(0, 0, 0, 0);
+              w[4 * j + 0] = bf16x2_to_f16x2(v.x);
+              w[4 * j + 1] = bf16x2_to_f16x2(v.y);
+              w[4 * j + 2] = bf16x2_to_f16x2(v.z);
+              w[4 * j + 3] = bf16x2_to_f16x2(v.w);
+            }
+            tmem_st32u(tmem + kTmemQ + 32 * k + q_lanes, w);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        tc_fence_before();
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
@@ -473,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       go = __all_sync(0xffffffffu, mbar_wait(q_ready, (uint32_t)(piece & 1), abort_flag, ctl,
                                              wait_info(warp, 0, 62)));
       if (!go) break;
+      tc_fence_after();  // Q's tensor-memory stores are ordered before the S MMAs
       long long ns = u0, np = u0;
       bool epi_ok = piece == 0;
       uint32_t idle = 0;
@@ -512,8 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
 #pragma unroll
             for (int st = 0; st < kDK / 16; ++st) {
               const uint32_t off = (uint32_t)((st >> 2) * BLK + (st & 3) * 32) >> 4;
-              mma_f16_if(leader, tmem + kTmemS + 64 * b, dq0 + off, dk0 + kvo + off, kIdescS,
-                         st > 0);
+              if (st < kQTmemSlices)  // A (Q) from tensor memory
+                mma_f16_ts_if(leader, tmem + kTmemS + 64 * b, tmem + kTmemQ + 8 * st,
+                              dk0 + kvo + off, kIdescS, st > 0);
+              else
+                mma_f16_if(leader, tmem + kTmemS + 64 * b, dq0 + off, dk0 + kvo + off, kIdescS,
+                           st > 0);
             }
             if (leader) {
               mma_commit(&s_full[b]);
