@@ -22,7 +22,10 @@
 //                   128B-swizzled K-major tiles (the same tile is the
 //                   MN-major V^T operand);
 //   MMA warp        S = Q K^T   (tcgen05, M = 64 rows, N = 64 tokens, K = 576,
-//                   f16 x f16 -> f32 into one of two tensor-memory buffers)
+//                   f16 x f16 -> f32 into one of two tensor-memory buffers;
+//                   Q's first 256 dims are read from tensor memory, where
+//                   the converters put them when a segment starts, the rest
+//                   from shared memory)
 //                   and O^T += V^T P^T (M = 128 dims x 4 blocks, N = 64 rows,
 //                   K = 64 tokens) accumulating in tensor memory, each issued
 //                   as soon as its inputs are ready, S up to one unit ahead;
