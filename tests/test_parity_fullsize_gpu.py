@@ -33,6 +33,25 @@ def test_gqa_batch_full_size_decode_steps(dtype):
     assert fs.dev.error() == 0
 
 
+def test_gqa_batch_full_size_every_request_and_head():
+    """The whole GQA batch (32 requests, 8 kv heads, e4m3) after a decode
+    step: cache bytes, scales and attention outputs of every request and
+    every kv head against the oracle (one one-kv-head oracle pool per pair,
+    256 in all)."""
+    w = wl.gqa_batch(steps=2)
+    fs = FullSize(w, 0, sample=list(range(w.B)), heads=list(range(w.num_kv_heads)))
+    fs.fill()
+    st, stop = fs.step_append(0)
+    assert (st, stop) == (0, w.B)
+    torch.cuda.synchronize()
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    m_d, m_h = fs.verify()
+    assert not m_h.any() and np.array_equal(m_d.cpu().numpy(), m_h)
+    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == w.B * w.num_kv_heads
+    assert fs.dev.error() == 0
+
+
 @pytest.mark.parametrize("B", [1, 8])
 def test_concurrency_128k_contexts(B):
     w = wl.concurrency(B)
