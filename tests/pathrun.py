@@ -343,3 +343,22 @@ class FullSize:
             for r in np.nonzero(abort_h)[0]:
                 assert np.all(got[r] == sentinel), f"aborted request {r} written"
         return checked
+
+
+def latent_oracle_request(args):
+    """One latent request in the oracle, for a process pool (started with
+    spawn): its rows appended to a fresh one-request pool, then every head
+    and draft token attended.  Returns (cache codes by logical page, scales,
+    attention output [T][Hq][Dv])."""
+    rows, L, q_bits, sm_scale, Hq, T = args
+    npg = -(-L // 64) + 1
+    pool = oracle.Pool(npg, 64, 1, 576, 512, dtype=0, layout=1)
+    ptr = np.full((1, npg), -1, np.int32)
+    slr = np.zeros(1, np.int32)
+    st, _ = oracle.append(pool, rows, None, np.array([0, L], np.int32), L, ptr,
+                          np.zeros((1, npg), np.uint32), slr)
+    assert st == 0
+    n = -(-L // 64)
+    ref, written = oracle.attn(pool, q_bits, ptr, slr, None, sm_scale, Hq, T)
+    assert written[0] == 1
+    return pool.k_cache[ptr[0, :n]], pool.k_scale[ptr[0, :n]], ref[0]
