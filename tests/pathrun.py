@@ -329,14 +329,24 @@ class FullSize:
         G = w.num_q_heads // w.num_kv_heads
         qh = q.cpu()
         checked = 0
+        jobs, keys = [], []
         for (r, h), (pool, pt, et, sl) in self.twins.items():
             if abort_h is not None and abort_h[r]:
                 assert np.all(got[r] == sentinel), f"aborted request {r} written"
                 continue
             qs = wl.bits_u16(qh[r:r + 1, :, h * G:(h + 1) * G, :])
-            ref, written = oracle.attn(pool, qs, pt, sl, None, w.sm_scale, G, w.q_tokens)
-            assert written[0] == 1
-            ok, mabs, mrel, _ = close(got[r, :, h * G:(h + 1) * G], ref[0])
+            jobs.append((pool, qs, pt, sl, w.sm_scale, G, w.q_tokens))
+            keys.append((r, h))
+        if len(jobs) > 8:  # many long twins: the oracle in a spawn-started process pool
+            import multiprocessing as mp
+            import os
+
+            with mp.get_context("spawn").Pool(min(16, os.cpu_count() or 1)) as workers:
+                refs = workers.map(gqa_oracle_attn, jobs)
+        else:
+            refs = [gqa_oracle_attn(j) for j in jobs]
+        for (r, h), ref in zip(keys, refs):
+            ok, mabs, mrel, _ = close(got[r, :, h * G:(h + 1) * G], ref)
             assert ok, (r, h, mabs, mrel)
             checked += 1
         if abort_h is not None:
@@ -362,3 +372,12 @@ def latent_oracle_request(args):
     ref, written = oracle.attn(pool, q_bits, ptr, slr, None, sm_scale, Hq, T)
     assert written[0] == 1
     return pool.k_cache[ptr[0, :n]], pool.k_scale[ptr[0, :n]], ref[0]
+
+
+def gqa_oracle_attn(args):
+    """Oracle attention of one one-kv-head twin pool (picklable, for a process
+    pool): returns the output [T][G][Dv] of its request."""
+    pool, qs, pt, sl, sm_scale, G, T = args
+    ref, written = oracle.attn(pool, qs, pt, sl, None, sm_scale, G, T)
+    assert written[0] == 1
+    return ref[0]

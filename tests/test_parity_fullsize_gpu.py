@@ -52,17 +52,24 @@ def test_gqa_batch_full_size_every_request_and_head():
     assert fs.dev.error() == 0
 
 
-@pytest.mark.parametrize("B", [1, 8])
+@pytest.mark.parametrize("B", [1, 8, 64])
 def test_concurrency_128k_contexts(B):
+    """Requests of 131,072 tokens: at 1 and 8 requests every request and kv
+    head is checked; at 64 a seeded 8 requests on three kv heads."""
     w = wl.concurrency(B)
     w.steps = 2
-    fs = FullSize(w, 0, sample=[0, B - 1] if B > 1 else [0], heads=[3])
+    if B <= 8:
+        sample, heads = list(range(B)), list(range(w.num_kv_heads))
+    else:
+        sample = sorted(np.random.default_rng(B).choice(B, 8, replace=False).tolist())
+        heads = [0, 3, 7]
+    fs = FullSize(w, 0, sample=sample, heads=heads)
     fs.fill(group=2)
     fs.step_append(0)
     torch.cuda.synchronize()
     fs.assert_bookkeeping()
     fs.assert_sampled_cache()
-    assert fs.attn_check(wl.queries(w, device="cuda"), None, None) >= 1
+    assert fs.attn_check(wl.queries(w, device="cuda"), None, None) == len(sample) * len(heads)
     assert fs.dev.error() == 0
 
 
