@@ -80,8 +80,13 @@ def test_skewed_stress_steps_with_stale_tags():
     w = wl.skewed(steps=4)
     rng = np.random.default_rng(5)
     live = [r for r in range(w.B) if r not in w.stale]
-    sample = sorted(rng.choice(live, 6, replace=False).tolist()) + [int(np.argmax(w.lens))] + list(w.stale)
-    fs = FullSize(w, 0, sample=sorted(set(sample)), heads=[1])
+    # a seeded 16 non-aborted requests (the longest among them) on every kv
+    # head, and the stale ones
+    picks = sorted(set(rng.choice(live, 15, replace=False).tolist()) | {int(np.argmax(w.lens))})
+    while len(picks) < 16:
+        picks = sorted(set(picks) | {int(rng.choice(live))})
+    fs = FullSize(w, 0, sample=sorted(set(picks) | set(w.stale)),
+                  heads=list(range(w.num_kv_heads)))
     fs.fill(group=16)
     fs.make_stale()
     for s in range(3):
@@ -90,8 +95,8 @@ def test_skewed_stress_steps_with_stale_tags():
         m_d, m_h = fs.verify()
         assert np.array_equal(m_d.cpu().numpy(), m_h)
         assert sorted(np.nonzero(m_h)[0].tolist()) == sorted(w.stale)
-    torch.cuda.synchronize()
-    fs.assert_bookkeeping()
+        torch.cuda.synchronize()
+        fs.assert_bookkeeping()  # every step
     fs.assert_sampled_cache()
-    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) >= 6
+    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == len(picks) * w.num_kv_heads
     assert fs.dev.error() == 0
