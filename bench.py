@@ -644,14 +644,17 @@ def churn_line(device, steps: int, warmup: int) -> dict:
 
 # ------------------------------------------------------------ wider query groups
 
-def wide_group_line(device, steps: int, warmup: int, peak: float) -> dict:
+def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32) -> dict:
     """The GQA batch's requests with 96 query heads on its 8 kv heads (the
-    GLM-class group of 12): 12 query rows per kv head, served as two blocks
-    of 8 by separate consumer warps over the same K/V tiles.  e4m3; the step
-    is append -> verify -> split -> combine as in the headline."""
+    GLM-class group of 12): 12 query rows per kv head, each kv head's rows
+    served by one 16-row consumer warp.  e4m3; the step is append -> verify
+    -> split -> combine as in the headline.  B < 32: the first B requests
+    (small profiling captures)."""
     import dataclasses
 
     w = dataclasses.replace(wl.gqa_batch(steps=steps + warmup + 2), num_q_heads=96)
+    if B != w.B:
+        w = wl.subset(w, B)
     arm = Arm(w, 0, device, steps + warmup)
     line = step_line(w, arm, 0, steps, warmup)
     line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
@@ -1008,6 +1011,9 @@ def main():
                     help="run only the bulk (prefill handoff) append of B requests of the GQA "
                          "batch workload into an e4m3 pool and print its line (small "
                          "profiling captures)")
+    ap.add_argument("--wide-only", type=int, default=0, metavar="B",
+                    help="run only the 96 q / 8 kv head step on B requests of the GQA batch "
+                         "workload and print its line (small profiling captures)")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests of the GQA batch workload to use (32 = the full workload; "
                          "fewer only for small profiling captures)")
@@ -1053,6 +1059,17 @@ def main():
         w.num_pages = int(w.B * (-(-(131072 + w.steps) // 16))) + 64
         arm = Arm(w, 0, device, args.steps + args.warmup)
         print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
+        return
+
+    if args.wide_only > 0:
+        device = torch.device("cuda", local)
+        peak = 6681.5
+        try:
+            peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+        except Exception:
+            pass
+        print(json.dumps(wide_group_line(device, args.steps, args.warmup, peak,
+                                         B=args.wide_only)))
         return
 
     if args.bulk_only > 0:

@@ -38,23 +38,25 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 32)
       return KV_ERR_UNSUPPORTED;
     const int rb = (int)((R + 7) / 8);
-    cfg->kind = d.dtype == KV_DTYPE_E4M3 ? 0 : 1;
+    // e4m3 with more than 8 rows: consumer warps of 16 rows (kind 3)
+    cfg->kind = d.dtype == KV_DTYPE_E4M3 ? (R > 8 ? 3 : 0) : 1;
+    const int rbw = cfg->kind == 3 ? (int)((R + 15) / 16) : rb;  // row blocks per consumer
     // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
     // tiles are twice as large) dividing Hkv, with heads x row blocks dividing
     // the consumer warp count; ring depth from the ring size
-    int hs = cfg->kind == 0 ? 8 : 4;
+    int hs = cfg->kind == 1 ? 4 : 8;
     while (hs > 0 &&
-           (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rb) != 0))
+           (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rbw) != 0))
       hs >>= 1;
     if (hs == 0) return KV_ERR_UNSUPPORTED;  // no split of the consumers fits
     cfg->Hs = hs;
-    const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 0 ? 1 : 2);
+    const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 1 ? 2 : 1);
     cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;
     if (cfg->stages > gqa_max_stages()) cfg->stages = gqa_max_stages();
     // A consumer warp serves every (consumers/Hs)-th unit; the ring depth must
     // be a multiple of that stride so each warp sees every phase of the stages
     // it uses (parity waits cannot tell phase n from phase n-2).
-    const int wph = gqa_consumer_warps(cfg->kind) / (hs * rb);
+    const int wph = gqa_consumer_warps(cfg->kind) / (hs * rbw);
     cfg->stages -= cfg->stages % wph;
     if (cfg->stages < 2 || cfg->stages < wph) return KV_ERR_UNSUPPORTED;
     const int sms = sm_count();

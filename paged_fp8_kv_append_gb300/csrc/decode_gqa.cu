@@ -25,7 +25,9 @@
 //
 // Per page a consumer computes S^T = K Q^T (M = 16 tokens, N = 8 query rows,
 // K = 128 dims) and O^T += V^T P^T (M = 128 dims, N = 8 rows, K = 16 tokens)
-// with mma.sync m16n8k16.  At 8 query rows per kv head the work is 16 flop per
+// with mma.sync m16n8k16.  With more than 8 query rows per kv head, e4m3
+// consumers take 16 rows as the M dimension instead (gqa_split_wide_kernel),
+// so each K/V byte is converted once for all the rows of its kv head.  At 8 query rows per kv head the work is 16 flop per
 // cache byte, beyond what the fp32 CUDA cores sustain at HBM speed, so the
 // tensor pipe carries the dot products and the CUDA cores only convert and
 // run the softmax.  e4m3 codes convert exactly to f16; the per-page K scale
@@ -233,9 +235,12 @@ struct StageMeta {
 };
 static_assert(sizeof(StageMeta) == 80, "StageMeta layout");
 
-template <bool FP8>
-__global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
-    gqa_split_kernel(const DecodeArgs a) {
+// WIDE (e4m3 only): a consumer warp takes 16 query rows of its kv head
+// instead of 8 (see the wide consumer below); the producer and the ring are
+// the same.
+template <bool FP8, bool WIDE>
+__device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
+  static_assert(!WIDE || FP8, "16-row consumers serve e4m3 pools");
   pdl_wait();
   pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
   using C = GqaCfg<FP8>;
@@ -253,9 +258,10 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, Hkv = a.d.num_kv_heads;
   const int Hs = a.Hs, HG = a.HG;              // heads per unit, head groups
-  // query rows of a kv head come in blocks of 8, one block per consumer warp:
-  // a unit is consumed by Hv = Hs * RB warps ("virtual heads")
-  const int RB = a.R8 / C::R8, Hv = Hs * RB;
+  // query rows of a kv head come in blocks of 8 (16 for WIDE), one block per
+  // consumer warp: a unit is consumed by Hv = Hs * RBW warps ("virtual heads")
+  const int RB = a.R8 / C::R8;
+  const int RBW = WIDE ? (RB + 1) / 2 : RB, Hv = Hs * RBW;
   const int rb_mul = (256 + RB - 1) / RB;  // v / RB == (v * rb_mul) >> 8 for v < 12
   const int S = a.stages;                      // ring stages (<= kMaxStages)
   const int stage_bytes = 2 * Hs * C::TILE;
@@ -413,6 +419,239 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
         while (!mbar_try_wait(&full[stage], par) && global_ns() - t0 < 100000000ull) {
         }
       }
+    }
+    return;
+  }
+
+  if constexpr (WIDE) {
+    // ================= consumer warps, 16 query rows each =================
+    // Rows are the mma M dimension: S = Q K^T (M = 16 rows, N = 8 tokens,
+    // two N tiles per page) and O += P V (M = 16 rows, N = 8 dims, 16 dim
+    // tiles, K = the page's 16 tokens).  The S accumulators are already in
+    // the A-fragment layout of P, so P never leaves registers, and each K/V
+    // byte of a kv head is converted once for all its rows.
+    //   k-slot order: in k-step j of S, thread t's slots 2t, 2t+1, 2t+8,
+    //   2t+9 are dims 32t + 4j + 0..3 (its 32 dims are contiguous: two
+    //   16-byte loads of a K row); column c of S's N tile nt is token
+    //   2c - (c & 1) + 2 nt, so P's slots 2t, 2t+1 (tile 0) and 2t+8, 2t+9
+    //   (tile 1) are tokens 4t .. 4t+3: one 4-byte load of the dim-major V
+    //   tile gives both B registers of a PV dim tile.
+    const int g = lane >> 2, t = lane & 3;
+    const int G = a.G, T = a.T, R = a.R;
+    const int WPH = C::CONSUMERS / Hv;      // warps per virtual head
+    const int vh = warp % Hv, lg = warp / Hv;
+    const int hw = vh / RBW;                // kv head within the group
+    const int n0 = (vh - hw * RBW) * 16;    // this warp's first query row of the head
+    Cursor cur = start;
+    long long x = x_begin;
+    long long k_base = 0;
+    const float ssl = a.sm_scale_log2;
+    const int tok0 = 2 * g - (g & 1);       // token of S column g in tile 0 (tile 1: +2)
+
+    while (x < x_end) {
+      const long long seg_end = cur.seg_start + cur.np;
+      const long long piece_end = min(seg_end, x_end);
+      const int npages = (int)(piece_end - x);
+      const int r = cur.r, h = cur.h * Hs + hw;
+      const int L = a.seq_lens[r];
+
+      // ---- Q as A fragments {a0, a1, a2, a3} of k-step j = rows g, g+8 x
+      // dims 32t+4j+0..1, +2..3, staged in this warp's merge buffer (4 KB,
+      // idle until the piece ends) as [j][lane] 16-byte words: registers
+      // hold the 16 x 128 output instead
+      uint32_t* qs = reinterpret_cast<uint32_t*>(merge_o + warp * C::R8 * D);
+      {
+        uint32_t qa[8][4];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = n0 + g + 8 * hr;
+          const bool live = row < R;
+          const int tq = live ? row / G : 0, hq = live ? h * G + row % G : 0;
+          const uint16_t* qrow = a.q + (((long long)r * T + tq) * a.Hq + hq) * D + 32 * t;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // dims 32t + 8u .. +7: k-steps 2u and 2u+1
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (live) v = *reinterpret_cast<const uint4*>(qrow + 8 * u);
+            qa[2 * u][hr] = bf16x2_to_f16x2(v.x);
+            qa[2 * u][2 + hr] = bf16x2_to_f16x2(v.y);
+            qa[2 * u + 1][hr] = bf16x2_to_f16x2(v.z);
+            qa[2 * u + 1][2 + hr] = bf16x2_to_f16x2(v.w);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(qs + (j * 32 + lane) * 4) =
+              make_uint4(qa[j][0], qa[j][1], qa[j][2], qa[j][3]);
+        __syncwarp();
+      }
+      // visibility limits (inclusive) of rows g and g+8
+      const int limA = L - T + min((n0 + g) / G, T - 1);
+      const int limB = L - T + min((n0 + g + 8) / G, T - 1);
+
+      float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
+      float acc[16][4];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+      const long long kfirst = k_base + (long long)((lg - (int)(k_base % WPH) + WPH) % WPH);
+      for (long long kk = kfirst; kk < k_base + npages; kk += WPH) {
+        const int stage = (int)(kk % S);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((kk / S) & 1),
+                                                          abort_flag, a.d.ctl,
+                                                          wait_info(warp, 0, stage)));
+        const StageMeta& mt = meta[stage];
+        if (ok && mt.unit != (int)kk) {  // would mean a stale stage: report, never compute on it
+          if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
+          *abort_flag = 1;
+        }
+        if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
+          const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
+          const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
+          // ---------------- S = Q K^T: N tile nt, column g = token tok0 + 2 nt
+          float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {  // dims 32t + 16 kh .. +15: k-steps 4kh .. 4kh+3
+            const uint4 k0 = lds128(Kt + tok0 * 128 + 32 * t + 16 * kh);
+            const uint4 k1 = lds128(Kt + (tok0 + 2) * 128 + 32 * t + 16 * kh);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint4 qa = lds128(qs + ((4 * kh + jj) * 32 + lane) * 4);
+              uint32_t b0, b1;
+              e4m3x4_to_f16(w_of(k0, jj), b0, b1);
+              mma16816<true>(s[0], qa.x, qa.y, qa.z, qa.w, b0, b1);
+              e4m3x4_to_f16(w_of(k1, jj), b0, b1);
+              mma16816<true>(s[1], qa.x, qa.y, qa.z, qa.w, b0, b1);
+            }
+          }
+          // s[nt][e]: row g (e < 2) or g+8, token 4t + 2 nt + (e & 1); log2 domain
+          const float sc = mt.ks[hw] * ssl;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] *= sc;
+          const int nv = mt.n_valid;
+          const bool full_page = nv == P;
+          if (!full_page || mt.pos0 + P - 1 > min(limA, limB)) {
+            // partial page or causal edge: mask invisible positions
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tk = 4 * t + 2 * nt + (e & 1);
+                const int lim = e < 2 ? limA : limB;
+                s[nt][e] = (tk < nv && mt.pos0 + tk <= lim) ? s[nt][e] : -INFINITY;
+              }
+          }
+          float mxA = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+          float mxB = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+#pragma unroll
+          for (int o = 1; o < 4; o <<= 1) {
+            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, o));
+            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, o));
+          }
+          // the page's V scale as an exponent bias, as in the 8-row consumer
+          const float bias = __log2f(mt.vs[hw]);
+          const float unbias = fast_exp2(-bias);
+          const float nA = fmaxf(mA, mxA + bias), nB = fmaxf(mB, mxB + bias);
+          const float alA = (nA == -INFINITY) ? 1.0f : fast_exp2(mA - nA);
+          const float alB = (nB == -INFINITY) ? 1.0f : fast_exp2(mB - nB);
+          const float cA = bias - nA, cB = bias - nB;
+          float p[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            p[nt][0] = (nA == -INFINITY) ? 0.0f : fast_exp2(s[nt][0] + cA);
+            p[nt][1] = (nA == -INFINITY) ? 0.0f : fast_exp2(s[nt][1] + cA);
+            p[nt][2] = (nB == -INFINITY) ? 0.0f : fast_exp2(s[nt][2] + cB);
+            p[nt][3] = (nB == -INFINITY) ? 0.0f : fast_exp2(s[nt][3] + cB);
+          }
+          mA = nA;
+          mB = nB;
+          // per-thread partial row sums (this thread's tokens); summed over t at the end
+          lA = lA * alA + (p[0][0] + p[0][1] + p[1][0] + p[1][1]) * unbias;
+          lB = lB * alB + (p[0][2] + p[0][3] + p[1][2] + p[1][3]) * unbias;
+          if (__any_sync(0xffffffffu, alA != 1.0f || alB != 1.0f)) {  // a running max moved
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              acc[i][0] *= alA;
+              acc[i][1] *= alA;
+              acc[i][2] *= alB;
+              acc[i][3] *= alB;
+            }
+          }
+          // ---------------- O += P V: P from registers, V tile dim-major
+          const uint32_t pa0 = f32x2_to_f16x2(p[0][0], p[0][1]);
+          const uint32_t pa1 = f32x2_to_f16x2(p[0][2], p[0][3]);
+          const uint32_t pa2 = f32x2_to_f16x2(p[1][0], p[1][1]);
+          const uint32_t pa3 = f32x2_to_f16x2(p[1][2], p[1][3]);
+          // tokens beyond the length are zeroed in V (stale bytes could be NaN)
+          const int keep = min(max(nv - 4 * t, 0), 4);
+          const uint32_t vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16(lds32(Vt + (8 * i + g) * 16 + 4 * t) & vmask, b0, b1);
+            mma16816<true>(acc[i], pa0, pa1, pa2, pa3, b0, b1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
+
+      // ---- merge the states of the warps that share a virtual head, 8 rows
+      // at a time (rows g, then g + 8) through the 8-row merge buffers
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        lA += __shfl_xor_sync(0xffffffffu, lA, o);
+        lB += __shfl_xor_sync(0xffffffffu, lB, o);
+      }
+      const long long slot = (long long)r * HG + cur.h + blockIdx.x;
+      __syncwarp();  // the warp's last reads of its staged Q come before the merge data
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float* mo = merge_o + warp * C::R8 * D + g * D;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float2*>(mo + 8 * i + 2 * t) =
+              half ? make_float2(acc[i][2], acc[i][3]) : make_float2(acc[i][0], acc[i][1]);
+        if (t == 0) {
+          float* ml = merge_ml + (warp * C::R8 + g) * 2;
+          ml[0] = half ? mB : mA;
+          ml[1] = half ? lB : lA;
+        }
+        named_bar_sync(1, C::CONSUMERS * 32);
+        // element e: dim dd of row nw of virtual head v (kv head hh, row block
+        // v - hh RBW); its row of the kv head is 16 (v - hh RBW) + 8 half + nw
+        static_assert(C::R8 == 8 && D == 128, "epilogue index shifts");
+        for (int e = threadIdx.x; e < Hv * C::R8 * D; e += C::CONSUMERS * 32) {
+          const int dd = e & (D - 1), nw = (e >> 7) & (C::R8 - 1), v = e >> 10;
+          const int hh = RBW == 2 ? v >> 1 : v;
+          const int n = (v - hh * RBW) * 16 + 8 * half + nw;
+          if (n >= a.R8) continue;  // padding rows past the partial layout
+          float M = -INFINITY;
+          for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * C::R8 + nw) * 2]);
+          float o = 0.0f, lsum = 0.0f;
+          if (M != -INFINITY) {
+            for (int q = 0; q < WPH; ++q) {
+              const int w = q * Hv + v;
+              const float mw = merge_ml[(w * C::R8 + nw) * 2];
+              const float scl = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+              o += merge_o[(w * C::R8 + nw) * D + dd] * scl;
+              lsum += merge_ml[(w * C::R8 + nw) * 2 + 1] * scl;
+            }
+          }
+          const long long row = (slot * Hs + hh) * a.R8 + n;
+          a.ws.o_part[row * D + dd] = o;
+          if (dd == 0) {
+            a.ws.ml_part[row * 2 + 0] = M;
+            a.ws.ml_part[row * 2 + 1] = lsum;
+          }
+        }
+        named_bar_sync(1, C::CONSUMERS * 32);
+      }
+
+      k_base += npages;
+      x = piece_end;
+      if (x == seg_end) cursor_next(cur, pfx, B, HG);
     }
     return;
   }
@@ -706,6 +945,17 @@ __global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
   }
 }
 
+template <bool FP8>
+__global__ void __launch_bounds__(GqaCfg<FP8>::THREADS, 1)
+    gqa_split_kernel(const DecodeArgs a) {
+  gqa_split_body<FP8, false>(a);
+}
+
+__global__ void __launch_bounds__(GqaCfg<true>::THREADS, 1)
+    gqa_split_wide_kernel(const DecodeArgs a) {
+  gqa_split_body<true, true>(a);
+}
+
 // ------------------------------------------------- combine
 
 constexpr int kCombineWarps = 8;
@@ -876,18 +1126,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
 
 // ------------------------------------------------- host side
 
-int gqa_ring_bytes(int kind) { return kind == 0 ? GqaCfg<true>::RING : GqaCfg<false>::RING; }
+// kinds: 0 = e4m3 (8-row consumers), 1 = bf16, 3 = e4m3 with 16-row consumers
+int gqa_ring_bytes(int kind) { return kind == 1 ? GqaCfg<false>::RING : GqaCfg<true>::RING; }
 int gqa_max_stages() { return kMaxStages; }
 int gqa_consumer_warps(int kind) {
-  return kind == 0 ? GqaCfg<true>::CONSUMERS : GqaCfg<false>::CONSUMERS;
+  return kind == 1 ? GqaCfg<false>::CONSUMERS : GqaCfg<true>::CONSUMERS;
 }
 
 int gqa_split_ctas_per_sm(int kind) {
-  static int cache[2] = {-1, -1};
+  static int cache[4] = {-1, -1, -1, -1};
+  if (kind < 0 || kind > 3 || kind == 2) return 0;
   if (cache[kind] >= 0) return cache[kind];
   int n = 0;
   cudaError_t e;
-  if (kind == 0) {
+  if (kind == 3) {
+    cudaFuncSetAttribute(gqa_split_wide_kernel,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, GqaCfg<true>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_wide_kernel,
+                                                      GqaCfg<true>::THREADS, GqaCfg<true>::SMEM);
+  } else if (kind == 0) {
     cudaFuncSetAttribute(gqa_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          GqaCfg<true>::SMEM);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_kernel<true>,
@@ -911,10 +1168,12 @@ cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s, int* launche
 
 cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches) {
   const cudaError_t e =
-      kind == 0 ? launch_pdl(gqa_split_kernel<true>, dim3(a.grid),
-                             dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)
-                : launch_pdl(gqa_split_kernel<false>, dim3(a.grid),
-                             dim3(GqaCfg<false>::THREADS), GqaCfg<false>::SMEM, s, a);
+      kind == 3   ? launch_pdl(gqa_split_wide_kernel, dim3(a.grid),
+                               dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)
+      : kind == 0 ? launch_pdl(gqa_split_kernel<true>, dim3(a.grid),
+                               dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)
+                  : launch_pdl(gqa_split_kernel<false>, dim3(a.grid),
+                               dim3(GqaCfg<false>::THREADS), GqaCfg<false>::SMEM, s, a);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
