@@ -363,11 +363,13 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       bool go = true;
       for (int g0 = 0; g0 < cnt && go; g0 += grp) {
         const bool mine = lane >= g0 && lane < min(g0 + grp, cnt);
-        const long long kl = k + lane;
-        const int stage = (int)(kl % S);
+        // stage numbers stay below 2^31 (the plan refuses larger batches), so
+        // 32-bit arithmetic suffices
+        const uint32_t kl = (uint32_t)(k + lane), us = (uint32_t)S;
+        const int stage = (int)(kl % us);
         bool ok = true;
-        if (mine && kl >= S)
-          ok = mbar_wait(&empty[stage], (uint32_t)(((kl / S) - 1) & 1), abort_flag, a.d.ctl,
+        if (mine && kl >= us)
+          ok = mbar_wait(&empty[stage], ((kl / us) - 1u) & 1u, abort_flag, a.d.ctl,
                          wait_info(warp, 1, stage));
         go = __all_sync(0xffffffffu, ok);
         if (!go) break;
@@ -494,9 +496,12 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 
       const long long kfirst = k_base + (long long)((lg - (int)(k_base % WPH) + WPH) % WPH);
+      // stage and phase of unit kk, advanced without a division per page (a
+      // step of WPH <= S wraps the ring at most once; S is a multiple of WPH)
+      int stage = (int)(kfirst % S);
+      uint32_t phase = (uint32_t)((kfirst / S) & 1);
       for (long long kk = kfirst; kk < k_base + npages; kk += WPH) {
-        const int stage = (int)(kk % S);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((kk / S) & 1),
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase,
                                                           abort_flag, a.d.ctl,
                                                           wait_info(warp, 0, stage)));
         const StageMeta& mt = meta[stage];
@@ -595,6 +600,11 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
+        stage += WPH;
+        if (stage >= S) {
+          stage -= S;
+          phase ^= 1u;
+        }
       }
 
       // ---- merge the states of the warps that share a virtual head, 8 rows
@@ -724,9 +734,12 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
 
     // this warp's units of the piece: stage numbers kk == lg (mod WPH)
     const long long kfirst = k_base + (long long)((lg - (int)(k_base % WPH) + WPH) % WPH);
+    // stage and phase of unit kk, advanced without a division per page (a
+    // step of WPH <= S wraps the ring at most once; S is a multiple of WPH)
+    int stage = (int)(kfirst % S);
+    uint32_t phase = (uint32_t)((kfirst / S) & 1);
     for (long long kk = kfirst; kk < k_base + npages; kk += WPH) {
-      const int stage = (int)(kk % S);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((kk / S) & 1),
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase,
                                                         abort_flag, a.d.ctl,
                                                         wait_info(warp, 0, stage)));
       const StageMeta& mt = meta[stage];
@@ -881,6 +894,11 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
+      stage += WPH;
+      if (stage >= S) {
+        stage -= S;
+        phase ^= 1u;
+      }
     }
 
     // ---- merge the states of the warps that share a head into one partial
