@@ -81,12 +81,23 @@ __device__ void mark_unserved(const AppendArgs& a, int stop) {
   for (int r = stop + threadIdx.x; r < a.B; r += blockDim.x) a.step_mask[r] |= KV_ABORT_UNSERVED;
 }
 
+// Open-addressing table of the chunk's partly filled pages (at most one per
+// request, so at most half full).
+constexpr int kPartialSlots = 2 * kPlanThreads;
+
+__device__ __forceinline__ int partial_slot(int p) {
+  return (int)(((uint32_t)p * 2654435761u) >> 21) & (kPartialSlots - 1);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
   __shared__ long long warp_sums[32];
   __shared__ long long s_incl[kPlanThreads];  // inclusive prefix of pages popped in the chunk
   __shared__ long long s_first[kPlanThreads]; // first new logical page of each request
+  __shared__ int s_pkey[kPartialSlots];       // partly filled page ids (-1: empty slot)
+  __shared__ short s_preq[kPartialSlots];     // chunk-local request checking that page
+  __shared__ unsigned char s_tagfail[kPlanThreads];
   __shared__ int s_stop, s_code;
   __shared__ long long s_badg;
   const kv_pool_desc& d = a.d;
@@ -111,7 +122,7 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     const int r = base + threadIdx.x;
     const int nreq = min(kPlanThreads, a.B - base);
     long long need = 0, L = 0, n = 0, first = 0;
-    int code = 0;
+    int code = 0, plast = -1;
     if (r < a.B) {
       L = a.seq_lens[r];
       n = req_rows(a, r);
@@ -129,6 +140,8 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
             code = KV_ERR_BAD_PAGE_ID;
           else if (d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jl])
             code = KV_ERR_TAG_MISMATCH;
+          else
+            plast = p;
         }
         first = (L + P - 1) / P;
         need = (L + n + P - 1) / P - first;
@@ -136,24 +149,49 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     }
     const long long incl = block_incl_scan(need, warp_sums);
     const long long pool0 = head0 + consumed;  // free-list position of the chunk's first pop
-    if (r < a.B && code == 0 && pool0 + incl > d.num_pages) code = KV_ERR_OUT_OF_PAGES;
     s_incl[threadIdx.x] = incl;
     s_first[threadIdx.x] = first;
+    s_tagfail[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < kPartialSlots; i += kPlanThreads) s_pkey[i] = -1;
     if (threadIdx.x == 0) {
       s_stop = a.B;
       s_code = 0;
       s_badg = LLONG_MAX;
     }
     __syncthreads();
-    const long long chunk_total = s_incl[nreq - 1];
-    // every entry the chunk would pop, all threads at once: the first one
-    // that is not a page id marks its request
-    for (long long g = threadIdx.x; g < chunk_total && pool0 + g < d.num_pages; g += kPlanThreads) {
-      const int p = d.free_list[pool0 + g];
-      if (p < 0 || p >= d.num_pages) atomicMin(reinterpret_cast<unsigned long long*>(&s_badg),
-                                               (unsigned long long)g);
+    // The tags read above are those before this call's pops.  Requests are
+    // served in order, so a partly filled page that an earlier request of the
+    // chunk pops (its tag is bumped first) fails the later request's check:
+    // the partly filled pages go into a table that the pop scan looks up.
+    if (plast >= 0) {
+      for (int h = partial_slot(plast);; h = (h + 1) & (kPartialSlots - 1)) {
+        if (atomicCAS(&s_pkey[h], -1, plast) == -1) {
+          s_preq[h] = (short)threadIdx.x;
+          break;
+        }
+      }
     }
     __syncthreads();
+    const long long chunk_total = s_incl[nreq - 1];
+    // every entry the chunk would pop, all threads at once: the first one
+    // that is not a page id marks its request; one that is the partly filled
+    // page of a later request fails that request's tag check
+    for (long long g = threadIdx.x; g < chunk_total && pool0 + g < d.num_pages; g += kPlanThreads) {
+      const int p = d.free_list[pool0 + g];
+      if (p < 0 || p >= d.num_pages) {
+        atomicMin(reinterpret_cast<unsigned long long*>(&s_badg), (unsigned long long)g);
+        continue;
+      }
+      for (int h = partial_slot(p); s_pkey[h] != -1; h = (h + 1) & (kPartialSlots - 1)) {
+        if (s_pkey[h] == p) {
+          const int rr = s_preq[h];
+          if (owner_of(s_incl, nreq, g) < rr) s_tagfail[rr] = 1;
+        }
+      }
+    }
+    __syncthreads();
+    if (r < a.B && code == 0 && s_tagfail[threadIdx.x]) code = KV_ERR_TAG_MISMATCH;
+    if (r < a.B && code == 0 && pool0 + incl > d.num_pages) code = KV_ERR_OUT_OF_PAGES;
     if (s_badg != LLONG_MAX && r < a.B && code == 0 &&
         threadIdx.x == owner_of(s_incl, nreq, s_badg))
       code = KV_ERR_BAD_PAGE_ID;

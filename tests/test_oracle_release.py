@@ -80,6 +80,26 @@ def test_append_refuses_a_reallocated_partial_page():
     assert (st, stop) == (oracle.ERR_BAD_PAGE_ID, 0)
 
 
+def test_append_sees_a_partial_page_popped_earlier_in_the_same_call():
+    """Requests are served in order: a partly filled page that an earlier
+    request of the same call pops has its tag bumped before the later
+    request's check, which then fails."""
+    pool = _pool()
+    pt, et, sl = _state()
+    oracle.alloc(pool, _ind([5, 3, 8]), 8, pt, et, sl)
+    # request 1's partly filled page 7 (3 of 4 slots) is listed free again,
+    # at the top of the free list (free_head = 5)
+    pool.free_list[5] = 7
+    st, stop = oracle.alloc(pool, _ind([4, 1, 0]), 4, pt, et, sl)
+    # request 0 (5 -> 9 rows) checks its page 2 (tag 31: ok) and pops page 7
+    # (tag 81 -> 82); request 1 then finds tag 82 against its recorded 81
+    assert (st, stop) == (oracle.ERR_TAG_MISMATCH, 1)
+    assert pt.tolist() == [[5, 2, 7, -1], [7, -1, -1, -1], [0, 3, -1, -1]]
+    assert et.tolist() == [[61, 31, 82, 0], [81, 0, 0, 0], [11, 41, 0, 0]]
+    assert sl.tolist() == [9, 3, 8] and int(pool.free_head[0]) == 6
+    assert int(pool.tags[7]) == 82
+
+
 def test_release_failures_change_nothing():
     pool = _pool()
     pt, et, sl = _state()

@@ -109,6 +109,34 @@ def test_append_stops_at_a_reallocated_partial_page(dtype):
     b.assert_state_equal()  # requests 0..2 appended, 3..5 untouched
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_append_stops_at_a_partial_page_popped_earlier_in_the_same_call(dtype):
+    """A partly filled page listed free again and popped by an earlier request
+    of the same call: the later request's check sees the bumped tag."""
+    w = _w([37, 300, 64, 1000, 5, 129], seed=45)
+    b = Both(w, dtype)
+    b.fill()
+    torch.cuda.synchronize()
+    # request 3's partly filled page (1000 = 62 * 16 + 8) goes on top of the
+    # free list; request 2 (64 rows: 4 full pages) pops it for its next row
+    p = int(b.pt_h[3, 1000 // 16])
+    head = int(b.ref.free_head[0])
+    b.ref.free_list[head] = p
+    b.dev.free_list[head] = p
+    ks, vs = [], []
+    for r in range(w.B):
+        k, v = wl.kv_rows(w, r, int(b.sl_h[r]), 1, device="cuda", tag=11)
+        ks.append(k)
+        vs.append(v)
+    st, stop = b.append(ks, vs, np.ones(w.B, np.int64))
+    torch.cuda.synchronize()
+    assert (st, stop) == (b.kv.KV_ERR_TAG_MISMATCH, 3)
+    assert b.dev.error() == b.kv.KV_ERR_TAG_MISMATCH
+    assert int(b.dev.ctl[2].item()) == 3
+    assert int(b.pt_h[2, 64 // 16]) == p
+    b.assert_state_equal()  # requests 0..2 appended (2 holds page p), 3..5 untouched
+
+
 def test_release_refused_when_more_than_handed_out():
     w = _w([37, 300, 64], seed=44)
     b = Both(w, 0)
