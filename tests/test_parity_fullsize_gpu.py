@@ -52,6 +52,30 @@ def test_gqa_batch_full_size_every_request_and_head():
     assert fs.dev.error() == 0
 
 
+def test_wide_group_full_size_sampled():
+    """The GQA batch with 96 query heads on its 8 kv heads (12 query rows per
+    kv head: the 16-row consumer warps), e4m3, at full size after a decode
+    step: bookkeeping of every request; cache bytes, scales and attention of
+    a seeded 4 requests (the longest among them) on three kv heads."""
+    import dataclasses
+
+    w = dataclasses.replace(wl.gqa_batch(steps=2), num_q_heads=96)
+    rng = np.random.default_rng(3)
+    sample = sorted(set(rng.choice(w.B, 3, replace=False).tolist()) | {int(np.argmax(w.lens))})
+    heads = [0, 4, 7]
+    fs = FullSize(w, 0, sample=sample, heads=heads)
+    fs.fill()
+    st, stop = fs.step_append(0)
+    assert (st, stop) == (0, w.B)
+    torch.cuda.synchronize()
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    m_d, m_h = fs.verify()
+    assert not m_h.any() and np.array_equal(m_d.cpu().numpy(), m_h)
+    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == len(sample) * len(heads)
+    assert fs.dev.error() == 0
+
+
 @pytest.mark.parametrize("B", [1, 8, 64])
 def test_concurrency_128k_contexts(B):
     """Requests of 131,072 tokens: at 1 and 8 requests every request and kv
