@@ -644,22 +644,24 @@ def churn_line(device, steps: int, warmup: int) -> dict:
 
 # ------------------------------------------------------------ wider query groups
 
-def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32) -> dict:
+def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
+                    dtype: int = 0) -> dict:
     """The GQA batch's requests with 96 query heads on its 8 kv heads (the
     GLM-class group of 12): 12 query rows per kv head, each kv head's rows
-    served by one 16-row consumer warp.  e4m3; the step is append -> verify
-    -> split -> combine as in the headline.  B < 32: the first B requests
-    (small profiling captures)."""
+    served by one 16-row consumer warp.  e4m3 (dtype 0) or bf16 (1); the step
+    is append -> verify -> split -> combine as in the headline.  B < 32: the
+    first B requests (small profiling captures)."""
     import dataclasses
 
     w = dataclasses.replace(wl.gqa_batch(steps=steps + warmup + 2), num_q_heads=96)
     if B != w.B:
         w = wl.subset(w, B)
-    arm = Arm(w, 0, device, steps + warmup)
-    line = step_line(w, arm, 0, steps, warmup)
+    arm = Arm(w, dtype, device, steps + warmup)
+    line = step_line(w, arm, dtype, steps, warmup)
     line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
-    line["workload"] = ("gqa_batch with 96 q / 8 kv heads (12 query rows per kv head): 32 "
-                        "requests, contexts U[4096, 32768], head dim 128, page 16, e4m3")
+    line["workload"] = (f"gqa_batch with 96 q / 8 kv heads (12 query rows per kv head): {w.B} "
+                        "requests, contexts U[4096, 32768], head dim 128, page 16, "
+                        + ("e4m3" if dtype == 0 else "bf16"))
     del arm
     torch.cuda.empty_cache()
     return line
@@ -1190,6 +1192,8 @@ def main():
     wide = None
     if not args.no_wide:
         wide = wide_group_line(device, args.steps, args.warmup, peak)
+        if not args.no_bf16:
+            wide["bf16"] = wide_group_line(device, args.steps, args.warmup, peak, dtype=1)
 
     # ---- continuous batching: requests leave and join between decode steps
     churn = None

@@ -38,19 +38,20 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 32)
       return KV_ERR_UNSUPPORTED;
     const int rb = (int)((R + 7) / 8);
-    // e4m3 with more than 8 rows: consumer warps of 16 rows (kind 3)
-    cfg->kind = d.dtype == KV_DTYPE_E4M3 ? (R > 8 ? 3 : 0) : 1;
-    const int rbw = cfg->kind == 3 ? (int)((R + 15) / 16) : rb;  // row blocks per consumer
+    // more than 8 rows: consumer warps of 16 rows (kinds 3: e4m3, 4: bf16)
+    cfg->kind = d.dtype == KV_DTYPE_E4M3 ? (R > 8 ? 3 : 0) : (R > 8 ? 4 : 1);
+    const bool bf16 = cfg->kind == 1 || cfg->kind == 4;
+    const int rbw = cfg->kind >= 3 ? (int)((R + 15) / 16) : rb;  // row blocks per consumer
     // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
     // tiles are twice as large) dividing Hkv, with heads x row blocks dividing
     // the consumer warp count; ring depth from the ring size
-    int hs = cfg->kind == 1 ? 4 : 8;
+    int hs = bf16 ? 4 : 8;
     while (hs > 0 &&
            (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rbw) != 0))
       hs >>= 1;
     if (hs == 0) return KV_ERR_UNSUPPORTED;  // no split of the consumers fits
     cfg->Hs = hs;
-    const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (cfg->kind == 1 ? 2 : 1);
+    const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (bf16 ? 2 : 1);
     cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;
     if (cfg->stages > gqa_max_stages()) cfg->stages = gqa_max_stages();
     // A consumer warp serves every (consumers/Hs)-th unit; the ring depth must

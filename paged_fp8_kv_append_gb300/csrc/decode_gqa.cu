@@ -25,9 +25,10 @@
 //
 // Per page a consumer computes S^T = K Q^T (M = 16 tokens, N = 8 query rows,
 // K = 128 dims) and O^T += V^T P^T (M = 128 dims, N = 8 rows, K = 16 tokens)
-// with mma.sync m16n8k16.  With more than 8 query rows per kv head, e4m3
-// consumers take 16 rows as the M dimension instead (gqa_split_wide_kernel),
-// so each K/V byte is converted once for all the rows of its kv head.  At 8 query rows per kv head the work is 16 flop per
+// with mma.sync m16n8k16.  With more than 8 query rows per kv head the
+// consumers take 16 rows as the M dimension instead (gqa_split_wide_kernel,
+// gqa_split_wide_bf16_kernel), so each K/V byte is read and converted once
+// for all the rows of its kv head.  At 8 query rows per kv head the work is 16 flop per
 // cache byte, beyond what the fp32 CUDA cores sustain at HBM speed, so the
 // tensor pipe carries the dot products and the CUDA cores only convert and
 // run the softmax.  e4m3 codes convert exactly to f16; the per-page K scale
@@ -235,12 +236,10 @@ struct StageMeta {
 };
 static_assert(sizeof(StageMeta) == 80, "StageMeta layout");
 
-// WIDE (e4m3 only): a consumer warp takes 16 query rows of its kv head
-// instead of 8 (see the wide consumer below); the producer and the ring are
-// the same.
+// WIDE: a consumer warp takes 16 query rows of its kv head instead of 8 (see
+// the wide consumer below); the producer and the ring are the same.
 template <bool FP8, bool WIDE>
 __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
-  static_assert(!WIDE || FP8, "16-row consumers serve e4m3 pools");
   pdl_wait();
   pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
   using C = GqaCfg<FP8>;
@@ -474,10 +473,11 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           for (int u = 0; u < 4; ++u) {  // dims 32t + 8u .. +7: k-steps 2u and 2u+1
             uint4 v = make_uint4(0, 0, 0, 0);
             if (live) v = *reinterpret_cast<const uint4*>(qrow + 8 * u);
-            qa[2 * u][hr] = bf16x2_to_f16x2(v.x);
-            qa[2 * u][2 + hr] = bf16x2_to_f16x2(v.y);
-            qa[2 * u + 1][hr] = bf16x2_to_f16x2(v.z);
-            qa[2 * u + 1][2 + hr] = bf16x2_to_f16x2(v.w);
+            // f16 for e4m3 pools (the codes convert exactly to f16), bf16 as is
+            qa[2 * u][hr] = FP8 ? bf16x2_to_f16x2(v.x) : v.x;
+            qa[2 * u][2 + hr] = FP8 ? bf16x2_to_f16x2(v.y) : v.y;
+            qa[2 * u + 1][hr] = FP8 ? bf16x2_to_f16x2(v.z) : v.z;
+            qa[2 * u + 1][2 + hr] = FP8 ? bf16x2_to_f16x2(v.w) : v.w;
           }
         }
 #pragma unroll
@@ -514,22 +514,40 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
           // ---------------- S = Q K^T: N tile nt, column g = token tok0 + 2 nt
           float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          if constexpr (FP8) {
 #pragma unroll
-          for (int kh = 0; kh < 2; ++kh) {  // dims 32t + 16 kh .. +15: k-steps 4kh .. 4kh+3
-            const uint4 k0 = lds128(Kt + tok0 * 128 + 32 * t + 16 * kh);
-            const uint4 k1 = lds128(Kt + (tok0 + 2) * 128 + 32 * t + 16 * kh);
+            for (int kh = 0; kh < 2; ++kh) {  // dims 32t + 16 kh .. +15: k-steps 4kh .. 4kh+3
+              const uint4 k0 = lds128(Kt + tok0 * 128 + 32 * t + 16 * kh);
+              const uint4 k1 = lds128(Kt + (tok0 + 2) * 128 + 32 * t + 16 * kh);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const uint4 qa = lds128(qs + ((4 * kh + jj) * 32 + lane) * 4);
-              uint32_t b0, b1;
-              e4m3x4_to_f16(w_of(k0, jj), b0, b1);
-              mma16816<true>(s[0], qa.x, qa.y, qa.z, qa.w, b0, b1);
-              e4m3x4_to_f16(w_of(k1, jj), b0, b1);
-              mma16816<true>(s[1], qa.x, qa.y, qa.z, qa.w, b0, b1);
+              for (int jj = 0; jj < 4; ++jj) {
+                const uint4 qa = lds128(qs + ((4 * kh + jj) * 32 + lane) * 4);
+                uint32_t b0, b1;
+                e4m3x4_to_f16(w_of(k0, jj), b0, b1);
+                mma16816<true>(s[0], qa.x, qa.y, qa.z, qa.w, b0, b1);
+                e4m3x4_to_f16(w_of(k1, jj), b0, b1);
+                mma16816<true>(s[1], qa.x, qa.y, qa.z, qa.w, b0, b1);
+              }
+            }
+          } else {
+            // bf16 rows of 256 bytes: thread t's 32 dims are 64 bytes, each
+            // 16-byte load two k-steps' B registers
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {  // dims 32t + 8 kq .. +7: k-steps 2kq, 2kq+1
+              const uint4 k0 = lds128(Kt + tok0 * 256 + 64 * t + 16 * kq);
+              const uint4 k1 = lds128(Kt + (tok0 + 2) * 256 + 64 * t + 16 * kq);
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj) {
+                const uint4 qa = lds128(qs + ((2 * kq + jj) * 32 + lane) * 4);
+                mma16816<false>(s[0], qa.x, qa.y, qa.z, qa.w, jj ? k0.z : k0.x,
+                                jj ? k0.w : k0.y);
+                mma16816<false>(s[1], qa.x, qa.y, qa.z, qa.w, jj ? k1.z : k1.x,
+                                jj ? k1.w : k1.y);
+              }
             }
           }
           // s[nt][e]: row g (e < 2) or g+8, token 4t + 2 nt + (e & 1); log2 domain
-          const float sc = mt.ks[hw] * ssl;
+          const float sc = FP8 ? mt.ks[hw] * ssl : ssl;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -555,8 +573,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
             mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, o));
           }
           // the page's V scale as an exponent bias, as in the 8-row consumer
-          const float bias = __log2f(mt.vs[hw]);
-          const float unbias = fast_exp2(-bias);
+          const float bias = FP8 ? __log2f(mt.vs[hw]) : 0.0f;
+          const float unbias = FP8 ? fast_exp2(-bias) : 1.0f;
           const float nA = fmaxf(mA, mxA + bias), nB = fmaxf(mB, mxB + bias);
           const float alA = (nA == -INFINITY) ? 1.0f : fast_exp2(mA - nA);
           const float alB = (nB == -INFINITY) ? 1.0f : fast_exp2(mB - nB);
@@ -583,19 +601,41 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
               acc[i][3] *= alB;
             }
           }
-          // ---------------- O += P V: P from registers, V tile dim-major
-          const uint32_t pa0 = f32x2_to_f16x2(p[0][0], p[0][1]);
-          const uint32_t pa1 = f32x2_to_f16x2(p[0][2], p[0][3]);
-          const uint32_t pa2 = f32x2_to_f16x2(p[1][0], p[1][1]);
-          const uint32_t pa3 = f32x2_to_f16x2(p[1][2], p[1][3]);
+          // ---------------- O += P V: P from registers, V tile dim-major;
           // tokens beyond the length are zeroed in V (stale bytes could be NaN)
           const int keep = min(max(nv - 4 * t, 0), 4);
-          const uint32_t vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+          if constexpr (FP8) {
+            const uint32_t pa0 = f32x2_to_f16x2(p[0][0], p[0][1]);
+            const uint32_t pa1 = f32x2_to_f16x2(p[0][2], p[0][3]);
+            const uint32_t pa2 = f32x2_to_f16x2(p[1][0], p[1][1]);
+            const uint32_t pa3 = f32x2_to_f16x2(p[1][2], p[1][3]);
+            const uint32_t vmask = keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16(lds32(Vt + (8 * i + g) * 16 + 4 * t) & vmask, b0, b1);
-            mma16816<true>(acc[i], pa0, pa1, pa2, pa3, b0, b1);
+            for (int i = 0; i < 16; ++i) {
+              uint32_t b0, b1;
+              e4m3x4_to_f16(lds32(Vt + (8 * i + g) * 16 + 4 * t) & vmask, b0, b1);
+              mma16816<true>(acc[i], pa0, pa1, pa2, pa3, b0, b1);
+            }
+          } else {
+            // P = hi + lo in bf16 keeps ~16 bits of the weights (two MMAs)
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float f0 = p[e >> 1][2 * (e & 1)], f1 = p[e >> 1][2 * (e & 1) + 1];
+              ph[e] = f32x2_to_bf16x2(f0, f1);
+              pl[e] = f32x2_to_bf16x2(f0 - __uint_as_float(ph[e] << 16),
+                                      f1 - __uint_as_float(ph[e] & 0xFFFF0000u));
+            }
+            // tokens (4t, 4t+1) and (4t+2, 4t+3) of a dim: one 8-byte load
+            const uint32_t mlo = keep >= 2 ? 0xFFFFFFFFu : (keep == 1 ? 0x0000FFFFu : 0u);
+            const uint32_t mhi = keep >= 4 ? 0xFFFFFFFFu : (keep == 3 ? 0x0000FFFFu : 0u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint2 vv = lds64(Vt + (8 * i + g) * 32 + 8 * t);
+              const uint32_t b0 = vv.x & mlo, b1 = vv.y & mhi;
+              mma16816<false>(acc[i], ph[0], ph[1], ph[2], ph[3], b0, b1);
+              mma16816<false>(acc[i], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            }
           }
         }
         __syncwarp();
@@ -974,6 +1014,11 @@ __global__ void __launch_bounds__(GqaCfg<true>::THREADS, 1)
   gqa_split_body<true, true>(a);
 }
 
+__global__ void __launch_bounds__(GqaCfg<false>::THREADS, 1)
+    gqa_split_wide_bf16_kernel(const DecodeArgs a) {
+  gqa_split_body<false, true>(a);
+}
+
 // ------------------------------------------------- combine
 
 constexpr int kCombineWarps = 8;
@@ -1144,20 +1189,28 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
 
 // ------------------------------------------------- host side
 
-// kinds: 0 = e4m3 (8-row consumers), 1 = bf16, 3 = e4m3 with 16-row consumers
-int gqa_ring_bytes(int kind) { return kind == 1 ? GqaCfg<false>::RING : GqaCfg<true>::RING; }
+// kinds: 0 = e4m3 (8-row consumers), 1 = bf16, 3 = e4m3 with 16-row consumers,
+// 4 = bf16 with 16-row consumers
+int gqa_ring_bytes(int kind) {
+  return (kind == 1 || kind == 4) ? GqaCfg<false>::RING : GqaCfg<true>::RING;
+}
 int gqa_max_stages() { return kMaxStages; }
 int gqa_consumer_warps(int kind) {
-  return kind == 1 ? GqaCfg<false>::CONSUMERS : GqaCfg<true>::CONSUMERS;
+  return (kind == 1 || kind == 4) ? GqaCfg<false>::CONSUMERS : GqaCfg<true>::CONSUMERS;
 }
 
 int gqa_split_ctas_per_sm(int kind) {
-  static int cache[4] = {-1, -1, -1, -1};
-  if (kind < 0 || kind > 3 || kind == 2) return 0;
+  static int cache[5] = {-1, -1, -1, -1, -1};
+  if (kind < 0 || kind > 4 || kind == 2) return 0;
   if (cache[kind] >= 0) return cache[kind];
   int n = 0;
   cudaError_t e;
-  if (kind == 3) {
+  if (kind == 4) {
+    cudaFuncSetAttribute(gqa_split_wide_bf16_kernel,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, GqaCfg<false>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_wide_bf16_kernel,
+                                                      GqaCfg<false>::THREADS, GqaCfg<false>::SMEM);
+  } else if (kind == 3) {
     cudaFuncSetAttribute(gqa_split_wide_kernel,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, GqaCfg<true>::SMEM);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_split_wide_kernel,
@@ -1186,7 +1239,9 @@ cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s, int* launche
 
 cudaError_t launch_gqa_split(const DecodeArgs& a, int kind, cudaStream_t s, int* launches) {
   const cudaError_t e =
-      kind == 3   ? launch_pdl(gqa_split_wide_kernel, dim3(a.grid),
+      kind == 4   ? launch_pdl(gqa_split_wide_bf16_kernel, dim3(a.grid),
+                               dim3(GqaCfg<false>::THREADS), GqaCfg<false>::SMEM, s, a)
+      : kind == 3 ? launch_pdl(gqa_split_wide_kernel, dim3(a.grid),
                                dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)
       : kind == 0 ? launch_pdl(gqa_split_kernel<true>, dim3(a.grid),
                                dim3(GqaCfg<true>::THREADS), GqaCfg<true>::SMEM, s, a)

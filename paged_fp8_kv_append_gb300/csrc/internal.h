@@ -95,7 +95,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
 
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {
-  int kind;         // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3, 3 = GQA e4m3 > 8 rows
+  int kind;         // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3, 3 / 4 = GQA e4m3 / bf16 > 8 rows
   int grid;         // split-kernel CTAs
   int R8;           // partial rows per (slot, head)
   int Hs;           // kv heads per unit of work

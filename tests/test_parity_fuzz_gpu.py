@@ -35,8 +35,6 @@ def test_random_shapes(seed):
     rng = np.random.default_rng(9000 + seed)
     B, Hkv, G, T, lens = _draw(rng)
     dtype = seed % 2
-    if dtype == 1 and 16 < T * G <= 24:
-        dtype = 0  # bf16 pools do not serve 17-24 rows per kv head
     npg = int((-(-lens.astype(np.int64) // 16)).sum()) + 16
     w = wl.Workload("fuzz", 7000 + seed, lens, Hkv * G, Hkv, 128, 128, 16, T, 0, npg,
                     float(np.float32(1 / np.sqrt(128))), steps=8)

@@ -108,8 +108,6 @@ def test_kv_magnitude_extremes(dtype, mag, T, Hq):
     are compared relative to the magnitude (the absolute term of the bound
     would otherwise hide a tiny-scale error).  8, 12 and 32 query rows per
     kv head (4 kv heads)."""
-    if dtype == 1 and T * Hq // 4 > 16:
-        pytest.skip("bf16 pools serve at most 16 query rows per kv head here")
     lens = np.array([37, 300, 1000, 5], np.int32)
     w = wl.Workload("magnitude", 123, lens, Hq, 4, 128, 128, 16, T, 0, 256,
                     float(np.float32(1 / np.sqrt(128))), magnitude=mag)
@@ -216,20 +214,14 @@ def test_append_many_requests_and_a_bad_free_list_entry(bad_at):
 @pytest.mark.parametrize("T,Hq,Hkv", [(1, 96, 8), (2, 16, 2), (4, 16, 2), (3, 24, 4),
                                       (1, 32, 1), (5, 10, 2)])
 def test_more_than_eight_rows_per_kv_head(dtype, T, Hq, Hkv):
-    """More than 8 query rows per kv head: each (kv head, block of 8 rows)
-    pair is served by its own consumer warps over the same K/V tiles.  bf16
-    pools have no split of their consumer warps for 17-24 rows and say so."""
-    R = T * Hq // Hkv
+    """More than 8 query rows per kv head: each (kv head, block of 16 rows)
+    pair is served by its own consumer warp over the kv head's K/V tiles
+    (e4m3 and bf16)."""
     lens = np.array([3, 9, 40, 129, 2, 1, 300], np.int32)
     w = wl.Workload("rows", 917 + T + Hq, lens, Hq, Hkv, 128, 128, 16, T, 0, 320,
                     float(np.float32(1 / np.sqrt(128))))
     b = Both(w, dtype)
     assert b.fill()[0] == 0
-    if dtype == 1 and 16 < R <= 24:
-        with pytest.raises(b.kv.KVError) as e:
-            b.dev.workspace_size(w.B, Hq, T)
-        assert e.value.status == b.kv.KV_ERR_UNSUPPORTED
-        return
     out, ref, written = b.attn(_q(w), None, None)
     assert b.dev.error() == 0
     _check_out(out, ref, written, None)
