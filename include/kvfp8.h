@@ -269,8 +269,8 @@ size_t paged_decode_workspace_size(const kv_pool* pool, int32_t B,
  * KV_ERR_BAD_PAGE_ID.  Split-K: pages are spread evenly over a persistent grid
  * sized to the device, partials (fp32 o, running max, sum) go to the
  * workspace, and a combine kernel merges them.  Output is bf16 (RNE).
- * Supported: GQA with head_dim 128, page_size 16 and up to 32 query rows per
- * kv head, q_tokens * (Hq/Hkv) <= 32 (e4m3 and bf16); LATENT
+ * Supported: GQA with head_dim 128, page_size 16 and up to 64 query rows per
+ * kv head, q_tokens * (Hq/Hkv) <= 64 (e4m3 and bf16); LATENT
  * with head_dim_k 576, head_dim_v 512, page_size 64, e4m3.  Other shapes
  * return KV_ERR_UNSUPPORTED.
  */

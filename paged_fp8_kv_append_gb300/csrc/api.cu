@@ -35,21 +35,26 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     const int G = Hq / d.num_kv_heads;
     // query rows per kv head, in blocks of 8 (one consumer warp each)
     const long long R = (long long)T * G;
-    if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 32)
+    if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 64)
       return KV_ERR_UNSUPPORTED;
-    const int rb = (int)((R + 7) / 8);
     // more than 8 rows: consumer warps of 16 rows (kinds 3: e4m3, 4: bf16)
     cfg->kind = d.dtype == KV_DTYPE_E4M3 ? (R > 8 ? 3 : 0) : (R > 8 ? 4 : 1);
-    const bool bf16 = cfg->kind == 1 || cfg->kind == 4;
-    const int rbw = cfg->kind >= 3 ? (int)((R + 15) / 16) : rb;  // row blocks per consumer
+    const bool bf16 = cfg->kind == 1 || cfg->kind == 4, wide = cfg->kind >= 3;
     // heads per unit: the largest power of two <= 8 (<= 4 for bf16, whose
     // tiles are twice as large) dividing Hkv, with heads x row blocks dividing
-    // the consumer warp count; ring depth from the ring size
-    int hs = bf16 ? 4 : 8;
-    while (hs > 0 &&
-           (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rbw) != 0))
-      hs >>= 1;
+    // the consumer warp count; 16-row blocks may be padded with whole unused
+    // blocks until such a split exists; ring depth from the ring size
+    int rbw = wide ? (int)((R + 15) / 16) : (int)((R + 7) / 8);  // row blocks, one warp each
+    int hs = 0;
+    for (; rbw <= (wide ? 4 : 1); ++rbw) {
+      hs = bf16 ? 4 : 8;
+      while (hs > 0 &&
+             (d.num_kv_heads % hs != 0 || gqa_consumer_warps(cfg->kind) % (hs * rbw) != 0))
+        hs >>= 1;
+      if (hs > 0) break;
+    }
     if (hs == 0) return KV_ERR_UNSUPPORTED;  // no split of the consumers fits
+    const int rb = wide ? 2 * rbw : rbw;  // row blocks of 8 in the partial layout
     cfg->Hs = hs;
     const int stage_bytes = 2 * hs * d.page_size * d.head_dim_k * (bf16 ? 2 : 1);
     cfg->stages = gqa_ring_bytes(cfg->kind) / stage_bytes;

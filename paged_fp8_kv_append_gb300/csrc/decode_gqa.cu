@@ -264,7 +264,12 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
   const int rb_mul = (256 + RB - 1) / RB;  // v / RB == (v * rb_mul) >> 8 for v < 12
   const int S = a.stages;                      // ring stages (<= kMaxStages)
   const int stage_bytes = 2 * Hs * C::TILE;
-  if (Hs < 1 || RB < 1 || RB > 4 || RB * C::R8 != a.R8 || (a.R + C::R8 - 1) / C::R8 != RB ||
+  // 8-row consumers: exactly ceil(R / 8) row blocks (at most 4); 16-row
+  // consumers: an even count of at most 8, which may include whole padding
+  // blocks (the host pads so that the warps divide evenly)
+  const bool rows_ok = WIDE ? (RB % 2 == 0 && RB <= 8 && a.R >= 1 && a.R <= C::R8 * RB)
+                            : (RB <= 4 && (a.R + C::R8 - 1) / C::R8 == RB);
+  if (Hs < 1 || RB < 1 || !rows_ok || RB * C::R8 != a.R8 ||
       C::CONSUMERS % Hv != 0 || S < 2 || S > kMaxStages || S % (C::CONSUMERS / Hv) != 0 ||
       stage_bytes * S > C::RING) {
     if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad ring
@@ -655,6 +660,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         lB += __shfl_xor_sync(0xffffffffu, lB, o);
       }
       const long long slot = (long long)r * HG + cur.h + blockIdx.x;
+      const int rbw_mul = (256 + RBW - 1) / RBW;  // v / RBW == (v * rbw_mul) >> 8 for v < 12
       __syncwarp();  // the warp's last reads of its staged Q come before the merge data
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -674,9 +680,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         static_assert(C::R8 == 8 && D == 128, "epilogue index shifts");
         for (int e = threadIdx.x; e < Hv * C::R8 * D; e += C::CONSUMERS * 32) {
           const int dd = e & (D - 1), nw = (e >> 7) & (C::R8 - 1), v = e >> 10;
-          const int hh = RBW == 2 ? v >> 1 : v;
+          const int hh = (v * rbw_mul) >> 8;  // v / RBW (v < 12)
           const int n = (v - hh * RBW) * 16 + 8 * half + nw;
-          if (n >= a.R8) continue;  // padding rows past the partial layout
           float M = -INFINITY;
           for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * C::R8 + nw) * 2]);
           float o = 0.0f, lsum = 0.0f;

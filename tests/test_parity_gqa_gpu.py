@@ -101,13 +101,13 @@ def test_multi_token_causal_and_group_sizes(T, Hq, Hkv):
 
 @pytest.mark.parametrize("dtype", [0, 1])
 @pytest.mark.parametrize("mag", [1e-4, 3e3])
-@pytest.mark.parametrize("T,Hq", [(2, 16), (1, 48), (4, 32)])
+@pytest.mark.parametrize("T,Hq", [(2, 16), (1, 48), (4, 32), (4, 64)])
 def test_kv_magnitude_extremes(dtype, mag, T, Hq):
     """K/V drawn at 1e-4 and 3e3: page scales far from 1 (about 1e-6 and 30)
     must not push the attention weights out of f16's normal range.  Outputs
     are compared relative to the magnitude (the absolute term of the bound
-    would otherwise hide a tiny-scale error).  8, 12 and 32 query rows per
-    kv head (4 kv heads)."""
+    would otherwise hide a tiny-scale error).  8, 12, 32 and 64 query rows
+    per kv head (4 kv heads)."""
     lens = np.array([37, 300, 1000, 5], np.int32)
     w = wl.Workload("magnitude", 123, lens, Hq, 4, 128, 128, 16, T, 0, 256,
                     float(np.float32(1 / np.sqrt(128))), magnitude=mag)
@@ -208,11 +208,13 @@ def test_append_many_requests_and_a_bad_free_list_entry(bad_at):
 
 
 # (T, Hq, Hkv): query rows per kv head R = T * Hq / Hkv beyond one block of 8 --
-# GLM-class groups (96 q / 8 kv heads), speculative tokens on G = 8 models,
-# and a ragged last block
+# GLM-class groups (96 q / 8 kv heads), speculative tokens on G = 8 and G = 16
+# models, 64 query heads on one kv head, and ragged last blocks (R = 18, 25,
+# 33, 40: row blocks padded where the consumer warps would not divide)
 @pytest.mark.parametrize("dtype", [0, 1])
 @pytest.mark.parametrize("T,Hq,Hkv", [(1, 96, 8), (2, 16, 2), (4, 16, 2), (3, 24, 4),
-                                      (1, 32, 1), (5, 10, 2)])
+                                      (1, 32, 1), (5, 10, 2), (1, 64, 1), (4, 64, 4),
+                                      (3, 44, 4), (2, 40, 2)])
 def test_more_than_eight_rows_per_kv_head(dtype, T, Hq, Hkv):
     """More than 8 query rows per kv head: each (kv head, block of 16 rows)
     pair is served by its own consumer warp over the kv head's K/V tiles

@@ -30,7 +30,8 @@ def test_ring_wraps(dtype, Hkv, Hq):
 
 
 @pytest.mark.parametrize("dtype", [0, 1])
-@pytest.mark.parametrize("T,Hq,Hkv", [(1, 96, 8), (4, 64, 8), (2, 16, 1), (3, 36, 4)])
+@pytest.mark.parametrize("T,Hq,Hkv", [(1, 96, 8), (4, 64, 8), (2, 16, 1), (3, 36, 4),
+                                      (4, 64, 4)])
 def test_ring_wraps_wide_groups(dtype, T, Hq, Hkv):
     R = T * Hq // Hkv
     lens = np.array([9000, 7003, 20000, 3001, 1, 5000], np.int32)
