@@ -336,7 +336,11 @@ static int64_t v_off(int64_t p, int64_t h, int64_t slot, int64_t d, int64_t H,
  * +-448 * scale.  Each element is stored as e4m3(x / scale).
  * dtype 1 (bf16): the bf16 bits are stored unchanged; scales are not used.
  * Bookkeeping is or_alloc's; rows of requests at or after the stopping
- * request are not written.  Returns or_alloc's status.
+ * request are not written.  Rows are written after all of the call's pops:
+ * a partly filled page that those pops handed to a later request (its tag
+ * changed in this call) is not written through the earlier, now stale,
+ * mapping (SFS, "Protecting a shared KV cache": a reallocated page is not
+ * used through a mapping recorded before).  Returns or_alloc's status.
  */
 int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
                   int Dv, int dtype, uint8_t* k_cache, uint8_t* v_cache,
@@ -366,6 +370,7 @@ int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
       int64_t pos_lo = (jp * P > L0) ? jp * P : L0;
       int64_t pos_hi = ((jp + 1) * P < L0 + n) ? (jp + 1) * P : L0 + n;
       int64_t h, pos, d;
+      if (jp * P < L0 && fresh[p]) continue; /* partly filled, re-allocated now */
       for (h = 0; h < H; ++h) {
         float ks = 1.0f, vs = 1.0f;
         if (dtype == 0) {
@@ -447,7 +452,8 @@ int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
  * Append to a latent (MLA-style) pool: one row of Dk dims per token; the
  * first Dv dims of the row double as V.  One fp32 scale per page, from the
  * amax over all Dk dims of every row this call writes into a fresh page;
- * frozen afterwards, as in or_append_gqa.  e4m3 only.
+ * frozen afterwards, as in or_append_gqa, which also states the rule for a
+ * partly filled page re-allocated by the same call.  e4m3 only.
  */
 int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
                      float* scale, uint32_t* tags, const int32_t* free_list,
@@ -475,6 +481,7 @@ int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
       int64_t pos_hi = ((jp + 1) * P < L0 + n) ? (jp + 1) * P : L0 + n;
       int64_t pos, d;
       float s;
+      if (jp * P < L0 && fresh[p]) continue; /* partly filled, re-allocated now */
       if (fresh[p]) {
         float a = 0.0f;
         for (pos = pos_lo; pos < pos_hi; ++pos) {

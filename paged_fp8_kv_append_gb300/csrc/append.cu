@@ -18,7 +18,9 @@
 //     the request's rows for that page, computes the amax of a fresh page
 //     (K and V separately), scale = amax/448 (IEEE division; 1 when 0), and stores
 //     e4m3(x / scale) with round-to-nearest-even and saturation; a page that
-//     already held rows keeps its scale.  bf16 pools copy the bits.
+//     already held rows keeps its scale.  bf16 pools copy the bits.  A partly
+//     filled page whose tag this call changed (a later request popped it) is
+//     not written through the stale mapping.
 #include <climits>
 
 #include "common.cuh"
@@ -397,6 +399,10 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
       return;  // uniform across the block
     }
     const bool fresh = jp * P >= L0;  // popped by this call
+    // a partly filled page that this call's pops handed to a later request
+    // (its tag changed after the plan's check) is not written through the
+    // stale mapping
+    if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
     if (d.layout == KV_LAYOUT_LATENT) {
       append_block(a.k_new + row0 * Dk, Dk, nrows, Dk, true, fresh, d.k_scale + p,
                    static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, false, (int)P,
@@ -733,6 +739,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
       continue;
     }
     const bool fresh = jp * P >= L0;  // popped by this call
+    // not through a stale mapping (see append_data_kernel)
+    if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
     const int h = t >> 1;
     if ((t & 1) == 0) {
       tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
@@ -820,6 +828,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
       continue;
     }
     const bool fresh = jp * P >= L0;
+    // not through a stale mapping (see append_data_kernel)
+    if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
     // warp w takes rows w, w + 8, ... of this call's rows in the page
     const int my_rows = nrows > warp ? (nrows - warp + kTileWarps - 1) / kTileWarps : 0;
     const uint16_t* src = a.k_new + (row0 + warp) * Dk;

@@ -221,3 +221,36 @@ def test_append_refuses_a_length_past_int32():
                       p(stop), None)
     assert st == oracle.ERR_INVALID_ARG and int(stop[0]) == 0
     assert int(head[0]) == 8 and sl.tolist() == [2 ** 31 - 16] and not tags.any()
+
+
+def test_no_write_into_a_partial_page_a_later_request_of_the_call_pops():
+    """Rows are written after all of the call's pops: a partly filled page
+    that a later request of the same call pops (its tag changes) is not
+    written through the earlier request's now stale mapping; the new owner's
+    rows and scale are its own.  Worked out by hand on a P = 2 pool."""
+    pool = _tiny_pool()  # tags [10, 20, 30, 40], free list [2, 0, 3, 1]
+    pt = np.full((2, 3), -1, np.int32)
+    et = np.zeros((2, 3), np.uint32)
+    sl = np.zeros(2, np.int32)
+    k = bf16_bits([[[1.0, 2.0]], [[1.0, 1.0]], [[1.0, 1.0]]])
+    assert oracle.append(pool, k, k, np.array([0, 1, 3]), 2, pt, et, sl) == (0, 2)
+    # request 0: page 2 (tag 31), 1 of 2 slots; request 1: page 0 (tag 11), full
+    assert pt.tolist() == [[2, -1, -1], [0, -1, -1]] and et[:, 0].tolist() == [31, 11]
+    assert int(pool.free_head[0]) == 2
+    pool.free_list[2] = 2  # request 0's partly filled page is listed free again
+    k2 = bf16_bits([[[4.0, 0.5]], [[2.0, -1.0]]])
+    st, stop = oracle.append(pool, k2, k2, np.array([0, 1, 2]), 1, pt, et, sl)
+    # request 0's check at its turn sees tag 31 (served); request 1 then pops
+    # page 2 (tag 32) for its new logical page 1
+    assert (st, stop) == (0, 2)
+    assert sl.tolist() == [2, 3] and int(pool.free_head[0]) == 3 and int(pool.tags[2]) == 32
+    assert pt.tolist() == [[2, -1, -1], [0, 2, -1]]
+    assert et.tolist() == [[31, 0, 0], [11, 32, 0]]
+    # page 2 holds request 1's row in slot 0 with its own scale 2/448:
+    # 2 / (2/448) = 448 -> 0x7E, -1 / (2/448) = -224 = -1.75 * 2^7 -> 0xF6;
+    # slot 1 (request 0's row) is not written
+    assert pool.k_scale[2, 0] == np.float32(2.0) / np.float32(448.0)
+    assert pool.k_cache[2, 0, 0].tolist() == [0x7E, 0xF6]
+    assert pool.k_cache[2, 0, 1].tolist() == [0, 0]
+    assert pool.v_cache[2, 0, :, 0].tolist() == [0x7E, 0xF6]
+    assert pool.v_cache[2, 0, :, 1].tolist() == [0, 0]

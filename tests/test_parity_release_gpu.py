@@ -137,6 +137,50 @@ def test_append_stops_at_a_partial_page_popped_earlier_in_the_same_call(dtype):
     b.assert_state_equal()  # requests 0..2 appended (2 holds page p), 3..5 untouched
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("scale_mode", [0, 1])
+def test_no_write_into_a_partial_page_a_later_request_of_the_call_pops(dtype, scale_mode):
+    """A partly filled page listed free again and popped by a later request of
+    the same call: the earlier request is served (its check comes first) but
+    its row does not go into the page, which now holds the later request's
+    rows and scale; the next check aborts the stale request."""
+    if dtype == 1 and scale_mode == 1:
+        pytest.skip("the re-quantising mode applies to e4m3 pools")
+    w = _w([37, 300, 64, 1000, 5, 129], seed=46)
+    b = Both(w, dtype, scale_mode=scale_mode)
+    b.fill()
+    torch.cuda.synchronize()
+    # request 1's partly filled page (300 = 18 * 16 + 12) goes on top of the
+    # free list; request 2 (64 rows: 4 full pages) pops it; request 3 joins
+    # with 20 rows of which the first 8 fill its own partly filled page
+    p = int(b.pt_h[1, 300 // 16])
+    head = int(b.ref.free_head[0])
+    b.ref.free_list[head] = p
+    b.dev.free_list[head] = p
+    counts = np.array([1, 1, 17, 20, 1, 1], np.int64)
+    ks, vs = [], []
+    for r in range(w.B):
+        k, v = wl.kv_rows(w, r, int(b.sl_h[r]), int(counts[r]), device="cuda", tag=13)
+        if r == 1:  # a row that would need a larger scale (exact: a power of two)
+            k, v = (k.float() * 4).to(torch.bfloat16), (v.float() * 4).to(torch.bfloat16)
+        ks.append(k)
+        vs.append(v)
+    st, stop = b.append(ks, vs, counts)
+    torch.cuda.synchronize()
+    assert (st, stop) == (0, w.B) and b.dev.error() == 0
+    assert int(b.pt_h[2, 64 // 16]) == p
+    b.assert_state_equal()  # cache bytes, scales and bookkeeping, bit-exact
+    m_d, m_h = b.verify()
+    assert np.array_equal(m_d.cpu().numpy(), m_h) and m_h.tolist() == [0, 1, 0, 0, 0, 0]
+    q = wl.queries(w, device="cuda")
+    out, ref, written = b.attn(q, m_d, m_h)
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    for r in range(w.B):
+        if written[r]:
+            ok, mabs, mrel, _ = close(got[r], ref[r])
+            assert ok, f"request {r}: max abs {mabs:.3g} max rel {mrel:.3g}"
+
+
 def test_release_refused_when_more_than_handed_out():
     w = _w([37, 300, 64], seed=44)
     b = Both(w, 0)
