@@ -157,28 +157,30 @@ def test_step_latent_draft_tokens():
         active -= set(victims)
 
 
-def test_step_in_a_cuda_graph():
+@pytest.mark.parametrize("dtype,Hq", [(0, 16), (0, 48), (1, 48)])
+def test_step_in_a_cuda_graph(dtype, Hq):
     """The step launches nothing that needs the host: one captured decode
     step (one new row per slot) replayed on new rows and queries matches the
     oracle every time, including a replay in which a request goes stale and
-    is removed inside the graph."""
+    is removed inside the graph.  4 or 12 query rows per kv head (the 8-row
+    and the 16-row consumer kernels)."""
     S = 8
     lens = np.array([37, 300, 16, 1, 700, 129, 64, 5], np.int32)
-    w = wl.Workload("step_graph", 55, lens, 16, 4, 128, 128, 16, 1, 0, 200,
+    w = wl.Workload("step_graph", 55 + Hq + dtype, lens, Hq, 4, 128, 128, 16, 1, 0, 200,
                     float(np.float32(1 / np.sqrt(128))), steps=64)
-    b = Both(w, 0)
+    b = Both(w, dtype)
     assert b.fill()[0] == 0
     kv = b.kv
     k_s = torch.zeros((S, 4, 128), dtype=torch.bfloat16, device="cuda")
     v_s = torch.zeros_like(k_s)
-    q_s = torch.zeros((S, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    q_s = torch.zeros((S, 1, Hq, 128), dtype=torch.bfloat16, device="cuda")
     ind = torch.arange(S + 1, dtype=torch.int32, device="cuda")
-    out = torch.full((S, 1, 16, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((S, 1, Hq, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
     m_d = torch.zeros(S, dtype=torch.uint8, device="cuda")
-    ws = torch.empty(b.dev.step_workspace_size(S, 16, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(b.dev.step_workspace_size(S, Hq, 1), dtype=torch.uint8, device="cuda")
 
     def launch():
-        b.dev.step(S, 16, 1, None, k_s, v_s, ind, 1, b.pt_d, b.et_d, b.sl_d, q_s, w.sm_scale, out,
+        b.dev.step(S, Hq, 1, None, k_s, v_s, ind, 1, b.pt_d, b.et_d, b.sl_d, q_s, w.sm_scale, out,
                    m_d, kv.KV_STEP_REMOVE_ABORTED, ws)
 
     # one eager attention (it changes no pool state) does the kernels'
@@ -203,22 +205,24 @@ def test_step_in_a_cuda_graph():
 
         st, m_h, ref, written = oracle.step(
             b.ref, None, wl.bits_u16(k), wl.bits_u16(v), np.arange(S + 1, dtype=np.int32), 1,
-            b.pt_h, b.et_h, b.sl_h, wl.bits_u16(q), w.sm_scale, 16, 1)
+            b.pt_h, b.et_h, b.sl_h, wl.bits_u16(q), w.sm_scale, Hq, 1)
         _check_step(b, (st, m_d, m_h, out, ref, written), rnd)
         if rnd == 2:
             assert m_h.tolist() == [0, 0, 0, 0, 1, 0, 0, 0] and b.sl_h[4] == 0
 
 
-@pytest.mark.parametrize("dtype,scale_mode", [(0, 0), (1, 0), (0, 1)])
-def test_step_random_rounds(dtype, scale_mode):
+@pytest.mark.parametrize("dtype,scale_mode,Hq", [(0, 0, 16), (1, 0, 16), (0, 1, 16), (0, 0, 80),
+                                                 (1, 0, 80)])
+def test_step_random_rounds(dtype, scale_mode, Hq):
     """Thirty random steps on a small pool: leaves, joins with prompts of up
     to a few pages, decode rows, injected stale tags, and steps that run out
     of pages (the longest request then leaves to make room).  Pool state,
-    abort mask and outputs match the oracle's step after every step."""
-    rng = np.random.default_rng(100 + 10 * dtype + scale_mode)
+    abort mask and outputs match the oracle's step after every step.  4 or
+    20 query rows per kv head."""
+    rng = np.random.default_rng(100 + 10 * dtype + scale_mode + Hq)
     S = 10
-    w = wl.Workload("step_rand", 301 + dtype + 7 * scale_mode, np.zeros(S, np.int32), 16, 4, 128,
-                    128, 16, 1, 0, 40, float(np.float32(1 / np.sqrt(128))), steps=400,
+    w = wl.Workload("step_rand", 301 + dtype + 7 * scale_mode + Hq, np.zeros(S, np.int32), Hq, 4,
+                    128, 128, 16, 1, 0, 40, float(np.float32(1 / np.sqrt(128))), steps=400,
                     magnitude=1.0)
     b = Both(w, dtype, scale_mode=scale_mode)
     rows = _Rows(b)

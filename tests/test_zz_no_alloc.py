@@ -23,9 +23,11 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("dtype", [0, 1])
-def test_noalloc_matches_workspace_entry_point_twice(dtype):
+@pytest.mark.parametrize("Hq", [32, 96])
+def test_noalloc_matches_workspace_entry_point_twice(dtype, Hq):
+    """8 or 24 query rows per kv head (the 8-row and the 16-row kernels)."""
     lens = np.array([37, 64, 100, 255, 1, 4097, 16, 900], np.int32)
-    w = wl.Workload("noalloc", 4242 + dtype, lens, 32, 4, 128, 128, 16, 1, 0, 1024,
+    w = wl.Workload("noalloc", 4242 + dtype + Hq, lens, Hq, 4, 128, 128, 16, 1, 0, 1024,
                     float(np.float32(1 / np.sqrt(128))), stale=[2])
     b = Both(w, dtype)
     assert b.fill()[0] == 0
