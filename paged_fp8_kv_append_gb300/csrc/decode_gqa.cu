@@ -435,13 +435,16 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
     // two N tiles per page) and O += P V (M = 16 rows, N = 8 dims, 16 dim
     // tiles, K = the page's 16 tokens).  The S accumulators are already in
     // the A-fragment layout of P, so P never leaves registers, and each K/V
-    // byte of a kv head is converted once for all its rows.
+    // byte of a kv head is read (and, e4m3, converted) once for all its rows.
+    // A kv head's rows take up to 4 such warps (RBW); rows past R are
+    // padding.
     //   k-slot order: in k-step j of S, thread t's slots 2t, 2t+1, 2t+8,
     //   2t+9 are dims 32t + 4j + 0..3 (its 32 dims are contiguous: two
-    //   16-byte loads of a K row); column c of S's N tile nt is token
-    //   2c - (c & 1) + 2 nt, so P's slots 2t, 2t+1 (tile 0) and 2t+8, 2t+9
-    //   (tile 1) are tokens 4t .. 4t+3: one 4-byte load of the dim-major V
-    //   tile gives both B registers of a PV dim tile.
+    //   16-byte loads of an e4m3 K row, four of a bf16 one); column c of S's
+    //   N tile nt is token 2c - (c & 1) + 2 nt, so P's slots 2t, 2t+1 (tile 0)
+    //   and 2t+8, 2t+9 (tile 1) are tokens 4t .. 4t+3: one 4-byte (e4m3) or
+    //   8-byte (bf16) load of the dim-major V tile gives both B registers of
+    //   a PV dim tile.
     const int g = lane >> 2, t = lane & 3;
     const int G = a.G, T = a.T, R = a.R;
     const int WPH = C::CONSUMERS / Hv;      // warps per virtual head
