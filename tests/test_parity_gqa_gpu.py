@@ -63,6 +63,34 @@ def test_phases_equal_single_call(dtype):
 
 
 @pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("Hq", [8, 24])
+def test_nothing_to_attend(dtype, Hq):
+    """Batches with no page to read: every request aborted (outputs left
+    untouched), and every request empty (no visible position: zero rows, as
+    the oracle gives).  The split grid then has no unit of work at all."""
+    w = wl.tiny(seed=88)
+    if Hq != w.num_q_heads:
+        import dataclasses
+
+        w = dataclasses.replace(w, num_q_heads=Hq)
+    b = Both(w, dtype)
+    assert b.fill()[0] == 0
+    q = _q(w)
+    m_h = np.ones(w.B, np.uint8)
+    m_d = torch.from_numpy(m_h).cuda()
+    out, ref, written = b.attn(q, m_d, m_h)
+    assert not written.any() and b.dev.error() == 0
+    _check_out(out, ref, written, m_h)
+    # the same pool with every request cut back to length 0
+    b.sl_h[:] = 0
+    b.sl_d.zero_()
+    out, ref, written = b.attn(q, None, None)
+    assert written.all() and b.dev.error() == 0
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.all(got == 0.0) and np.all(ref == 0.0)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
 def test_ragged_lengths_and_single_token_appends(dtype):
     """Lengths that end mid-page, zero-length requests, then decode-style
     one-row appends into partly filled pages (frozen scales), several rounds."""
