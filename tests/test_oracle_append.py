@@ -254,3 +254,27 @@ def test_no_write_into_a_partial_page_a_later_request_of_the_call_pops():
     assert pool.k_cache[2, 0, 1].tolist() == [0, 0]
     assert pool.v_cache[2, 0, :, 0].tolist() == [0x7E, 0xF6]
     assert pool.v_cache[2, 0, :, 1].tolist() == [0, 0]
+
+
+def test_latent_no_write_into_a_partial_page_a_later_request_pops():
+    """The latent layout follows the same rule: one scale per page, set by
+    the new owner's rows alone."""
+    pool = oracle.Pool(num_pages=4, page_size=2, num_kv_heads=1, dk=4, dv=2, layout=1,
+                       tags=[10, 20, 30, 40], free_list=[2, 0, 3, 1])
+    pt = np.full((2, 3), -1, np.int32)
+    et = np.zeros((2, 3), np.uint32)
+    sl = np.zeros(2, np.int32)
+    rows = bf16_bits([[1.0, 2.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0], [1.0, 1.0, 1.0, 1.0]])
+    assert oracle.append(pool, rows, None, np.array([0, 1, 3]), 2, pt, et, sl) == (0, 2)
+    assert pt[:, 0].tolist() == [2, 0]
+    pool.free_list[2] = 2  # request 0's partly filled page is listed free again
+    rows2 = bf16_bits([[64.0, 0.5, 0.0, 0.0], [2.0, -1.0, 0.0, 0.25]])
+    st, stop = oracle.append(pool, rows2, None, np.array([0, 1, 2]), 1, pt, et, sl)
+    assert (st, stop) == (0, 2) and sl.tolist() == [2, 3]
+    assert pt.tolist() == [[2, -1, -1], [0, 2, -1]] and int(pool.tags[2]) == 32
+    # page 2: request 1's row in slot 0 with scale 2/448 (amax over all 4 dims):
+    # [448, -224, 0, 0.25 * 224 = 56 = 1.75 * 2^5] -> [0x7E, 0xF6, 0x00, 0x66];
+    # slot 1 (request 0's row, which would have needed a scale of 64/448) not written
+    assert pool.k_scale[2] == np.float32(2.0) / np.float32(448.0)
+    assert pool.k_cache[2, 0].tolist() == [0x7E, 0xF6, 0x00, 0x66]
+    assert pool.k_cache[2, 1].tolist() == [0, 0, 0, 0]

@@ -181,6 +181,35 @@ def test_no_write_into_a_partial_page_a_later_request_of_the_call_pops(dtype, sc
             assert ok, f"request {r}: max abs {mabs:.3g} max rel {mrel:.3g}"
 
 
+@pytest.mark.parametrize("scale_mode", [0, 1])
+def test_no_write_into_a_partial_page_a_later_request_pops_latent(scale_mode):
+    """The same on a latent pool (page 64, one scale per page): request 0's
+    partly filled page (130 = 2 * 64 + 2) is popped by request 1 of the same
+    call and holds only request 1's rows and scale afterwards."""
+    w = _w([130, 64, 700, 2], layout=1, seed=47)
+    b = Both(w, 0, scale_mode=scale_mode)
+    b.fill()
+    torch.cuda.synchronize()
+    p = int(b.pt_h[0, 130 // 64])
+    head = int(b.ref.free_head[0])
+    b.ref.free_list[head] = p
+    b.dev.free_list[head] = p
+    counts = np.array([1, 70, 1, 1], np.int64)
+    ks = []
+    for r in range(w.B):
+        k, _ = wl.kv_rows(w, r, int(b.sl_h[r]), int(counts[r]), device="cuda", tag=14)
+        if r == 0:  # a row that would need a larger scale (exact: a power of two)
+            k = (k.float() * 4).to(torch.bfloat16)
+        ks.append(k)
+    st, stop = b.append(ks, [None] * w.B, counts)
+    torch.cuda.synchronize()
+    assert (st, stop) == (0, w.B) and b.dev.error() == 0
+    assert int(b.pt_h[1, 1]) == p
+    b.assert_state_equal()
+    m_d, m_h = b.verify()
+    assert np.array_equal(m_d.cpu().numpy(), m_h) and m_h.tolist() == [1, 0, 0, 0]
+
+
 def test_release_refused_when_more_than_handed_out():
     w = _w([37, 300, 64], seed=44)
     b = Both(w, 0)
