@@ -7,31 +7,32 @@
 // Section "Protecting a shared KV cache": aborted requests read nothing and
 // return nothing.
 //
-// Work decomposition.  The unit of work is one (page, kv head) pair.  Units
-// are laid out request-major, kv-head-minor ("segments" of ceil(L_r/P) pages
-// each; aborted requests have none) and cut into gridDim.x equal contiguous
-// ranges, one per persistent CTA, so every CTA streams the same number of
-// bytes whatever the length mix.  A CTA range crosses segment boundaries;
-// each (CTA, segment) piece yields one partial (o, running max, sum) in slot
-// segment + cta (injective because both are sorted along the range), and the
-// combine kernel merges the pieces of a segment.
+// Work decomposition.  The unit of work is one page of one request for a
+// group of Hs kv heads.  Units are laid out request-major, head-group-minor
+// ("segments" of ceil(L_r/P) pages each; aborted requests have none) and cut
+// into gridDim.x equal contiguous ranges, one per persistent CTA, so every
+// CTA streams the same number of bytes whatever the length mix.  A CTA range
+// crosses segment boundaries; each (CTA, segment) piece yields one partial
+// (o, running max, sum) in slot segment + cta (injective because both are
+// sorted along the range), and the combine kernel merges the pieces of a
+// segment.
 //
 // CTA layout: the last warp is the producer: it reads page ids and scales
-// and moves each (page, kv head) K tile and V tile into a shared-memory ring
-// with bulk async copies (cp.async.bulk, completion on an mbarrier).  The
-// other warps are consumers: page k of the range goes to consumer k % C,
-// which keeps its own online-softmax state and merges with the others at the
-// end of a piece.
+// and moves each unit's K tiles and V tiles into a shared-memory ring with
+// bulk async copies (cp.async.bulk, completion on an mbarrier).  The other
+// warps are consumers, each serving one (kv head, block of query rows) of
+// every few units; it keeps its own online-softmax state and merges with the
+// warps that share its rows at the end of a piece.
 //
 // Per page a consumer computes S^T = K Q^T (M = 16 tokens, N = 8 query rows,
 // K = 128 dims) and O^T += V^T P^T (M = 128 dims, N = 8 rows, K = 16 tokens)
 // with mma.sync m16n8k16.  With more than 8 query rows per kv head the
 // consumers take 16 rows as the M dimension instead (gqa_split_wide_kernel,
 // gqa_split_wide_bf16_kernel), so each K/V byte is read and converted once
-// for all the rows of its kv head.  At 8 query rows per kv head the work is 16 flop per
-// cache byte, beyond what the fp32 CUDA cores sustain at HBM speed, so the
-// tensor pipe carries the dot products and the CUDA cores only convert and
-// run the softmax.  e4m3 codes convert exactly to f16; the per-page K scale
+// for all the rows of its kv head.  At 8 query rows per kv head the work is
+// 16 flop per cache byte, beyond what the fp32 CUDA cores sustain at HBM
+// speed, so the tensor pipe carries the dot products and the CUDA cores only
+// convert and run the softmax.  e4m3 codes convert exactly to f16; the per-page K scale
 // multiplies the scores and the V scale enters P as an exponent bias.
 #include <float.h>
 
