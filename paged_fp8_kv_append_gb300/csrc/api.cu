@@ -33,7 +33,7 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
   if (d.layout == KV_LAYOUT_GQA) {
     if (Hq % d.num_kv_heads != 0) return KV_ERR_INVALID_ARG;
     const int G = Hq / d.num_kv_heads;
-    // query rows per kv head, in blocks of 8 (one consumer warp each)
+    // query rows per kv head, in blocks of 8 or 16 (one consumer warp each)
     const long long R = (long long)T * G;
     if (d.head_dim_k != 128 || d.head_dim_v != 128 || d.page_size != 16 || R > 64)
       return KV_ERR_UNSUPPORTED;
@@ -74,8 +74,10 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     cfg->unit_tokens = d.page_size;
     return KV_OK;
   }
-  // latent layout: query rows (T tokens x Hq heads) in blocks of 64
+  // latent layout: query rows (T tokens x Hq heads) in blocks of 64; the
+  // row count stays far inside int range (2^20 rows)
   const int rb = latent_row_block();
+  if ((long long)T * Hq > (1ll << 20)) return KV_ERR_UNSUPPORTED;
   if (d.head_dim_k != 576 || d.head_dim_v != 512 || d.page_size != 64 || (T * Hq) % rb != 0 ||
       d.dtype != KV_DTYPE_E4M3)
     return KV_ERR_UNSUPPORTED;
