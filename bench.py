@@ -1,18 +1,27 @@
 """Benchmark of the paged FP8 KV decode hot path on GB300.
 
-One step = one decode step of the GQA batch workload (32 requests, contexts
-uniform in 4k..32k, 64 query / 8 kv heads, head dim 128, page size 16):
-every request appends its new token's K/V (bf16 -> e4m3 with per-(page,
-kv-head) scales), the batched page-tag check runs, then split-K decode
-attention and the combine.  The FP8 cache is the headline; the same step over
-a BF16 cache is reported beside it.
+Headline step: 64 requests of 131,072 tokens each (64 query / 8 kv heads,
+head dim 128, page size 16, FP8 e4m3 cache): every request appends its new
+token's K/V (bf16 -> e4m3 with per-(page, kv-head) scales), the batched
+page-tag check runs, then split-K decode attention and the combine.  `value`
+is decode tokens/s with each step replayed as a CUDA graph; `roofline` is the
+split phase against the measured HBM copy bandwidth (and split + combine with
+Q and O counted, under `roofline.attn`).  The same line carries, under
+`roofline.points`, the other configurations: the 1..32-request points and the
+BF16 cache at 128k, the 32-request GQA batch (4k..32k), the skewed
+256-request stress step, the 96 q / 8 kv group, the latent tensor-core
+verify, the tag-check overhead and the bulk append.  `cpu_baseline` is the
+CPU oracle replaying sampled requests' first step, with the element-wise
+comparison of the GPU's outputs for those requests (`parity`).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--detail FILE]
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle, as it
-stands, on a bounded sample of the same workload.  Multi-GPU runs are
-data-parallel replicas (one pool and one request shard per rank, no
-collective on the data path); the step time is the max over ranks.
+Prints one JSON line (rank 0); --detail also writes every measured line to a
+file.  --impl reference times the CPU oracle, as it stands, on the headline
+workload.  Multi-GPU runs are data-parallel replicas (one pool and one
+request shard per rank, no collective on the data path); the step time is the
+max over ranks.
 """
 from __future__ import annotations
 
@@ -35,14 +44,13 @@ import workloads as wl  # noqa: E402
 METRIC = ("decode attn tokens/s & achieved HBM GB/s vs ~8 TB/s, FP8 vs BF16 KV, 1×GB300")
 NOMINAL_HBM_GBS = 8000.0
 
-# DRAM counters of gqa_split_kernel<e4m3> from one ncu capture of a small case
-# (the first 8 requests of the GQA batch workload; profiles/
-# gqa_split_e4m3_small_full.md): reads per algorithmic byte, and the partial
-# (o, m, l) writes of its 8 * 2 + 152 pieces.  Re-take them whenever the
-# kernel changes.
-SPLIT_NCU = {"read_per_alg_byte": 377.359104 / 377.100912, "write_bytes": 3236352.0,
-             "pieces": 8 * 2 + 152, "heads_per_unit": 4,
-             "profile": "profiles/gqa_split_e4m3_small_full.md"}
+# DRAM bytes of gqa_split_kernel<e4m3> per launch from one ncu capture
+# (dram__bytes_read.sum per algorithmic byte, dram__bytes_write.sum per
+# (CTA, segment) piece), valid only while the kernel's sources hash to `sha`
+# (sha256 of the listed files, first 16 hex digits); otherwise the line
+# reports traffic null.
+SPLIT_DRAM = {"sources": ["decode_gqa.cu", "decode_plan.cuh", "common.cuh"], "sha": None,
+              "read_per_alg_byte": None, "write_per_piece": None}
 
 
 # ------------------------------------------------------------ distributed
@@ -267,6 +275,18 @@ class Arm:
             launches.append(n)
         self.step_no += 1
         self.lens[:B] += 1
+
+    def first_step_output(self, rs) -> dict:
+        """Run the arm's first decode step (step rows 0, queries of step 0) and
+        return the output rows of requests rs as bf16 bit patterns (host):
+        the CPU-baseline leg replays the same step in the oracle."""
+        assert self.step_no == 0
+        self.out.fill_(7.0)
+        self.step()
+        torch.cuda.synchronize()
+        if self.pool.error() != 0:
+            raise RuntimeError(f"first step: {self.kv.kv_status_string(self.pool.error())}")
+        return {int(r): wl.bits_u16(self.out[int(r)]) for r in rs}
 
     def run(self, steps: int, warmup: int, B=None, sync_ranks=True):
         B = self.w.B if B is None else B
@@ -645,7 +665,7 @@ def churn_line(device, steps: int, warmup: int) -> dict:
 # ------------------------------------------------------------ wider query groups
 
 def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
-                    dtype: int = 0) -> dict:
+                    dtype: int = 0, parity=None) -> dict:
     """The GQA batch's requests with 96 query heads on its 8 kv heads (the
     GLM-class group of 12): 12 query rows per kv head, each kv head's rows
     served by one 16-row consumer warp.  e4m3 (dtype 0) or bf16 (1); the step
@@ -656,7 +676,11 @@ def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
     w = dataclasses.replace(wl.gqa_batch(steps=steps + warmup + 2), num_q_heads=96)
     if B != w.B:
         w = wl.subset(w, B)
-    arm = Arm(w, dtype, device, steps + warmup)
+    arm = Arm(w, dtype, device, steps + warmup + 1)
+    if parity is not None:
+        r = int(np.argmax(w.lens))
+        parity.append({"name": f"wide96_{'e4m3' if dtype == 0 else 'bf16'}", "w": w,
+                       "dtype": dtype, "pairs": [(r, 6)], "outs": arm.first_step_output([r])})
     line = step_line(w, arm, dtype, steps, warmup)
     line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
     line["workload"] = (f"gqa_batch with 96 q / 8 kv heads (12 query rows per kv head): {w.B} "
@@ -753,31 +777,15 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
                           for i, k in enumerate(("append", "verify", "split", "combine"))}}
 
 
-def concurrency_sweep(device, steps: int, warmup: int, peak: float, replays: int,
-                      points=(1, 8, 16, 32, 64)) -> dict:
-    """The concurrency sweep: 1..64 requests of 131,072 tokens (64 q / 8 kv
-    heads, D 128, P 16), e4m3 and bf16.  One pool per dtype is filled with 64
-    requests; each point steps the first B of them."""
-    out = {}
-    graph_points = (1, 8)
-    n_steps = len(points) * (steps + warmup) + 2 * len(graph_points) * (replays + 8) + 2
-    for dtype, name in ((0, "e4m3"), (1, "bf16")):
-        w = wl.concurrency(max(points))
-        w.steps = n_steps
-        w.num_pages = int(w.B * (-(-(131072 + n_steps) // 16))) + 64
-        arm = Arm(w, dtype, device, n_steps)
-        pts = []
-        for B in points:
-            line = step_line(w, arm, dtype, steps, warmup, B=B)
-            line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
-            pts.append(line)
-        out[name] = pts
-        if dtype == 0:  # the tag check at small batch, as CUDA graphs
-            out["verify_overhead_e4m3"] = [graph_overhead(arm, replays, B=b) for b in graph_points]
-        del arm
-        torch.cuda.empty_cache()
-    out["workload"] = ("concurrency: B requests of 131,072 tokens, 64 q / 8 kv heads, head dim "
-                       "128, page 16; step = append 1 token/request + tag check + attention")
+def sweep_lines(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, peak: float,
+                points) -> list:
+    """Step lines (tokens/s, attention GB/s) for the first B requests of a
+    filled 131,072-token pool, for each B in points."""
+    out = []
+    for B in points:
+        line = step_line(w, arm, dtype, steps, warmup, B=B)
+        line["pct_of_measured"] = 100.0 * line["attn_gbs"] / peak
+        out.append(line)
     return out
 
 
@@ -815,7 +823,7 @@ def release_lines(arm: "Arm") -> list:
     return out
 
 
-def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float):
+def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float, parity=None):
     """The skewed long-context stress workload (256 requests, lognormal
     contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
     428k pages checked per step): the verify overhead with every tag valid,
@@ -823,7 +831,12 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float):
     w = wl.skewed(steps=2 * (replays + 8) + steps + warmup + 8)
     stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
-    arm = Arm(w, 0, device, steps + warmup)
+    arm = Arm(w, 0, device, steps + warmup + 1)
+    if parity is not None:  # a seeded live request, all tags valid at this step
+        live = [r for r in range(w.B) if r not in stale and w.lens[r] <= 65536]
+        r = int(np.random.default_rng(w.seed + 11).choice(live))
+        parity.append({"name": "skewed_e4m3", "w": w, "dtype": 0, "pairs": [(r, 3)],
+                       "outs": arm.first_step_output([r])})
     over = graph_overhead(arm, replays)
     over["workload"] = ("skewed: 256 requests, lognormal contexts (median 16k) in [1, 256k], "
                         "32 q / 4 kv heads, head dim 128, page 16, e4m3; all tags valid")
@@ -834,7 +847,7 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float):
     for r, j in wl.stale_slots(w):
         et[r, j] = np.uint32(et[r, j]) - np.uint32(1)
     arm.et.copy_(torch.from_numpy(et.view(np.int32)))
-    arm.step_no = 0
+    arm.step_no = 1
     line = step_line(w, arm, 0, steps, warmup, aborted=stale)
     if not np.array_equal(np.flatnonzero(arm.mask.cpu().numpy()), np.array(sorted(stale))):
         raise RuntimeError("skewed step: abort mask differs from the stale requests")
@@ -944,42 +957,182 @@ def latent_bench(steps: int, warmup: int, device, peaks: dict, B: int = 64) -> d
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample(w: wl.Workload, budget_s: float, device, start_req: int = 0,
-                  max_requests=None):
-    """Time the oracle on whole requests of the workload (one decode step
-    each: append the step's row, check the tags, fp64 attention) until the
-    budget is spent.  Returns (requests, seconds, description)."""
+TOL_ABS, TOL_REL = 2e-3, 1e-2  # attention tolerance: |o - r| <= abs + rel * |r|
+
+
+def _bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+
+
+def oracle_pair_step(w: wl.Workload, r: int, h: int, dtype: int, device):
+    """The oracle's replay of the first decode step of request r of a GQA
+    workload, for its kv head h only (a one-kv-head pool fed that head's
+    rows, as the GPU arms feed all heads): the request's first L_r - 1 rows
+    appended in one call (untimed), then the timed step -- the step's new row
+    appended, the tag check, fp64 attention for the G query heads of kv head
+    h.  Returns (seconds of the timed step, output [T][G][Dv])."""
     import oracle
 
-    done, spent, r = 0, 0.0, start_req
-    names = []
-    cap = max_requests if max_requests is not None else 10 ** 9
-    while done < cap and (done == 0 or spent < budget_s):
-        r = r % w.B
-        L = int(w.lens[r])
-        k, v = wl.kv_rows(w, r, 0, L - 1, device=device)
-        ks, vs = wl.step_rows(w, 0, device=device)
-        npg = -(-L // w.page_size) + 1
-        pool = oracle.Pool(npg, w.page_size, w.num_kv_heads, w.head_dim_k, w.head_dim_v, 0)
-        pt = np.full((1, npg), -1, np.int32)
-        et = np.zeros((1, npg), np.uint32)
-        sl = np.zeros(1, np.int32)
-        oracle.append(pool, wl.bits_u16(k), wl.bits_u16(v), np.array([0, L - 1], np.int32), L,
-                      pt, et, sl)
-        q = wl.bits_u16(wl.queries(w, device=device)[r:r + 1])
-        krow, vrow = wl.bits_u16(ks[r:r + 1]), wl.bits_u16(vs[r:r + 1])
+    T, P = w.q_tokens, w.page_size
+    G = w.num_q_heads // w.num_kv_heads
+    L = int(w.lens[r])
+    npg = -(-L // P) + 1
+    ptab = np.full((1, npg), -1, np.int32)
+    et = np.zeros((1, npg), np.uint32)
+    sl = np.zeros(1, np.int32)
+    n0 = L - T
+    k, v = wl.kv_rows(w, r, 0, n0, device=device)
+    pool = oracle.Pool(npg, P, 1, w.head_dim_k, w.head_dim_v, dtype=dtype)
+    oracle.append(pool, wl.bits_u16(k[:, h:h + 1]), wl.bits_u16(v[:, h:h + 1]),
+                  np.array([0, n0], np.int32), n0, ptab, et, sl)
+    del k, v
+    ks, vs = wl.step_rows(w, 0, device=device)
+    krow, vrow = wl.bits_u16(ks[r:r + 1, h:h + 1]), wl.bits_u16(vs[r:r + 1, h:h + 1])
+    q = wl.bits_u16(wl.queries(w, device=device)[r:r + 1, :, h * G:(h + 1) * G])
+    t0 = time.perf_counter()
+    oracle.append(pool, krow, vrow, np.array([0, T], np.int32), T, ptab, et, sl)
+    mask = oracle.verify(pool.num_pages, P, pool.tags, ptab, et, sl)
+    ref, written = oracle.attn(pool, q, ptab, sl, mask, w.sm_scale, G, T)
+    sec = time.perf_counter() - t0
+    if not written[0]:
+        raise RuntimeError(f"oracle: request {r} of {w.name} aborted with every tag valid")
+    return sec, ref[0]
+
+
+def cpu_baseline_leg(samples: list, device, budget_s: float) -> tuple:
+    """The CPU oracle, as it stands, on one host core: it replays the first
+    decode step of sampled (request, kv head) pairs of the timed workloads
+    (the GPU's output rows of that step were kept) and compares them element
+    by element.  The headline's pairs give the baseline's tokens/s (a pair is
+    1/Hkv of a request's decode token); every pair gives a parity record.
+    Samples after the first two stop once budget_s of timed oracle work is
+    spent."""
+    head_sec, head_tok, head_names = 0.0, 0.0, []
+    parity, spent = {}, 0.0
+    for i, smp in enumerate(samples):
+        w, name = smp["w"], smp["name"]
+        G = w.num_q_heads // w.num_kv_heads
+        for r, h in smp["pairs"]:
+            if i >= 2 and spent > budget_s:
+                break
+            sec, ref = oracle_pair_step(w, r, h, smp["dtype"], device)
+            spent += sec
+            got = _bf16_bits_to_f64(smp["outs"][r])[:, h * G:(h + 1) * G]
+            err = np.abs(got - ref)
+            ok = bool(np.all(err <= TOL_ABS + TOL_REL * np.abs(ref)))
+            rel = float((err / np.maximum(np.abs(ref), 1e-30)).max())
+            p = parity.setdefault(name, {"ok": True, "max_abs": 0.0, "max_rel": 0.0,
+                                         "pairs": []})
+            p["ok"] = p["ok"] and ok
+            p["max_abs"] = max(p["max_abs"], float(err.max()))
+            p["max_rel"] = max(p["max_rel"], rel)
+            p["pairs"].append([int(r), int(h)])
+            if smp.get("headline"):
+                head_sec += sec
+                head_tok += w.q_tokens / w.num_kv_heads
+                head_names.append(f"r{r}/kv{h}(L={int(w.lens[r])})")
+    return head_tok, head_sec, head_names, parity
+
+
+def reference_arm(args):
+    """--impl reference: the oracle, as it stands, on the headline workload
+    (requests of 131,072 tokens; 64 q / 8 kv heads, head dim 128, page 16,
+    e4m3), on one host core.  Each step is one decode step of one (request,
+    kv head) pair -- its new row appended, the tag check, fp64 attention for
+    the kv head's 8 query heads -- so a step is 1/8 of a request's decode
+    token; the pair's earlier rows are appended once before the first step."""
+    import oracle
+
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.concurrency(64)
+    r, h, L, P = 0, 0, int(w.lens[0]), w.page_size
+    G = w.num_q_heads // w.num_kv_heads
+    n = args.warmup + args.steps
+    npg = -(-(L + n) // P) + 1
+    pool = oracle.Pool(npg, P, 1, w.head_dim_k, w.head_dim_v, dtype=0)
+    ptab = np.full((1, npg), -1, np.int32)
+    et = np.zeros((1, npg), np.uint32)
+    sl = np.zeros(1, np.int32)
+    k, v = wl.kv_rows(w, r, 0, L - 1, device=device)
+    oracle.append(pool, wl.bits_u16(k[:, h:h + 1]), wl.bits_u16(v[:, h:h + 1]),
+                  np.array([0, L - 1], np.int32), L - 1, ptab, et, sl)
+    del k, v
+    per_step = []
+    for i in range(n):
+        ks, vs = wl.step_rows(w, i, device=device)
+        q = wl.bits_u16(wl.queries(w, device=device, step=i)[r:r + 1, :, h * G:(h + 1) * G])
+        krow, vrow = wl.bits_u16(ks[r:r + 1, h:h + 1]), wl.bits_u16(vs[r:r + 1, h:h + 1])
         t0 = time.perf_counter()
-        oracle.append(pool, krow, vrow, np.array([0, 1], np.int32), 1, pt, et, sl)
-        mask = oracle.verify(pool.num_pages, w.page_size, pool.tags, pt, et, sl)
-        oracle.attn(pool, q, pt, sl, mask, w.sm_scale, w.num_q_heads, w.q_tokens)
-        spent += time.perf_counter() - t0
-        done += 1
-        names.append(f"r{r}(L={L})")
-        r += 1
-    return done, spent, names
+        oracle.append(pool, krow, vrow, np.array([0, 1], np.int32), 1, ptab, et, sl)
+        mask = oracle.verify(pool.num_pages, P, pool.tags, ptab, et, sl)
+        oracle.attn(pool, q, ptab, sl, mask, w.sm_scale, G, w.q_tokens)
+        if i >= args.warmup:
+            per_step.append(time.perf_counter() - t0)
+    total = sum(per_step)
+    value = args.steps * w.q_tokens / w.num_kv_heads / total
+    sample = (f"{args.steps} decode steps of request 0 (131,072+ tokens), kv head 0 (8 query "
+              "heads, 1/8 of a request's token each) of the 64 x 131,072 e4m3 workload, one per "
+              "step, on one host core")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE_NAME, "batch_per_step": "1 (request, kv head) pair",
+                   "note": "CPU oracle: each step is one (request, kv head) decode step (append "
+                           "1 row, tag check, fp64 attention of 8 query heads)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
 
 
 # ------------------------------------------------------------ main
+
+HEADLINE_NAME = ("concurrency 64 x 131072: 64 requests of 131,072 tokens, 64 q / 8 kv heads, "
+                 "head dim 128, page 16, e4m3")
+
+
+def _peaks() -> dict:
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:  # noqa: BLE001
+        return {}
+
+
+def _pt(line: dict, peak: float) -> dict:
+    """Compact summary of a step line: tokens/s, attention GB/s, fraction of
+    the measured copy bandwidth and of 8 TB/s."""
+    return {"tok_s": round(line["tokens_per_s"], 1), "gbs": round(line["attn_gbs"], 1),
+            "frac": round(line["attn_gbs"] / peak, 4),
+            "frac_8000": round(line["attn_gbs"] / NOMINAL_HBM_GBS, 4),
+            "attn_us": round(line["attn_us"], 2)}
+
+
+def split_traffic(alg_bytes: float, pieces: int):
+    """DRAM bytes of one split launch from the recorded ncu counters, scaled
+    to this launch (reads in proportion to the algorithmic bytes, partial
+    writes to the pieces), or None when the kernel's sources differ from the
+    ones the counters were taken on."""
+    import hashlib
+
+    rec = SPLIT_DRAM
+    if not rec.get("sha"):
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, "paged_fp8_kv_append_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != rec["sha"]:
+        return None
+    return rec["read_per_alg_byte"] * alg_bytes + rec["write_per_piece"] * pieces
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -987,22 +1140,27 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=25.0)
+    ap.add_argument("--detail", default="",
+                    help="also write every measured line (JSON) to this file")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-latent", action="store_true")
     ap.add_argument("--no-overhead", action="store_true",
-                    help="skip the CUDA-graph verify-overhead measurement")
+                    help="skip the CUDA-graph verify-overhead measurements")
     ap.add_argument("--overhead-replays", type=int, default=20)
     ap.add_argument("--no-requant", action="store_true",
                     help="skip the re-quantising scale mode lines")
     ap.add_argument("--no-wide", action="store_true",
-                    help="skip the 96 q / 8 kv head (12 rows per kv head) step line")
+                    help="skip the 96 q / 8 kv head (12 rows per kv head) step lines")
     ap.add_argument("--no-churn", action="store_true",
                     help="skip the continuous-batching line")
     ap.add_argument("--no-bulk", action="store_true",
                     help="skip the bulk-append (prefill handoff) lines")
-    ap.add_argument("--no-sweep", action="store_true",
-                    help="skip the 1..64-request concurrency sweep at 128k")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="only the 128k concurrency configs (headline, sweep) and the CPU leg")
+    ap.add_argument("--requests", type=int, default=64,
+                    help="requests of 131,072 tokens in the headline step (64 = the workload; "
+                         "fewer only for small profiling captures)")
     ap.add_argument("--conc-only", type=int, default=0, metavar="B",
                     help="run only the e4m3 step on B requests of 131,072 tokens and print its "
                          "line (small profiling captures)")
@@ -1025,34 +1183,12 @@ def main():
         raise SystemExit("warmup must be >= 3")
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        device = "cuda" if torch.cuda.is_available() else "cpu"
-        w = wl.gqa_batch()
-        per_step = []
-        req = 0
-        for i in range(args.warmup + args.steps):
-            n, sec, names = oracle_sample(w, 0.0, device, start_req=req, max_requests=1)
-            req += n
-            if i >= args.warmup:
-                per_step.append(sec)
-        total = sum(per_step)
-        value = args.steps * w.q_tokens / total
-        line = {
-            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "gqa_batch", "batch_per_step": 1,
-                       "note": "each step: one request of the GQA batch workload (append 1 row, "
-                               "tag check, fp64 attention) on one host core"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} requests of gqa_batch, one per step"},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0},
-        }
-        print(json.dumps(line))
+        reference_arm(args)
         return
+
+    peaks = _peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     if args.conc_only > 0:
         device = torch.device("cuda", local)
@@ -1062,38 +1198,20 @@ def main():
         arm = Arm(w, 0, device, args.steps + args.warmup)
         print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
         return
-
     if args.wide_only > 0:
         device = torch.device("cuda", local)
-        peak = 6681.5
-        try:
-            peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
-        except Exception:
-            pass
         print(json.dumps(wide_group_line(device, args.steps, args.warmup, peak,
                                          B=args.wide_only)))
         return
-
     if args.bulk_only > 0:
         device = torch.device("cuda", local)
-        peak = 6681.5
-        try:
-            peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
-        except Exception:
-            pass
         w = wl.subset(wl.gqa_batch(), args.bulk_only)
         for _ in range(args.warmup):
             bulk_append_line(w, 0, device, peak)
         print(json.dumps([bulk_append_line(w, 0, device, peak) for _ in range(args.steps)]))
         return
-
     if args.latent_only > 0:
         device = torch.device("cuda", local)
-        peaks = {}
-        try:
-            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-        except Exception:
-            pass
         print(json.dumps(latent_bench(args.steps, args.warmup, device, peaks,
                                       B=args.latent_only)))
         return
@@ -1104,165 +1222,207 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    total_steps = 4 * (args.steps + args.warmup)
-    graph_steps = 0 if args.no_overhead else 2 * (args.overhead_replays + 8)
-    w = wl.gqa_batch(seed=shard_seed(20262, rank), steps=total_steps + graph_steps + 2)
-    if args.batch != w.B:
-        w = wl.subset(w, args.batch)
+    K, W, R = args.steps, args.warmup, args.overhead_replays
+    detail, parity_samples = {}, []
+    run_extra = not args.no_extra
 
-    # ---- FP8 (headline)
-    arm = Arm(w, 0, device, total_steps)
+    # ---- headline: B requests of 131,072 tokens, e4m3 cache
+    B = args.requests
+    sweep_pts = [b for b in (1, 8, 16, 32) if b < B]
+    head_steps = 1 + 4 * (K + W) + len(sweep_pts) * (K + W)
+    over_steps = 0 if args.no_overhead else 2 * (2 * (3 + R) + 2)
+    w = wl.concurrency(B, seed=shard_seed(20264, rank))
+    w.steps = head_steps + over_steps + 4
+    w.num_pages = int(B * (-(-(131072 + w.steps) // 16))) + 64
+    arm = Arm(w, 0, device, head_steps)
+    rng = np.random.default_rng(w.seed + 5)
+    picks = sorted({0, int(rng.integers(1, B))}) if B > 1 else [0]
+    pairs = [(r, int(rng.integers(0, w.num_kv_heads))) for r in picks]
+    parity_samples.append({"name": "concurrency64_e4m3", "w": w, "dtype": 0, "headline": True,
+                           "pairs": pairs, "outs": arm.first_step_output(picks)})
     sampler = ClockSampler(smi_index(local))
-    total_ms, per, lens_timed, launches = arm.run(args.steps, args.warmup)
-    graph_ms = arm.run_graphs(args.steps, args.warmup)
+    total_ms, per, lens_timed, launches = arm.run(K, W)
+    graph_ms = arm.run_graphs(K, W)
     clocks = sampler.stop()
-    e2e_ms, h2d, d2h = arm.run_e2e(args.steps, args.warmup, graph=True)
-    e2e_eager_ms, _, _ = arm.run_e2e(args.steps, args.warmup, graph=False)
-    overhead = None
+    e2e_ms, h2d, d2h = arm.run_e2e(K, W, graph=True)
+    e2e_eager_ms, _, _ = arm.run_e2e(K, W, graph=False)
+    conc_e4m3 = sweep_lines(w, arm, 0, K, W, peak, sweep_pts)
+    overhead = {}
     if not args.no_overhead:
-        overhead = {"gqa_batch": graph_overhead(arm, args.overhead_replays)}
+        for b in (1, 8):
+            if b <= B:
+                overhead[f"concurrency_{b}"] = graph_overhead(arm, R, B=b)
     del arm
     torch.cuda.empty_cache()
 
     eager_ms = reduce_max(total_ms)
     max_ms = reduce_max(graph_ms)
-    tokens = reduce_sum(args.steps * w.B * w.q_tokens)
+    tokens = reduce_sum(K * w.B * w.q_tokens)
     value = tokens / (max_ms / 1e3)
-    eager_value = tokens / (eager_ms / 1e3)
-    e2e_value = tokens / (reduce_max(e2e_ms) / 1e3)
-    e2e_eager_value = tokens / (reduce_max(e2e_eager_ms) / 1e3)
     split_ms = per[:, 2]
+    attn_ms = per[:, 2] + per[:, 3]
     attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_timed]
     split_bytes = [algorithmic_bytes(w, L, 0, include_out=False) for L in lens_timed]
     achieved = float(np.mean([b / (t * 1e6) for b, t in zip(split_bytes, split_ms)]))
-    # DRAM traffic per split launch, scaled from the small-case capture: reads
-    # in proportion to the algorithmic bytes, partial writes to the pieces
-    pieces = w.B * (w.num_kv_heads // SPLIT_NCU["heads_per_unit"]) + 152
-    traffic = (SPLIT_NCU["read_per_alg_byte"] * float(np.mean(split_bytes))
-               + SPLIT_NCU["write_bytes"] * pieces / SPLIT_NCU["pieces"])
-    attn_gbs = float(np.mean([b / ((p[2] + p[3]) * 1e6) for b, p in zip(attn_bytes, per)]))
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    attn_gbs = float(np.mean([b / (t * 1e6) for b, t in zip(attn_bytes, attn_ms)]))
+    head_line = {"requests": B, "attended": B, "tokens_per_s": tokens / (eager_ms / 1e3),
+                 "ms_per_step": eager_ms / K, "attn_us": float(attn_ms.mean() * 1e3),
+                 "attn_gbs": attn_gbs, "pct_of_8000": 100.0 * attn_gbs / NOMINAL_HBM_GBS,
+                 "pct_of_measured": 100.0 * attn_gbs / peak,
+                 "kernel_us": {k: float(per[:, i].mean() * 1e3)
+                               for i, k in enumerate(("append", "verify", "split", "combine"))}}
+    conc_e4m3.append(head_line)
+    detail["concurrency_e4m3"] = conc_e4m3
+    detail["verify_overhead"] = overhead
 
-    # ---- BF16 cache, same workload
-    bf16 = None
+    # ---- the same requests over a BF16 cache
+    conc_bf16 = []
     if not args.no_bf16:
-        arm16 = Arm(w, 1, device, total_steps)
-        t16, per16, lens16, _ = arm16.run(args.steps, args.warmup)
+        arm16 = Arm(w, 1, device, 1 + (len(sweep_pts) + 1) * (K + W))
+        parity_samples.append({"name": "concurrency64_bf16", "w": w, "dtype": 1,
+                               "pairs": pairs[:1], "outs": arm16.first_step_output(picks[:1])})
+        conc_bf16 = sweep_lines(w, arm16, 1, K, W, peak, sweep_pts + [B])
         del arm16
         torch.cuda.empty_cache()
-        b16 = [algorithmic_bytes(w, L, 1, include_out=False) for L in lens16]
-        bf16 = {
-            "value": reduce_sum(args.steps * w.B * w.q_tokens) / (reduce_max(t16) / 1e3),
-            "unit": "tokens/s", "ms_per_step": t16 / args.steps,
-            "split_us": float(per16[:, 2].mean() * 1e3),
-            "split_gbs": float(np.mean([b / (t * 1e6) for b, t in zip(b16, per16[:, 2])])),
-        }
+        detail["concurrency_bf16"] = conc_bf16
 
-    # ---- latent speculative-verify workload (tcgen05 path)
-    latent = None
-    if not args.no_latent:
-        latent = latent_bench(args.steps, args.warmup, device, peaks)
-
-    # ---- skewed stress workload: verify overhead (the step it is defined on)
-    # and the full step with its stale tags
-    skewed = None
-    if overhead is not None:
-        overhead["skewed"], skewed = skewed_lines(device, args.overhead_replays, args.steps,
-                                                  args.warmup, peak)
-
-    # ---- re-quantising scale mode (decode-step append cost, accuracy effect)
-    requant = None
-    if not args.no_requant:
-        requant = requant_lines(device, args.steps, args.warmup, w)
-        requant["append_us_frozen"] = float(per[:, 0].mean() * 1e3)
-
-    # ---- bulk append (prefill handoff): the whole GQA batch and latent workloads
-    bulk = None
-    if not args.no_bulk:
-        bulk = [bulk_append_line(w, 0, device, peak), bulk_append_line(w, 1, device, peak),
-                bulk_append_line(wl.latent_verify(), 0, device, peak)]
-
-    # ---- a wider query group (12 rows per kv head)
-    wide = None
-    if not args.no_wide:
-        wide = wide_group_line(device, args.steps, args.warmup, peak)
+    gqa = skewed = latent = requant = bulk = wide = churn = None
+    if run_extra:
+        # ---- GQA batch (32 requests, 4k..32k), e4m3 and bf16
+        gsteps = 1 + 2 * (K + W)
+        gw = wl.gqa_batch(seed=shard_seed(20262, rank), steps=gsteps + over_steps + 2)
+        if args.batch != gw.B:
+            gw = wl.subset(gw, args.batch)
+        garm = Arm(gw, 0, device, gsteps)
+        rg = int(np.argmax(gw.lens))
+        parity_samples.append({"name": "gqa_batch_e4m3", "w": gw, "dtype": 0,
+                               "pairs": [(rg, 5)], "outs": garm.first_step_output([rg])})
+        g_ms, g_per, g_lens, _ = garm.run(K, W)
+        g_graph_ms = garm.run_graphs(K, W)
+        if not args.no_overhead:
+            overhead["gqa_batch"] = graph_overhead(garm, R)
+        del garm
+        torch.cuda.empty_cache()
+        g_attn = g_per[:, 2] + g_per[:, 3]
+        g_gbs = float(np.mean([algorithmic_bytes(gw, L, 0) / (t * 1e6)
+                               for L, t in zip(g_lens, g_attn)]))
+        gqa = {"e4m3": {"tokens_per_s": K * gw.B / (g_graph_ms / 1e3),
+                        "eager_tokens_per_s": K * gw.B / (g_ms / 1e3),
+                        "attn_us": float(g_attn.mean() * 1e3), "attn_gbs": g_gbs,
+                        "pct_of_measured": 100.0 * g_gbs / peak,
+                        "kernel_us": {k: float(g_per[:, i].mean() * 1e3) for i, k in
+                                      enumerate(("append", "verify", "split", "combine"))}}}
         if not args.no_bf16:
-            wide["bf16"] = wide_group_line(device, args.steps, args.warmup, peak, dtype=1)
+            garm16 = Arm(gw, 1, device, 1 + K + W)
+            parity_samples.append({"name": "gqa_batch_bf16", "w": gw, "dtype": 1,
+                                   "pairs": [(rg, 2)], "outs": garm16.first_step_output([rg])})
+            gqa["bf16"] = step_line(gw, garm16, 1, K, W)
+            gqa["bf16"]["pct_of_measured"] = 100.0 * gqa["bf16"]["attn_gbs"] / peak
+            del garm16
+            torch.cuda.empty_cache()
+        detail["gqa_batch"] = gqa
 
-    # ---- continuous batching: requests leave and join between decode steps
-    churn = None
-    if not args.no_churn:
-        churn = churn_line(device, args.steps, args.warmup)
+        # ---- skewed stress workload: verify overhead (the step it is defined
+        # on) and the full step with its stale tags
+        if not args.no_overhead:
+            overhead["skewed"], skewed = skewed_lines(device, R, K, W, peak, parity_samples)
+            detail["skewed_step"] = skewed
 
-    # ---- concurrency sweep (1..64 requests at 128k), e4m3 and bf16
-    conc = None
-    if not args.no_sweep:
-        conc = concurrency_sweep(device, args.steps, args.warmup, peak, args.overhead_replays)
+        if not args.no_latent:
+            latent = latent_bench(K, W, device, peaks)
+            detail["latent_verify"] = latent
+        if not args.no_requant:
+            requant = requant_lines(device, K, W, gw)
+            detail["requantize"] = requant
+        if not args.no_bulk:
+            bulk = [bulk_append_line(gw, 0, device, peak), bulk_append_line(gw, 1, device, peak),
+                    bulk_append_line(wl.latent_verify(), 0, device, peak)]
+            detail["bulk_append"] = bulk
+        if not args.no_wide:
+            wide = {"e4m3": wide_group_line(device, K, W, peak, parity=parity_samples)}
+            if not args.no_bf16:
+                wide["bf16"] = wide_group_line(device, K, W, peak, dtype=1, parity=parity_samples)
+            detail["wide_group"] = wide
+        if not args.no_churn:
+            churn = churn_line(device, K, W)
+            detail["churn"] = churn
 
-    # ---- CPU oracle baseline (rank 0, bounded sample)
-    cpu = None
+    # ---- CPU oracle baseline and parity of the sampled outputs (rank 0)
+    cpu, parity = None, {}
     if rank == 0 and args.cpu_budget > 0:
-        n, sec, names = oracle_sample(w, args.cpu_budget, device)
-        cpu = {"value": n * w.q_tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} request(s) of gqa_batch, one decode step each "
-                         f"({', '.join(names)}); {sec:.1f} s on one host core"}
+        n_tok, sec, names, parity = cpu_baseline_leg(parity_samples, device, args.cpu_budget)
+        cpu = {"value": n_tok / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first decode step of {len(names)} (request, kv head) pair(s) of the "
+                         f"headline workload ({', '.join(names)}), each 1/8 of a request's "
+                         f"token; {sec:.1f} s on one host core",
+               "parity": parity}
+        detail["parity"] = parity
 
     if rank != 0:
         return
-    step_ms = per.sum(axis=1).mean()
+    if args.detail:
+        with open(args.detail, "w") as fh:
+            json.dump(detail, fh)
+    pieces = B * (w.num_kv_heads // 8) + 152
+    traffic = split_traffic(float(np.mean(split_bytes)), pieces)
+    points = {"concurrency_e4m3": {str(l["requests"]): _pt(l, peak) for l in conc_e4m3}}
+    if conc_bf16:
+        points["concurrency_bf16"] = {str(l["requests"]): _pt(l, peak) for l in conc_bf16}
+    if skewed:
+        points["skewed_e4m3"] = _pt(skewed, peak)
+    if gqa:
+        points["gqa_batch_e4m3"] = {"tok_s": round(gqa["e4m3"]["tokens_per_s"], 1),
+                                    "gbs": round(gqa["e4m3"]["attn_gbs"], 1),
+                                    "frac": round(gqa["e4m3"]["attn_gbs"] / peak, 4)}
+        if "bf16" in gqa:
+            points["gqa_batch_bf16"] = _pt(gqa["bf16"], peak)
+    if wide:
+        points["wide96_e4m3"] = _pt(wide["e4m3"], peak)
+        if "bf16" in wide:
+            points["wide96_bf16"] = _pt(wide["bf16"], peak)
+    if latent:
+        points["latent_tc"] = {"tok_s": round(latent["value"], 1),
+                               "tflops": round(latent["attn_tflops"], 1),
+                               "frac": round(latent["tensor_frac"], 4)}
+    if overhead:
+        points["verify_overhead_pct"] = {k: round(v["verify_overhead_pct"], 2)
+                                         for k, v in overhead.items()}
+    if bulk:
+        points["bulk_append_frac"] = {f"{b_['workload']}_{b_['cache']}":
+                                      round(b_["pct_of_measured"] / 100.0, 4) for b_ in bulk}
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 KV, f16 MMA, f32 accumulate",
         "data": "synthetic",
-        "config": {
-            "workload": "gqa_batch: 32 requests, contexts U[4096,32768], 64 q / 8 kv heads, "
-                        "head dim 128, page 16, e4m3 KV; step = append 1 token/request + tag "
-                        "check + split-K attention + combine",
-            "batch": w.B, "mean_context": float(w.lens.mean()), "kv_bytes_per_step":
-                int(np.mean(attn_bytes)), "l2": "inputs larger than L2 (>1.2 GB of KV per step)",
-            "parallelism": f"dp{ws} replicas" if ws > 1 else "1 GPU"},
-        "step_mode": "each step replayed as a CUDA graph (one per step's inputs); eager_value: "
-                     "the same steps launched one call at a time",
-        "eager_value": eager_value, "eager_ms_per_step": eager_ms / args.steps,
-        "attn_gbs": attn_gbs,
-        "attn_pct_of_8000": 100.0 * attn_gbs / NOMINAL_HBM_GBS,
-        "kernel_us": {"append": float(per[:, 0].mean() * 1e3),
-                      "verify": float(per[:, 1].mean() * 1e3),
-                      "split": float(per[:, 2].mean() * 1e3),
-                      "combine": float(per[:, 3].mean() * 1e3)},
-        "verify_share_pct": float(100.0 * per[:, 1].mean() / step_ms),
-        "verify_overhead": overhead,
-        "skewed_step": skewed,
-        "bulk_append": bulk,
-        "requantize": requant,
-        "churn": churn,
-        "wide_group": wide,
-        "concurrency": conc,
+        "config": {"workload": HEADLINE_NAME if B == 64 else f"concurrency {B} x 131072, e4m3",
+                   "requests": B, "context": 131072, "q_heads": 64, "kv_heads": 8,
+                   "head_dim": 128, "page": 16,
+                   "step": "append 1 token/request, tag check, split-K attention, combine; "
+                           "each step a CUDA graph replay",
+                   "kv_bytes_per_step": int(np.mean(attn_bytes)),
+                   "l2": "inputs larger than L2 (KV read per step >> 129 MB)",
+                   "parallelism": f"dp{ws} replicas" if ws > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "traffic_note": "bytes per launch, ncu dram read+write of a small-case "
-                                     "capture scaled to this launch (" + SPLIT_NCU["profile"] + ")",
-                     "algorithmic_bytes": float(np.mean(split_bytes)),
                      "kernel": "paged_decode_attn_split (plan + gqa_split_kernel<e4m3>)",
-                     "peak_source": peak_src},
-        "bf16_kv": bf16,
-        "latent_verify": latent,
+                     "achieved_def": "K/V rows + scales + page-table entries + Q over the "
+                                     "plan+split CUDA-event time",
+                     "algorithmic_bytes": float(np.mean(split_bytes)),
+                     "peak_source": peak_src,
+                     "attn": {"achieved": attn_gbs, "frac": attn_gbs / peak,
+                              "frac_8000": attn_gbs / NOMINAL_HBM_GBS,
+                              "def": "K/V + scales + page table + Q + O over split+combine"},
+                     "points": points},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h),
-                "mode": "per step: one H2D copy of its rows and queries from pinned memory, "
-                        "one kv_decode_step call, one D2H copy of output and abort mask; each "
-                        "step captured as a CUDA graph and replayed in order",
-                "eager_value": e2e_eager_value},
+        "e2e": {"value": tokens / (reduce_max(e2e_ms) / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "mode": "per step: H2D of its rows and queries, kv_decode_step, D2H of output "
+                        "and abort mask; CUDA graph per step",
+                "eager_value": tokens / (reduce_max(e2e_eager_ms) / 1e3)},
         "gpu_launches": launches,
         "clocks": clocks,
+        "eager_value": tokens / (eager_ms / 1e3),
     }
     print(json.dumps(line))
 

@@ -314,9 +314,12 @@ kv_status paged_decode_attn_combine(kv_pool* pool, void* stream, int32_t B,
  *     exits).  A batch whose workspace (paged_decode_workspace_size) exceeds
  *     32 MiB is rejected with KV_ERR_UNSUPPORTED before anything is enqueued.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture on that device.
+ *   - A call made outside stream capture looks up the array's device
+ *     address (cudaGetSymbolAddress) with the current device, so the address
+ *     stays right after a device reset.  A call made while its stream is
+ *     being captured reuses the address that the last uncaptured call on the
+ *     same device found; make the first call on a device before any stream
+ *     capture on it (the first lookup may load the library's device code).
  *   - All calls share the one array and nothing in it needs clearing between
  *     calls (each call rewrites what it reads), but calls that overlap on the
  *     GPU (concurrent streams) race on it: serialise them.

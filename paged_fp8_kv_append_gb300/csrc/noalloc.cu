@@ -10,8 +10,13 @@
 // one file-scope __device__ array.  Nothing here calls cudaMalloc, cudaFree or
 // any allocating routine.
 //
-// The array's host-side name is only a stand-in for the symbol; the device
-// address is obtained once per device with cudaGetSymbolAddress and cached.
+// The array's host-side name is only a stand-in for the symbol; its device
+// address comes from cudaGetSymbolAddress with the device current.  A call
+// made outside stream capture looks it up again (cheap once the module is
+// loaded), so a device reset, after which the module may load at another
+// address, leaves no stale pointer behind; a call made while its stream is
+// being captured uses the address found by the last uncaptured call on that
+// device (or looks it up, if there was none).
 #include <mutex>
 
 #include "internal.h"
@@ -29,14 +34,15 @@ constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of g_decode_scratch on the current device (set up on first
-// use per device, with that device current).
-kv_status scratch_address(void** out) {
+// Device address of g_decode_scratch on the current device.
+kv_status scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KV_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return KV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone || g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
       return KV_ERR_CUDA;
@@ -63,7 +69,7 @@ extern "C" kv_status paged_decode_attn_noalloc(kv_pool* pool, void* stream, int3
   const size_t need = paged_decode_workspace_size(pool, B, num_q_heads, q_tokens);
   if (need > kStaticScratchBytes) return KV_ERR_UNSUPPORTED;  // batch too large for the array
   void* ws = nullptr;
-  const kv_status st = scratch_address(&ws);
+  const kv_status st = scratch_address(static_cast<cudaStream_t>(stream), &ws);
   if (st != KV_OK) return st;
   // Nothing in the scratch needs clearing: each call's plan kernel rewrites
   // every word of it that the later kernels read.

@@ -52,18 +52,20 @@ def test_gqa_batch_full_size_every_request_and_head():
     assert fs.dev.error() == 0
 
 
-def test_wide_group_full_size_sampled():
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_wide_group_full_size_sampled(dtype):
     """The GQA batch with 96 query heads on its 8 kv heads (12 query rows per
-    kv head: the 16-row consumer warps), e4m3, at full size after a decode
-    step: bookkeeping of every request; cache bytes, scales and attention of
-    a seeded 4 requests (the longest among them) on three kv heads."""
+    kv head: the 16-row consumer warps), e4m3 and bf16, at full size after a
+    decode step: bookkeeping of every request; cache bytes, scales and
+    attention of a seeded 4 requests (the longest among them) on three kv
+    heads."""
     import dataclasses
 
     w = dataclasses.replace(wl.gqa_batch(steps=2), num_q_heads=96)
     rng = np.random.default_rng(3)
     sample = sorted(set(rng.choice(w.B, 3, replace=False).tolist()) | {int(np.argmax(w.lens))})
     heads = [0, 4, 7]
-    fs = FullSize(w, 0, sample=sample, heads=heads)
+    fs = FullSize(w, dtype, sample=sample, heads=heads)
     fs.fill()
     st, stop = fs.step_append(0)
     assert (st, stop) == (0, w.B)
@@ -76,10 +78,12 @@ def test_wide_group_full_size_sampled():
     assert fs.dev.error() == 0
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
 @pytest.mark.parametrize("B", [1, 8, 64])
-def test_concurrency_128k_contexts(B):
-    """Requests of 131,072 tokens: at 1 and 8 requests every request and kv
-    head is checked; at 64 a seeded 8 requests on three kv heads."""
+def test_concurrency_128k_contexts(B, dtype):
+    """Requests of 131,072 tokens, e4m3 and bf16 caches: at 1 and 8 requests
+    every request and kv head is checked; at 64 a seeded 8 requests on three
+    kv heads."""
     w = wl.concurrency(B)
     w.steps = 2
     if B <= 8:
@@ -87,7 +91,7 @@ def test_concurrency_128k_contexts(B):
     else:
         sample = sorted(np.random.default_rng(B).choice(B, 8, replace=False).tolist())
         heads = [0, 3, 7]
-    fs = FullSize(w, 0, sample=sample, heads=heads)
+    fs = FullSize(w, dtype, sample=sample, heads=heads)
     fs.fill(group=2)
     fs.step_append(0)
     torch.cuda.synchronize()
