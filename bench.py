@@ -704,50 +704,58 @@ def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
     B = w.B if B is None else B
     k0, v0, q0 = arm.k_steps[0], arm.v_steps[0], arm.q_steps[0]
 
-    def body(check: bool):
+    def body(check: str):
         arm.pool.append(B, k0, v0, arm.ones, 1, arm.pt, arm.et, arm.sl)
+        if check == "fused":  # the tag check inside the page reads
+            kv.paged_decode_attn_checked(h, B, w.num_q_heads, w.q_tokens, q0, arm.pt, arm.et,
+                                         arm.sl, w.sm_scale, arm.out, arm.mask, arm.ws)
+            return
         mask = None
-        if check:
+        if check == "separate":
             arm.pool.verify(B, arm.pt, arm.et, arm.sl, arm.mask)
             mask = arm.mask
         kv.paged_decode_attn_split(h, B, w.num_q_heads, w.q_tokens, q0, arm.pt, arm.sl, mask,
                                    w.sm_scale, arm.ws)
         kv.paged_decode_attn_combine(h, B, w.num_q_heads, w.q_tokens, mask, arm.out, arm.ws)
 
+    modes = ("separate", "none", "fused")
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        body(True)
-        body(False)
+        for m in modes:
+            body(m)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    g_with, g_without = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_with):
-        body(True)
-    with torch.cuda.graph(g_without):
-        body(False)
+    graphs = {m: torch.cuda.CUDAGraph() for m in modes}
+    for m in modes:
+        with torch.cuda.graph(graphs[m]):
+            body(m)
     for _ in range(3):
-        g_with.replay()
-        g_without.replay()
+        for m in modes:
+            graphs[m].replay()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(replays)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(replays)]
     for i in range(replays):
         ev[i][0].record()
-        g_with.replay()
-        ev[i][1].record()
-        g_without.replay()
-        ev[i][2].record()
+        for j, m in enumerate(modes):
+            graphs[m].replay()
+            ev[i][j + 1].record()
     torch.cuda.synchronize()
     if arm.pool.error() != 0:
         raise RuntimeError(f"verify overhead: device error {kv.kv_status_string(arm.pool.error())}")
-    arm.lens[:B] += 2 + 2 * 3 + 2 * replays  # every run of the body appended one token
-    t_with = [e[0].elapsed_time(e[1]) for e in ev]
-    t_without = [e[1].elapsed_time(e[2]) for e in ev]
-    mw, mo = statistics.median(t_with), statistics.median(t_without)
-    del g_with, g_without
-    return {"workload": w.name, "requests": B, "replays": replays, "ms_with_verify": mw,
-            "ms_without_verify": mo, "verify_overhead_pct": 100.0 * (mw / mo - 1.0),
-            "mean_overhead_pct": 100.0 * (sum(t_with) / sum(t_without) - 1.0)}
+    if int(arm.mask[:B].sum().item()) != 0:
+        raise RuntimeError("verify overhead: a request was aborted with every tag valid")
+    # every run of the body appended one token
+    arm.lens[:B] += len(modes) * (1 + 3 + replays)
+    t = {m: [e[j].elapsed_time(e[j + 1]) for e in ev] for j, m in enumerate(modes)}
+    med = {m: statistics.median(t[m]) for m in modes}
+    del graphs
+    return {"workload": w.name, "requests": B, "replays": replays,
+            "ms_with_verify": med["separate"], "ms_without_verify": med["none"],
+            "ms_fused_check": med["fused"],
+            "verify_overhead_pct": 100.0 * (med["separate"] / med["none"] - 1.0),
+            "fused_overhead_pct": 100.0 * (med["fused"] / med["none"] - 1.0),
+            "mean_overhead_pct": 100.0 * (sum(t["separate"]) / sum(t["none"]) - 1.0)}
 
 
 def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B=None,
@@ -828,7 +836,7 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float, par
     contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
     428k pages checked per step): the verify overhead with every tag valid,
     then the full step with its seeded stale tags (those requests abort)."""
-    w = wl.skewed(steps=2 * (replays + 8) + steps + warmup + 8)
+    w = wl.skewed(steps=3 * (replays + 8) + steps + warmup + 8)
     stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
     arm = Arm(w, 0, device, steps + warmup + 1)
@@ -1230,7 +1238,7 @@ def main():
     B = args.requests
     sweep_pts = [b for b in (1, 8, 16, 32) if b < B]
     head_steps = 1 + 4 * (K + W) + len(sweep_pts) * (K + W)
-    over_steps = 0 if args.no_overhead else 2 * (2 * (3 + R) + 2)
+    over_steps = 0 if args.no_overhead else 2 * (3 * (4 + R) + 2)
     w = wl.concurrency(B, seed=shard_seed(20264, rank))
     w.steps = head_steps + over_steps + 4
     w.num_pages = int(B * (-(-(131072 + w.steps) // 16))) + 64
@@ -1387,6 +1395,8 @@ def main():
     if overhead:
         points["verify_overhead_pct"] = {k: round(v["verify_overhead_pct"], 2)
                                          for k, v in overhead.items()}
+        points["fused_check_overhead_pct"] = {k: round(v["fused_overhead_pct"], 2)
+                                              for k, v in overhead.items()}
     if bulk:
         points["bulk_append_frac"] = {f"{b_['workload']}_{b_['cache']}":
                                       round(b_["pct_of_measured"] / 100.0, 4) for b_ in bulk}

@@ -284,11 +284,37 @@ kv_status paged_decode_attn(kv_pool* pool, void* stream, int32_t B,
                             const uint8_t* abort_mask, float sm_scale,
                             void* out, void* workspace, size_t workspace_bytes);
 
+/*
+ * paged_decode_attn with the page-tag check fused into the page reads (SFS
+ * "Protecting a shared KV cache": each request's expected (page, tag) list
+ * is compared with the physical tags before decode reads the cache, and a
+ * request that fails is aborted and returns no data).  Instead of a separate
+ * kv_verify_tags pass, the thread that fetches a page compares tags[p] with
+ * exp_tags[r][j] (uint32 [B][max_pages_per_req], device) first and fetches
+ * only a page that matches; the combine step then writes abort_mask
+ * (uint8 [B], device, out): 1 for a request that met a stale tag or a page id
+ * outside [0, num_pages) or whose length is invalid (as kv_verify_tags
+ * decides it), else 0.  An aborted request's output rows are left untouched.
+ * Unlike the separate pass, the pages of an aborted request whose tags do
+ * match may still be read (their data never reaches an output); a page whose
+ * tag does not match is never read.  Other arguments, results and errors are
+ * those of paged_decode_attn (a page id out of range also sets
+ * KV_ERR_BAD_PAGE_ID); the same workspace size applies.
+ */
+kv_status paged_decode_attn_checked(kv_pool* pool, void* stream, int32_t B,
+                                    int32_t num_q_heads, int32_t q_tokens,
+                                    const void* q, const int32_t* page_table,
+                                    const uint32_t* exp_tags, int32_t max_pages_per_req,
+                                    const int32_t* seq_lens, float sm_scale, void* out,
+                                    uint8_t* abort_mask, void* workspace,
+                                    size_t workspace_bytes);
+
 /* The two phases of paged_decode_attn, for callers that schedule or time
- * them separately.  _split plans the batch and writes the partials (two
- * launches); _combine merges them into `out` (one launch).  Calling _split
- * then _combine with the same arguments and workspace is exactly
- * paged_decode_attn. */
+ * them separately.  _split plans the batch (inside the split kernel for
+ * batches of up to 1023 requests on GQA pools, else in a plan launch) and
+ * writes the partials; _combine merges them into `out` (one launch).
+ * Calling _split then _combine with the same arguments and workspace is
+ * exactly paged_decode_attn. */
 kv_status paged_decode_attn_split(kv_pool* pool, void* stream, int32_t B,
                                   int32_t num_q_heads, int32_t q_tokens,
                                   const void* q, const int32_t* page_table,

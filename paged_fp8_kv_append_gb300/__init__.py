@@ -72,6 +72,9 @@ _lib.paged_decode_attn_split.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _
 _lib.paged_decode_attn_split.restype = _i32
 _lib.paged_decode_attn_combine.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz]
 _lib.paged_decode_attn_combine.restype = _i32
+_lib.paged_decode_attn_checked.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp,
+                                           _f32, _vp, _vp, _vp, _sz]
+_lib.paged_decode_attn_checked.restype = _i32
 _lib.paged_decode_attn_noalloc.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp,
                                            _vp, _f32, _vp]
 _lib.paged_decode_attn_noalloc.restype = _i32
@@ -198,6 +201,20 @@ def paged_decode_attn(handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,
         _ptr(out, torch.bfloat16, "out"), _ptr(workspace, torch.uint8, "workspace"),
         int(workspace.numel()))
     _check(st, "paged_decode_attn")
+
+
+def paged_decode_attn_checked(handle, B, num_q_heads, q_tokens, q, page_table, exp_tags,
+                              seq_lens, sm_scale, out, abort_mask, workspace, stream=None):
+    """paged_decode_attn with the page-tag check fused into the page reads;
+    writes abort_mask (see kvfp8.h)."""
+    st = _lib.paged_decode_attn_checked(
+        handle, _stream(stream), int(B), int(num_q_heads), int(q_tokens),
+        _ptr(q, torch.bfloat16, "q"), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(exp_tags, _U32, "exp_tags"), int(page_table.shape[-1]),
+        _ptr(seq_lens, torch.int32, "seq_lens"), float(sm_scale),
+        _ptr(out, torch.bfloat16, "out"), _ptr(abort_mask, torch.uint8, "abort_mask"),
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()))
+    _check(st, "paged_decode_attn_checked")
 
 
 def paged_decode_attn_noalloc(handle, B, num_q_heads, q_tokens, q, page_table, seq_lens,

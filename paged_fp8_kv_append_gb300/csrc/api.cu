@@ -72,6 +72,9 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
     cfg->R8 = 8 * rb;
     cfg->HG = d.num_kv_heads / hs;
     cfg->unit_tokens = d.page_size;
+    // the split kernel's CTAs plan a batch that fits their shared-memory
+    // prefix cache themselves: no separate plan launch
+    cfg->self_plan = (gqa_kind_self_plans(cfg->kind) && B <= gqa_self_plan_max_batch()) ? 1 : 0;
     return KV_OK;
   }
   // latent layout: query rows (T tokens x Hq heads) in blocks of 64; the
@@ -85,6 +88,7 @@ kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig*
   const int per_sm = sms > 0 ? latent_split_ctas_per_sm() : 0;
   if (sms <= 0 || per_sm <= 0) return KV_ERR_CUDA;
   cfg->kind = 2;
+  cfg->self_plan = 0;
   cfg->grid = sms * per_sm;
   cfg->R8 = rb;
   cfg->Hs = 1;
@@ -105,8 +109,6 @@ size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfi
   off = align256(off + sizeof(int32_t) * (size_t)(B + 1));
   const size_t o_skip = off;
   off = align256(off + (size_t)B);
-  const size_t o_bad = off;
-  off = align256(off + (size_t)B);
   const size_t o_ml = off;
   off = align256(off + sizeof(float) * 2 * (size_t)slots * cfg.Hs * cfg.R8);
   const size_t o_o = off;
@@ -115,7 +117,6 @@ size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfi
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->pfx = reinterpret_cast<int32_t*>(b + o_pfx);
     ws->rq_skip = b + o_skip;
-    ws->rq_bad = b + o_bad;
     ws->ml_part = reinterpret_cast<float*>(b + o_ml);
     ws->o_part = reinterpret_cast<float*>(b + o_o);
     ws->bytes = off;
@@ -167,6 +168,9 @@ kv_status decode_prepare(kv_pool* pool, int32_t B, int32_t Hq, int32_t T, const 
   x.HG = cfg.HG;
   x.stages = cfg.stages;
   x.unit_tokens = cfg.unit_tokens;
+  x.self_plan = cfg.self_plan;
+  x.exp_tags = nullptr;
+  x.abort_out = nullptr;
   const size_t need = decode_ws_layout(d, B, Hkv, cfg, workspace, &x.ws);
   if (B > 0 && workspace_bytes < need) return KV_ERR_INVALID_ARG;
   *kind = cfg.kind;
@@ -327,7 +331,7 @@ kv_status paged_decode_attn_split(kv_pool* pool, void* stream, int32_t B, int32_
   if (st != KV_OK || B == 0) return st;
   int n = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_plan(a, s, &n);
+  cudaError_t e = a.self_plan ? cudaSuccess : launch_decode_plan(a, s, &n);
   if (e == cudaSuccess) e = launch_decode_split(a, kind, s, &n);
   pool->last_launches = n;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
@@ -366,6 +370,32 @@ kv_status paged_decode_attn(kv_pool* pool, void* stream, int32_t B, int32_t num_
                                  workspace, workspace_bytes);
   pool->last_launches += n;
   return st;
+}
+
+kv_status paged_decode_attn_checked(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
+                                    int32_t q_tokens, const void* q, const int32_t* page_table,
+                                    const uint32_t* exp_tags, int32_t max_pages_per_req,
+                                    const int32_t* seq_lens, float sm_scale, void* out,
+                                    uint8_t* abort_mask, void* workspace,
+                                    size_t workspace_bytes) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  if (B > 0 && (!out || !exp_tags || !abort_mask)) return KV_ERR_INVALID_ARG;
+  DecodeArgs a;
+  int kind = 0;
+  const kv_status st =
+      decode_prepare(pool, B, num_q_heads, q_tokens, q, page_table, max_pages_per_req, seq_lens,
+                     nullptr, sm_scale, out, workspace, workspace_bytes, true, true, &a, &kind);
+  if (st != KV_OK || B == 0) return st;
+  a.exp_tags = exp_tags;
+  a.abort_out = abort_mask;
+  int n = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = a.self_plan ? cudaSuccess : launch_decode_plan(a, s, &n);
+  if (e == cudaSuccess) e = launch_decode_split(a, kind, s, &n);
+  if (e == cudaSuccess) e = launch_decode_combine(a, s, &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 size_t kv_decode_step_workspace_size(const kv_pool* pool, int32_t B, int32_t num_q_heads,
@@ -439,6 +469,7 @@ kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_h
   aa.seq_lens = seq_lens;
   aa.step_mask = abort_mask;
   aa.fuse_plan = true;  // the append's plan kernel also writes the attention plan
+  da.self_plan = 0;     // ... so the split kernel reads it
   aa.plan = da;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -219,8 +219,10 @@ struct GqaCfg {
   static constexpr int OFF_META = OFF_PBUF + CONSUMERS * PBUF;               // [S] StageMeta
   static constexpr int OFF_BAR = OFF_META + kMaxStages * 80;                  // full, empty
   static constexpr int OFF_PFX = OFF_BAR + 2 * kMaxStages * 8;
-  static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;
-  static constexpr int SMEM = OFF_FLAG + 16;
+  static constexpr int OFF_FLAG = OFF_PFX + PFX_CACHE * 4;  // abort flag, piece-bad flag
+  static constexpr int OFF_WSUM = OFF_FLAG + 16;              // [32] plan scan warp sums
+  static constexpr int SMEM = OFF_WSUM + 32 * 4;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 // Most units a producer warp issues per warp instruction (one per lane; at most
@@ -228,7 +230,8 @@ struct GqaCfg {
 constexpr int kIssueGroup = 8;
 
 struct StageMeta {
-  int n_valid;    // tokens of this page below the request length (0: skip page)
+  int n_valid;    // tokens of this page below the request length; -1: a page
+                  // that must not be read (id out of range or stale tag)
   int pos0;       // position of the page's first token
   float ks[8];    // K scales of the unit's heads (1 for bf16)
   float vs[8];    // V scales
@@ -236,6 +239,58 @@ struct StageMeta {
   int pad;
 };
 static_assert(sizeof(StageMeta) == 80, "StageMeta layout");
+
+// End of a piece: merges the online-softmax states of the WPH warps that
+// share each of the Hv virtual heads (8 rows each) into the piece's partial.
+// merge_ml[(w * 8 + nw) * 2 + {0, 1}] holds warp w's running max and sum of
+// row nw, merge_o[(w * 8 + nw) * 128 + dd] its unnormalised output.  Pass 1,
+// one thread per row: the row's max M over the warps, each warp's weight
+// 2^(m_w - M) (written over m_w) and the weighted sum, stored with M (a
+// piece that met a page it must not read stores the sum -1 instead).  Pass
+// 2, every consumer thread: the weighted outputs, four dims at a time.
+// row_of(v, nw) is the partial row of virtual head v's row nw.  Starts and
+// ends with the consumer warps synchronised.
+template <class C, class RowOf>
+__device__ __forceinline__ void merge_piece(float* merge_o, float* merge_ml, int Hv, int WPH,
+                                            const DecodeArgs& a, RowOf row_of,
+                                            volatile int* piece_bad, bool reset_bad) {
+  constexpr int R8 = C::R8, D = C::D, NT = C::CONSUMERS * 32;
+  static_assert(R8 == 8 && D == 128, "index shifts");
+  const int tid = threadIdx.x;
+  named_bar_sync(1, NT);  // every warp's state is in the merge buffers
+  if (tid < Hv * R8) {
+    const int v = tid >> 3, nw = tid & 7;
+    float M = -INFINITY;
+    for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * R8 + nw) * 2]);
+    float lsum = 0.0f;
+    for (int q = 0; q < WPH; ++q) {
+      float* ml = merge_ml + ((q * Hv + v) * R8 + nw) * 2;
+      const float w = (ml[0] == -INFINITY) ? 0.0f : exp2f(ml[0] - M);
+      lsum += ml[1] * w;
+      ml[0] = w;
+    }
+    const long long row = row_of(v, nw);
+    a.ws.ml_part[row * 2 + 0] = M;
+    a.ws.ml_part[row * 2 + 1] = *piece_bad ? -1.0f : lsum;
+  }
+  named_bar_sync(1, NT);
+  if (reset_bad && tid == 0) *piece_bad = 0;
+  for (int e = tid; e < Hv * R8 * (D / 4); e += NT) {
+    const int d4 = e & 31, rr = e >> 5, v = rr >> 3, nw = rr & 7;
+    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int q = 0; q < WPH; ++q) {
+      const int w = (q * Hv + v) * R8 + nw;
+      const float wt = merge_ml[w * 2];
+      const float4 x = *reinterpret_cast<const float4*>(merge_o + w * D + 4 * d4);
+      o.x = fmaf(wt, x.x, o.x);
+      o.y = fmaf(wt, x.y, o.y);
+      o.z = fmaf(wt, x.z, o.z);
+      o.w = fmaf(wt, x.w, o.w);
+    }
+    *reinterpret_cast<float4*>(a.ws.o_part + row_of(v, nw) * D + 4 * d4) = o;
+  }
+  named_bar_sync(1, NT);
+}
 
 // WIDE: a consumer warp takes 16 query rows of its kv head instead of 8 (see
 // the wide consumer below); the producer and the ring are the same.
@@ -254,6 +309,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
   uint64_t* empty = full + kMaxStages;
   int32_t* pfx_s = reinterpret_cast<int32_t*>(smem + C::OFF_PFX);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  volatile int* piece_bad = abort_flag + 1;
+  int* wsum_s = reinterpret_cast<int*>(smem + C::OFF_WSUM);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B, Hkv = a.d.num_kv_heads;
@@ -270,32 +327,45 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
   // blocks (the host pads so that the warps divide evenly)
   const bool rows_ok = WIDE ? (RB % 2 == 0 && RB <= 8 && a.R >= 1 && a.R <= C::R8 * RB)
                             : (RB <= 4 && (a.R + C::R8 - 1) / C::R8 == RB);
+  // (not in the 16-row e4m3 kernel: at its 128-register cap the plan code
+  // made it spill)
+  constexpr bool kCanSelfPlan = !(FP8 && WIDE);
   if (Hs < 1 || RB < 1 || !rows_ok || RB * C::R8 != a.R8 ||
       C::CONSUMERS % Hv != 0 || S < 2 || S > kMaxStages || S % (C::CONSUMERS / Hv) != 0 ||
-      stage_bytes * S > C::RING) {
-    if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad ring
+      stage_bytes * S > C::RING ||
+      (a.self_plan && (B + 1 > C::PFX_CACHE || !kCanSelfPlan))) {
+    if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad configuration
     return;
   }
+  // the batch plan: built here (self_plan; CTA 0 stores it for the combine)
+  // or read from the plan kernel's output, cached in shared memory
   const int32_t* pfx_g = a.ws.pfx;
-  const long long total = (long long)pfx_g[B] * HG;
+  const bool cached = B + 1 <= C::PFX_CACHE;
+  if (kCanSelfPlan && a.self_plan) {
+    const bool refused = decode_plan_shared(a, pfx_s, wsum_s);
+    if (blockIdx.x == 0) decode_plan_store(a, pfx_s, refused);
+  } else if (cached) {
+    for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
+    __syncthreads();
+  }
+  const int32_t* pfx = cached ? pfx_s : pfx_g;
+  const long long total = (long long)pfx[B] * HG;
   const long long per = (total + gridDim.x - 1) / gridDim.x;
   const long long x_begin = (long long)blockIdx.x * per;
   const long long x_end = min(total, x_begin + per);
   if (x_begin >= x_end) return;
 
-  const bool cached = B + 1 <= C::PFX_CACHE;
-  if (cached)
-    for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      // two arrivals: the copies' expected bytes, then the stage metadata
+      mbar_init(&full[s], 2);
       mbar_init(&empty[s], Hv);
     }
     *abort_flag = 0;
+    *piece_bad = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  const int32_t* pfx = cached ? pfx_s : pfx_g;
   const Cursor start = cursor_at(pfx, B, HG, x_begin);
   const int P = C::P, D = C::D;
 
@@ -328,26 +398,34 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       }
       return u;
     };
+    // a page may be read only if its id is in range and, with the fused
+    // check, its tag is the expected one; the tag and the scales are loaded
+    // together (both depend only on the page id)
     auto scales = [&](const Unit& u, long long xu, float (&ks)[8], float (&vs)[8], bool& ok) {
       ok = false;
 #pragma unroll
       for (int hh = 0; hh < 8; ++hh) ks[hh] = vs[hh] = 1.0f;
       if (xu < x_end) {
-        ok = u.p >= 0 && u.p < a.d.num_pages;
-        if (ok && FP8) {
-          const long long base = (long long)u.p * Hkv + (long long)u.hg * Hs;
+        const bool in_range = u.p >= 0 && u.p < a.d.num_pages;
+        uint32_t tag = 0, et = 0;
+        if (in_range) {
+          if (a.exp_tags != nullptr) {
+            tag = a.d.tags[u.p];
+            et = a.exp_tags[(long long)u.r * maxp + u.j];
+          }
+          if (FP8) {
+            const long long base = (long long)u.p * Hkv + (long long)u.hg * Hs;
 #pragma unroll
-          for (int hh = 0; hh < 8; ++hh) {
-            if (hh < Hs) {
-              ks[hh] = a.d.k_scale[base + hh];
-              vs[hh] = a.d.v_scale[base + hh];
+            for (int hh = 0; hh < 8; ++hh) {
+              if (hh < Hs) {
+                ks[hh] = a.d.k_scale[base + hh];
+                vs[hh] = a.d.v_scale[base + hh];
+              }
             }
           }
         }
-        if (!ok) {
-          a.ws.rq_bad[u.r] = 1;
-          set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
-        }
+        ok = in_range && tag == et;
+        if (!in_range) set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
       }
     };
     Unit u0 = locate_load(x_begin + lane);
@@ -379,17 +457,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         go = __all_sync(0xffffffffu, ok);
         if (!go) break;
         if (mine) {
-          StageMeta m;
-          m.n_valid = ok0 ? min(P, u0.L - u0.j * P) : 0;
-          m.pos0 = u0.j * P;
-#pragma unroll
-          for (int hh = 0; hh < 8; ++hh) {
-            m.ks[hh] = ks0[hh];
-            m.vs[hh] = vs0[hh];
-          }
-          m.unit = (int)kl;
-          m.pad = 0;
-          meta[stage] = m;
+          // the copies first (they need only the page id), then the metadata
+          // (scales), whose arrival completes the stage with the copies' bytes
           if (ok0) {
             uint8_t* dst = ring + (size_t)stage * stage_bytes;
             const long long ph = (long long)u0.p * Hkv + (long long)u0.hg * Hs;
@@ -401,6 +470,18 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           } else {
             mbar_arrive(&full[stage]);
           }
+          StageMeta m;
+          m.n_valid = ok0 ? min(P, u0.L - u0.j * P) : -1;
+          m.pos0 = u0.j * P;
+#pragma unroll
+          for (int hh = 0; hh < 8; ++hh) {
+            m.ks[hh] = ks0[hh];
+            m.vs[hh] = vs0[hh];
+          }
+          m.unit = (int)kl;
+          m.pad = 0;
+          meta[stage] = m;
+          mbar_arrive(&full[stage]);
         }
         __syncwarp();
         issued = k + min(g0 + grp, cnt);
@@ -518,6 +599,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
           *abort_flag = 1;
         }
+        if (ok && mt.unit == (int)kk && mt.n_valid < 0 && lane == 0) *piece_bad = 1;
         if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
           const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
           const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
@@ -678,34 +760,15 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           ml[0] = half ? mB : mA;
           ml[1] = half ? lB : lA;
         }
-        named_bar_sync(1, C::CONSUMERS * 32);
-        // element e: dim dd of row nw of virtual head v (kv head hh, row block
-        // v - hh RBW); its row of the kv head is 16 (v - hh RBW) + 8 half + nw
-        static_assert(C::R8 == 8 && D == 128, "epilogue index shifts");
-        for (int e = threadIdx.x; e < Hv * C::R8 * D; e += C::CONSUMERS * 32) {
-          const int dd = e & (D - 1), nw = (e >> 7) & (C::R8 - 1), v = e >> 10;
-          const int hh = (v * rbw_mul) >> 8;  // v / RBW (v < 12)
-          const int n = (v - hh * RBW) * 16 + 8 * half + nw;
-          float M = -INFINITY;
-          for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * C::R8 + nw) * 2]);
-          float o = 0.0f, lsum = 0.0f;
-          if (M != -INFINITY) {
-            for (int q = 0; q < WPH; ++q) {
-              const int w = q * Hv + v;
-              const float mw = merge_ml[(w * C::R8 + nw) * 2];
-              const float scl = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-              o += merge_o[(w * C::R8 + nw) * D + dd] * scl;
-              lsum += merge_ml[(w * C::R8 + nw) * 2 + 1] * scl;
-            }
-          }
-          const long long row = (slot * Hs + hh) * a.R8 + n;
-          a.ws.o_part[row * D + dd] = o;
-          if (dd == 0) {
-            a.ws.ml_part[row * 2 + 0] = M;
-            a.ws.ml_part[row * 2 + 1] = lsum;
-          }
-        }
-        named_bar_sync(1, C::CONSUMERS * 32);
+        // row nw of virtual head v (kv head hh, row block v - hh RBW) is row
+        // 16 (v - hh RBW) + 8 half + nw of the kv head
+        merge_piece<C>(merge_o, merge_ml, Hv, WPH, a,
+                       [&](int v, int nw) -> long long {
+                         const int hh = (v * rbw_mul) >> 8;  // v / RBW (v < 12)
+                         const int n = (v - hh * RBW) * 16 + 8 * half + nw;
+                         return (slot * Hs + hh) * a.R8 + n;
+                       },
+                       piece_bad, half == 1);
       }
 
       k_base += npages;
@@ -796,6 +859,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
         *abort_flag = 1;
       }
+      if (ok && mt.unit == (int)kk && mt.n_valid < 0 && lane == 0) *piece_bad = 1;
       if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
         const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
         const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
@@ -971,40 +1035,18 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       ml[(2 * t + 1) * 2 + 0] = m1;
       ml[(2 * t + 1) * 2 + 1] = l1;
     }
-    named_bar_sync(1, C::CONSUMERS * 32);
     {
-      // slot of this (CTA, segment) piece; rows (head in group, query row)
+      // slot of this (CTA, segment) piece; row nw of virtual head v (kv head
+      // hh's row block j) is row 8 j + nw of the kv head.  v < Hv <= 12,
+      // where (v * ceil(256 / RB)) >> 8 is exactly v / RB for RB <= 4.
       const long long slot = (long long)r * HG + cur.h + blockIdx.x;
-      const int tid = threadIdx.x;  // consumer thread index
-      // element e is dim dd of row nw of virtual head v (shifts only: this
-      // loop is on every piece's critical path); v is kv head hh's row block
-      // j, so the row of the kv head is 8 j + nw.  v < Hv <= 12, where
-      // (v * ceil(256 / RB)) >> 8 is exactly v / RB for RB <= 4.
-      static_assert(C::R8 == 8 && D == 128, "epilogue index shifts");
-      for (int e = tid; e < Hv * C::R8 * D; e += C::CONSUMERS * 32) {
-        const int dd = e & (D - 1), nw = (e >> 7) & (C::R8 - 1), v = e >> 10;
-        const int hh = (v * rb_mul) >> 8, n = (v - hh * RB) * C::R8 + nw;
-        float M = -INFINITY;
-        for (int q = 0; q < WPH; ++q) M = fmaxf(M, merge_ml[((q * Hv + v) * C::R8 + nw) * 2]);
-        float o = 0.0f, lsum = 0.0f;
-        if (M != -INFINITY) {
-          for (int q = 0; q < WPH; ++q) {
-            const int w = q * Hv + v;
-            const float mw = merge_ml[(w * C::R8 + nw) * 2];
-            const float sc = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-            o += merge_o[(w * C::R8 + nw) * D + dd] * sc;
-            lsum += merge_ml[(w * C::R8 + nw) * 2 + 1] * sc;
-          }
-        }
-        const long long row = (slot * Hs + hh) * a.R8 + n;
-        a.ws.o_part[row * D + dd] = o;
-        if (dd == 0) {
-          a.ws.ml_part[row * 2 + 0] = M;
-          a.ws.ml_part[row * 2 + 1] = lsum;
-        }
-      }
+      merge_piece<C>(merge_o, merge_ml, Hv, WPH, a,
+                     [&](int v, int nw) -> long long {
+                       const int hh = (v * rb_mul) >> 8, n = (v - hh * RB) * C::R8 + nw;
+                       return (slot * Hs + hh) * a.R8 + n;
+                     },
+                     piece_bad, true);
     }
-    named_bar_sync(1, C::CONSUMERS * 32);
 
     k_base += npages;
     x = piece_end;
@@ -1046,6 +1088,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
     combine_kernel(const DecodeArgs a, int S) {
   __shared__ float st_o[kCombineWarps][512];
   __shared__ float st_ml[kCombineWarps][2];
+  __shared__ int st_bad[kCombineWarps];
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1067,8 +1110,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
     const long long rh = item / a.R;
     r = (int)(rh / Hkv);
     h = (int)(rh % Hkv);
-    skip = a.ws.rq_skip[r] || a.ws.rq_bad[r];  // aborted: output left untouched
+    skip = a.ws.rq_skip[r];  // aborted or invalid length: output left untouched
   }
+  // a piece whose sum is -1 met a page it must not read: no output either
+  bool bad = false;
   if (!skip) {
     const int Hs = a.Hs, HG = a.HG;
     // segment (request, head group | row block) and row inside its partials
@@ -1100,6 +1145,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
           mj = ml.x;
           lj = ml.y;
         }
+        bad = bad || __any_sync(0xffffffffu, lj < 0.0f);
         const float Mc = warp_max(mj);
         if (Mc == -INFINITY) continue;  // no piece of the chunk saw anything visible
         const float Mn = fmaxf(M, Mc);
@@ -1148,6 +1194,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
     if (lane == 0) {
       st_ml[warp][0] = M;
       st_ml[warp][1] = L;
+      st_bad[warp] = bad ? 1 : 0;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -1156,6 +1203,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
             make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
     __syncthreads();
     if (sub == 0 && !skip) {
+      for (int k = 1; k < S; ++k) bad = bad || st_bad[warp + k] != 0;
       for (int k = 1; k < S; ++k) {
         const float Mk = st_ml[warp + k][0], Lk = st_ml[warp + k][1];
         if (Mk == -INFINITY) continue;
@@ -1176,7 +1224,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
       }
     }
   }
-  if (sub != 0 || skip) return;
+  // fused tag check: the warp of the request's first row writes its abort
+  // bit (every segment and row of a request meets the same pages)
+  if (a.abort_out != nullptr && sub == 0 && item < nitems && h == 0 && n == 0)
+    a.abort_out[r] = (skip || bad) ? 1 : 0;
+  if (sub != 0 || skip || bad) return;
   const int tq = n / a.G, hq = h * a.G + n % a.G;
   uint16_t* out = a.out + (((long long)r * a.T + tq) * a.Hq + hq) * Dv;
   const float inv = (M == -INFINITY) ? 0.0f : 1.0f / L;  // nothing visible: zeros
@@ -1204,6 +1256,11 @@ int gqa_ring_bytes(int kind) {
   return (kind == 1 || kind == 4) ? GqaCfg<false>::RING : GqaCfg<true>::RING;
 }
 int gqa_max_stages() { return kMaxStages; }
+bool gqa_kind_self_plans(int kind) { return kind == 0 || kind == 1 || kind == 4; }
+int gqa_self_plan_max_batch() {
+  static_assert(GqaCfg<true>::PFX_CACHE == GqaCfg<false>::PFX_CACHE, "one prefix cache size");
+  return GqaCfg<true>::PFX_CACHE - 1;
+}
 int gqa_consumer_warps(int kind) {
   return (kind == 1 || kind == 4) ? GqaCfg<false>::CONSUMERS : GqaCfg<true>::CONSUMERS;
 }

@@ -39,6 +39,8 @@
 // Every wait is bounded; on timeout the kernel records KV_ERR_TIMEOUT, lets
 // the asynchronous work it issued finish (bounded) and frees its tensor
 // memory before returning.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -88,8 +90,11 @@ constexpr uint32_t kTmemS = 256;   // S: 2 buffers x 64 columns
 constexpr uint32_t kTmemQ = 384;
 constexpr int kQTmemDims = 256, kQTmemSlices = kQTmemDims / 16;
 
+// page id standing for a page whose tag failed the fused check
+constexpr int kStaleTag = INT_MIN;
+
 struct UnitMeta {
-  int n_valid;  // valid tokens of the unit (0: skip)
+  int n_valid;  // valid tokens of the unit; -1: a page that must not be read
   int pos0;     // position of its first token
   float scale;  // page scale (K and V share the row)
   int unit;     // unit sequence number (checked by consumers)
@@ -432,11 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
       }
-      // unit j of the request is page j
-      auto page_of = [&](long long xu) -> int {
-        return (xu < piece_end) ? prow[xu - s.start] : -1;
-      };
       auto page_ok = [&](int pg) { return pg >= 0 && pg < a.d.num_pages; };
+      // unit j of the request is page j; with the fused tag check a page
+      // whose tag is not the expected one becomes kStaleTag here, before
+      // anything (the L2 prefetch included) reads it
+      auto page_of = [&](long long xu) -> int {
+        if (xu >= piece_end) return -1;
+        const int pg = prow[xu - s.start];
+        if (a.exp_tags == nullptr || !page_ok(pg)) return pg;
+        return a.d.tags[pg] == a.exp_tags[(long long)s.r * maxp + (xu - s.start)] ? pg
+                                                                                  : kStaleTag;
+      };
       auto src_of = [&](int pg) -> const uint8_t* {
         return cache + (long long)(page_ok(pg) ? pg : 0) * kUnitBytes;
       };
@@ -482,14 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         // meta of this unit (its scale load is the only dependent one)
         UnitMeta m;
         const bool ok = page_ok(pg0);
-        m.n_valid = ok ? min(kUT, L - (int)(xu - s.start) * kUT) : 0;
+        m.n_valid = ok ? min(kUT, L - (int)(xu - s.start) * kUT) : -1;
         m.pos0 = (int)(xu - s.start) * kUT;
         m.scale = ok ? a.d.k_scale[pg0] : 1.0f;
         m.unit = (int)u;
-        if (!ok && ct == 0) {
-          a.ws.rq_bad[s.r] = 1;
-          set_error(ctl, KV_ERR_BAD_PAGE_ID);
-        }
+        if (!ok && pg0 != kStaleTag && ct == 0) set_error(ctl, KV_ERR_BAD_PAGE_ID);
         // tile b is free once PV(u - 2) has completed
         if (u >= kNKV && !mbar_wait(&kv_free[b], (uint32_t)(((u >> 1) - 1) & 1), abort_flag, ctl,
                                     wait_info(warp, 1, 32 + b))) {
@@ -644,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       const int tq = (s.rb * kRB + r) / a.Hq;
       const int lim = L - a.T + min(tq, a.T - 1);  // last visible position (inclusive)
       float M = -INFINITY, l = 0.0f;
+      bool bad = false;  // the piece met a page it must not read
       const long long u0 = u;
       // every softmax warp runs every unit (and every named barrier), even
       // after a wait gave up, so the barrier sequence never diverges
@@ -660,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
           tmem_ld16x2(tmem + kTmemS + 64 * b + lane_off, v);
         }
         const UnitMeta m = kv_meta[b];
+        bad = bad || (go && m.unit == (int)u && m.n_valid < 0);
         if (go && m.unit != (int)u) {
           if (lane == 0) set_error(ctl, KV_ERR_INTERNAL);
           *abort_flag = 1;
@@ -760,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
       if (h == 0 && go) {
         a.ws.ml_part[(slot * kRB + r) * 2 + 0] = M;
-        a.ws.ml_part[(slot * kRB + r) * 2 + 1] = l_row;
+        a.ws.ml_part[(slot * kRB + r) * 2 + 1] = bad ? -1.0f : l_row;
       }
       tc_fence_before();
       __syncwarp();

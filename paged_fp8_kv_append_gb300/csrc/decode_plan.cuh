@@ -14,11 +14,10 @@ namespace kvfp8 {
 
 constexpr int kDecodePlanThreads = 1024;
 
-// pfx[r] = exclusive prefix of units of work (pages, or half pages for the
-// latent layout) over requests that get output, rq_skip,
-// rq_bad cleared.  A request is skipped (no pages, no output) when aborted or
-// when its length is negative or needs more pages than its page table holds
-// (that also sets KV_ERR_INVALID_ARG).
+// pfx[r] = exclusive prefix of units of work (pages) over requests that get
+// output, and rq_skip.  A request is skipped (no pages, no output) when
+// aborted or when its length is negative or needs more pages than its page
+// table holds (that also sets KV_ERR_INVALID_ARG).
 __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
   __shared__ int warp_sums[32];
   __shared__ int s_overflow;
@@ -41,7 +40,6 @@ __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
       // at most ceil(2^31 / P) units: an int
       np = skip ? 0 : (int)((L + a.unit_tokens - 1) / a.unit_tokens);
       a.ws.rq_skip[r] = skip ? 1 : 0;
-      a.ws.rq_bad[r] = 0;
     }
     int v = np;
 #pragma unroll
@@ -78,6 +76,70 @@ __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
     return;
   }
   if (threadIdx.x == 0) a.ws.pfx[a.B] = (int)carry;
+}
+
+// The same plan computed by one CTA of any size (a multiple of 32 threads, at
+// most 1024) into shared memory, pfx_s[0 .. B] (B + 1 entries must fit), for
+// a split kernel that plans its batch itself.  wsum: 32 ints of shared
+// memory.  Every thread of the CTA must call it; returns (in every thread)
+// whether the batch was refused (then nothing is attended).
+__device__ __forceinline__ bool decode_plan_shared(const DecodeArgs& a, int32_t* pfx_s, int* wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int P = a.d.page_size;
+  long long carry = 0;
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    int np = 0;
+    if (r < a.B) {
+      const long long L = a.seq_lens[r];
+      const bool aborted = a.abort_mask != nullptr && a.abort_mask[r] != 0;
+      const bool bad_len = L < 0 || (L + P - 1) / P > a.max_pages;
+      if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+      np = (aborted || bad_len) ? 0 : (int)((L + a.unit_tokens - 1) / a.unit_tokens);
+    }
+    int v = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) wsum[wid] = v;
+    __syncthreads();
+    long long before = carry;
+    for (int k = 0; k < wid; ++k) before += wsum[k];
+    long long chunk = 0;
+    for (int k = 0; k < nw; ++k) chunk += wsum[k];
+    const long long excl = before + v - np;
+    if (r < a.B) pfx_s[r] = excl > INT_MAX ? INT_MAX : (int)excl;
+    carry += chunk;
+    __syncthreads();
+  }
+  // same refusal as decode_plan_block: more than 2^28 units attends nothing
+  const bool refuse = carry > INT_MAX / 8;
+  if (refuse) {
+    for (int r = threadIdx.x; r <= a.B; r += blockDim.x) pfx_s[r] = 0;
+    if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+  } else if (threadIdx.x == 0) {
+    pfx_s[a.B] = (int)carry;
+  }
+  __syncthreads();
+  return refuse;
+}
+
+// The plan of decode_plan_shared stored into the workspace for the combine
+// kernel (pfx and rq_skip, as decode_plan_block writes them); one CTA.
+static __device__ __noinline__ void decode_plan_store(const DecodeArgs& a, const int32_t* pfx_s,
+                                               bool refused) {
+  const int P = a.d.page_size;
+  for (int r = threadIdx.x; r <= a.B; r += blockDim.x) {
+    a.ws.pfx[r] = pfx_s[r];
+    if (r < a.B) {
+      const long long L = a.seq_lens[r];
+      const bool aborted = a.abort_mask != nullptr && a.abort_mask[r] != 0;
+      const bool bad_len = L < 0 || (L + P - 1) / P > a.max_pages;
+      a.ws.rq_skip[r] = (refused || aborted || bad_len) ? 1 : 0;
+    }
+  }
 }
 
 }  // namespace kvfp8

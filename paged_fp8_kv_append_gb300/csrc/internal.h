@@ -44,9 +44,11 @@ cudaError_t launch_release(const ReleaseArgs& a, cudaStream_t s, int* launches);
 // Workspace carve-up (all offsets 256-byte aligned).
 struct DecodeWs {
   int32_t* pfx;       // [B+1] exclusive prefix of pages per request (0 if skipped)
-  uint8_t* rq_skip;   // [B] 1: request gets no output (aborted / invalid)
-  uint8_t* rq_bad;    // [B] 1: a page id out of range was met while reading
-  float* ml_part;     // [slots][Hs][R8][2]  running max (log2 domain) and sum
+  uint8_t* rq_skip;   // [B] 1: request gets no output (aborted / invalid length)
+  // [slots][Hs][R8][2]  running max (log2 domain) and sum; a sum of -1 marks a
+  // piece that met a page it must not read (id out of range, or, with the
+  // fused tag check, a stale tag): its request gets no output
+  float* ml_part;
   float* o_part;      // [slots][Hs][R8][Dv] unnormalised partial outputs
   size_t bytes;
 };
@@ -67,6 +69,15 @@ struct DecodeArgs {
   int32_t HG;           // segments per request: head groups (GQA) or 64-row blocks (latent)
   int32_t stages;       // ring stages of the split kernel
   int32_t unit_tokens;  // tokens per unit of work (a page)
+  // the split kernel builds the batch plan itself (B + 1 <= its shared-memory
+  // prefix cache) instead of reading the plan kernel's; its CTA 0 writes the
+  // plan to the workspace for the combine
+  int32_t self_plan;
+  // fused tag check (NULL: none): the split reads a page only after its tag
+  // matched exp_tags[r][j]; the combine writes abort_out[r] (1: a stale tag,
+  // an out-of-range page id or an invalid length; 0 otherwise)
+  const uint32_t* exp_tags;
+  uint8_t* abort_out;
   DecodeWs ws;
 };
 
@@ -96,6 +107,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {
   int kind;         // 0 = GQA e4m3, 1 = GQA bf16, 2 = latent e4m3, 3 / 4 = GQA e4m3 / bf16 > 8 rows
+  int self_plan;    // the split kernel plans the batch itself (no plan launch)
   int grid;         // split-kernel CTAs
   int R8;           // partial rows per (slot, head)
   int Hs;           // kv heads per unit of work
@@ -109,6 +121,8 @@ struct DecodeConfig {
 int gqa_ring_bytes(int kind);
 int gqa_max_stages();
 int gqa_consumer_warps(int kind);
+int gqa_self_plan_max_batch();
+bool gqa_kind_self_plans(int kind);
 
 kv_status decode_config(const kv_pool* pool, int B, int Hq, int T, DecodeConfig* cfg);
 size_t decode_ws_layout(const kv_pool_desc& d, int B, int Hkv, const DecodeConfig& cfg,
