@@ -424,7 +424,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
             }
           }
         }
-        ok = in_range && tag == et;
+        // without the fused check `ok` must not wait for any load
+        ok = in_range && (a.exp_tags == nullptr || tag == et);
         if (!in_range) set_error(a.d.ctl, KV_ERR_BAD_PAGE_ID);
       }
     };
@@ -599,7 +600,9 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
           *abort_flag = 1;
         }
-        if (ok && mt.unit == (int)kk && mt.n_valid < 0 && lane == 0) *piece_bad = 1;
+        // (a plain store on the rare path: a register here made this kernel
+        // spill; the merge reads the flag after a barrier)
+        if (mt.n_valid < 0 && lane == 0) *const_cast<int*>(piece_bad) = 1;
         if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
           const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
           const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
@@ -840,6 +843,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
     const int lim1 = L - T + min((n0 + 2 * t + 1) / G, T - 1);
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    int bad_units = 0;  // OR of the units' n_valid: negative if one must not be read
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -859,7 +863,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
         if (lane == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);
         *abort_flag = 1;
       }
-      if (ok && mt.unit == (int)kk && mt.n_valid < 0 && lane == 0) *piece_bad = 1;
+      bad_units |= mt.n_valid;  // sign bit: a page that must not be read
       if (ok && mt.unit == (int)kk && mt.n_valid > 0) {
         const uint8_t* Kt = ring + (size_t)stage * stage_bytes + hw * C::TILE;
         const uint8_t* Vt = ring + (size_t)stage * stage_bytes + (Hs + hw) * C::TILE;
@@ -1028,6 +1032,7 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       mo[(2 * t) * D + 16 * i + g + 8] = acc[i][2];
       mo[(2 * t + 1) * D + 16 * i + g + 8] = acc[i][3];
     }
+    if (bad_units < 0 && lane == 0) *piece_bad = 1;  // read after the merge's first barrier
     if (g == 0) {
       float* ml = merge_ml + warp * C::R8 * 2;
       ml[(2 * t) * 2 + 0] = m0;
