@@ -265,7 +265,7 @@ class Arm:
         kv.paged_decode_attn_split(h, B, w.num_q_heads, w.q_tokens, self.q_steps[s], self.pt,
                                    self.sl, self.mask, w.sm_scale, self.ws)
         n += kv.kv_last_launch_count(h)
-        if ev is not None:
+        if ev is not None and ev[3] is not None:
             ev[3].record()
         kv.paged_decode_attn_combine(h, B, w.num_q_heads, w.q_tokens, self.mask, self.out, self.ws)
         n += kv.kv_last_launch_count(h)
@@ -288,7 +288,13 @@ class Arm:
             raise RuntimeError(f"first step: {self.kv.kv_status_string(self.pool.error())}")
         return {int(r): wl.bits_u16(self.out[int(r)]) for r in rs}
 
-    def run(self, steps: int, warmup: int, B=None, sync_ranks=True):
+    def run(self, steps: int, warmup: int, B=None, sync_ranks=True, split_event=True):
+        """Eager steps, each call bracketed by CUDA events.  Returns (total ms,
+        per-step ms [append, verify, split, combine], lengths, launches).
+        split_event=False leaves out the event between the split and the
+        combine (an event there keeps the combine's launch from overlapping
+        the split's tail): column 2 is then the whole attention call and
+        column 3 is zero."""
         B = self.w.B if B is None else B
         for _ in range(warmup):
             self.step(B=B)
@@ -297,6 +303,9 @@ class Arm:
             barrier()
         lens_timed = [self.lens[:B] + i for i in range(steps)]
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        if not split_event:
+            for e in evs:
+                e[3] = None
         launches = []
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -307,7 +316,11 @@ class Arm:
         t1.record()
         torch.cuda.synchronize()
         total_ms = t0.elapsed_time(t1)
-        per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])
+        if split_event:
+            per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])
+        else:
+            per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]),
+                             e[2].elapsed_time(e[4]), 0.0] for e in evs])
         err = self.pool.error()
         if err != 0:
             info = int(self.pool.ctl[3].item())
@@ -316,12 +329,13 @@ class Arm:
                                f"barrier={(info >> 6) & 1} stage={info & 63}; dtype={self.dtype})")
         return total_ms, per, lens_timed, int(sum(launches))
 
-    def run_graphs(self, steps: int, warmup: int):
+    def run_graphs(self, steps: int, warmup: int, B=None):
         """The next warmup + steps steps as CUDA graphs, one per step's inputs
         (a serving loop replays its decode step the same way), replayed in
-        order; each replay is a real decode step.  Returns the timed steps'
-        total ms."""
-        kv, w, h, B = self.kv, self.w, self.pool.handle, self.w.B
+        order, for the first B requests; each replay is a real decode step.
+        Returns the timed steps' total ms."""
+        kv, w, h = self.kv, self.w, self.pool.handle
+        B = w.B if B is None else B
 
         def body(s):
             self.pool.append(B, self.k_steps[s], self.v_steps[s], self.ones, 1, self.pt,
@@ -353,7 +367,7 @@ class Arm:
         if self.pool.error() != 0:
             raise RuntimeError(f"graph steps: {self.kv.kv_status_string(self.pool.error())}")
         self.step_no += n
-        self.lens += n
+        self.lens[:B] += n
         del graphs
         return t0.elapsed_time(t1)
 
@@ -673,10 +687,10 @@ def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
     first B requests (small profiling captures)."""
     import dataclasses
 
-    w = dataclasses.replace(wl.gqa_batch(steps=steps + warmup + 2), num_q_heads=96)
+    w = dataclasses.replace(wl.gqa_batch(steps=2 * (steps + warmup) + 2), num_q_heads=96)
     if B != w.B:
         w = wl.subset(w, B)
-    arm = Arm(w, dtype, device, steps + warmup + 1)
+    arm = Arm(w, dtype, device, 1 + 2 * (steps + warmup))
     if parity is not None:
         r = int(np.argmax(w.lens))
         parity.append({"name": f"wide96_{'e4m3' if dtype == 0 else 'bf16'}", "w": w,
@@ -764,7 +778,9 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
     and GB/s of split + combine over the algorithmic bytes of the requests
     attended, for the first B requests of an Arm."""
     B = w.B if B is None else B
-    total_ms, per, lens_timed, _ = arm.run(steps, warmup, B=B, sync_ranks=False)
+    total_ms, per, lens_timed, _ = arm.run(steps, warmup, B=B, sync_ranks=False,
+                                           split_event=False)
+    graph_ms = arm.run_graphs(steps, warmup, B=B)
     keep = np.array([r not in set(aborted) for r in range(B)])
     sub = wl.subset(w, B)
     byt = []
@@ -775,14 +791,17 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
         b -= (B - int(keep.sum())) * sub.q_tokens * sub.num_q_heads * (sub.head_dim_k +
                                                                        sub.head_dim_v) * 2
         byt.append(b)
-    attn_ms = per[:, 2] + per[:, 3]
+    attn_ms = per[:, 2]
     gbs = float(np.mean([b / (t * 1e6) for b, t in zip(byt, attn_ms)]))
     return {"requests": B, "attended": int(keep.sum()),
-            "tokens_per_s": int(keep.sum()) * w.q_tokens * steps / (total_ms / 1e3),
-            "ms_per_step": total_ms / steps, "attn_us": float(attn_ms.mean() * 1e3),
+            "tokens_per_s": int(keep.sum()) * w.q_tokens * steps / (graph_ms / 1e3),
+            "ms_per_step": graph_ms / steps, "eager_ms_per_step": total_ms / steps,
+            "attn_us": float(attn_ms.mean() * 1e3),
             "attn_gbs": gbs, "pct_of_8000": 100.0 * gbs / NOMINAL_HBM_GBS,
             "kernel_us": {k: float(per[:, i].mean() * 1e3)
-                          for i, k in enumerate(("append", "verify", "split", "combine"))}}
+                          for i, k in enumerate(("append", "verify", "attention"))},
+            "timing": "tokens/s: each step a CUDA graph replay; attention: CUDA events around "
+                      "the split + combine calls of eager steps"}
 
 
 def sweep_lines(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, peak: float,
@@ -836,10 +855,10 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float, par
     contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
     428k pages checked per step): the verify overhead with every tag valid,
     then the full step with its seeded stale tags (those requests abort)."""
-    w = wl.skewed(steps=3 * (replays + 8) + steps + warmup + 8)
+    w = wl.skewed(steps=3 * (replays + 8) + 2 * (steps + warmup) + 8)
     stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
-    arm = Arm(w, 0, device, steps + warmup + 1)
+    arm = Arm(w, 0, device, 1 + 2 * (steps + warmup))
     if parity is not None:  # a seeded live request, all tags valid at this step
         live = [r for r in range(w.B) if r not in stale and w.lens[r] <= 65536]
         r = int(np.random.default_rng(w.seed + 11).choice(live))
@@ -1201,9 +1220,9 @@ def main():
     if args.conc_only > 0:
         device = torch.device("cuda", local)
         w = wl.concurrency(args.conc_only)
-        w.steps = args.steps + args.warmup + 2
+        w.steps = 2 * (args.steps + args.warmup) + 2
         w.num_pages = int(w.B * (-(-(131072 + w.steps) // 16))) + 64
-        arm = Arm(w, 0, device, args.steps + args.warmup)
+        arm = Arm(w, 0, device, 2 * (args.steps + args.warmup))
         print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
         return
     if args.wide_only > 0:
@@ -1237,7 +1256,7 @@ def main():
     # ---- headline: B requests of 131,072 tokens, e4m3 cache
     B = args.requests
     sweep_pts = [b for b in (1, 8, 16, 32) if b < B]
-    head_steps = 1 + 4 * (K + W) + len(sweep_pts) * (K + W)
+    head_steps = 1 + 5 * (K + W) + 2 * len(sweep_pts) * (K + W)
     over_steps = 0 if args.no_overhead else 2 * (3 * (4 + R) + 2)
     w = wl.concurrency(B, seed=shard_seed(20264, rank))
     w.steps = head_steps + over_steps + 4
@@ -1254,6 +1273,8 @@ def main():
     clocks = sampler.stop()
     e2e_ms, h2d, d2h = arm.run_e2e(K, W, graph=True)
     e2e_eager_ms, _, _ = arm.run_e2e(K, W, graph=False)
+    # the attention call as one interval (no event between split and combine)
+    _, per_attn, lens_attn, _ = arm.run(K, W, split_event=False)
     conc_e4m3 = sweep_lines(w, arm, 0, K, W, peak, sweep_pts)
     overhead = {}
     if not args.no_overhead:
@@ -1268,13 +1289,14 @@ def main():
     tokens = reduce_sum(K * w.B * w.q_tokens)
     value = tokens / (max_ms / 1e3)
     split_ms = per[:, 2]
-    attn_ms = per[:, 2] + per[:, 3]
-    attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_timed]
+    attn_ms = per_attn[:, 2]
+    attn_bytes = [algorithmic_bytes(w, L, 0) for L in lens_attn]
     split_bytes = [algorithmic_bytes(w, L, 0, include_out=False) for L in lens_timed]
     achieved = float(np.mean([b / (t * 1e6) for b, t in zip(split_bytes, split_ms)]))
     attn_gbs = float(np.mean([b / (t * 1e6) for b, t in zip(attn_bytes, attn_ms)]))
-    head_line = {"requests": B, "attended": B, "tokens_per_s": tokens / (eager_ms / 1e3),
-                 "ms_per_step": eager_ms / K, "attn_us": float(attn_ms.mean() * 1e3),
+    head_line = {"requests": B, "attended": B, "tokens_per_s": value,
+                 "ms_per_step": max_ms / K, "eager_ms_per_step": eager_ms / K,
+                 "attn_us": float(attn_ms.mean() * 1e3),
                  "attn_gbs": attn_gbs, "pct_of_8000": 100.0 * attn_gbs / NOMINAL_HBM_GBS,
                  "pct_of_measured": 100.0 * attn_gbs / peak,
                  "kernel_us": {k: float(per[:, i].mean() * 1e3)
@@ -1286,7 +1308,7 @@ def main():
     # ---- the same requests over a BF16 cache
     conc_bf16 = []
     if not args.no_bf16:
-        arm16 = Arm(w, 1, device, 1 + (len(sweep_pts) + 1) * (K + W))
+        arm16 = Arm(w, 1, device, 1 + 2 * (len(sweep_pts) + 1) * (K + W))
         parity_samples.append({"name": "concurrency64_bf16", "w": w, "dtype": 1,
                                "pairs": pairs[:1], "outs": arm16.first_step_output(picks[:1])})
         conc_bf16 = sweep_lines(w, arm16, 1, K, W, peak, sweep_pts + [B])
@@ -1321,7 +1343,7 @@ def main():
                         "kernel_us": {k: float(g_per[:, i].mean() * 1e3) for i, k in
                                       enumerate(("append", "verify", "split", "combine"))}}}
         if not args.no_bf16:
-            garm16 = Arm(gw, 1, device, 1 + K + W)
+            garm16 = Arm(gw, 1, device, 1 + 2 * (K + W))
             parity_samples.append({"name": "gqa_batch_bf16", "w": gw, "dtype": 1,
                                    "pairs": [(rg, 2)], "outs": garm16.first_step_output([rg])})
             gqa["bf16"] = step_line(gw, garm16, 1, K, W)

@@ -269,9 +269,11 @@ size_t paged_decode_workspace_size(const kv_pool* pool, int32_t B,
  * KV_ERR_BAD_PAGE_ID.  Split-K: pages are spread evenly over a persistent grid
  * sized to the device, partials (fp32 o, running max, sum) go to the
  * workspace, and a combine kernel merges them.  Output is bf16 (RNE).
- * e4m3 pools multiply in f16 (every e4m3 code is exact in f16): query
- * elements must stay below 65504 in magnitude (the largest finite f16
- * value); bf16 pools keep the query in bf16.
+ * e4m3 pools multiply in f16 (every e4m3 code is exact in f16): each query
+ * row is scaled by an exact power of two that puts its largest magnitude in
+ * [2^15, 2^16) before it is narrowed to f16, and the row's scores take the
+ * inverse factor, so any finite bf16 query is accepted; bf16 pools keep the
+ * query in bf16.
  * Supported: GQA with head_dim 128, page_size 16 and up to 64 query rows per
  * kv head, q_tokens * (Hq/Hkv) <= 64 (e4m3 and bf16); LATENT
  * with head_dim_k 576, head_dim_v 512, page_size 64, e4m3.  Other shapes

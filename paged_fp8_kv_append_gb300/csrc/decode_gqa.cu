@@ -128,8 +128,32 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+// The e4m3 paths multiply the bf16 query in f16.  Each query row is first
+// scaled by an exact power of two 2^e that puts its largest magnitude in
+// [2^15, 2^16): inside f16's range (below 65504) with all of its bits, and
+// small elements stay clear of f16's subnormals.  The row's scores are then
+// 2^e times the true ones and its score scale takes 2^-e.  For a row whose
+// elements are all normal f16 values either way, scores are bit-identical to
+// the unscaled ones (a power-of-two factor commutes with rounding).
+// Largest magnitude of 8 bf16 values as a bit pattern with the sign cleared
+// (bit-pattern order is magnitude order for finite values).
+__device__ __forceinline__ uint32_t bf16_absbits_max8(const uint4& v) {
+  const uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
+  const uint32_t b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+  const uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
+  const uint32_t d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+  return max(max(a, b), max(c, d));
+}
+// e for a row whose largest magnitude has bf16 bits mb: 15 - floor(log2),
+// within [-112, 112] so that 2^e and 2^-e times the score scale stay normal
+// fp32 numbers (all-zero or subnormal rows take 112).
+__device__ __forceinline__ int q_row_exp(uint32_t mb) {
+  const int E = (int)(mb >> 7);
+  return E == 0 ? 112 : min(112, max(-112, 142 - E));
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float pw) {
+  const float lo = __uint_as_float(w << 16) * pw, hi = __uint_as_float(w & 0xFFFF0000u) * pw;
   return f32x2_to_f16x2(lo, hi);
 }
 
@@ -552,6 +576,8 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       // idle until the piece ends) as [j][lane] 16-byte words: registers
       // hold the 16 x 128 output instead
       uint32_t* qs = reinterpret_cast<uint32_t*>(merge_o + warp * C::R8 * D);
+      // score scales of rows g and g+8 (with the row's 2^-e for e4m3 pools)
+      float qscA = ssl, qscB = ssl;
       {
         uint32_t qa[8][4];
 #pragma unroll
@@ -560,15 +586,27 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           const bool live = row < R;
           const int tq = live ? row / G : 0, hq = live ? h * G + row % G : 0;
           const uint16_t* qrow = a.q + (((long long)r * T + tq) * a.Hq + hq) * D + 32 * t;
+          uint4 v[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // dims 32t + 8u .. +7: k-steps 2u and 2u+1
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (live) v = *reinterpret_cast<const uint4*>(qrow + 8 * u);
+          for (int u = 0; u < 4; ++u)  // dims 32t + 8u .. +7: k-steps 2u and 2u+1
+            v[u] = live ? *reinterpret_cast<const uint4*>(qrow + 8 * u) : make_uint4(0, 0, 0, 0);
+          float pw = 1.0f;
+          if constexpr (FP8) {  // the row's 128 dims are spread over the 4 threads t
+            uint32_t mb = max(max(bf16_absbits_max8(v[0]), bf16_absbits_max8(v[1])),
+                              max(bf16_absbits_max8(v[2]), bf16_absbits_max8(v[3])));
+            mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const int e = q_row_exp(mb);
+            pw = pow2f(e);
+            if (hr == 0) qscA = ssl * pow2f(-e); else qscB = ssl * pow2f(-e);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
             // f16 for e4m3 pools (the codes convert exactly to f16), bf16 as is
-            qa[2 * u][hr] = FP8 ? bf16x2_to_f16x2(v.x) : v.x;
-            qa[2 * u][2 + hr] = FP8 ? bf16x2_to_f16x2(v.y) : v.y;
-            qa[2 * u + 1][hr] = FP8 ? bf16x2_to_f16x2(v.z) : v.z;
-            qa[2 * u + 1][2 + hr] = FP8 ? bf16x2_to_f16x2(v.w) : v.w;
+            qa[2 * u][hr] = FP8 ? bf16x2_to_f16x2_scaled(v[u].x, pw) : v[u].x;
+            qa[2 * u][2 + hr] = FP8 ? bf16x2_to_f16x2_scaled(v[u].y, pw) : v[u].y;
+            qa[2 * u + 1][hr] = FP8 ? bf16x2_to_f16x2_scaled(v[u].z, pw) : v[u].z;
+            qa[2 * u + 1][2 + hr] = FP8 ? bf16x2_to_f16x2_scaled(v[u].w, pw) : v[u].w;
           }
         }
 #pragma unroll
@@ -641,11 +679,12 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
             }
           }
           // s[nt][e]: row g (e < 2) or g+8, token 4t + 2 nt + (e & 1); log2 domain
-          const float sc = FP8 ? mt.ks[hw] * ssl : ssl;
+          const float ksc = FP8 ? mt.ks[hw] : 1.0f;
+          const float scA = ksc * qscA, scB = ksc * qscB;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[nt][e] *= sc;
+            for (int e = 0; e < 4; ++e) s[nt][e] *= e < 2 ? scA : scB;
           const int nv = mt.n_valid;
           const bool full_page = nv == P;
           if (!full_page || mt.pos0 + P - 1 > min(limA, limB)) {
@@ -805,25 +844,41 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
     // dims of k-step j: chunk c = t + 4*(j/4) (fp8) -- 16 dims per chunk --
     // or chunk c = t + 4*(j/2) (bf16) -- 8 dims per chunk.
     uint32_t qf[8][2];
+    // score scales of rows 2t and 2t+1 (with the row's 2^-e for e4m3 pools)
+    float qsc0 = ssl, qsc1 = ssl;
     {
       const int row = n0 + g;
       const bool live = row < R;
       const int tq = live ? row / G : 0, hq = live ? h * G + row % G : 0;
       const uint16_t* qrow = a.q + (((long long)r * T + tq) * a.Hq + hq) * D;
       if constexpr (FP8) {
+        uint4 v[2][2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half)  // chunk t + 4 half: 16 dims = 2 uint4
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            v[half][u] = live ? *reinterpret_cast<const uint4*>(qrow + 16 * (t + 4 * half) + 8 * u)
+                              : make_uint4(0, 0, 0, 0);
+        // the row's 128 dims are spread over the 4 threads t of group g
+        uint32_t mb = max(max(bf16_absbits_max8(v[0][0]), bf16_absbits_max8(v[0][1])),
+                          max(bf16_absbits_max8(v[1][0]), bf16_absbits_max8(v[1][1])));
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        const int e = q_row_exp(mb);
+        const float pw = pow2f(e);
+        // rows 2t and 2t+1 are held by groups 2t and 2t+1
+        qsc0 = ssl * pow2f(-__shfl_sync(0xffffffffu, e, 8 * t));
+        qsc1 = ssl * pow2f(-__shfl_sync(0xffffffffu, e, 8 * t + 4));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int c = t + 4 * half;  // 16 dims = 32 bytes = 2 uint4
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (live) v = *reinterpret_cast<const uint4*>(qrow + 16 * c + 8 * u);
             // words of v: dims 16c + 8u + {0,1}, {2,3}, {4,5}, {6,7}
             const int j0 = 4 * half + 2 * u;
-            qf[j0][0] = bf16x2_to_f16x2(v.x);
-            qf[j0][1] = bf16x2_to_f16x2(v.y);
-            qf[j0 + 1][0] = bf16x2_to_f16x2(v.z);
-            qf[j0 + 1][1] = bf16x2_to_f16x2(v.w);
+            qf[j0][0] = bf16x2_to_f16x2_scaled(v[half][u].x, pw);
+            qf[j0][1] = bf16x2_to_f16x2_scaled(v[half][u].y, pw);
+            qf[j0 + 1][0] = bf16x2_to_f16x2_scaled(v[half][u].z, pw);
+            qf[j0 + 1][1] = bf16x2_to_f16x2_scaled(v[half][u].w, pw);
           }
         }
       } else {
@@ -896,9 +951,10 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
           }
         }
         // scores (log2 domain) for (token g | g+8, row 2t | 2t+1)
-        const float sc = FP8 ? mt.ks[hw] * ssl : ssl;
-        float s[4] = {(sa[0] + sb[0]) * sc, (sa[1] + sb[1]) * sc, (sa[2] + sb[2]) * sc,
-                      (sa[3] + sb[3]) * sc};
+        const float ksc = FP8 ? mt.ks[hw] : 1.0f;
+        const float sc0 = ksc * qsc0, sc1 = ksc * qsc1;
+        float s[4] = {(sa[0] + sb[0]) * sc0, (sa[1] + sb[1]) * sc1, (sa[2] + sb[2]) * sc0,
+                      (sa[3] + sb[3]) * sc1};
         const int nv = mt.n_valid;
         const bool full_page = nv == P;
         if (!full_page || mt.pos0 + P - 1 > min(lim0, lim1)) {
@@ -1110,11 +1166,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
   // every warp reaches the block barrier below, so no early return
   bool skip = item >= nitems;
   int r = 0, h = 0, n = 0;
+  int pfx_r = 0, pfx_r1 = 0, pfx_B = 0;
   if (!skip) {
     n = (int)(item % a.R);
     const long long rh = item / a.R;
     r = (int)(rh / Hkv);
     h = (int)(rh % Hkv);
+    // the plan's prefix and the skip flag are independent loads
+    pfx_r = a.ws.pfx[r];
+    pfx_r1 = a.ws.pfx[r + 1];
+    pfx_B = a.ws.pfx[a.B];
     skip = a.ws.rq_skip[r];  // aborted or invalid length: output left untouched
   }
   // a piece whose sum is -1 met a page it must not read: no output either
@@ -1126,27 +1187,54 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
     const int hg = latent ? n / a.R8 : h / Hs, hw = latent ? 0 : h % Hs;
     const int nl = latent ? n % a.R8 : n;
     const long long seg = (long long)r * HG + hg;
-    const int32_t* pfx = a.ws.pfx;
-    const int np = pfx[r + 1] - pfx[r];
+    const int np = pfx_r1 - pfx_r;
     if (np > 0) {
-      const long long total = (long long)pfx[a.B] * HG;
+      const long long total = (long long)pfx_B * HG;
       const long long per = (total + a.grid - 1) / a.grid;
-      const long long start = (long long)HG * pfx[r] + (long long)hg * np;
+      const long long start = (long long)HG * pfx_r + (long long)hg * np;
       const int c0 = (int)(start / per), c1 = (int)((start + np - 1) / per);
       const long long slot0 = seg + c0;
       const int R8 = a.R8;
-      // this warp's pieces c = sub + S j, j < cnt, merged 32 at a time: each
-      // lane reads one piece's (max, sum), the chunk's max and weights come
-      // from warp reductions, then the weighted outputs are summed with
-      // independent loads (no chain through a running max)
+      // partial row of this warp's piece jj (pieces c = sub + S jj)
+      auto row_of = [&](int jj) -> long long {
+        return ((slot0 + sub + (long long)S * jj) * Hs + hw) * R8 + nl;
+      };
+      auto load_o = [&](long long row, int q) -> float4 {
+        return *reinterpret_cast<const float4*>(a.ws.o_part + row * Dv + 128 * q + 4 * lane);
+      };
+      constexpr int kU = 8 / NG;  // pieces whose output loads are in flight together
+      auto accumulate = [&](const float4 (&o)[kU][NG], const float (&wk)[kU]) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          // a piece that saw nothing has weight 0 and adds nothing
+          const bool use = wk[u] != 0.0f;
+#pragma unroll
+          for (int q = 0; q < NG; ++q) {
+            acc[q][0] = use ? __fmaf_rn(o[u][q].x, wk[u], acc[q][0]) : acc[q][0];
+            acc[q][1] = use ? __fmaf_rn(o[u][q].y, wk[u], acc[q][1]) : acc[q][1];
+            acc[q][2] = use ? __fmaf_rn(o[u][q].z, wk[u], acc[q][2]) : acc[q][2];
+            acc[q][3] = use ? __fmaf_rn(o[u][q].w, wk[u], acc[q][3]) : acc[q][3];
+          }
+        }
+      };
+      // this warp's pieces, merged 32 at a time: each lane reads one piece's
+      // (max, sum) while the outputs of the chunk's first kU pieces are
+      // already loading; the chunk's max and weights come from warp
+      // reductions, then the weighted outputs are summed with independent
+      // loads (no chain through a running max)
       const int cnt = (c1 - c0 + 1 - sub + S - 1) / S;
       for (int j0 = 0; j0 < cnt; j0 += 32) {
+        const int nj = min(32, cnt - j0);
+        float4 o[kU][NG];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int q = 0; q < NG; ++q)
+            o[u][q] = u < nj ? load_o(row_of(j0 + u), q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         const int j = j0 + lane;
         float mj = -INFINITY, lj = 0.0f;
-        long long rowj = 0;
         if (j < cnt) {
-          rowj = ((slot0 + sub + (long long)S * j) * Hs + hw) * R8 + nl;
-          const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + rowj * 2);
+          const float2 ml = *reinterpret_cast<const float2*>(a.ws.ml_part + row_of(j) * 2);
           mj = ml.x;
           lj = ml.y;
         }
@@ -1160,36 +1248,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           acc[q][0] *= sa, acc[q][1] *= sa, acc[q][2] *= sa, acc[q][3] *= sa;
-        const int nj = min(32, cnt - j0);
-        // kU pieces' loads are issued before their products are summed
-        constexpr int kU = 8 / NG;
-        for (int k0 = 0; k0 < nj; k0 += kU) {
-          float4 o[kU][NG];
-          float wk[kU];
+        float wk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, wj, u);
+          wk[u] = u < nj ? wu : 0.0f;
+        }
+        accumulate(o, wk);
+        for (int k0 = kU; k0 < nj; k0 += kU) {
 #pragma unroll
           for (int u = 0; u < kU; ++u) {
             const bool ok = k0 + u < nj;  // uniform across the warp
-            wk[u] = __shfl_sync(0xffffffffu, wj, ok ? k0 + u : 0);
-            const long long rk = __shfl_sync(0xffffffffu, rowj, ok ? k0 + u : 0);
+            const float wu = __shfl_sync(0xffffffffu, wj, ok ? k0 + u : 0);
+            wk[u] = ok ? wu : 0.0f;
 #pragma unroll
             for (int q = 0; q < NG; ++q)
-              o[u][q] = ok ? *reinterpret_cast<const float4*>(a.ws.o_part + rk * Dv + 128 * q +
-                                                              4 * lane)
-                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (!ok) wk[u] = 0.0f;
+              o[u][q] = ok ? load_o(row_of(j0 + k0 + u), q) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           }
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            // a piece that saw nothing has weight 0 and adds nothing
-            const bool use = wk[u] != 0.0f;
-#pragma unroll
-            for (int q = 0; q < NG; ++q) {
-              acc[q][0] = use ? __fmaf_rn(o[u][q].x, wk[u], acc[q][0]) : acc[q][0];
-              acc[q][1] = use ? __fmaf_rn(o[u][q].y, wk[u], acc[q][1]) : acc[q][1];
-              acc[q][2] = use ? __fmaf_rn(o[u][q].z, wk[u], acc[q][2]) : acc[q][2];
-              acc[q][3] = use ? __fmaf_rn(o[u][q].w, wk[u], acc[q][3]) : acc[q][3];
-            }
-          }
+          accumulate(o, wk);
         }
         M = Mn;
       }

@@ -75,7 +75,8 @@ constexpr int OFF_META = OFF_FLAG + 16;                    // unit meta [2]
 constexpr int OFF_BAR = OFF_META + kNKV * 16;
 constexpr int NBAR = 4 * kNKV + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM = OFF_MISC + 64;
+constexpr int OFF_QEXP = OFF_MISC + 64;                    // [64] query row exponents
+constexpr int SMEM = OFF_QEXP + kRB * 4;
 static_assert(OFF_KV % 1024 == 0 && KV_BYTES % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
@@ -265,8 +266,47 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
       : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+// The bf16 query is multiplied in f16.  Each query row is first scaled by an
+// exact power of two 2^e that puts its largest magnitude in [2^15, 2^16):
+// inside f16's range (below 65504) with all of its bits, and small elements
+// clear of f16's subnormals; the row's score scale takes 2^-e.  For a row
+// whose elements are normal f16 values either way the scores are
+// bit-identical to unscaled ones (a power-of-two factor commutes with
+// rounding).  Largest magnitude of 8 bf16 values, sign cleared:
+__device__ __forceinline__ uint32_t bf16_absbits_max8(const uint4& v) {
+  const uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
+  const uint32_t b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+  const uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
+  const uint32_t d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+  return max(max(a, b), max(c, d));
+}
+// e = 15 - floor(log2 max), within [-112, 112] (all-zero or subnormal rows: 112)
+__device__ __forceinline__ int q_row_exp(uint32_t mb) {
+  const int E = (int)(mb >> 7);
+  return E == 0 ? 112 : min(112, max(-112, 142 - E));
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+// exponent of query row `row` of a 576-dim block: two threads per row (the
+// pair differ in lane bit `pair_bit`), each taking 288 dims
+__device__ __forceinline__ int q_row_exp_pair(const uint16_t* qrow, int half, int pair_bit) {
+  constexpr int kN = kDK / 16, kG = 12;  // 36 loads per thread, 12 in flight at a time
+  static_assert(kN % kG == 0, "load groups");
+  const uint16_t* base = qrow + half * (kDK / 2);
+  uint32_t mb = 0;
+#pragma unroll
+  for (int k0 = 0; k0 < kN; k0 += kG) {
+    uint4 v[kG];
+#pragma unroll
+    for (int k = 0; k < kG; ++k) v[k] = *reinterpret_cast<const uint4*>(base + 8 * (k0 + k));
+#pragma unroll
+    for (int k = 0; k < kG; ++k) mb = max(mb, bf16_absbits_max8(v[k]));
+  }
+  mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, pair_bit));
+  return q_row_exp(mb);
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float pw) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * pw,
+                                      __uint_as_float(w & 0xFFFF0000u) * pw);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
@@ -330,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
   uint64_t* epi_done = q_free + 1;         // softmax: O of the piece read out
   uint64_t* drain = epi_done + 1;          // MMA commit at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  int* qexp_s = reinterpret_cast<int*>(smem + OFF_QEXP);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,26 +436,39 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       tc_fence_after();  // the previous piece's S MMAs have read Q's tensor memory
       {
         const uint16_t* qbase = a.q + ((long long)s.r * a.T * a.Hq + (long long)s.rb * kRB) * kDK;
-        // dims kQTmemDims.. to shared memory, 128B-swizzled (the A operand
-        // of S's remaining slices; the blocks below them stay unused)
+        // this warp stages the 16 rows of its tensor-memory lane quarter qq:
+        // first their exponents (lanes i and i + 16 take the two halves of
+        // row 16 qq + i), so that no other warp's rows are involved
+        const int qq = warp & 3;
+        {
+          const int e = q_row_exp_pair(qbase + (long long)(16 * qq + (lane & 15)) * kDK,
+                                       lane >> 4, 16);
+          if (lane < 16) qexp_s[16 * qq + lane] = e;
+          __syncwarp();
+        }
+        // dims kQTmemDims.. of these rows to shared memory, 128B-swizzled
+        // (the A operand of S's remaining slices; the blocks below them stay
+        // unused)
         constexpr int kCk0 = kQTmemDims / 8, kCkN = kDK / 8 - kCk0;
-        for (int c = ct; c < kRB * kCkN; c += kConvWarps * 32) {
-          const int n = c / kCkN, ck = kCk0 + c % kCkN;
+        for (int c = lane; c < 16 * kCkN; c += 32) {
+          const int n = 16 * qq + c / kCkN, ck = kCk0 + c % kCkN;
           const uint4 v = *reinterpret_cast<const uint4*>(qbase + (long long)n * kDK + ck * 8);
+          const float pw = pow2f(qexp_s[n]);
           uint4 o;
-          o.x = bf16x2_to_f16x2(v.x);
-          o.y = bf16x2_to_f16x2(v.y);
-          o.z = bf16x2_to_f16x2(v.z);
-          o.w = bf16x2_to_f16x2(v.w);
+          o.x = bf16x2_to_f16x2_scaled(v.x, pw);
+          o.y = bf16x2_to_f16x2_scaled(v.y, pw);
+          o.z = bf16x2_to_f16x2_scaled(v.z, pw);
+          o.w = bf16x2_to_f16x2_scaled(v.w, pw);
           *reinterpret_cast<uint4*>(q_s + (ck >> 3) * (kRB * 128) + swz(n, ck & 7)) = o;
         }
         // dims 0..kQTmemDims-1 to tensor memory: converter warp w writes lane
         // quarter w % 4; its lane i < 16 holds row 16 (w % 4) + i of the block
         // (lanes 16..31 write zeros to columns nothing else uses)
         {
-          const int qq = warp & 3, row = 16 * qq + (lane & 15);
+          const int row = 16 * qq + (lane & 15);
           const uint16_t* qrow = qbase + (long long)row * kDK;
           const uint32_t q_lanes = (uint32_t)(32 * qq) << 16;
+          const float pw = pow2f(qexp_s[row]);
 #pragma unroll 1
           for (int k = 0; k < kQTmemDims / 64; ++k) {  // 64 dims = 32 columns per store
             uint32_t w[32];
@@ -423,10 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
               const uint4 v = lane < 16
                                   ? *reinterpret_cast<const uint4*>(qrow + 64 * k + 8 * j)
                                   : make_uint4(0, 0, 0, 0);
-              w[4 * j + 0] = bf16x2_to_f16x2(v.x);
-              w[4 * j + 1] = bf16x2_to_f16x2(v.y);
-              w[4 * j + 2] = bf16x2_to_f16x2(v.z);
-              w[4 * j + 3] = bf16x2_to_f16x2(v.w);
+              w[4 * j + 0] = bf16x2_to_f16x2_scaled(v.x, pw);
+              w[4 * j + 1] = bf16x2_to_f16x2_scaled(v.y, pw);
+              w[4 * j + 2] = bf16x2_to_f16x2_scaled(v.z, pw);
+              w[4 * j + 3] = bf16x2_to_f16x2_scaled(v.w, pw);
             }
             tmem_st32u(tmem + kTmemQ + 32 * k + q_lanes, w);
           }
@@ -441,10 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       // unit j of the request is page j; with the fused tag check a page
       // whose tag is not the expected one becomes kStaleTag here, before
       // anything (the L2 prefetch included) reads it
+      // (without the check nothing here may depend on the loaded id: the
+      // id of the unit three ahead is only used a unit later)
       auto page_of = [&](long long xu) -> int {
         if (xu >= piece_end) return -1;
         const int pg = prow[xu - s.start];
-        if (a.exp_tags == nullptr || !page_ok(pg)) return pg;
+        if (a.exp_tags == nullptr) return pg;
+        if (!page_ok(pg)) return pg;
         return a.d.tags[pg] == a.exp_tags[(long long)s.r * maxp + (xu - s.start)] ? pg
                                                                                   : kStaleTag;
       };
@@ -651,6 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
       // row rb*64 + r of the request's (t, hq) rows: draft token t = row / Hq
       const int tq = (s.rb * kRB + r) / a.Hq;
       const int lim = L - a.T + min(tq, a.T - 1);  // last visible position (inclusive)
+      // this row's query scale 2^e (the converters staged Q times 2^e): its
+      // scores take 2^-e; the two threads of the row (lanes l, l ^ 16) each
+      // read half of it
+      const float qsc = ssl * pow2f(-q_row_exp_pair(
+          a.q + ((long long)s.r * a.T * a.Hq + (long long)s.rb * kRB + r) * kDK, h, 16));
       float M = -INFINITY, l = 0.0f;
       bool bad = false;  // the piece met a page it must not read
       const long long u0 = u;
@@ -678,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) latent_split_kernel(const DecodeA
         go = __all_sync(0xffffffffu, go);
         float alpha = 1.0f;
         if (go) {
-          const float sc = m.scale * ssl, bias = __log2f(m.scale);
+          const float sc = m.scale * qsc, bias = __log2f(m.scale);
           // tokens i <= thr of this thread's 32 are visible
           const int thr = min(m.n_valid - 1, lim - m.pos0) - 32 * h;
           float mx = -INFINITY;
