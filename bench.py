@@ -49,8 +49,12 @@ NOMINAL_HBM_GBS = 8000.0
 # (CTA, segment) piece), valid only while the kernel's sources hash to `sha`
 # (sha256 of the listed files, first 16 hex digits); otherwise the line
 # reports traffic null.
-SPLIT_DRAM = {"sources": ["decode_gqa.cu", "decode_plan.cuh", "common.cuh"], "sha": None,
-              "read_per_alg_byte": None, "write_per_piece": None}
+SPLIT_DRAM = {"sources": ["decode_gqa.cu", "decode_plan.cuh", "common.cuh"],
+              "sha": "08dd09f15aac0fd0",
+              # 8 requests of 131,075 tokens: 2.152534 GB read (as ncu prints it)
+              # for 2,152,120,864 algorithmic bytes; 3.031296 MB written by
+              # 8 * 2 + 152 pieces
+              "read_per_alg_byte": 2.152534e9 / 2152120864, "write_per_piece": 3.031296e6 / 168}
 
 
 # ------------------------------------------------------------ distributed
@@ -1393,7 +1397,9 @@ def main():
     if args.detail:
         with open(args.detail, "w") as fh:
             json.dump(detail, fh)
-    pieces = B * (w.num_kv_heads // 8) + 152
+    # (CTA, segment) pieces: the e4m3 kernel takes 4 of the 8 kv heads per
+    # unit, so each request is 2 segments, plus at most one boundary per CTA
+    pieces = B * (w.num_kv_heads // 4) + 152
     traffic = split_traffic(float(np.mean(split_bytes)), pieces)
     points = {"concurrency_e4m3": {str(l["requests"]): _pt(l, peak) for l in conc_e4m3}}
     if conc_bf16:
