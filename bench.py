@@ -507,6 +507,66 @@ def bulk_append_line(w: wl.Workload, dtype: int, device, peak: float) -> dict:
             "pct_of_measured": 100.0 * byt / (ms * 1e6) / peak, "bytes": byt}
 
 
+def handoff_line(w: wl.Workload, device, peak: float) -> dict:
+    """kv_append_from_pool of every request of a workload: its rows read from
+    a bf16 pool through that pool's page table into an empty e4m3 pool (the
+    prefill-to-decode handoff without a gather copy), timed three times
+    (median).  Algorithmic bytes: the bf16 rows read, the codes and one fp32
+    scale per (page, kv head, K|V) written, the source page ids read and the
+    destination page-table and expected-tag entries written."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    B, P, mp = w.B, w.page_size, w.max_pages
+    lens = w.lens.astype(np.int64)
+    mk = lambda dt: kv.KVPool(w.num_pages, P, w.num_kv_heads, w.head_dim_k,  # noqa: E731
+                              w.head_dim_v, dtype=dt, layout=w.layout, device=device,
+                              tags=wl.initial_tags(w), free_list=wl.free_list(w))
+    tabs = lambda: (torch.full((B, mp), -1, dtype=torch.int32, device=device),  # noqa: E731
+                    torch.zeros((B, mp), dtype=torch.int32, device=device),
+                    torch.zeros(B, dtype=torch.int32, device=device))
+    src, (spt, set_, ssl) = mk(kv.KV_DTYPE_BF16), tabs()
+    ind = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+    for r0 in range(0, B, 8):  # the source filled a few requests per call
+        counts = np.zeros(B, np.int64)
+        ks, vs = [], []
+        for r in range(r0, min(B, r0 + 8)):
+            k, v = wl.kv_rows(w, r, 0, int(lens[r]), device=device)
+            ks.append(k)
+            vs.append(v)
+            counts[r] = lens[r]
+        ind = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+        src.append(B, torch.cat(ks), torch.cat(vs) if w.layout == 0 else None, ind.to(device),
+                   int(counts.max()), spt, set_, ssl)
+        del ks, vs
+    dst, (pt, et, sl) = mk(kv.KV_DTYPE_E4M3), tabs()
+    rel_ws = torch.empty(kv.kv_release_workspace_size(B), dtype=torch.uint8, device=device)
+    times = []
+    for rep in range(3):
+        if rep > 0:
+            dst.release(B, pt, et, sl, None, rel_ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1_000_000)
+        e0.record()
+        dst.append_from_pool(B, src, spt, ssl, pt, et, sl)
+        e1.record()
+        torch.cuda.synchronize()
+        if dst.error() != 0 or src.error() != 0:
+            raise RuntimeError(f"handoff: {kv.kv_status_string(dst.error() or src.error())}")
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.median(times))
+    rows = int(lens.sum())
+    width = w.num_kv_heads * (w.head_dim_k + (w.head_dim_v if w.layout == 0 else 0))
+    pages = int((-(-lens // P)).sum())
+    scales = pages * (w.num_kv_heads * 2 if w.layout == 0 else 1) * 4
+    byt = rows * width * 2 + rows * width + scales + pages * (4 + 8)
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "cache": "bf16 pool -> e4m3 pool", "rows": rows, "ms": ms,
+            "rows_per_s": rows / (ms / 1e3), "gbs": byt / (ms * 1e6),
+            "pct_of_measured": 100.0 * byt / (ms * 1e6) / peak, "bytes": byt}
+
+
 # ------------------------------------------------------------ re-quantising scale mode
 
 def dequant_rel_error(pool, pt, lens, src_k, P: int) -> float:
@@ -1320,7 +1380,7 @@ def main():
         torch.cuda.empty_cache()
         detail["concurrency_bf16"] = conc_bf16
 
-    gqa = skewed = latent = requant = bulk = wide = churn = None
+    gqa = skewed = latent = requant = bulk = wide = churn = handoff = None
     if run_extra:
         # ---- GQA batch (32 requests, 4k..32k), e4m3 and bf16
         gsteps = 1 + 2 * (K + W)
@@ -1372,6 +1432,9 @@ def main():
             bulk = [bulk_append_line(gw, 0, device, peak), bulk_append_line(gw, 1, device, peak),
                     bulk_append_line(wl.latent_verify(), 0, device, peak)]
             detail["bulk_append"] = bulk
+            handoff = [handoff_line(wl.gqa_batch(), device, peak),
+                       handoff_line(wl.latent_verify(), device, peak)]
+            detail["handoff"] = handoff
         if not args.no_wide:
             wide = {"e4m3": wide_group_line(device, K, W, peak, parity=parity_samples)}
             if not args.no_bf16:
@@ -1428,6 +1491,9 @@ def main():
     if bulk:
         points["bulk_append_frac"] = {f"{b_['workload']}_{b_['cache']}":
                                       round(b_["pct_of_measured"] / 100.0, 4) for b_ in bulk}
+    if handoff:
+        points["handoff_frac"] = {b_["workload"]: round(b_["pct_of_measured"] / 100.0, 4)
+                                  for b_ in handoff}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,

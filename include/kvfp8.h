@@ -66,7 +66,9 @@ typedef enum {
    * one fp32 scale per (page, kv-head) for K and one for V (e4m3) */
   KV_LAYOUT_GQA = 0,
   /* MLA-style latent cache: one row of head_dim_k values per token, the
-   * first head_dim_v of which are V; one KV head; one fp32 scale per page */
+   * first head_dim_v of which are V; one KV head; one fp32 scale per page
+   * (e4m3).  A bf16 latent pool can be appended to and be the source of
+   * kv_append_from_pool; attention needs an e4m3 latent pool. */
   KV_LAYOUT_LATENT = 1
 } kv_layout;
 
@@ -188,6 +190,36 @@ kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B,
                              const int32_t* new_indptr, int32_t max_new_per_req,
                              int32_t* page_table, uint32_t* exp_tags,
                              int32_t max_pages_per_req, int32_t* seq_lens);
+
+/*
+ * Prefill-to-decode handoff without a gather copy (SFS "Quantizing the KV
+ * cache": prefill keeps a BF16 cache, decode reads an FP8 one).  For each
+ * request r in index order, the first src_seq_lens[r] rows of request r in
+ * the bf16 pool `src` -- read through src_page_table (int32
+ * [B][src_max_pages_per_req], device) -- are appended to request r of
+ * `pool` exactly as kv_append_quantize would append the same rows given as
+ * k_new / v_new (page pops, tag stamps, per-(page, kv head) scales, codes;
+ * bf16 destinations copy the bits).
+ *   src          a pool with dtype KV_DTYPE_BF16 and the same layout, kv heads,
+ *                head dims and page size as `pool` (else KV_ERR_INVALID_ARG);
+ *                read only.
+ *   src_seq_lens int32 [B] (device): rows to hand off per request (0: none).
+ *   page_table, exp_tags, max_pages_per_req, seq_lens: `pool`'s, as for
+ *                kv_append_quantize.
+ * A request with rows to hand off must be empty in `pool` (seq_lens 0) and
+ * its rows must fit src_page_table; otherwise it and every later request are
+ * left untouched (KV_ERR_INVALID_ARG in ctl, stop index in
+ * ctl[KV_CTL_APPEND_STOP]), like the other stops of kv_append_quantize.  A
+ * source page id outside `src` sets KV_ERR_BAD_PAGE_ID and the rows of that
+ * page are not written.  Shapes outside the bulk append kernels' limits
+ * (GQA: page_size * head_dim <= 2048; latent: page_size <= 64) and batches
+ * of more than 16,384 requests return KV_ERR_UNSUPPORTED.  Two kernel
+ * launches; nothing is allocated.
+ */
+kv_status kv_append_from_pool(kv_pool* pool, void* stream, int32_t B, const kv_pool* src,
+                              const int32_t* src_page_table, int32_t src_max_pages_per_req,
+                              const int32_t* src_seq_lens, int32_t* page_table,
+                              uint32_t* exp_tags, int32_t max_pages_per_req, int32_t* seq_lens);
 
 /*
  * Batched page-tag integrity check (SFS "Protecting a shared KV cache"; run

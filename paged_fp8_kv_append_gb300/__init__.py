@@ -56,6 +56,8 @@ _lib.kv_pool_destroy.argtypes = [_vp]
 _lib.kv_pool_destroy.restype = _i32
 _lib.kv_append_quantize.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp]
 _lib.kv_append_quantize.restype = _i32
+_lib.kv_append_from_pool.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp]
+_lib.kv_append_from_pool.restype = _i32
 _lib.kv_verify_tags.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp]
 _lib.kv_verify_tags.restype = _i32
 _lib.kv_release_workspace_size.argtypes = [_i32]
@@ -163,6 +165,19 @@ def kv_append_quantize(handle, B, k_new, v_new, new_indptr, max_new_per_req, pag
         _ptr(exp_tags, _U32, "exp_tags"), int(page_table.shape[-1]),
         _ptr(seq_lens, torch.int32, "seq_lens"))
     _check(st, "kv_append_quantize")
+
+
+def kv_append_from_pool(handle, B, src_handle, src_page_table, src_seq_lens, page_table,
+                        exp_tags, seq_lens, stream=None):
+    """Append each request's rows of a bf16 source pool (read through its page
+    table) to this pool, as kv_append_quantize would (see kvfp8.h)."""
+    st = _lib.kv_append_from_pool(
+        handle, _stream(stream), int(B), src_handle,
+        _ptr(src_page_table, torch.int32, "src_page_table"), int(src_page_table.shape[-1]),
+        _ptr(src_seq_lens, torch.int32, "src_seq_lens"),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(exp_tags, _U32, "exp_tags"),
+        int(page_table.shape[-1]), _ptr(seq_lens, torch.int32, "seq_lens"))
+    _check(st, "kv_append_from_pool")
 
 
 def kv_verify_tags(handle, B, page_table, exp_tags, seq_lens, abort_mask, stream=None):
@@ -304,7 +319,8 @@ class KVPool:
         else:
             self.k_cache = torch.zeros((num_pages, page_size, head_dim_k), dtype=edt, device=dev)
             self.v_cache = None
-            self.k_scale = torch.zeros((num_pages,), dtype=torch.float32, device=dev)
+            self.k_scale = (torch.zeros((num_pages,), dtype=torch.float32, device=dev)
+                            if dtype == KV_DTYPE_E4M3 else None)
             self.v_scale = None
         # uint32 tags held in an int32 tensor (same bits; torch has few uint32 ops)
         self.tags = (torch.zeros(num_pages, dtype=torch.int32, device=dev) if tags is None
@@ -342,6 +358,11 @@ class KVPool:
                seq_lens, stream=None):
         kv_append_quantize(self.handle, B, k_new, v_new, new_indptr, max_new_per_req,
                            page_table, exp_tags, seq_lens, stream)
+
+    def append_from_pool(self, B, src, src_page_table, src_seq_lens, page_table, exp_tags,
+                         seq_lens, stream=None):
+        kv_append_from_pool(self.handle, B, src.handle, src_page_table, src_seq_lens, page_table,
+                            exp_tags, seq_lens, stream)
 
     def verify(self, B, page_table, exp_tags, seq_lens, abort_mask, stream=None):
         kv_verify_tags(self.handle, B, page_table, exp_tags, seq_lens, abort_mask, stream)

@@ -204,8 +204,10 @@ kv_status kv_pool_create(const kv_pool_desc* desc, kv_pool** out) {
     if ((long long)d.head_dim_v * d.page_size * (d.dtype == KV_DTYPE_E4M3 ? 1 : 2) > 160 * 1024)
       return KV_ERR_UNSUPPORTED;
   } else {
-    if (d.dtype != KV_DTYPE_E4M3) return KV_ERR_UNSUPPORTED;
-    if (d.num_kv_heads != 1 || d.head_dim_v > d.head_dim_k || !d.k_scale)
+    // a bf16 latent pool holds rows for appends and handoffs (attention over
+    // it is not supported)
+    if (d.num_kv_heads != 1 || d.head_dim_v > d.head_dim_k ||
+        (d.dtype == KV_DTYPE_E4M3 && !d.k_scale))
       return KV_ERR_INVALID_ARG;
   }
   kv_pool* p = new (std::nothrow) kv_pool;
@@ -249,6 +251,49 @@ kv_status kv_append_quantize(kv_pool* pool, void* stream, int32_t B, const void*
   a.seq_lens = seq_lens;
   a.step_mask = nullptr;
   a.fuse_plan = false;
+  a.from_pool = false;
+  int n = 0;
+  const cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status kv_append_from_pool(kv_pool* pool, void* stream, int32_t B, const kv_pool* src,
+                              const int32_t* src_page_table, int32_t src_max_pages_per_req,
+                              const int32_t* src_seq_lens, int32_t* page_table,
+                              uint32_t* exp_tags, int32_t max_pages_per_req, int32_t* seq_lens) {
+  if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
+  if (!src || B < 0 || max_pages_per_req <= 0 || src_max_pages_per_req <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!src_page_table || !src_seq_lens || !page_table || !exp_tags || !seq_lens)
+    return KV_ERR_INVALID_ARG;
+  const kv_pool_desc& d = pool->d;
+  const kv_pool_desc& sd = src->d;
+  if (sd.dtype != KV_DTYPE_BF16 || sd.layout != d.layout || sd.num_kv_heads != d.num_kv_heads ||
+      sd.head_dim_k != d.head_dim_k || sd.head_dim_v != d.head_dim_v ||
+      sd.page_size != d.page_size)
+    return KV_ERR_INVALID_ARG;
+  if (!append_handoff_supported(d, B, src_max_pages_per_req)) return KV_ERR_UNSUPPORTED;
+  AppendArgs a;
+  a.d = d;
+  a.B = B;
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.new_indptr = nullptr;
+  a.max_new = INT32_MAX;  // bounded by the page tables instead
+  a.page_table = page_table;
+  a.exp_tags = exp_tags;
+  a.max_pages = max_pages_per_req;
+  a.seq_lens = seq_lens;
+  a.step_mask = nullptr;
+  a.fuse_plan = false;
+  a.from_pool = true;
+  a.src = sd;
+  a.src_page_table = src_page_table;
+  a.src_max_pages = src_max_pages_per_req;
+  a.src_lens = src_seq_lens;
   int n = 0;
   const cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), &n);
   pool->last_launches = n;
@@ -468,6 +513,7 @@ kv_status kv_decode_step(kv_pool* pool, void* stream, int32_t B, int32_t num_q_h
   aa.max_pages = max_pages_per_req;
   aa.seq_lens = seq_lens;
   aa.step_mask = abort_mask;
+  aa.from_pool = false;
   aa.fuse_plan = true;  // the append's plan kernel also writes the attention plan
   da.self_plan = 0;     // ... so the split kernel reads it
   aa.plan = da;

@@ -74,6 +74,7 @@ __device__ __forceinline__ int owner_of(const long long* incl, int n, long long 
 // Rows request r appends in this call (none when the step mask drops it).
 __device__ __forceinline__ long long req_rows(const AppendArgs& a, int r) {
   if (a.step_mask != nullptr && a.step_mask[r] != 0) return 0;
+  if (a.from_pool) return a.src_lens[r];
   return (long long)a.new_indptr[r + 1] - a.new_indptr[r];
 }
 
@@ -128,9 +129,11 @@ __global__ void __launch_bounds__(kPlanThreads) append_plan_kernel(AppendArgs a)
     if (r < a.B) {
       L = a.seq_lens[r];
       n = req_rows(a, r);
-      // the new length must fit the page table and stay an int32 length
+      // the new length must fit the page table and stay an int32 length; a
+      // handoff fills empty requests from rows its source table maps
       if (n < 0 || L < 0 || n > a.max_new || L + n > (long long)a.max_pages * P ||
-          L + n > INT_MAX) {
+          L + n > INT_MAX ||
+          (a.from_pool && n > 0 && (L != 0 || n > (long long)a.src_max_pages * P))) {
         code = KV_ERR_INVALID_ARG;
       } else {
         if (n > 0 && L % P != 0) {
@@ -403,13 +406,13 @@ __global__ void __launch_bounds__(kDataThreads) append_data_kernel(AppendArgs a)
     // (its tag changed after the plan's check) is not written through the
     // stale mapping
     if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
+    const int es = fp8 ? 1 : 2;
     if (d.layout == KV_LAYOUT_LATENT) {
-      append_block(a.k_new + row0 * Dk, Dk, nrows, Dk, true, fresh, d.k_scale + p,
-                   static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, false, (int)P,
+      append_block(a.k_new + row0 * Dk, Dk, nrows, Dk, fp8, fresh, fp8 ? d.k_scale + p : nullptr,
+                   static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk * es, false, (int)P,
                    slot0, tile, red, requant);
       continue;
     }
-    const int es = fp8 ? 1 : 2;
     if (!is_v) {
       const long long kp = (((long long)p * H + h) * P) * Dk;
       append_block(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
@@ -656,6 +659,65 @@ __device__ __forceinline__ void tile_warp(const uint16_t* src, long long src_str
                     wtile, requant);
 }
 
+// A V tile of a pool-to-pool handoff: read from a bf16 pool's dim-major tile
+// (element (slot, dd) at src[dd * P + slot]) into this pool's dim-major tile
+// at dst.  Only the first nrows slots (the source request's rows) are read
+// and written; the page is fresh, so e4m3 codes take the scale of their own
+// amax (the same division as every other path), and bf16 copies the bits.
+// One warp; a whole 16-slot page takes 16-byte loads (lane l: dims l,
+// l + 32, ...), anything else goes element by element.
+__device__ __forceinline__ void v_tile_from_dim_major(const uint16_t* src, int nrows, int D, int P,
+                                                   bool fp8, float* scale_slot, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+  const bool whole = nrows == P && P == 16;
+  if (!fp8) {
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+    if (whole) {
+      for (int k = lane; k < D * 2; k += 32)
+        reinterpret_cast<uint4*>(d16)[k] = reinterpret_cast<const uint4*>(src)[k];
+    } else {
+      for (int e = lane; e < D * nrows; e += 32) {
+        const int dd = e / nrows, i = e - dd * nrows;
+        d16[dd * P + i] = src[dd * P + i];
+      }
+    }
+    return;
+  }
+  float m = 0.0f;  // fmaxf skips a NaN, as the amax of every other path does
+  if (whole) {
+    for (int dd = lane; dd < D; dd += 32) {
+      const uint4* row = reinterpret_cast<const uint4*>(src + dd * 16);
+      m = fmaxf(m, fmaxf(amax8(row[0]), amax8(row[1])));
+    }
+  } else {
+    for (int e = lane; e < D * nrows; e += 32) {
+      const int dd = e / nrows, i = e - dd * nrows;
+      m = fmaxf(m, fabsf(bf16_bits_to_f32(src[dd * P + i])));
+    }
+  }
+  const float s = scale_from_amax(warp_max(m));
+  if (lane == 0) *scale_slot = s;
+  const float rs = __frcp_rn(s);
+  const bool fast = scale_fast_ok(s);
+  if (whole && fast) {
+    for (int dd = lane; dd < D; dd += 32) {
+      const uint4* row = reinterpret_cast<const uint4*>(src + dd * 16);
+      const uint4 a = row[0], b = row[1];
+      *reinterpret_cast<uint4*>(dst + dd * 16) = make_uint4(
+          quant_word_fresh(a.x, s, rs) | (quant_word_fresh(a.y, s, rs) << 16),
+          quant_word_fresh(a.z, s, rs) | (quant_word_fresh(a.w, s, rs) << 16),
+          quant_word_fresh(b.x, s, rs) | (quant_word_fresh(b.y, s, rs) << 16),
+          quant_word_fresh(b.z, s, rs) | (quant_word_fresh(b.w, s, rs) << 16));
+    }
+    return;
+  }
+  for (int e = lane; e < D * nrows; e += 32) {
+    const int dd = e / nrows, i = e - dd * nrows;
+    const float x = bf16_bits_to_f32(src[dd * P + i]);
+    dst[dd * P + i] = (uint8_t)(e4m3x2(fast ? div_fresh(x, s, rs) : __fdiv_rn(x, s), 0.0f) & 0xFFu);
+  }
+}
+
 // Work items of a bulk append: every (request, page this call touches),
 // times per_page (tiles per page for GQA, 1 for latent), in request order.
 // The CTA's threads build the inclusive prefix pre[0..B] in shared memory, so
@@ -706,6 +768,9 @@ __device__ __forceinline__ int item_owner(const int* pre, int B, int i) {
 }
 
 // GQA: persistent CTAs; each warp takes (request, page, tile) items in turn.
+// FROM_POOL: the pool-to-pool handoff (its own instance, so that the source
+// addressing does not change the register allocation of the common append).
+template <bool FROM_POOL>
 __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -732,21 +797,40 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
     const int nrows = (int)(pos_hi - pos_lo);
     const int slot0 = (int)(pos_lo - jp * P);
-    const long long row0 = a.new_indptr[r] + (pos_lo - L0);
+    const long long row0 = FROM_POOL ? 0 : a.new_indptr[r] + (pos_lo - L0);
     const int p = a.page_table[(long long)r * a.max_pages + jp];
     if (p < 0 || p >= d.num_pages) {  // uniform across the warp
       if ((threadIdx.x & 31) == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
       continue;
     }
+    // rows of this tile: the caller's (row0 of k_new / v_new) or, in a
+    // handoff, source page jp of the request (the destination was empty, so
+    // every page is fresh and takes source page j whole)
+    const int h = t >> 1;
+    long long src_tile = -1;
+    if constexpr (FROM_POOL) {
+      const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
+      if (sp < 0 || sp >= a.src.num_pages) {  // uniform across the warp
+        if ((threadIdx.x & 31) == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+        continue;
+      }
+      src_tile = (long long)sp * H + h;
+    }
     const bool fresh = jp * P >= L0;  // popped by this call
     // not through a stale mapping (see append_data_kernel)
     if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
-    const int h = t >> 1;
     if ((t & 1) == 0) {
-      tile_warp(a.k_new + (row0 * H + h) * Dk, (long long)H * Dk, nrows, Dk, fp8, fresh,
+      const uint16_t* src = FROM_POOL
+                                ? static_cast<const uint16_t*>(a.src.k_cache) + src_tile * P * Dk
+                                : a.k_new + (row0 * H + h) * Dk;
+      tile_warp(src, FROM_POOL ? (long long)Dk : (long long)H * Dk, nrows, Dk, fp8, fresh,
                 fp8 ? d.k_scale + (long long)p * H + h : nullptr,
                 static_cast<uint8_t*>(d.k_cache) + (((long long)p * H + h) * P * Dk) * es, false,
                 (int)P, slot0, wtile, requant);
+    } else if (FROM_POOL) {  // the source V tile is dim-major already
+      v_tile_from_dim_major(static_cast<const uint16_t*>(a.src.v_cache) + src_tile * Dv * P,
+                            nrows, Dv, (int)P, fp8, fp8 ? d.v_scale + (long long)p * H + h : nullptr,
+                            static_cast<uint8_t*>(d.v_cache) + (((long long)p * H + h) * Dv * P) * es);
     } else {
       tile_warp(a.v_new + (row0 * H + h) * Dv, (long long)H * Dv, nrows, Dv, fp8, fresh,
                 fp8 ? d.v_scale + (long long)p * H + h : nullptr,
@@ -821,18 +905,28 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
     const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
     const int nrows = (int)(pos_hi - pos_lo);
     const int slot0 = (int)(pos_lo - jp * P);
-    const long long row0 = a.new_indptr[r] + (pos_lo - L0);
+    const long long row0 = a.from_pool ? 0 : a.new_indptr[r] + (pos_lo - L0);
     const int p = a.page_table[(long long)r * a.max_pages + jp];
     if (p < 0 || p >= d.num_pages) {  // uniform across the block
       if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
       continue;
+    }
+    int sp = 0;  // handoff: source page jp (the destination request was empty)
+    if (a.from_pool) {
+      sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
+      if (sp < 0 || sp >= a.src.num_pages) {  // uniform across the block
+        if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+        continue;
+      }
     }
     const bool fresh = jp * P >= L0;
     // not through a stale mapping (see append_data_kernel)
     if (!fresh && d.tags[p] != a.exp_tags[(long long)r * a.max_pages + jp]) continue;
     // warp w takes rows w, w + 8, ... of this call's rows in the page
     const int my_rows = nrows > warp ? (nrows - warp + kTileWarps - 1) / kTileWarps : 0;
-    const uint16_t* src = a.k_new + (row0 + warp) * Dk;
+    const uint16_t* src = a.from_pool ? static_cast<const uint16_t*>(a.src.k_cache) +
+                                            ((long long)sp * P + warp) * Dk
+                                      : a.k_new + (row0 + warp) * Dk;
     // chunk t of this lane: q = lane + 32 t, row q / cpr of the warp's rows
     uint4 v[kLatChunks];
 #pragma unroll
@@ -841,6 +935,16 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
       v[t] = qd < my_rows
                  ? *reinterpret_cast<const uint4*>(src + (long long)qd * kTileWarps * Dk + 8 * qm)
                  : make_uint4(0, 0, 0, 0);
+    }
+    if (d.dtype != KV_DTYPE_E4M3) {  // a bf16 latent pool: the rows' bits
+      uint16_t* dst16 = static_cast<uint16_t*>(d.k_cache) + (long long)(p * P + slot0 + warp) * Dk;
+#pragma unroll
+      for (int t = 0; t < kLatChunks; ++t) {
+        const int q = lane + 32 * t, qd = q / cpr, qm = q - qd * cpr;
+        if (qd < my_rows)
+          *reinterpret_cast<uint4*>(dst16 + (long long)qd * kTileWarps * Dk + 8 * qm) = v[t];
+      }
+      continue;
     }
     float s;
     bool own_rows = false;  // every row of the page's block is in this call
@@ -881,21 +985,45 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_latent_kernel(AppendAr
 
 }  // namespace
 
+namespace {
+
+// the persistent kernels' shape limits (a GQA tile in one warp's registers;
+// a latent page over one CTA's warps)
+bool gqa_tile_fits(const kv_pool_desc& d) {
+  return (long long)d.page_size * d.head_dim_k <= 32 * 8 * kTileChunks &&
+         (long long)d.page_size * d.head_dim_v <= 32 * 8 * kTileChunks;
+}
+bool latent_page_fits(const kv_pool_desc& d) {
+  return d.page_size <= 8 * kTileWarps &&
+         (long long)((d.page_size + kTileWarps - 1) / kTileWarps) * (d.head_dim_k / 8) <=
+             32 * kLatChunks;
+}
+
+}  // namespace
+
+bool append_handoff_supported(const kv_pool_desc& d, int B, int src_max_pages) {
+  const long long per_page = d.layout == KV_LAYOUT_GQA ? 2LL * d.num_kv_heads : 1LL;
+  if (B > kMaxPersistB || (long long)B * src_max_pages * per_page > INT_MAX) return false;
+  return d.layout == KV_LAYOUT_GQA ? gqa_tile_fits(d) : latent_page_fits(d);
+}
+
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = launch_pdl(append_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   ++*launches;
   // pages a request can touch in one call: ceil((max_new + P - 1) / P)
   const long long P = a.d.page_size;
-  long long pieces = (a.max_new + 2 * P - 2) / P;
+  long long pieces = a.from_pool ? (long long)a.src_max_pages : (a.max_new + 2 * P - 2) / P;
   if (pieces <= 0 || a.B <= 0) return cudaSuccess;
+  const long long pages_per_req = pieces;
   if (pieces > 65535) pieces = 65535;  // the kernel strides over the rest
   const long long Pl = a.d.page_size;
   const int es = a.d.dtype == KV_DTYPE_E4M3 ? 1 : 2;
   // The register-resident kernels are large: a decode-size append (a few
   // rows per request, a handful of CTAs) spends its time fetching their
   // instructions, so it takes the compact per-tile kernel below.
-  const bool bulk = a.max_new >= 2 * Pl;
+  // (a handoff always takes them: the host checked its shape fits)
+  const bool bulk = a.from_pool || a.max_new >= 2 * Pl;
   static int sms = 0;
   if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess)
     sms = 0;
@@ -903,23 +1031,25 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   // the work-item count is held in an int
   const long long per_page = a.d.layout == KV_LAYOUT_GQA ? 2LL * a.d.num_kv_heads : 1LL;
   const bool persist = bulk && sms > 0 && a.B <= kMaxPersistB &&
-                       (long long)a.B * ((a.max_new + 2 * P - 2) / P) * per_page <= INT_MAX;
-  if (persist && a.d.layout == KV_LAYOUT_GQA &&
-      Pl * a.d.head_dim_k <= 32 * 8 * kTileChunks && Pl * a.d.head_dim_v <= 32 * 8 * kTileChunks) {
+                       (long long)a.B * pages_per_req * per_page <= INT_MAX;
+  if (a.from_pool && !persist) return cudaErrorNotSupported;
+  if (persist && a.d.layout == KV_LAYOUT_GQA && gqa_tile_fits(a.d)) {
     const size_t smem = (size_t)kTileWarps * a.d.head_dim_v * Pl * es + pre_bytes;
     if (smem > 48 * 1024) {
-      e = cudaFuncSetAttribute(append_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+      e = a.from_pool ? cudaFuncSetAttribute(append_gqa_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                      : cudaFuncSetAttribute(append_gqa_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(append_gqa_kernel, dim3((unsigned)(2 * sms)), dim3(kTileWarps * 32), smem, s,
-                   a);
+    e = a.from_pool ? launch_pdl(append_gqa_kernel<true>, dim3((unsigned)(2 * sms)),
+                                 dim3(kTileWarps * 32), smem, s, a)
+                    : launch_pdl(append_gqa_kernel<false>, dim3((unsigned)(2 * sms)),
+                                 dim3(kTileWarps * 32), smem, s, a);
     if (e == cudaSuccess) ++*launches;
     return e;
   }
-  if (persist && a.d.layout == KV_LAYOUT_LATENT &&
-      Pl <= 8 * kTileWarps &&
-      (long long)((Pl + kTileWarps - 1) / kTileWarps) * (a.d.head_dim_k / 8) <= 32 * kLatChunks) {
+  if (persist && a.d.layout == KV_LAYOUT_LATENT && latent_page_fits(a.d)) {
     const bool k72 = a.d.head_dim_k == 576;
     if (pre_bytes > 48 * 1024) {
       e = k72 ? cudaFuncSetAttribute(append_latent_kernel<72>,

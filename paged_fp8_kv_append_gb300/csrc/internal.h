@@ -101,8 +101,20 @@ struct AppendArgs {
   // (the one-call step: the lengths and abort bits it leaves are final)
   bool fuse_plan;
   DecodeArgs plan;
+  // pool-to-pool handoff: request r's rows are the first src_lens[r] rows of
+  // request r in the bf16 pool `src`, read through src_page_table (then
+  // k_new, v_new and new_indptr are unused and every request appends into an
+  // empty destination, so that destination page j takes source page j)
+  bool from_pool;
+  kv_pool_desc src;
+  const int32_t* src_page_table;
+  int32_t src_max_pages;
+  const int32_t* src_lens;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches);
+// whether a pool-to-pool handoff of B requests into a pool of this shape fits
+// the bulk append kernels
+bool append_handoff_supported(const kv_pool_desc& d, int B, int src_max_pages);
 
 // Kernel configuration chosen for a pool (shape checks + grid).
 struct DecodeConfig {

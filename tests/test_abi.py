@@ -54,11 +54,43 @@ def test_pool_create_validation(kv):
         with pytest.raises(kv.KVError) as e:
             kv.kv_pool_create(_desc(kv, **bad))
         assert e.value.status == kv.KV_ERR_INVALID_ARG, bad
-    with pytest.raises(kv.KVError) as e:
-        kv.kv_pool_create(_desc(kv, layout=1, num_kv_heads=1, dtype=kv.KV_DTYPE_BF16))
-    assert e.value.status == kv.KV_ERR_UNSUPPORTED
+    # a bf16 latent pool holds rows (appends, handoff source); attention over
+    # it is refused (no workspace size: the shape is unsupported)
+    lat16 = kv.kv_pool_create(_desc(kv, layout=1, num_kv_heads=1, head_dim_k=576,
+                                    head_dim_v=512, page_size=64, dtype=kv.KV_DTYPE_BF16,
+                                    k_scale=None, v_cache=None, v_scale=None))
+    assert kv._lib.paged_decode_workspace_size(lat16, 4, 16, 4) == 0
+    kv.kv_pool_destroy(lat16)
     bf = _desc(kv, dtype=kv.KV_DTYPE_BF16, k_scale=None, v_scale=None)
     kv.kv_pool_destroy(kv.kv_pool_create(bf))
+
+
+def test_handoff_argument_checks(kv):
+    """kv_append_from_pool refuses bad arguments before enqueuing anything."""
+    dst = kv.kv_pool_create(_desc(kv))
+    src = kv.kv_pool_create(_desc(kv, dtype=kv.KV_DTYPE_BF16, k_scale=None, v_scale=None))
+    src8 = kv.kv_pool_create(_desc(kv))  # an e4m3 source is refused
+    other = kv.kv_pool_create(_desc(kv, dtype=kv.KV_DTYPE_BF16, k_scale=None, v_scale=None,
+                                    page_size=32))
+    f = 0x10000
+    h = kv._lib.kv_append_from_pool
+    bad = kv.KV_ERR_INVALID_ARG
+    try:
+        assert h(None, None, 2, src, f, 8, f, f, f, 8, f) == bad
+        assert h(dst, None, 2, None, f, 8, f, f, f, 8, f) == bad
+        assert h(dst, None, -1, src, f, 8, f, f, f, 8, f) == bad
+        assert h(dst, None, 2, src, f, 0, f, f, f, 8, f) == bad
+        assert h(dst, None, 2, src, f, 8, f, f, f, 0, f) == bad
+        assert h(dst, None, 2, src, None, 8, f, f, f, 8, f) == bad
+        assert h(dst, None, 2, src, f, 8, None, f, f, 8, f) == bad
+        assert h(dst, None, 2, src, f, 8, f, None, f, 8, f) == bad
+        assert h(dst, None, 2, src8, f, 8, f, f, f, 8, f) == bad    # source not bf16
+        assert h(dst, None, 2, other, f, 8, f, f, f, 8, f) == bad   # page sizes differ
+        assert h(dst, None, 0, src, None, 8, None, None, None, 8, None) == kv.KV_OK
+        assert h(dst, None, 20000, src, f, 8, f, f, f, 8, f) == kv.KV_ERR_UNSUPPORTED
+    finally:
+        for x in (dst, src, src8, other):
+            kv.kv_pool_destroy(x)
 
 
 def test_entry_points_reject_bad_arguments(kv):
