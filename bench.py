@@ -333,11 +333,12 @@ class Arm:
                                f"barrier={(info >> 6) & 1} stage={info & 63}; dtype={self.dtype})")
         return total_ms, per, lens_timed, int(sum(launches))
 
-    def run_graphs(self, steps: int, warmup: int, B=None):
+    def run_graphs(self, steps: int, warmup: int, B=None, attention=True):
         """The next warmup + steps steps as CUDA graphs, one per step's inputs
         (a serving loop replays its decode step the same way), replayed in
         order, for the first B requests; each replay is a real decode step.
-        Returns the timed steps' total ms."""
+        attention=False leaves the split and combine out (append and tag
+        check only).  Returns the timed steps' total ms."""
         kv, w, h = self.kv, self.w, self.pool.handle
         B = w.B if B is None else B
 
@@ -345,6 +346,8 @@ class Arm:
             self.pool.append(B, self.k_steps[s], self.v_steps[s], self.ones, 1, self.pt,
                              self.et, self.sl)
             self.pool.verify(B, self.pt, self.et, self.sl, self.mask)
+            if not attention:
+                return
             kv.paged_decode_attn_split(h, B, w.num_q_heads, w.q_tokens, self.q_steps[s],
                                        self.pt, self.sl, self.mask, w.sm_scale, self.ws)
             kv.paged_decode_attn_combine(h, B, w.num_q_heads, w.q_tokens, self.mask, self.out,
@@ -751,10 +754,10 @@ def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
     first B requests (small profiling captures)."""
     import dataclasses
 
-    w = dataclasses.replace(wl.gqa_batch(steps=2 * (steps + warmup) + 2), num_q_heads=96)
+    w = dataclasses.replace(wl.gqa_batch(steps=3 * (steps + warmup) + 2), num_q_heads=96)
     if B != w.B:
         w = wl.subset(w, B)
-    arm = Arm(w, dtype, device, 1 + 2 * (steps + warmup))
+    arm = Arm(w, dtype, device, 1 + 3 * (steps + warmup))
     if parity is not None:
         r = int(np.argmax(w.lens))
         parity.append({"name": f"wide96_{'e4m3' if dtype == 0 else 'bf16'}", "w": w,
@@ -845,6 +848,7 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
     total_ms, per, lens_timed, _ = arm.run(steps, warmup, B=B, sync_ranks=False,
                                            split_event=False)
     graph_ms = arm.run_graphs(steps, warmup, B=B)
+    graph_noattn_ms = arm.run_graphs(steps, warmup, B=B, attention=False)
     keep = np.array([r not in set(aborted) for r in range(B)])
     sub = wl.subset(w, B)
     byt = []
@@ -857,7 +861,12 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
         byt.append(b)
     attn_ms = per[:, 2]
     gbs = float(np.mean([b / (t * 1e6) for b, t in zip(byt, attn_ms)]))
+    # the attention's share of a CUDA-graph step: the step with it minus the
+    # same step without it (append and tag check only)
+    attn_graph_us = (graph_ms - graph_noattn_ms) / steps * 1e3
+    gbs_graph = float(np.mean(byt)) / (attn_graph_us * 1e3)
     return {"requests": B, "attended": int(keep.sum()),
+            "attn_us_graph": attn_graph_us, "attn_gbs_graph": gbs_graph,
             "tokens_per_s": int(keep.sum()) * w.q_tokens * steps / (graph_ms / 1e3),
             "ms_per_step": graph_ms / steps, "eager_ms_per_step": total_ms / steps,
             "attn_us": float(attn_ms.mean() * 1e3),
@@ -865,7 +874,8 @@ def step_line(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, B
             "kernel_us": {k: float(per[:, i].mean() * 1e3)
                           for i, k in enumerate(("append", "verify", "attention"))},
             "timing": "tokens/s: each step a CUDA graph replay; attention: CUDA events around "
-                      "the split + combine calls of eager steps"}
+                      "the split + combine calls of eager steps; attn_us_graph: CUDA-graph "
+                      "step time with the attention minus without it"}
 
 
 def sweep_lines(w: wl.Workload, arm: "Arm", dtype: int, steps: int, warmup: int, peak: float,
@@ -919,10 +929,10 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float, par
     contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
     428k pages checked per step): the verify overhead with every tag valid,
     then the full step with its seeded stale tags (those requests abort)."""
-    w = wl.skewed(steps=3 * (replays + 8) + 2 * (steps + warmup) + 8)
+    w = wl.skewed(steps=3 * (replays + 8) + 3 * (steps + warmup) + 8)
     stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
-    arm = Arm(w, 0, device, 1 + 2 * (steps + warmup))
+    arm = Arm(w, 0, device, 1 + 3 * (steps + warmup))
     if parity is not None:  # a seeded live request, all tags valid at this step
         live = [r for r in range(w.B) if r not in stale and w.lens[r] <= 65536]
         r = int(np.random.default_rng(w.seed + 11).choice(live))
@@ -1198,12 +1208,17 @@ def _peaks() -> dict:
 
 
 def _pt(line: dict, peak: float) -> dict:
-    """Compact summary of a step line: tokens/s, attention GB/s, fraction of
-    the measured copy bandwidth and of 8 TB/s."""
-    return {"tok_s": round(line["tokens_per_s"], 1), "gbs": round(line["attn_gbs"], 1),
-            "frac": round(line["attn_gbs"] / peak, 4),
-            "frac_8000": round(line["attn_gbs"] / NOMINAL_HBM_GBS, 4),
-            "attn_us": round(line["attn_us"], 2)}
+    """Compact summary of a step line: tokens/s, attention GB/s (eager call)
+    and its fraction of the measured copy bandwidth and of 8 TB/s, and the
+    same from the attention's share of a CUDA-graph step (`*_graph`)."""
+    d = {"tok_s": round(line["tokens_per_s"], 1), "gbs": round(line["attn_gbs"], 1),
+         "frac": round(line["attn_gbs"] / peak, 4),
+         "frac_8000": round(line["attn_gbs"] / NOMINAL_HBM_GBS, 4),
+         "attn_us": round(line["attn_us"], 2)}
+    if "attn_gbs_graph" in line:
+        d["frac_graph"] = round(line["attn_gbs_graph"] / peak, 4)
+        d["attn_us_graph"] = round(line["attn_us_graph"], 2)
+    return d
 
 
 def split_traffic(alg_bytes: float, pieces: int):
@@ -1284,9 +1299,9 @@ def main():
     if args.conc_only > 0:
         device = torch.device("cuda", local)
         w = wl.concurrency(args.conc_only)
-        w.steps = 2 * (args.steps + args.warmup) + 2
+        w.steps = 3 * (args.steps + args.warmup) + 2
         w.num_pages = int(w.B * (-(-(131072 + w.steps) // 16))) + 64
-        arm = Arm(w, 0, device, 2 * (args.steps + args.warmup))
+        arm = Arm(w, 0, device, 3 * (args.steps + args.warmup))
         print(json.dumps(step_line(w, arm, 0, args.steps, args.warmup)))
         return
     if args.wide_only > 0:
@@ -1320,7 +1335,7 @@ def main():
     # ---- headline: B requests of 131,072 tokens, e4m3 cache
     B = args.requests
     sweep_pts = [b for b in (1, 8, 16, 32) if b < B]
-    head_steps = 1 + 5 * (K + W) + 2 * len(sweep_pts) * (K + W)
+    head_steps = 1 + 6 * (K + W) + 3 * len(sweep_pts) * (K + W)
     over_steps = 0 if args.no_overhead else 2 * (3 * (4 + R) + 2)
     w = wl.concurrency(B, seed=shard_seed(20264, rank))
     w.steps = head_steps + over_steps + 4
@@ -1339,6 +1354,7 @@ def main():
     e2e_eager_ms, _, _ = arm.run_e2e(K, W, graph=False)
     # the attention call as one interval (no event between split and combine)
     _, per_attn, lens_attn, _ = arm.run(K, W, split_event=False)
+    graph_noattn_ms = arm.run_graphs(K, W, attention=False)
     conc_e4m3 = sweep_lines(w, arm, 0, K, W, peak, sweep_pts)
     overhead = {}
     if not args.no_overhead:
@@ -1358,7 +1374,10 @@ def main():
     split_bytes = [algorithmic_bytes(w, L, 0, include_out=False) for L in lens_timed]
     achieved = float(np.mean([b / (t * 1e6) for b, t in zip(split_bytes, split_ms)]))
     attn_gbs = float(np.mean([b / (t * 1e6) for b, t in zip(attn_bytes, attn_ms)]))
+    attn_graph_us = (graph_ms - graph_noattn_ms) / K * 1e3
     head_line = {"requests": B, "attended": B, "tokens_per_s": value,
+                 "attn_us_graph": attn_graph_us,
+                 "attn_gbs_graph": float(np.mean(attn_bytes)) / (attn_graph_us * 1e3),
                  "ms_per_step": max_ms / K, "eager_ms_per_step": eager_ms / K,
                  "attn_us": float(attn_ms.mean() * 1e3),
                  "attn_gbs": attn_gbs, "pct_of_8000": 100.0 * attn_gbs / NOMINAL_HBM_GBS,
@@ -1372,7 +1391,7 @@ def main():
     # ---- the same requests over a BF16 cache
     conc_bf16 = []
     if not args.no_bf16:
-        arm16 = Arm(w, 1, device, 1 + 2 * (len(sweep_pts) + 1) * (K + W))
+        arm16 = Arm(w, 1, device, 1 + 3 * (len(sweep_pts) + 1) * (K + W))
         parity_samples.append({"name": "concurrency64_bf16", "w": w, "dtype": 1,
                                "pairs": pairs[:1], "outs": arm16.first_step_output(picks[:1])})
         conc_bf16 = sweep_lines(w, arm16, 1, K, W, peak, sweep_pts + [B])
@@ -1383,7 +1402,7 @@ def main():
     gqa = skewed = latent = requant = bulk = wide = churn = handoff = None
     if run_extra:
         # ---- GQA batch (32 requests, 4k..32k), e4m3 and bf16
-        gsteps = 1 + 2 * (K + W)
+        gsteps = 1 + 3 * (K + W)
         gw = wl.gqa_batch(seed=shard_seed(20262, rank), steps=gsteps + over_steps + 2)
         if args.batch != gw.B:
             gw = wl.subset(gw, args.batch)
@@ -1407,7 +1426,7 @@ def main():
                         "kernel_us": {k: float(g_per[:, i].mean() * 1e3) for i, k in
                                       enumerate(("append", "verify", "split", "combine"))}}}
         if not args.no_bf16:
-            garm16 = Arm(gw, 1, device, 1 + 2 * (K + W))
+            garm16 = Arm(gw, 1, device, 1 + 3 * (K + W))
             parity_samples.append({"name": "gqa_batch_bf16", "w": gw, "dtype": 1,
                                    "pairs": [(rg, 2)], "outs": garm16.first_step_output([rg])})
             gqa["bf16"] = step_line(gw, garm16, 1, K, W)

@@ -320,8 +320,6 @@ __device__ __forceinline__ void merge_piece(float* merge_o, float* merge_ml, int
 // the wide consumer below); the producer and the ring are the same.
 template <bool FP8, bool WIDE>
 __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
-  pdl_wait();
-  pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
   using C = GqaCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem + C::OFF_RING;
@@ -358,27 +356,13 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
       C::CONSUMERS % Hv != 0 || S < 2 || S > kMaxStages || S % (C::CONSUMERS / Hv) != 0 ||
       stage_bytes * S > C::RING ||
       (a.self_plan && (B + 1 > C::PFX_CACHE || !kCanSelfPlan))) {
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) set_error(a.d.ctl, KV_ERR_INTERNAL);  // host chose a bad configuration
     return;
   }
-  // the batch plan: built here (self_plan; CTA 0 stores it for the combine)
-  // or read from the plan kernel's output, cached in shared memory
-  const int32_t* pfx_g = a.ws.pfx;
-  const bool cached = B + 1 <= C::PFX_CACHE;
-  if (kCanSelfPlan && a.self_plan) {
-    const bool refused = decode_plan_shared(a, pfx_s, wsum_s);
-    if (blockIdx.x == 0) decode_plan_store(a, pfx_s, refused);
-  } else if (cached) {
-    for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
-    __syncthreads();
-  }
-  const int32_t* pfx = cached ? pfx_s : pfx_g;
-  const long long total = (long long)pfx[B] * HG;
-  const long long per = (total + gridDim.x - 1) / gridDim.x;
-  const long long x_begin = (long long)blockIdx.x * per;
-  const long long x_end = min(total, x_begin + per);
-  if (x_begin >= x_end) return;
-
+  // Before the wait for the kernels ahead of this one: only this CTA's shared
+  // memory (the ring barriers), so the set-up overlaps their tail.
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // two arrivals: the copies' expected bytes, then the stage metadata
@@ -389,7 +373,25 @@ __device__ __forceinline__ void gqa_split_body(const DecodeArgs& a) {
     *piece_bad = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  pdl_wait();
+  pdl_trigger();  // the combine's CTAs may wait resident in what this kernel leaves free
+  // the batch plan: built here (self_plan; CTA 0 stores it for the combine)
+  // or read from the plan kernel's output, cached in shared memory
+  const int32_t* pfx_g = a.ws.pfx;
+  const bool cached = B + 1 <= C::PFX_CACHE;
+  if (kCanSelfPlan && a.self_plan) {
+    const bool refused = decode_plan_shared(a, pfx_s, wsum_s);
+    if (blockIdx.x == 0) decode_plan_store(a, pfx_s, refused);
+  } else if (cached) {
+    for (int i = threadIdx.x; i <= B; i += C::THREADS) pfx_s[i] = pfx_g[i];
+  }
+  __syncthreads();  // the plan and the barrier set-up are visible to every warp
+  const int32_t* pfx = cached ? pfx_s : pfx_g;
+  const long long total = (long long)pfx[B] * HG;
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  const long long x_begin = (long long)blockIdx.x * per;
+  const long long x_end = min(total, x_begin + per);
+  if (x_begin >= x_end) return;
   const Cursor start = cursor_at(pfx, B, HG, x_begin);
   const int P = C::P, D = C::D;
 

@@ -86,6 +86,35 @@ __device__ __forceinline__ void decode_plan_block(const DecodeArgs& a) {
 __device__ __forceinline__ bool decode_plan_shared(const DecodeArgs& a, int32_t* pfx_s, int* wsum) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int P = a.d.page_size;
+  if (a.B <= 32) {  // one warp scans the batch: no block-wide rounds
+    if (wid == 0) {
+      long long np = 0;
+      if (lane < a.B) {
+        const long long L = a.seq_lens[lane];
+        const bool aborted = a.abort_mask != nullptr && a.abort_mask[lane] != 0;
+        const bool bad_len = L < 0 || (L + P - 1) / P > a.max_pages;
+        if (!aborted && bad_len) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+        np = (aborted || bad_len) ? 0 : (L + a.unit_tokens - 1) / a.unit_tokens;
+      }
+      long long v = np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      const long long total = __shfl_sync(0xffffffffu, v, 31);
+      // same refusal as decode_plan_block: more than 2^28 units attends nothing
+      const bool refuse = total > INT_MAX / 8;
+      if (lane < a.B) pfx_s[lane] = refuse ? 0 : (int)(v - np);
+      if (lane == 0) {
+        pfx_s[a.B] = refuse ? 0 : (int)total;
+        wsum[0] = refuse ? 1 : 0;
+        if (refuse) set_error(a.d.ctl, KV_ERR_INVALID_ARG);
+      }
+    }
+    __syncthreads();
+    return wsum[0] != 0;
+  }
   long long carry = 0;
   for (int base = 0; base < a.B; base += blockDim.x) {
     const int r = base + threadIdx.x;
