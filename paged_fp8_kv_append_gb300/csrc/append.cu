@@ -840,6 +840,180 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
   }
 }
 
+// ---- staged bulk append (GQA) ----------------------------------------------
+//
+// The same work as append_gqa_kernel, organised per page so that loads stay in
+// flight: one CTA per SM takes (request, page) items in turn; a producer warp
+// moves an item's rows into a ring of shared-memory stages with bulk
+// asynchronous copies, up to S items ahead -- the page's K rows and V rows,
+// two contiguous runs of k_new / v_new (a handoff: the source page's K tiles
+// and V tiles, also two contiguous runs) -- and 8 consumer warps quantise (or
+// copy) the page's 2 H tiles from there with the register-resident tile code.
+// The one-tile-per-warp kernel had at most one tile's loads in flight per
+// warp and spent its time waiting on them.
+constexpr int kStgWarps = 12;
+constexpr int kStgThreads = (kStgWarps + 1) * 32;
+constexpr int kStgMaxStages = 4;
+constexpr int kStgMaxB = 4096;  // requests whose item prefix fits shared memory
+
+// bytes of shared memory besides the stages
+__host__ __device__ constexpr size_t stg_fixed_bytes(int Dv, int P, int es, int B) {
+  return (size_t)kStgWarps * Dv * P * es      // per-warp tiles of the generic V path
+         + kStgMaxStages * 16                  // item metadata
+         + 2 * kStgMaxStages * 8               // full / empty barriers
+         + 16 + 16 * 4                         // abort flag; scan warp sums
+         + (size_t)(B + 1) * 4;                // item prefix
+}
+
+template <bool FROM_POOL>
+__global__ void __launch_bounds__(kStgThreads, 1)
+    append_gqa_staged_kernel(AppendArgs a, int S, int stage_bytes) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t smem[];
+  const kv_pool_desc& d = a.d;
+  const long long P = d.page_size;
+  const bool fp8 = d.dtype == KV_DTYPE_E4M3;
+  const bool requant = fp8 && d.scale_mode == KV_SCALE_REQUANTIZE;
+  const int es = fp8 ? 1 : 2;
+  const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* stages = smem;
+  uint8_t* wtiles = stages + (size_t)S * stage_bytes;
+  int4* meta = reinterpret_cast<int4*>(wtiles + (size_t)kStgWarps * Dv * P * es);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStgMaxStages);
+  uint64_t* empty = full + kStgMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStgMaxStages);
+  int* wsum = reinterpret_cast<int*>(empty + kStgMaxStages) + 4;
+  int* pre = wsum + 16;
+  const int B = min(a.B, (int)d.ctl[KV_CTL_APPEND_STOP]);
+  if (S < 2 || S > kStgMaxStages) {  // the host chose a bad ring
+    if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_INTERNAL);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < S; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kStgWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const int total = B > 0 ? bulk_items_prefix(a, B, 1, pre, wsum) : 0;
+  __syncthreads();
+  const int kbytes = (int)(P * H * Dk * 2);  // the K part of a stage
+
+  if (warp == kStgWarps) {
+    // ---- producer: lane 0 issues each item's two bulk copies
+    if (lane == 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      long long k = 0, issued = 0;
+      for (int it = blockIdx.x; it < total; it += gridDim.x, ++k) {
+        const int stage = (int)(k % S);
+        if (k >= S && !mbar_wait(&empty[stage], (uint32_t)(((k / S) - 1) & 1), abort_flag, d.ctl,
+                                 wait_info(warp, 1, stage)))
+          break;
+        const int r = item_owner(pre, B, it);
+        const long long n = req_rows(a, r);
+        const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
+        const long long jp = L0 / P + (it - pre[r]);
+        const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
+        int nrows = (int)(pos_hi - pos_lo);
+        const uint16_t *ksrc = nullptr, *vsrc = nullptr;
+        uint32_t kb = 0, vb = 0;
+        if constexpr (FROM_POOL) {  // the destination request was empty: source page jp
+          const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
+          if (sp >= 0 && sp < a.src.num_pages) {
+            ksrc = static_cast<const uint16_t*>(a.src.k_cache) + (long long)sp * H * P * Dk;
+            vsrc = static_cast<const uint16_t*>(a.src.v_cache) + (long long)sp * H * Dv * P;
+            kb = (uint32_t)kbytes;
+            vb = (uint32_t)(P * H * Dv * 2);
+          } else {
+            nrows = -1;  // the consumers report it
+          }
+        } else {
+          const long long row0 = a.new_indptr[r] + (pos_lo - L0);
+          ksrc = a.k_new + row0 * H * Dk;
+          vsrc = a.v_new + row0 * H * Dv;
+          kb = (uint32_t)(nrows * H * Dk * 2);
+          vb = (uint32_t)(nrows * H * Dv * 2);
+        }
+        meta[stage] = make_int4(r, (int)jp, nrows, (int)(pos_lo - jp * P));
+        uint8_t* dst = stages + (size_t)stage * stage_bytes;
+        if (kb + vb > 0) {
+          mbar_arrive_expect_tx(&full[stage], kb + vb);
+          bulk_g2s(dst, ksrc, kb, &full[stage], policy);
+          bulk_g2s(dst + kbytes, vsrc, vb, &full[stage], policy);
+        } else {
+          mbar_arrive(&full[stage]);
+        }
+        issued = k + 1;
+      }
+      // after a wait gave up, copies already issued may still be landing
+      if (*abort_flag) {
+        for (long long q = max(0ll, issued - S); q < issued; ++q) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&full[q % S], (uint32_t)((q / S) & 1)) &&
+                 global_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: warp w takes tiles w, w + 8, ... of the page's 2 H
+  // (even: K of head t / 2, odd: V)
+  uint8_t* wtile = wtiles + (size_t)warp * Dv * P * es;
+  long long k = 0;
+  for (int it = blockIdx.x; it < total; it += gridDim.x, ++k) {
+    const int stage = (int)(k % S);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((k / S) & 1),
+                                                      abort_flag, d.ctl,
+                                                      wait_info(warp, 0, stage)));
+    if (!ok) break;
+    const int4 m = meta[stage];
+    const int r = m.x, nrows = m.z, slot0 = m.w;
+    const long long jp = m.y;
+    const uint8_t* src = stages + (size_t)stage * stage_bytes;
+    const int p = a.page_table[(long long)r * a.max_pages + jp];
+    if (nrows < 0 || p < 0 || p >= d.num_pages) {  // a bad source or destination page id
+      if (warp == 0 && lane == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+    } else {
+      const long long n = req_rows(a, r);
+      const long long L0 = a.seq_lens[r] - n;
+      const bool fresh = jp * P >= L0;  // popped by this call
+      // not through a stale mapping (see append_data_kernel)
+      if (fresh || d.tags[p] == a.exp_tags[(long long)r * a.max_pages + jp]) {
+        for (int t = warp; t < 2 * H; t += kStgWarps) {
+          const int h = t >> 1;
+          const long long tile = (long long)p * H + h;
+          if ((t & 1) == 0) {
+            const uint16_t* ks = reinterpret_cast<const uint16_t*>(src) +
+                                 (FROM_POOL ? (long long)h * P * Dk : (long long)h * Dk);
+            tile_warp(ks, FROM_POOL ? (long long)Dk : (long long)H * Dk, nrows, Dk, fp8, fresh,
+                      fp8 ? d.k_scale + tile : nullptr,
+                      static_cast<uint8_t*>(d.k_cache) + tile * P * Dk * es, false, (int)P,
+                      slot0, wtile, requant);
+          } else if constexpr (FROM_POOL) {  // the source V tile is dim-major already
+            v_tile_from_dim_major(reinterpret_cast<const uint16_t*>(src + kbytes) +
+                                      (long long)h * Dv * P,
+                                  nrows, Dv, (int)P, fp8, fp8 ? d.v_scale + tile : nullptr,
+                                  static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es);
+          } else {
+            tile_warp(reinterpret_cast<const uint16_t*>(src + kbytes) + (long long)h * Dv,
+                      (long long)H * Dv, nrows, Dv, fp8, fresh, fp8 ? d.v_scale + tile : nullptr,
+                      static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es, true, (int)P, slot0,
+                      wtile, requant);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+  }
+}
+
 // Block-wide largest magnitude of the latent rows a CTA holds (bit-pattern
 // maximum; a NaN falls back to the float maximum, which skips it).
 __device__ float latent_block_amax(const uint4 (&v)[kLatChunks], uint32_t* redu) {
@@ -1033,6 +1207,28 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
   const bool persist = bulk && sms > 0 && a.B <= kMaxPersistB &&
                        (long long)a.B * pages_per_req * per_page <= INT_MAX;
   if (a.from_pool && !persist) return cudaErrorNotSupported;
+  if (persist && a.d.layout == KV_LAYOUT_GQA && gqa_tile_fits(a.d) && a.B <= kStgMaxB) {
+    // the staged kernel: a page's K and V rows per stage, 2..4 stages
+    const long long stage = (Pl * a.d.num_kv_heads * (a.d.head_dim_k + a.d.head_dim_v) * 2 + 127) /
+                            128 * 128;
+    const size_t fixed = stg_fixed_bytes(a.d.head_dim_v, (int)Pl, es, a.B);
+    const long long room = 227LL * 1024 - (long long)fixed;
+    const int S = (int)min((long long)kStgMaxStages, room > 0 ? room / stage : 0);
+    if (S >= 2) {
+      const size_t smem = (size_t)S * stage + fixed;
+      e = a.from_pool ? cudaFuncSetAttribute(append_gqa_staged_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                      : cudaFuncSetAttribute(append_gqa_staged_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      e = a.from_pool ? launch_pdl(append_gqa_staged_kernel<true>, dim3((unsigned)sms),
+                                   dim3(kStgThreads), smem, s, a, S, (int)stage)
+                      : launch_pdl(append_gqa_staged_kernel<false>, dim3((unsigned)sms),
+                                   dim3(kStgThreads), smem, s, a, S, (int)stage);
+      if (e == cudaSuccess) ++*launches;
+      return e;
+    }
+  }
   if (persist && a.d.layout == KV_LAYOUT_GQA && gqa_tile_fits(a.d)) {
     const size_t smem = (size_t)kTileWarps * a.d.head_dim_v * Pl * es + pre_bytes;
     if (smem > 48 * 1024) {
