@@ -607,7 +607,29 @@ __device__ __noinline__ void tile_warp_generic(const uint16_t* src, long long sr
     return;
   }
   // dim-major destination: element (row i, dim dd) at (dd * P + slot0 + i),
-  // assembled in this warp's shared tile
+  // assembled in this warp's shared tile, or without one (wtile null)
+  // stored element by element
+  if (wtile == nullptr) {
+#pragma unroll
+    for (int t = 0; t < kTileChunks; ++t) {
+      const int q = lane + 32 * t;
+      if (q < total) {
+        const int o = 8 * (q % cpr) * P + slot0 + q / cpr;
+        if (fp8) {
+          const uint2 c8 = quant8_rs(v[t], s, rs);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[o + k * P] = (uint8_t)(((k < 4 ? c8.x : c8.y) >> (8 * (k & 3))) & 0xFFu);
+        } else {
+          const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+          uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) d16[o + k * P] = (uint16_t)(w[k >> 1] >> (16 * (k & 1)));
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int t = 0; t < kTileChunks; ++t) {
     const int q = lane + 32 * t;
@@ -847,22 +869,33 @@ __global__ void __launch_bounds__(kTileWarps * 32) append_gqa_kernel(AppendArgs 
 // moves an item's rows into a ring of shared-memory stages with bulk
 // asynchronous copies, up to S items ahead -- the page's K rows and V rows,
 // two contiguous runs of k_new / v_new (a handoff: the source page's K tiles
-// and V tiles, also two contiguous runs) -- and 8 consumer warps quantise (or
+// and V tiles, also two contiguous runs) -- and 12 consumer warps quantise (or
 // copy) the page's 2 H tiles from there with the register-resident tile code.
+// The producer also does each item's bookkeeping (owner, rows, page ids, tag
+// check), so the consumers read nothing from global memory but the rows.
 // The one-tile-per-warp kernel had at most one tile's loads in flight per
-// warp and spent its time waiting on them.
+// warp and spent its time waiting on them.  For 16-row, 128-wide pages the V
+// tiles of partly filled pages (a few per request) are stored element by
+// element rather than through per-warp shared tiles, which leaves that shared
+// memory to the ring (a third stage for bf16 pages).
 constexpr int kStgWarps = 12;
 constexpr int kStgThreads = (kStgWarps + 1) * 32;
 constexpr int kStgMaxStages = 4;
 constexpr int kStgMaxB = 4096;  // requests whose item prefix fits shared memory
 
+// whether the staged kernel keeps per-warp shared tiles for the V tiles of
+// partly filled pages
+__host__ __device__ constexpr bool stg_wtiles(long long P, int Dv) {
+  return !(P == 16 && Dv == 128);
+}
+
 // bytes of shared memory besides the stages
 __host__ __device__ constexpr size_t stg_fixed_bytes(int Dv, int P, int es, int B) {
-  return (size_t)kStgWarps * Dv * P * es      // per-warp tiles of the generic V path
-         + kStgMaxStages * 16                  // item metadata
-         + 2 * kStgMaxStages * 8               // full / empty barriers
-         + 16 + 16 * 4                         // abort flag; scan warp sums
-         + (size_t)(B + 1) * 4;                // item prefix
+  return (stg_wtiles(P, Dv) ? (size_t)kStgWarps * Dv * P * es : 0)  // per-warp V tiles
+         + kStgMaxStages * 16                                        // item metadata
+         + 2 * kStgMaxStages * 8                                     // full / empty barriers
+         + 16 + 16 * 4                                               // abort flag; warp sums
+         + (size_t)(B + 1) * 4;                                      // item prefix
 }
 
 template <bool FROM_POOL>
@@ -880,7 +913,9 @@ __global__ void __launch_bounds__(kStgThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* stages = smem;
   uint8_t* wtiles = stages + (size_t)S * stage_bytes;
-  int4* meta = reinterpret_cast<int4*>(wtiles + (size_t)kStgWarps * Dv * P * es);
+  const bool use_wtiles = stg_wtiles(P, Dv);
+  int4* meta =
+      reinterpret_cast<int4*>(wtiles + (use_wtiles ? (size_t)kStgWarps * Dv * P * es : 0));
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStgMaxStages);
   uint64_t* empty = full + kStgMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStgMaxStages);
@@ -904,67 +939,150 @@ __global__ void __launch_bounds__(kStgThreads, 1)
   const int kbytes = (int)(P * H * Dk * 2);  // the K part of a stage
 
   if (warp == kStgWarps) {
-    // ---- producer: lane 0 issues each item's two bulk copies
-    if (lane == 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      long long k = 0, issued = 0;
-      for (int it = blockIdx.x; it < total; it += gridDim.x, ++k) {
-        const int stage = (int)(k % S);
-        if (k >= S && !mbar_wait(&empty[stage], (uint32_t)(((k / S) - 1) & 1), abort_flag, d.ctl,
-                                 wait_info(warp, 1, stage)))
-          break;
-        const int r = item_owner(pre, B, it);
-        const long long n = req_rows(a, r);
-        const long long Lnew = a.seq_lens[r], L0 = Lnew - n;
-        const long long jp = L0 / P + (it - pre[r]);
-        const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
-        int nrows = (int)(pos_hi - pos_lo);
-        const uint16_t *ksrc = nullptr, *vsrc = nullptr;
-        uint32_t kb = 0, vb = 0;
-        if constexpr (FROM_POOL) {  // the destination request was empty: source page jp
-          const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
-          if (sp >= 0 && sp < a.src.num_pages) {
-            ksrc = static_cast<const uint16_t*>(a.src.k_cache) + (long long)sp * H * P * Dk;
-            vsrc = static_cast<const uint16_t*>(a.src.v_cache) + (long long)sp * H * Dv * P;
-            kb = (uint32_t)kbytes;
-            vb = (uint32_t)(P * H * Dv * 2);
-          } else {
-            nrows = -1;  // the consumers report it
-          }
+    // ---- producer: the warp works out 32 items' bookkeeping at a time (one
+    // lane per item), then lane 0 issues each item's two bulk copies as its
+    // stage frees up.  The bookkeeping is a chain of dependent loads (owner's
+    // lengths; then source and destination page ids; then the destination's
+    // tag), so the next batch's loads are issued while the current batch's
+    // copies go out: its lengths before the first copy, its page ids half way.
+    struct Item {
+      const uint16_t *ks, *vs;
+      uint32_t kb, vb, et;
+      int p, nrows, slot0, flags;  // flags: 1 fresh page, 2 skip
+      bool live, bad;
+    };
+    const uint64_t policy = l2_evict_first_policy();
+    const long long cnt =
+        (long long)blockIdx.x < total ? (total - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x
+                                      : 0;
+    // phase A: the item's owner and its lengths
+    auto phase_a = [&](long long kk, int& r, long long& n, long long& Lnew, long long& ind0) {
+      r = -1;
+      if (kk < cnt) {
+        r = item_owner(pre, B, (int)(blockIdx.x + kk * gridDim.x));
+        n = req_rows(a, r);
+        Lnew = a.seq_lens[r];
+        ind0 = FROM_POOL ? 0 : a.new_indptr[r];
+      }
+    };
+    // phase B: rows and source; loads of the page ids and the expected tag
+    auto phase_b = [&](long long kk, int r, long long n, long long Lnew, long long ind0, Item& m) {
+      m.live = r >= 0;
+      m.bad = false;
+      m.kb = m.vb = 0;
+      m.ks = m.vs = nullptr;
+      m.p = -1;
+      m.nrows = m.slot0 = m.flags = 0;
+      m.et = 0;
+      if (!m.live) return;
+      const int it = (int)(blockIdx.x + kk * gridDim.x);
+      const long long L0 = Lnew - n;
+      const long long jp = L0 / P + (it - pre[r]);
+      const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
+      m.nrows = (int)(pos_hi - pos_lo);
+      m.slot0 = (int)(pos_lo - jp * P);
+      if constexpr (FROM_POOL) {  // the destination request was empty: source page jp
+        const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
+        if (sp >= 0 && sp < a.src.num_pages) {
+          m.ks = static_cast<const uint16_t*>(a.src.k_cache) + (long long)sp * H * P * Dk;
+          m.vs = static_cast<const uint16_t*>(a.src.v_cache) + (long long)sp * H * Dv * P;
+          m.kb = (uint32_t)kbytes;
+          m.vb = (uint32_t)(P * H * Dv * 2);
         } else {
-          const long long row0 = a.new_indptr[r] + (pos_lo - L0);
-          ksrc = a.k_new + row0 * H * Dk;
-          vsrc = a.v_new + row0 * H * Dv;
-          kb = (uint32_t)(nrows * H * Dk * 2);
-          vb = (uint32_t)(nrows * H * Dv * 2);
+          m.bad = true;
         }
-        meta[stage] = make_int4(r, (int)jp, nrows, (int)(pos_lo - jp * P));
-        uint8_t* dst = stages + (size_t)stage * stage_bytes;
-        if (kb + vb > 0) {
-          mbar_arrive_expect_tx(&full[stage], kb + vb);
-          bulk_g2s(dst, ksrc, kb, &full[stage], policy);
-          bulk_g2s(dst + kbytes, vsrc, vb, &full[stage], policy);
-        } else {
-          mbar_arrive(&full[stage]);
+      } else {
+        const long long row0 = ind0 + (pos_lo - L0);
+        m.ks = a.k_new + row0 * H * Dk;
+        m.vs = a.v_new + row0 * H * Dv;
+        m.kb = (uint32_t)(m.nrows * H * Dk * 2);
+        m.vb = (uint32_t)(m.nrows * H * Dv * 2);
+      }
+      m.p = a.page_table[(long long)r * a.max_pages + jp];
+      m.flags = jp * P >= L0 ? 1 : 0;  // popped by this call
+      if (m.flags == 0) m.et = a.exp_tags[(long long)r * a.max_pages + jp];
+    };
+    // phase C: checks on the destination page
+    auto phase_c = [&](Item& m) {
+      if (!m.live) return;
+      if (m.bad || m.p < 0 || m.p >= d.num_pages) {
+        set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+        m.flags = 2;
+      } else if (m.flags == 0 && d.tags[m.p] != m.et) {
+        m.flags = 2;  // not through a stale mapping (see append_data_kernel)
+      }
+      if (m.flags & 2) m.kb = m.vb = 0;  // nothing to read for an item that is skipped
+    };
+    int ar = -1;
+    long long an = 0, aL = 0, ai = 0;
+    Item cur, nxt;
+    phase_a(lane, ar, an, aL, ai);
+    phase_b(lane, ar, an, aL, ai, cur);
+    phase_c(cur);
+    long long issued = 0;
+    bool go = true;
+    for (long long k0 = 0; go && k0 < cnt; k0 += 32) {
+      const int nb = (int)min(32ll, cnt - k0);
+      const bool more = k0 + 32 < cnt;
+      if (more) phase_a(k0 + 32 + lane, ar, an, aL, ai);
+      for (int j = 0; j < nb; ++j) {
+        const long long k = k0 + j;
+        const int stage = (int)(k % S);
+        bool ok = true;
+        if (lane == 0 && k >= S)
+          ok = mbar_wait(&empty[stage], (uint32_t)(((k / S) - 1) & 1), abort_flag, d.ctl,
+                         wait_info(warp, 1, stage));
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+          go = false;
+          break;
+        }
+        const int jp_ = __shfl_sync(0xffffffffu, cur.p, j);
+        const int jn = __shfl_sync(0xffffffffu, cur.nrows, j);
+        const int js = __shfl_sync(0xffffffffu, cur.slot0, j);
+        const int jf = __shfl_sync(0xffffffffu, cur.flags, j);
+        const uint32_t jkb = __shfl_sync(0xffffffffu, cur.kb, j);
+        const uint32_t jvb = __shfl_sync(0xffffffffu, cur.vb, j);
+        const uint16_t* jks = reinterpret_cast<const uint16_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.ks), j));
+        const uint16_t* jvs = reinterpret_cast<const uint16_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.vs), j));
+        if (lane == 0) {
+          meta[stage] = make_int4(jp_, jn, js, jf);
+          uint8_t* dst = stages + (size_t)stage * stage_bytes;
+          if (jkb + jvb > 0) {
+            mbar_arrive_expect_tx(&full[stage], jkb + jvb);
+            bulk_g2s(dst, jks, jkb, &full[stage], policy);
+            bulk_g2s(dst + kbytes, jvs, jvb, &full[stage], policy);
+          } else {
+            mbar_arrive(&full[stage]);
+          }
         }
         issued = k + 1;
+        if (more && j == (nb >> 1)) phase_b(k0 + 32 + lane, ar, an, aL, ai, nxt);
       }
-      // after a wait gave up, copies already issued may still be landing
-      if (*abort_flag) {
-        for (long long q = max(0ll, issued - S); q < issued; ++q) {
-          const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&full[q % S], (uint32_t)((q / S) & 1)) &&
-                 global_ns() - t0 < 100000000ull) {
-          }
+      if (go && more) {
+        phase_c(nxt);
+        cur = nxt;
+      }
+    }
+    // after a wait gave up, copies already issued may still be landing
+    if (lane == 0 && *abort_flag) {
+      for (long long q = max(0ll, issued - S); q < issued; ++q) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&full[q % S], (uint32_t)((q / S) & 1)) &&
+               global_ns() - t0 < 100000000ull) {
         }
       }
     }
     return;
   }
 
-  // ---- consumers: warp w takes tiles w, w + 8, ... of the page's 2 H
-  // (even: K of head t / 2, odd: V)
-  uint8_t* wtile = wtiles + (size_t)warp * Dv * P * es;
+  // ---- consumers: the page's 2 H tiles (even: K of head t / 2, odd: V) are
+  // dealt round-robin over the warps, continuing from one page to the next,
+  // so every warp gets the same share of the work over a few pages
+  uint8_t* wtile = use_wtiles ? wtiles + (size_t)warp * Dv * P * es : nullptr;
+  const int T = 2 * H;
+  int first = warp;  // this warp's first tile of the current page
   long long k = 0;
   for (int it = blockIdx.x; it < total; it += gridDim.x, ++k) {
     const int stage = (int)(k % S);
@@ -973,42 +1091,37 @@ __global__ void __launch_bounds__(kStgThreads, 1)
                                                       wait_info(warp, 0, stage)));
     if (!ok) break;
     const int4 m = meta[stage];
-    const int r = m.x, nrows = m.z, slot0 = m.w;
-    const long long jp = m.y;
+    const int p = m.x, nrows = m.y, slot0 = m.z;
+    const bool fresh = (m.w & 1) != 0;
     const uint8_t* src = stages + (size_t)stage * stage_bytes;
-    const int p = a.page_table[(long long)r * a.max_pages + jp];
-    if (nrows < 0 || p < 0 || p >= d.num_pages) {  // a bad source or destination page id
-      if (warp == 0 && lane == 0) set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
-    } else {
-      const long long n = req_rows(a, r);
-      const long long L0 = a.seq_lens[r] - n;
-      const bool fresh = jp * P >= L0;  // popped by this call
-      // not through a stale mapping (see append_data_kernel)
-      if (fresh || d.tags[p] == a.exp_tags[(long long)r * a.max_pages + jp]) {
-        for (int t = warp; t < 2 * H; t += kStgWarps) {
-          const int h = t >> 1;
-          const long long tile = (long long)p * H + h;
-          if ((t & 1) == 0) {
-            const uint16_t* ks = reinterpret_cast<const uint16_t*>(src) +
-                                 (FROM_POOL ? (long long)h * P * Dk : (long long)h * Dk);
-            tile_warp(ks, FROM_POOL ? (long long)Dk : (long long)H * Dk, nrows, Dk, fp8, fresh,
-                      fp8 ? d.k_scale + tile : nullptr,
-                      static_cast<uint8_t*>(d.k_cache) + tile * P * Dk * es, false, (int)P,
-                      slot0, wtile, requant);
-          } else if constexpr (FROM_POOL) {  // the source V tile is dim-major already
-            v_tile_from_dim_major(reinterpret_cast<const uint16_t*>(src + kbytes) +
-                                      (long long)h * Dv * P,
-                                  nrows, Dv, (int)P, fp8, fp8 ? d.v_scale + tile : nullptr,
-                                  static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es);
-          } else {
-            tile_warp(reinterpret_cast<const uint16_t*>(src + kbytes) + (long long)h * Dv,
-                      (long long)H * Dv, nrows, Dv, fp8, fresh, fp8 ? d.v_scale + tile : nullptr,
-                      static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es, true, (int)P, slot0,
-                      wtile, requant);
-          }
+    int t = first;
+    if ((m.w & 2) == 0) {
+      for (; t < T; t += kStgWarps) {
+        const int h = t >> 1;
+        const long long tile = (long long)p * H + h;
+        if ((t & 1) == 0) {
+          const uint16_t* ks = reinterpret_cast<const uint16_t*>(src) +
+                               (FROM_POOL ? (long long)h * P * Dk : (long long)h * Dk);
+          tile_warp(ks, FROM_POOL ? (long long)Dk : (long long)H * Dk, nrows, Dk, fp8, fresh,
+                    fp8 ? d.k_scale + tile : nullptr,
+                    static_cast<uint8_t*>(d.k_cache) + tile * P * Dk * es, false, (int)P, slot0,
+                    wtile, requant);
+        } else if constexpr (FROM_POOL) {  // the source V tile is dim-major already
+          v_tile_from_dim_major(reinterpret_cast<const uint16_t*>(src + kbytes) +
+                                    (long long)h * Dv * P,
+                                nrows, Dv, (int)P, fp8, fp8 ? d.v_scale + tile : nullptr,
+                                static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es);
+        } else {
+          tile_warp(reinterpret_cast<const uint16_t*>(src + kbytes) + (long long)h * Dv,
+                    (long long)H * Dv, nrows, Dv, fp8, fresh, fp8 ? d.v_scale + tile : nullptr,
+                    static_cast<uint8_t*>(d.v_cache) + tile * Dv * P * es, true, (int)P, slot0,
+                    wtile, requant);
         }
       }
+    } else {
+      while (t < T) t += kStgWarps;
     }
+    first = t - T;  // where this warp's turn falls on the next page
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }

@@ -1,4 +1,5 @@
-// Exhaustive check of div_by_scale and div_fresh (quant.cuh) against CUDA's
+// Exhaustive check of div_by_scale, div_fresh and the two-value quant_word_fresh
+// (quant.cuh) against CUDA's
 // correctly rounded division: for every bf16 bit pattern x and every scale the append
 // kernels can produce (amax / 448 of a positive finite bf16 amax, and 1.0),
 // the e4m3 code of the quotient must be the same.  Test infrastructure:
@@ -27,8 +28,14 @@ __global__ void check(const float* scales, long long nscales, unsigned long long
     // div_fresh serves a block's own rows (|x| <= its amax, so |x * rs| <=
     // 448 (1 + 2^-22)); checked here on the wider |x * rs| < 1024
     bool fresh_bad = false;
-    if (kvfp8::scale_fast_ok(s) && fabsf(x * rs) < 1024.0f)
+    if (kvfp8::scale_fast_ok(s) && fabsf(x * rs) < 1024.0f) {
       fresh_bad = (kvfp8::e4m3x2(kvfp8::div_fresh(x, s, rs), 0.0f) & 0xFFu) != ref;
+      // the two-value word path on (x, -x): both codes
+      const uint32_t b = (uint32_t)(i & 0xFFFF), nb = b ^ 0x8000u;
+      const uint32_t ref_n = kvfp8::e4m3x2(__fdiv_rn(kvfp8::bf16_bits_to_f32(nb), s), 0.0f) & 0xFFu;
+      const uint32_t pair = kvfp8::quant_word_fresh(b | (nb << 16), s, rs);
+      fresh_bad = fresh_bad || (pair & 0xFFu) != ref || ((pair >> 8) & 0xFFu) != ref_n;
+    }
     if (ref != got || fresh_bad) {
       atomicAdd(bad, 1ull);
       atomicMin(first, (unsigned long long)i);
