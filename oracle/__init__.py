@@ -72,7 +72,7 @@ def _load():
             )
             lib.or_append_gqa.restype = i32
             lib.or_append_latent.argtypes = (
-                [i32, i32, i32] + [vp] * 5 + [i32, vp, vp, i32, vp, vp, i32, vp, vp, i32]
+                [i32, i32, i32, i32] + [vp] * 5 + [i32, vp, vp, i32, vp, vp, i32, vp, vp, i32]
             )
             lib.or_append_latent.restype = i32
             lib.or_verify.argtypes = [i32, i32, vp, i32, vp, vp, i32, vp, vp]
@@ -145,8 +145,8 @@ class Pool:
             self.k_scale = np.zeros((num_pages, num_kv_heads), np.float32)
             self.v_scale = np.zeros((num_pages, num_kv_heads), np.float32)
         else:
-            assert dtype == 0 and num_kv_heads == 1
-            self.k_cache = np.zeros((num_pages, page_size, dk), np.uint8)
+            assert num_kv_heads == 1
+            self.k_cache = np.zeros((num_pages, page_size, dk), edt)
             self.v_cache = None
             self.k_scale = np.zeros((num_pages,), np.float32)
             self.v_scale = None
@@ -187,7 +187,8 @@ def append(pool: Pool, k_new, v_new, new_indptr, max_new, page_table, exp_tags, 
             _p(seq_lens), _p(stop), pool.scale_mode)
     else:
         st = lib.or_append_latent(
-            pool.num_pages, pool.page_size, pool.dk, _p(pool.k_cache), _p(pool.k_scale),
+            pool.num_pages, pool.page_size, pool.dk, pool.dtype, _p(pool.k_cache),
+            _p(pool.k_scale),
             _p(pool.tags), _p(pool.free_list), _p(pool.free_head), B,
             _p(np.ascontiguousarray(k_new, np.uint16)), _p(new_indptr), int(max_new),
             _p(page_table), _p(exp_tags), page_table.shape[1], _p(seq_lens), _p(stop),
@@ -239,6 +240,7 @@ def attn(pool: Pool, q_bits, page_table, seq_lens, abort_mask, sm_scale, num_q_h
                         B, Hq, T, _p(pt), pt.shape[1], _p(sl), _p(am), _p(q_bits),
                         float(np.float32(sm_scale)), _p(out), _p(written))
     else:
+        assert pool.dtype == 0, "latent attention reads an e4m3 pool"
         lib.or_attn_latent(pool.num_pages, pool.page_size, pool.dk, pool.dv,
                            _p(pool.k_cache), _p(pool.k_scale), B, Hq, T, _p(pt), pt.shape[1],
                            _p(sl), _p(am), _p(q_bits), float(np.float32(sm_scale)), _p(out),

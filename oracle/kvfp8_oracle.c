@@ -453,9 +453,12 @@ int or_append_gqa(int num_pages, int page_size, int num_kv_heads, int Dk,
  * first Dv dims of the row double as V.  One fp32 scale per page, from the
  * amax over all Dk dims of every row this call writes into a fresh page;
  * frozen afterwards, as in or_append_gqa, which also states the rule for a
- * partly filled page re-allocated by the same call.  e4m3 only.
+ * partly filled page re-allocated by the same call.  dtype 0 (e4m3): codes
+ * as above.  dtype 1 (bf16, the prefill pool a handoff reads from): the
+ * rows' bf16 bits are stored unchanged (cache holds 2-byte elements) and no
+ * scale is used, as for the BF16 cache of or_append_gqa.
  */
-int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
+int or_append_latent(int num_pages, int page_size, int Dk, int dtype, uint8_t* cache,
                      float* scale, uint32_t* tags, const int32_t* free_list,
                      int32_t* free_head, int B, const uint16_t* kv_new,
                      const int32_t* new_indptr, int max_new,
@@ -482,6 +485,14 @@ int or_append_latent(int num_pages, int page_size, int Dk, uint8_t* cache,
       int64_t pos, d;
       float s;
       if (jp * P < L0 && fresh[p]) continue; /* partly filled, re-allocated now */
+      if (dtype == 1) {
+        for (pos = pos_lo; pos < pos_hi; ++pos) {
+          int64_t row = row0 + (pos - L0);
+          int64_t slot = pos - jp * P;
+          memcpy(cache + 2 * ((p * P + slot) * Dk), kv_new + row * Dk, 2 * (size_t)Dk);
+        }
+        continue;
+      }
       if (fresh[p]) {
         float a = 0.0f;
         for (pos = pos_lo; pos < pos_hi; ++pos) {

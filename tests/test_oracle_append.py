@@ -278,3 +278,31 @@ def test_latent_no_write_into_a_partial_page_a_later_request_pops():
     assert pool.k_scale[2] == np.float32(2.0) / np.float32(448.0)
     assert pool.k_cache[2, 0].tolist() == [0x7E, 0xF6, 0x00, 0x66]
     assert pool.k_cache[2, 1].tolist() == [0, 0, 0, 0]
+
+
+def test_latent_bf16_pool_holds_the_rows_bits():
+    """A bf16 latent pool (the prefill pool a handoff reads from) keeps every
+    row's bits in the slot its position names (page = page_table[r][pos / P],
+    slot = pos % P), across two calls, the second into partly filled pages;
+    pages no call wrote stay zero and no scale is set."""
+    rng = np.random.default_rng(17)
+    P, Dk, B = 4, 8, 3
+    pool = oracle.Pool(12, P, 1, Dk, 8, dtype=1, layout=1, free_list=rng.permutation(12))
+    pt = np.full((B, 5), -1, np.int32)
+    et = np.zeros((B, 5), np.uint32)
+    sl = np.zeros(B, np.int32)
+    rows = [[] for _ in range(B)]
+    for counts in ([5, 0, 3], [6, 2, 1]):
+        kb = rng.integers(0, 2 ** 16, (sum(counts), Dk)).astype(np.uint16)
+        ind = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        for r in range(B):
+            rows[r].extend(kb[ind[r]:ind[r + 1]])
+        st, stop = oracle.append(pool, kb, None, ind, max(counts), pt, et, sl)
+        assert (st, stop) == (0, B)
+    want = np.zeros_like(pool.k_cache)
+    for r in range(B):
+        for pos, row in enumerate(rows[r]):
+            want[pt[r, pos // P], pos % P] = row
+    assert sl.tolist() == [11, 2, 4]
+    assert np.array_equal(pool.k_cache, want)
+    assert not pool.k_scale.any()
