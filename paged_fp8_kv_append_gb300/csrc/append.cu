@@ -889,13 +889,169 @@ __host__ __device__ constexpr bool stg_wtiles(long long P, int Dv) {
   return !(P == 16 && Dv == 128);
 }
 
-// bytes of shared memory besides the stages
+// bytes of shared memory after the stages: item metadata, full / empty
+// barriers, abort flag, warp sums, item prefix
+__host__ __device__ constexpr size_t stg_ring_bytes(int B) {
+  return kStgMaxStages * 16 + 2 * kStgMaxStages * 8 + 16 + 16 * 4 + (size_t)(B + 1) * 4;
+}
+// GQA: besides the stages, also the per-warp V tiles
 __host__ __device__ constexpr size_t stg_fixed_bytes(int Dv, int P, int es, int B) {
-  return (stg_wtiles(P, Dv) ? (size_t)kStgWarps * Dv * P * es : 0)  // per-warp V tiles
-         + kStgMaxStages * 16                                        // item metadata
-         + 2 * kStgMaxStages * 8                                     // full / empty barriers
-         + 16 + 16 * 4                                               // abort flag; warp sums
-         + (size_t)(B + 1) * 4;                                      // item prefix
+  return (stg_wtiles(P, Dv) ? (size_t)kStgWarps * Dv * P * es : 0) + stg_ring_bytes(B);
+}
+
+// The producer warp of the staged bulk-append kernels: items (request, page)
+// of this CTA, each one stage -- the page's K rows (latent: its rows) and V
+// rows, copied in bulk from k_new / v_new (a handoff: the source pool's page)
+// -- with the item's metadata (destination page, rows, first slot, flags:
+// 1 fresh page, 2 skip) in meta[stage].
+template <bool FROM_POOL, bool LATENT>
+__device__ __forceinline__ void stg_produce(const AppendArgs& a, int B, int total, const int* pre,
+                                            int S, int stage_bytes, uint8_t* stages, int4* meta,
+                                            uint64_t* full, uint64_t* empty,
+                                            volatile int* abort_flag) {
+  const kv_pool_desc& d = a.d;
+  const long long P = d.page_size;
+  const int H = d.num_kv_heads, Dk = d.head_dim_k, Dv = d.head_dim_v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kbytes = (int)(P * H * Dk * 2);  // the K part of a stage
+  // The warp works out 32 items' bookkeeping at a time (one lane per item),
+  // then lane 0 issues each item's bulk copies as its stage frees up.  The bookkeeping is a chain of dependent loads (owner's
+  // lengths; then source and destination page ids; then the destination's
+  // tag), so the next batch's loads are issued while the current batch's
+  // copies go out: its lengths before the first copy, its page ids half way.
+  struct Item {
+    const uint16_t *ks, *vs;
+    uint32_t kb, vb, et;
+    int p, nrows, slot0, flags;  // flags: 1 fresh page, 2 skip
+    bool live, bad;
+  };
+  const uint64_t policy = l2_evict_first_policy();
+  const long long cnt =
+      (long long)blockIdx.x < total ? (total - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x
+                                    : 0;
+  // phase A: the item's owner and its lengths
+  auto phase_a = [&](long long kk, int& r, long long& n, long long& Lnew, long long& ind0) {
+    r = -1;
+    if (kk < cnt) {
+      r = item_owner(pre, B, (int)(blockIdx.x + kk * gridDim.x));
+      n = req_rows(a, r);
+      Lnew = a.seq_lens[r];
+      ind0 = FROM_POOL ? 0 : a.new_indptr[r];
+    }
+  };
+  // phase B: rows and source; loads of the page ids and the expected tag
+  auto phase_b = [&](long long kk, int r, long long n, long long Lnew, long long ind0, Item& m) {
+    m.live = r >= 0;
+    m.bad = false;
+    m.kb = m.vb = 0;
+    m.ks = m.vs = nullptr;
+    m.p = -1;
+    m.nrows = m.slot0 = m.flags = 0;
+    m.et = 0;
+    if (!m.live) return;
+    const int it = (int)(blockIdx.x + kk * gridDim.x);
+    const long long L0 = Lnew - n;
+    const long long jp = L0 / P + (it - pre[r]);
+    const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
+    m.nrows = (int)(pos_hi - pos_lo);
+    m.slot0 = (int)(pos_lo - jp * P);
+    if constexpr (FROM_POOL) {  // the destination request was empty: source page jp
+      const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
+      if (sp >= 0 && sp < a.src.num_pages) {
+        m.ks = static_cast<const uint16_t*>(a.src.k_cache) + (long long)sp * H * P * Dk;
+        m.kb = (uint32_t)kbytes;
+        if constexpr (!LATENT) {
+          m.vs = static_cast<const uint16_t*>(a.src.v_cache) + (long long)sp * H * Dv * P;
+          m.vb = (uint32_t)(P * H * Dv * 2);
+        }
+      } else {
+        m.bad = true;
+      }
+    } else {
+      const long long row0 = ind0 + (pos_lo - L0);
+      m.ks = a.k_new + row0 * H * Dk;
+      m.kb = (uint32_t)(m.nrows * H * Dk * 2);
+      if constexpr (!LATENT) {
+        m.vs = a.v_new + row0 * H * Dv;
+        m.vb = (uint32_t)(m.nrows * H * Dv * 2);
+      }
+    }
+    m.p = a.page_table[(long long)r * a.max_pages + jp];
+    m.flags = jp * P >= L0 ? 1 : 0;  // popped by this call
+    if (m.flags == 0) m.et = a.exp_tags[(long long)r * a.max_pages + jp];
+  };
+  // phase C: checks on the destination page
+  auto phase_c = [&](Item& m) {
+    if (!m.live) return;
+    if (m.bad || m.p < 0 || m.p >= d.num_pages) {
+      set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
+      m.flags = 2;
+    } else if (m.flags == 0 && d.tags[m.p] != m.et) {
+      m.flags = 2;  // not through a stale mapping (see append_data_kernel)
+    }
+    if (m.flags & 2) m.kb = m.vb = 0;  // nothing to read for an item that is skipped
+  };
+  int ar = -1;
+  long long an = 0, aL = 0, ai = 0;
+  Item cur, nxt;
+  phase_a(lane, ar, an, aL, ai);
+  phase_b(lane, ar, an, aL, ai, cur);
+  phase_c(cur);
+  long long issued = 0;
+  bool go = true;
+  for (long long k0 = 0; go && k0 < cnt; k0 += 32) {
+    const int nb = (int)min(32ll, cnt - k0);
+    const bool more = k0 + 32 < cnt;
+    if (more) phase_a(k0 + 32 + lane, ar, an, aL, ai);
+    for (int j = 0; j < nb; ++j) {
+      const long long k = k0 + j;
+      const int stage = (int)(k % S);
+      bool ok = true;
+      if (lane == 0 && k >= S)
+        ok = mbar_wait(&empty[stage], (uint32_t)(((k / S) - 1) & 1), abort_flag, d.ctl,
+                       wait_info(warp, 1, stage));
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+        go = false;
+        break;
+      }
+      const int jp_ = __shfl_sync(0xffffffffu, cur.p, j);
+      const int jn = __shfl_sync(0xffffffffu, cur.nrows, j);
+      const int js = __shfl_sync(0xffffffffu, cur.slot0, j);
+      const int jf = __shfl_sync(0xffffffffu, cur.flags, j);
+      const uint32_t jkb = __shfl_sync(0xffffffffu, cur.kb, j);
+      const uint32_t jvb = __shfl_sync(0xffffffffu, cur.vb, j);
+      const uint16_t* jks = reinterpret_cast<const uint16_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.ks), j));
+      const uint16_t* jvs = reinterpret_cast<const uint16_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.vs), j));
+      if (lane == 0) {
+        meta[stage] = make_int4(jp_, jn, js, jf);
+        uint8_t* dst = stages + (size_t)stage * stage_bytes;
+        if (jkb + jvb > 0) {
+          mbar_arrive_expect_tx(&full[stage], jkb + jvb);
+          bulk_g2s(dst, jks, jkb, &full[stage], policy);
+          if (jvb > 0) bulk_g2s(dst + kbytes, jvs, jvb, &full[stage], policy);
+        } else {
+          mbar_arrive(&full[stage]);
+        }
+      }
+      issued = k + 1;
+      if (more && j == (nb >> 1)) phase_b(k0 + 32 + lane, ar, an, aL, ai, nxt);
+    }
+    if (go && more) {
+      phase_c(nxt);
+      cur = nxt;
+    }
+  }
+  // after a wait gave up, copies already issued may still be landing
+  if (lane == 0 && *abort_flag) {
+    for (long long q = max(0ll, issued - S); q < issued; ++q) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&full[q % S], (uint32_t)((q / S) & 1)) &&
+             global_ns() - t0 < 100000000ull) {
+      }
+    }
+  }
 }
 
 template <bool FROM_POOL>
@@ -939,141 +1095,8 @@ __global__ void __launch_bounds__(kStgThreads, 1)
   const int kbytes = (int)(P * H * Dk * 2);  // the K part of a stage
 
   if (warp == kStgWarps) {
-    // ---- producer: the warp works out 32 items' bookkeeping at a time (one
-    // lane per item), then lane 0 issues each item's two bulk copies as its
-    // stage frees up.  The bookkeeping is a chain of dependent loads (owner's
-    // lengths; then source and destination page ids; then the destination's
-    // tag), so the next batch's loads are issued while the current batch's
-    // copies go out: its lengths before the first copy, its page ids half way.
-    struct Item {
-      const uint16_t *ks, *vs;
-      uint32_t kb, vb, et;
-      int p, nrows, slot0, flags;  // flags: 1 fresh page, 2 skip
-      bool live, bad;
-    };
-    const uint64_t policy = l2_evict_first_policy();
-    const long long cnt =
-        (long long)blockIdx.x < total ? (total - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x
-                                      : 0;
-    // phase A: the item's owner and its lengths
-    auto phase_a = [&](long long kk, int& r, long long& n, long long& Lnew, long long& ind0) {
-      r = -1;
-      if (kk < cnt) {
-        r = item_owner(pre, B, (int)(blockIdx.x + kk * gridDim.x));
-        n = req_rows(a, r);
-        Lnew = a.seq_lens[r];
-        ind0 = FROM_POOL ? 0 : a.new_indptr[r];
-      }
-    };
-    // phase B: rows and source; loads of the page ids and the expected tag
-    auto phase_b = [&](long long kk, int r, long long n, long long Lnew, long long ind0, Item& m) {
-      m.live = r >= 0;
-      m.bad = false;
-      m.kb = m.vb = 0;
-      m.ks = m.vs = nullptr;
-      m.p = -1;
-      m.nrows = m.slot0 = m.flags = 0;
-      m.et = 0;
-      if (!m.live) return;
-      const int it = (int)(blockIdx.x + kk * gridDim.x);
-      const long long L0 = Lnew - n;
-      const long long jp = L0 / P + (it - pre[r]);
-      const long long pos_lo = max(jp * P, L0), pos_hi = min((jp + 1) * P, Lnew);
-      m.nrows = (int)(pos_hi - pos_lo);
-      m.slot0 = (int)(pos_lo - jp * P);
-      if constexpr (FROM_POOL) {  // the destination request was empty: source page jp
-        const int sp = a.src_page_table[(long long)r * a.src_max_pages + jp];
-        if (sp >= 0 && sp < a.src.num_pages) {
-          m.ks = static_cast<const uint16_t*>(a.src.k_cache) + (long long)sp * H * P * Dk;
-          m.vs = static_cast<const uint16_t*>(a.src.v_cache) + (long long)sp * H * Dv * P;
-          m.kb = (uint32_t)kbytes;
-          m.vb = (uint32_t)(P * H * Dv * 2);
-        } else {
-          m.bad = true;
-        }
-      } else {
-        const long long row0 = ind0 + (pos_lo - L0);
-        m.ks = a.k_new + row0 * H * Dk;
-        m.vs = a.v_new + row0 * H * Dv;
-        m.kb = (uint32_t)(m.nrows * H * Dk * 2);
-        m.vb = (uint32_t)(m.nrows * H * Dv * 2);
-      }
-      m.p = a.page_table[(long long)r * a.max_pages + jp];
-      m.flags = jp * P >= L0 ? 1 : 0;  // popped by this call
-      if (m.flags == 0) m.et = a.exp_tags[(long long)r * a.max_pages + jp];
-    };
-    // phase C: checks on the destination page
-    auto phase_c = [&](Item& m) {
-      if (!m.live) return;
-      if (m.bad || m.p < 0 || m.p >= d.num_pages) {
-        set_error(d.ctl, KV_ERR_BAD_PAGE_ID);
-        m.flags = 2;
-      } else if (m.flags == 0 && d.tags[m.p] != m.et) {
-        m.flags = 2;  // not through a stale mapping (see append_data_kernel)
-      }
-      if (m.flags & 2) m.kb = m.vb = 0;  // nothing to read for an item that is skipped
-    };
-    int ar = -1;
-    long long an = 0, aL = 0, ai = 0;
-    Item cur, nxt;
-    phase_a(lane, ar, an, aL, ai);
-    phase_b(lane, ar, an, aL, ai, cur);
-    phase_c(cur);
-    long long issued = 0;
-    bool go = true;
-    for (long long k0 = 0; go && k0 < cnt; k0 += 32) {
-      const int nb = (int)min(32ll, cnt - k0);
-      const bool more = k0 + 32 < cnt;
-      if (more) phase_a(k0 + 32 + lane, ar, an, aL, ai);
-      for (int j = 0; j < nb; ++j) {
-        const long long k = k0 + j;
-        const int stage = (int)(k % S);
-        bool ok = true;
-        if (lane == 0 && k >= S)
-          ok = mbar_wait(&empty[stage], (uint32_t)(((k / S) - 1) & 1), abort_flag, d.ctl,
-                         wait_info(warp, 1, stage));
-        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
-          go = false;
-          break;
-        }
-        const int jp_ = __shfl_sync(0xffffffffu, cur.p, j);
-        const int jn = __shfl_sync(0xffffffffu, cur.nrows, j);
-        const int js = __shfl_sync(0xffffffffu, cur.slot0, j);
-        const int jf = __shfl_sync(0xffffffffu, cur.flags, j);
-        const uint32_t jkb = __shfl_sync(0xffffffffu, cur.kb, j);
-        const uint32_t jvb = __shfl_sync(0xffffffffu, cur.vb, j);
-        const uint16_t* jks = reinterpret_cast<const uint16_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.ks), j));
-        const uint16_t* jvs = reinterpret_cast<const uint16_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(cur.vs), j));
-        if (lane == 0) {
-          meta[stage] = make_int4(jp_, jn, js, jf);
-          uint8_t* dst = stages + (size_t)stage * stage_bytes;
-          if (jkb + jvb > 0) {
-            mbar_arrive_expect_tx(&full[stage], jkb + jvb);
-            bulk_g2s(dst, jks, jkb, &full[stage], policy);
-            bulk_g2s(dst + kbytes, jvs, jvb, &full[stage], policy);
-          } else {
-            mbar_arrive(&full[stage]);
-          }
-        }
-        issued = k + 1;
-        if (more && j == (nb >> 1)) phase_b(k0 + 32 + lane, ar, an, aL, ai, nxt);
-      }
-      if (go && more) {
-        phase_c(nxt);
-        cur = nxt;
-      }
-    }
-    // after a wait gave up, copies already issued may still be landing
-    if (lane == 0 && *abort_flag) {
-      for (long long q = max(0ll, issued - S); q < issued; ++q) {
-        const uint64_t t0 = global_ns();
-        while (!mbar_try_wait(&full[q % S], (uint32_t)((q / S) & 1)) &&
-               global_ns() - t0 < 100000000ull) {
-        }
-      }
-    }
+    stg_produce<FROM_POOL, false>(a, B, total, pre, S, stage_bytes, stages, meta, full, empty,
+                                  abort_flag);
     return;
   }
 
@@ -1122,6 +1145,179 @@ __global__ void __launch_bounds__(kStgThreads, 1)
       while (t < T) t += kStgWarps;
     }
     first = t - T;  // where this warp's turn falls on the next page
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+  }
+}
+
+// The latent layout's staged kernel: one stage per page (its rows, one row of
+// head_dim_k values per token, contiguous in k_new or in the source pool), and
+// the 12 consumer warps share each page: thread t holds 16-byte chunks
+// t, t + 384, ... of the page's rows, the page's amax is reduced over the 12
+// warps, and every thread quantises and stores its chunks -- consecutive
+// threads, consecutive chunks.  The consumers meet on an mbarrier (bounded
+// waits, so a consumer that gave up cannot leave the others waiting), and the
+// reduction words alternate between two rows by meeting number: a row is
+// rewritten two meetings later, after every warp has read it.
+constexpr int kLatStgThreads = kStgWarps * 32;
+constexpr int kLatStgChunks = 12;  // per thread: 64 rows x 72 chunks / 384
+
+// meeting number n of the consumer warps; false when a wait gave up
+__device__ __forceinline__ bool lat_meet(uint64_t* cbar, uint32_t& n, volatile int* abort_flag,
+                                         int32_t* ctl) {
+  const int warp = threadIdx.x >> 5;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(cbar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(cbar, n & 1u, abort_flag, ctl,
+                                                    wait_info(warp, 0, 63)));
+  ++n;
+  return ok;
+}
+
+// largest magnitude of the page's rows over the consumer warps (bit-pattern
+// maximum; a NaN falls back to the float maximum, which skips it); false when
+// a meeting gave up
+__device__ bool lat_stg_amax(const uint4 (&v)[kLatStgChunks], uint32_t (*red)[kStgWarps],
+                             uint64_t* cbar, uint32_t& n, volatile int* abort_flag, int32_t* ctl,
+                             float& amax) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t mb = 0;
+#pragma unroll
+  for (int t = 0; t < kLatStgChunks; ++t) mb = absbits_max8(mb, v[t]);
+  mb = absbits_warp_max(mb);
+  uint32_t* row = red[n & 1u];
+  if (lane == 0) row[warp] = mb;
+  if (!lat_meet(cbar, n, abort_flag, ctl)) return false;
+  mb = __reduce_max_sync(0xffffffffu, lane < kStgWarps ? row[lane] : 0u);
+  amax = __uint_as_float(mb << 16);
+  if (mb > 0x7F80u) {  // a NaN (uniform): the float maximum over the same chunks
+    float m = 0.0f;
+#pragma unroll
+    for (int t = 0; t < kLatStgChunks; ++t) m = fmaxf(m, amax8(v[t]));
+    m = warp_max(m);
+    float* frow = reinterpret_cast<float*>(red[n & 1u]);
+    if (lane == 0) frow[warp] = m;
+    if (!lat_meet(cbar, n, abort_flag, ctl)) return false;
+    amax = warp_max(lane < kStgWarps ? frow[lane] : 0.0f);
+  }
+  return true;
+}
+
+template <bool FROM_POOL>
+__global__ void __launch_bounds__(kStgThreads, 1)
+    append_latent_staged_kernel(AppendArgs a, int S, int stage_bytes) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t red[2][kStgWarps];
+  __shared__ __align__(8) uint64_t cbar;  // the consumers' meetings
+  const kv_pool_desc& d = a.d;
+  const long long P = d.page_size;
+  const int Dk = d.head_dim_k;
+  const bool fp8 = d.dtype == KV_DTYPE_E4M3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* stages = smem;
+  int4* meta = reinterpret_cast<int4*>(stages + (size_t)S * stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStgMaxStages);
+  uint64_t* empty = full + kStgMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStgMaxStages);
+  int* wsum = reinterpret_cast<int*>(empty + kStgMaxStages) + 4;
+  int* pre = wsum + 16;
+  const int B = min(a.B, (int)d.ctl[KV_CTL_APPEND_STOP]);
+  if (S < 2 || S > kStgMaxStages || P * Dk > 8LL * kLatStgThreads * kLatStgChunks) {
+    if (threadIdx.x == 0) set_error(d.ctl, KV_ERR_INTERNAL);  // the host chose a bad ring
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < S; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kStgWarps);
+    }
+    mbar_init(&cbar, kStgWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const int total = B > 0 ? bulk_items_prefix(a, B, 1, pre, wsum) : 0;
+  __syncthreads();
+  if (warp == kStgWarps) {
+    stg_produce<FROM_POOL, true>(a, B, total, pre, S, stage_bytes, stages, meta, full, empty,
+                                 abort_flag);
+    return;
+  }
+
+  // ---- consumers
+  const int tid = threadIdx.x;
+  uint32_t meets = 0;
+  long long k = 0;
+  for (int it = blockIdx.x; it < total; it += gridDim.x, ++k) {
+    const int stage = (int)(k % S);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (uint32_t)((k / S) & 1),
+                                                      abort_flag, d.ctl,
+                                                      wait_info(warp, 0, stage)));
+    if (!ok) return;
+    const int4 m = meta[stage];
+    const int p = m.x, nrows = m.y, slot0 = m.z;
+    if ((m.w & 2) == 0) {
+      const bool fresh = (m.w & 1) != 0;
+      const int nch = nrows * (Dk / 8);  // 16-byte chunks of this call's rows
+      const uint4* src = reinterpret_cast<const uint4*>(stages + (size_t)stage * stage_bytes);
+      uint4 v[kLatStgChunks];
+#pragma unroll
+      for (int t = 0; t < kLatStgChunks; ++t) {
+        const int c = tid + kLatStgThreads * t;
+        v[t] = c < nch ? src[c] : make_uint4(0, 0, 0, 0);
+      }
+      const long long row_base = (long long)p * P + slot0;  // destination row of chunk row 0
+      if (!fp8) {  // a bf16 latent pool: the rows' bits
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(d.k_cache) + row_base * Dk);
+#pragma unroll
+        for (int t = 0; t < kLatStgChunks; ++t) {
+          const int c = tid + kLatStgThreads * t;
+          if (c < nch) dst[c] = v[t];
+        }
+      } else {
+        float s, amax;
+        bool own_rows = false;  // the scale is the amax of exactly these rows
+        if (fresh) {
+          if (!lat_stg_amax(v, red, &cbar, meets, abort_flag, d.ctl, amax)) return;
+          s = scale_from_amax(amax);
+          if (tid == 0) d.k_scale[p] = s;
+          own_rows = true;
+        } else {
+          s = d.k_scale[p];
+          if (d.scale_mode == KV_SCALE_REQUANTIZE) {  // re-encode the rows already written
+            // (every thread has read the old scale before the reduction's meeting)
+            if (!lat_stg_amax(v, red, &cbar, meets, abort_flag, d.ctl, amax)) return;
+            const float s_new = scale_from_amax(amax);
+            if (s_new > s) {
+              requant_block(static_cast<uint8_t*>(d.k_cache) + (long long)p * P * Dk, slot0, Dk,
+                            false, (int)P, s, s_new, tid, kLatStgThreads);
+              if (tid == 0) d.k_scale[p] = s_new;
+              s = s_new;
+              own_rows = true;
+            }
+          }
+        }
+        const float rs = __frcp_rn(s);
+        uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(d.k_cache) + row_base * Dk);
+        if (own_rows && scale_fast_ok(s)) {  // uniform across the consumers
+#pragma unroll
+          for (int t = 0; t < kLatStgChunks; ++t) {
+            const int c = tid + kLatStgThreads * t;
+            if (c < nch)
+              dst[c] = make_uint2(
+                  quant_word_fresh(v[t].x, s, rs) | (quant_word_fresh(v[t].y, s, rs) << 16),
+                  quant_word_fresh(v[t].z, s, rs) | (quant_word_fresh(v[t].w, s, rs) << 16));
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < kLatStgChunks; ++t) {
+            const int c = tid + kLatStgThreads * t;
+            if (c < nch) dst[c] = quant8_rs(v[t], s, rs);
+          }
+        }
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -1357,6 +1553,27 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
                                  dim3(kTileWarps * 32), smem, s, a);
     if (e == cudaSuccess) ++*launches;
     return e;
+  }
+  if (persist && a.d.layout == KV_LAYOUT_LATENT && latent_page_fits(a.d) && a.B <= kStgMaxB &&
+      Pl * a.d.head_dim_k <= 8LL * kLatStgThreads * kLatStgChunks) {
+    // the staged kernel: one page's rows per stage, 2..4 stages
+    const long long stage = (Pl * a.d.head_dim_k * 2 + 127) / 128 * 128;
+    const long long room = 227LL * 1024 - (long long)stg_ring_bytes(a.B);
+    const int S = (int)min((long long)kStgMaxStages, room > 0 ? room / stage : 0);
+    if (S >= 2) {
+      const size_t smem = (size_t)S * stage + stg_ring_bytes(a.B);
+      e = a.from_pool ? cudaFuncSetAttribute(append_latent_staged_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                      : cudaFuncSetAttribute(append_latent_staged_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      e = a.from_pool ? launch_pdl(append_latent_staged_kernel<true>, dim3((unsigned)sms),
+                                   dim3(kStgThreads), smem, s, a, S, (int)stage)
+                      : launch_pdl(append_latent_staged_kernel<false>, dim3((unsigned)sms),
+                                   dim3(kStgThreads), smem, s, a, S, (int)stage);
+      if (e == cudaSuccess) ++*launches;
+      return e;
+    }
   }
   if (persist && a.d.layout == KV_LAYOUT_LATENT && latent_page_fits(a.d)) {
     const bool k72 = a.d.head_dim_k == 576;

@@ -1,18 +1,20 @@
-"""GPU parity of the bulk append's staged kernel over page shapes.
+"""GPU parity of the bulk append's staged kernels over page shapes.
 
 A bulk append (at least two pages' worth of rows per call, at most 4096
 requests) runs one CTA per SM: a producer warp bulk-copies each page's K rows
-and V rows into shared-memory slots and consumer warps quantise or copy the
-page's tiles from there ("Smaller, faster, safer: running Kimi and GLM at
+and V rows (latent layout: its rows) into shared-memory stages and consumer
+warps quantise or copy the page from there ("Smaller, faster, safer: running Kimi and GLM at
 scale", section "Quantizing the KV cache": the cache is written as FP8
 e4m3, or kept as BF16).  Two calls per case: the first fills every request
 from empty (fresh pages, ragged last pages), the second appends into the
 partly filled last pages (the page's existing scale, its tag checked) and
 pops new ones.  After each call the whole pool -- codes or bf16 bits,
 scales, tags, page tables, expected tags, lengths, free-list head -- must
-equal the oracle's bit for bit.  Shapes: the 16-row, 128-wide pages (whose
-partly filled V tiles are written element by element) and others (which
-assemble them in a per-warp shared tile), and K and V of different widths."""
+equal the oracle's bit for bit.  GQA shapes: the 16-row, 128-wide pages
+(whose partly filled V tiles are written element by element) and others
+(which assemble them in a per-warp shared tile), and K and V of different
+widths.  Latent shapes: the 64-row, 576-wide pages (12 chunks per consumer
+thread, every one used) and smaller ones."""
 import numpy as np
 import pytest
 import torch
@@ -32,13 +34,45 @@ SHAPES = [  # page size, kv heads, K width, V width
 ]
 
 
+LATENT_SHAPES = [  # page size, K width (the row), V width (its leading part)
+    (64, 576, 512),
+    (32, 256, 256),
+    (16, 64, 64),
+]
+
+
 def _rows(g, n, H, D, mags):
-    """bf16 rows [n][H][D]; each row drawn at one of a few magnitudes, so that
-    pages get different scales."""
-    x = torch.randn((n, H, D), generator=g, device="cuda")
-    m = torch.tensor(mags, device="cuda")[torch.randint(0, len(mags), (n, 1, 1), generator=g,
-                                                       device="cuda")]
-    return (x * m).to(torch.bfloat16)
+    """bf16 rows [n][H][D] ([n][D] when H is None); each row drawn at one of a
+    few magnitudes, so that pages get different scales."""
+    shape = (n, D) if H is None else (n, H, D)
+    x = torch.randn(shape, generator=g, device="cuda")
+    pick = torch.randint(0, len(mags), (n,) + (1,) * (len(shape) - 1), generator=g,
+                         device="cuda")
+    return (x * torch.tensor(mags, device="cuda")[pick]).to(torch.bfloat16)
+
+
+def _counts(rng, P, B):
+    first = rng.integers(2 * P, 9 * P, B)
+    first[rng.choice(B, 4, replace=False)] = 0                 # no rows in the first call
+    exact = rng.choice(np.flatnonzero(first), 5, replace=False)
+    first[exact] = (first[exact] // P) * P                     # whole last pages
+    second = rng.integers(2 * P, 5 * P, B)
+    second[rng.choice(B, 3, replace=False)] = 0
+    return first, second
+
+
+def _two_calls(b, first, second, mode, rows):
+    B = b.w.B
+    # in requantising mode the second call's rows are larger, so the partly
+    # filled pages take a larger scale and their old codes are re-encoded
+    for counts, mags in ((first, [0.25, 1.0, 8.0]), (second, [0.5, 4.0, 64.0] if mode else
+                                                      [0.25, 1.0, 8.0])):
+        ks, vs = rows(counts, mags)
+        st, stop = b.append(ks, vs, counts)
+        assert (st, stop) == (0, B)
+        torch.cuda.synchronize()
+        assert b.dev.error() == 0
+        b.assert_state_equal()
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -47,26 +81,34 @@ def test_staged_bulk_append_two_calls(shape, dtype, mode):
     P, H, Dk, Dv = shape
     rng = np.random.default_rng(P * 100003 + H * 1009 + Dk * 31 + Dv * 7 + dtype * 3 + mode)
     B = 37
-    first = rng.integers(2 * P, 9 * P, B)
-    first[rng.choice(B, 4, replace=False)] = 0                 # no rows in the first call
-    exact = rng.choice(np.flatnonzero(first), 5, replace=False)
-    first[exact] = (first[exact] // P) * P                     # whole last pages
-    second = rng.integers(2 * P, 5 * P, B)
-    second[rng.choice(B, 3, replace=False)] = 0
+    first, second = _counts(rng, P, B)
     total = first + second
     need = int((-(-total // P)).sum()) + 8
     w = wl.Workload("staged", 8100 + P + H, total.astype(np.int32), H, H, Dk, Dv, P, 1, 0,
                     need, float(np.float32(1 / np.sqrt(Dk))))
     b = Both(w, dtype, scale_mode=mode)
     g = torch.Generator(device="cuda").manual_seed(int(rng.integers(0, 2 ** 31)))
-    # in requantising mode the second call's rows are larger, so the partly
-    # filled pages take a larger scale and their old codes are re-encoded
-    for counts, mags in ((first, [0.25, 1.0, 8.0]), (second, [0.5, 4.0, 64.0] if mode else
-                                                      [0.25, 1.0, 8.0])):
-        ks = [_rows(g, int(c), H, Dk, mags) for c in counts]
-        vs = [_rows(g, int(c), H, Dv, mags) for c in counts]
-        st, stop = b.append(ks, vs, counts)
-        assert (st, stop) == (0, B)
-        torch.cuda.synchronize()
-        assert b.dev.error() == 0
-        b.assert_state_equal()
+    _two_calls(b, first, second, mode,
+               lambda counts, mags: ([_rows(g, int(c), H, Dk, mags) for c in counts],
+                                     [_rows(g, int(c), H, Dv, mags) for c in counts]))
+
+
+@pytest.mark.parametrize("shape", LATENT_SHAPES)
+@pytest.mark.parametrize("dtype,mode", [(0, 0), (1, 0), (0, 1)])
+def test_staged_latent_bulk_append_two_calls(shape, dtype, mode):
+    P, Dk, Dv = shape
+    rng = np.random.default_rng(P * 7919 + Dk * 13 + dtype * 3 + mode)
+    B = 29
+    first, second = _counts(rng, P, B)
+    total = first + second
+    need = int((-(-total // P)).sum()) + 8
+    w = wl.Workload("staged_lat", 8200 + P, total.astype(np.int32), 16, 1, Dk, Dv, P, 1, 1,
+                    need, float(np.float32(1 / np.sqrt(Dk))))
+    b = Both(w, dtype, scale_mode=mode)
+    g = torch.Generator(device="cuda").manual_seed(int(rng.integers(0, 2 ** 31)))
+
+    def rows(counts, mags):
+        ks = [_rows(g, int(c), None, Dk, mags) for c in counts]
+        return ks, ks
+
+    _two_calls(b, first, second, mode, rows)
