@@ -50,11 +50,11 @@ NOMINAL_HBM_GBS = 8000.0
 # (sha256 of the listed files, first 16 hex digits); otherwise the line
 # reports traffic null.
 SPLIT_DRAM = {"sources": ["decode_gqa.cu", "decode_plan.cuh", "common.cuh"],
-              "sha": "08dd09f15aac0fd0",
-              # 8 requests of 131,075 tokens: 2.152534 GB read (as ncu prints it)
-              # for 2,152,120,864 algorithmic bytes; 3.031296 MB written by
+              "sha": "ebc51633c8807473",
+              # 8 requests of 131,075 tokens: 2,152,513,536 bytes read (as ncu prints
+              # them) for 2,152,120,864 algorithmic bytes; 3,049,728 bytes written by
               # 8 * 2 + 152 pieces
-              "read_per_alg_byte": 2.152534e9 / 2152120864, "write_per_piece": 3.031296e6 / 168}
+              "read_per_alg_byte": 2152513536 / 2152120864, "write_per_piece": 3049728 / 168}
 
 
 # ------------------------------------------------------------ distributed
@@ -1277,6 +1277,10 @@ def main():
                     help="run only the bulk (prefill handoff) append of B requests of the GQA "
                          "batch workload into an e4m3 pool and print its line (small "
                          "profiling captures)")
+    ap.add_argument("--bulk-latent-only", type=int, default=0, metavar="B",
+                    help="run only the bulk append of B requests of the latent verify "
+                         "workload into an e4m3 pool and print its line (small profiling "
+                         "captures)")
     ap.add_argument("--wide-only", type=int, default=0, metavar="B",
                     help="run only the 96 q / 8 kv head step on B requests of the GQA batch "
                          "workload and print its line (small profiling captures)")
@@ -1312,6 +1316,13 @@ def main():
     if args.bulk_only > 0:
         device = torch.device("cuda", local)
         w = wl.subset(wl.gqa_batch(), args.bulk_only)
+        for _ in range(args.warmup):
+            bulk_append_line(w, 0, device, peak)
+        print(json.dumps([bulk_append_line(w, 0, device, peak) for _ in range(args.steps)]))
+        return
+    if args.bulk_latent_only > 0:
+        device = torch.device("cuda", local)
+        w = wl.subset(wl.latent_verify(), args.bulk_latent_only)
         for _ in range(args.warmup):
             bulk_append_line(w, 0, device, peak)
         print(json.dumps([bulk_append_line(w, 0, device, peak) for _ in range(args.steps)]))
