@@ -405,16 +405,22 @@ kv_status paged_decode_attn(kv_pool* pool, void* stream, int32_t B, int32_t num_
                             const uint8_t* abort_mask, float sm_scale, void* out,
                             void* workspace, size_t workspace_bytes) {
   if (!pool) return KV_ERR_INVALID_ARG;
+  pool->last_launches = 0;
   if (B > 0 && !out) return KV_ERR_INVALID_ARG;
-  kv_status st = paged_decode_attn_split(pool, stream, B, num_q_heads, q_tokens, q, page_table,
-                                         max_pages_per_req, seq_lens, abort_mask, sm_scale,
-                                         workspace, workspace_bytes);
-  if (st != KV_OK) return st;
-  const int n = pool->last_launches;
-  st = paged_decode_attn_combine(pool, stream, B, num_q_heads, q_tokens, abort_mask, out,
-                                 workspace, workspace_bytes);
-  pool->last_launches += n;
-  return st;
+  // one argument set (and one validation) for the plan, the split and the combine
+  DecodeArgs a;
+  int kind = 0;
+  const kv_status st =
+      decode_prepare(pool, B, num_q_heads, q_tokens, q, page_table, max_pages_per_req, seq_lens,
+                     abort_mask, sm_scale, out, workspace, workspace_bytes, true, true, &a, &kind);
+  if (st != KV_OK || B == 0) return st;
+  int n = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = a.self_plan ? cudaSuccess : launch_decode_plan(a, s, &n);
+  if (e == cudaSuccess) e = launch_decode_split(a, kind, s, &n);
+  if (e == cudaSuccess) e = launch_decode_combine(a, s, &n);
+  pool->last_launches = n;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 kv_status paged_decode_attn_checked(kv_pool* pool, void* stream, int32_t B, int32_t num_q_heads,
