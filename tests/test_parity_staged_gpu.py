@@ -19,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from pathrun import Both
 
@@ -112,3 +113,53 @@ def test_staged_latent_bulk_append_two_calls(shape, dtype, mode):
         return ks, ks
 
     _two_calls(b, first, second, mode, rows)
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_staged_and_register_kernels_agree_at_the_batch_limit(layout):
+    """4096 requests take the staged kernels, 4097 the register-resident
+    ones: the same rows appended from empty (the 4097th request empty) leave
+    the same pool bit for bit, and both equal the oracle."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    rng = np.random.default_rng(9100 + layout)
+    B = 4096
+    if layout == 0:
+        P, H, Dk, Dv = 16, 1, 128, 128
+    else:
+        P, H, Dk, Dv = 64, 1, 64, 64
+    counts = rng.integers(2 * P, 3 * P + 5, B)
+    counts[rng.choice(B, 64, replace=False)] = 0
+    need = int((-(-counts // P)).sum()) + 8
+    g = torch.Generator(device="cuda").manual_seed(9100 + layout)
+    n = int(counts.sum())
+    if layout == 0:
+        k = _rows(g, n, H, Dk, [0.25, 1.0, 8.0])
+        v = _rows(g, n, H, Dv, [0.25, 1.0, 8.0])
+    else:
+        k = _rows(g, n, None, Dk, [0.25, 1.0, 8.0])
+        v = None
+    pools = []
+    for Bc in (B, B + 1):
+        cnt = np.concatenate([counts, np.zeros(Bc - B, np.int64)])
+        w = wl.Workload("limit", 9100, cnt.astype(np.int32), H, H, Dk, Dv, P, 1, layout, need,
+                        float(np.float32(1 / np.sqrt(Dk))))
+        b = Both(w, 0)
+        ind = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        b.dev.append(Bc, k, v, torch.from_numpy(ind).cuda(), int(cnt.max()), b.pt_d, b.et_d,
+                     b.sl_d)
+        torch.cuda.synchronize()
+        assert b.dev.error() == 0
+        pools.append(b)
+    a, c = pools
+    assert torch.equal(a.dev.k_cache, c.dev.k_cache) and torch.equal(a.dev.k_scale, c.dev.k_scale)
+    if layout == 0:
+        assert torch.equal(a.dev.v_cache, c.dev.v_cache)
+        assert torch.equal(a.dev.v_scale, c.dev.v_scale)
+    assert torch.equal(a.pt_d, c.pt_d[:B]) and torch.equal(a.sl_d, c.sl_d[:B])
+    # and the staged result is the oracle's
+    ind = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    st, stop = oracle.append(a.ref, wl.bits_u16(k), None if v is None else wl.bits_u16(v), ind,
+                             int(counts.max()), a.pt_h, a.et_h, a.sl_h)
+    assert (st, stop) == (0, B)
+    a.assert_state_equal()
