@@ -1277,6 +1277,8 @@ def main():
                     help="run only the bulk (prefill handoff) append of B requests of the GQA "
                          "batch workload into an e4m3 pool and print its line (small "
                          "profiling captures)")
+    ap.add_argument("--bulk-dtype", type=int, default=0, choices=[0, 1],
+                    help="pool dtype of --bulk-only (0 e4m3, 1 bf16)")
     ap.add_argument("--bulk-latent-only", type=int, default=0, metavar="B",
                     help="run only the bulk append of B requests of the latent verify "
                          "workload into an e4m3 pool and print its line (small profiling "
@@ -1317,8 +1319,9 @@ def main():
         device = torch.device("cuda", local)
         w = wl.subset(wl.gqa_batch(), args.bulk_only)
         for _ in range(args.warmup):
-            bulk_append_line(w, 0, device, peak)
-        print(json.dumps([bulk_append_line(w, 0, device, peak) for _ in range(args.steps)]))
+            bulk_append_line(w, args.bulk_dtype, device, peak)
+        print(json.dumps([bulk_append_line(w, args.bulk_dtype, device, peak)
+                          for _ in range(args.steps)]))
         return
     if args.bulk_latent_only > 0:
         device = torch.device("cuda", local)
