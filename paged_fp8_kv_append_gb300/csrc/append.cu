@@ -915,10 +915,11 @@ __device__ __forceinline__ void stg_produce(const AppendArgs& a, int B, int tota
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kbytes = (int)(P * H * Dk * 2);  // the K part of a stage
   // The warp works out 32 items' bookkeeping at a time (one lane per item),
-  // then lane 0 issues each item's bulk copies as its stage frees up.  The bookkeeping is a chain of dependent loads (owner's
-  // lengths; then source and destination page ids; then the destination's
-  // tag), so the next batch's loads are issued while the current batch's
-  // copies go out: its lengths before the first copy, its page ids half way.
+  // then lane 0 issues each item's bulk copies as its stage frees up.  The
+  // bookkeeping is a chain of dependent loads (owner's lengths; then source
+  // and destination page ids; then the destination's tag), so the next
+  // batch's loads are issued while the current batch's copies go out: its
+  // lengths before the first copy, its page ids half way.
   struct Item {
     const uint16_t *ks, *vs;
     uint32_t kb, vb, et;
@@ -1558,7 +1559,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int* launches) {
       Pl * a.d.head_dim_k <= 8LL * kLatStgThreads * kLatStgChunks) {
     // the staged kernel: one page's rows per stage, 2..4 stages
     const long long stage = (Pl * a.d.head_dim_k * 2 + 127) / 128 * 128;
-    const long long room = 227LL * 1024 - (long long)stg_ring_bytes(a.B);
+    // (256 bytes left for the kernel's static shared memory)
+    const long long room = 227LL * 1024 - 256 - (long long)stg_ring_bytes(a.B);
     const int S = (int)min((long long)kStgMaxStages, room > 0 ? room / stage : 0);
     if (S >= 2) {
       const size_t smem = (size_t)S * stage + stg_ring_bytes(a.B);
