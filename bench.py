@@ -774,6 +774,12 @@ def wide_group_line(device, steps: int, warmup: int, peak: float, B: int = 32,
 
 # ------------------------------------------------------------ verify overhead
 
+def overhead_tokens(replays: int) -> int:
+    """Tokens one graph_overhead call appends to each measured request (at
+    most: a short step takes five times the rounds)."""
+    return 3 * (5 + 5 * replays) + 1
+
+
 def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
     """Cost of the page-tag check inside a whole step: two CUDA graphs of the
     same step structure, append -> verify -> split -> combine and append ->
@@ -815,10 +821,23 @@ def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
         for m in modes:
             graphs[m].replay()
     torch.cuda.synchronize()
+    # each round replays the three graphs in a rotated order (no mode always
+    # runs first after the round's start); short steps take more rounds
+    for m in modes:
+        graphs[m].replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graphs["none"].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if e0.elapsed_time(e1) < 0.5:
+        replays *= 5
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(replays)]
+    order = [[modes[(i + j) % 3] for j in range(3)] for i in range(replays)]
     for i in range(replays):
         ev[i][0].record()
-        for j, m in enumerate(modes):
+        for j, m in enumerate(order[i]):
             graphs[m].replay()
             ev[i][j + 1].record()
     torch.cuda.synchronize()
@@ -827,8 +846,11 @@ def graph_overhead(arm: "Arm", replays: int, B=None) -> dict:
     if int(arm.mask[:B].sum().item()) != 0:
         raise RuntimeError("verify overhead: a request was aborted with every tag valid")
     # every run of the body appended one token
-    arm.lens[:B] += len(modes) * (1 + 3 + replays)
-    t = {m: [e[j].elapsed_time(e[j + 1]) for e in ev] for j, m in enumerate(modes)}
+    arm.lens[:B] += len(modes) * (1 + 3 + 1 + replays) + 1
+    t = {m: [] for m in modes}
+    for i in range(replays):
+        for j, m in enumerate(order[i]):
+            t[m].append(ev[i][j].elapsed_time(ev[i][j + 1]))
     med = {m: statistics.median(t[m]) for m in modes}
     del graphs
     return {"workload": w.name, "requests": B, "replays": replays,
@@ -929,7 +951,7 @@ def skewed_lines(device, replays: int, steps: int, warmup: int, peak: float, par
     contexts, median 16k, up to 256k; 32 q / 4 kv heads, e4m3, page 16; about
     428k pages checked per step): the verify overhead with every tag valid,
     then the full step with its seeded stale tags (those requests abort)."""
-    w = wl.skewed(steps=3 * (replays + 8) + 3 * (steps + warmup) + 8)
+    w = wl.skewed(steps=overhead_tokens(replays) + 3 * (steps + warmup) + 8)
     stale = list(w.stale)
     w.stale = []  # every tag valid: both graphs attend the same requests
     arm = Arm(w, 0, device, 1 + 3 * (steps + warmup))
@@ -1350,7 +1372,7 @@ def main():
     B = args.requests
     sweep_pts = [b for b in (1, 8, 16, 32) if b < B]
     head_steps = 1 + 6 * (K + W) + 3 * len(sweep_pts) * (K + W)
-    over_steps = 0 if args.no_overhead else 2 * (3 * (4 + R) + 2)
+    over_steps = 0 if args.no_overhead else 2 * overhead_tokens(R) + 2
     w = wl.concurrency(B, seed=shard_seed(20264, rank))
     w.steps = head_steps + over_steps + 4
     w.num_pages = int(B * (-(-(131072 + w.steps) // 16))) + 64
