@@ -78,8 +78,9 @@ def test_step_join_leave_abort(dtype):
             counts[r] = 1
         victims = []
         if rnd in (2, 5) and active:
-            # round 2: a live request's partly filled last page went stale (an
-            # append that wrote first would have hit it); round 5: an inner page
+            # step 2 of the loop: a live request's partly filled last page went
+            # stale (an append that wrote first would have hit it); step 5: an
+            # inner page
             cand = sorted(active)
             part = [r for r in cand if b.sl_h[r] % 16 != 0 and b.sl_h[r] > 16]
             r = (part or cand)[0]
