@@ -163,3 +163,48 @@ def test_staged_and_register_kernels_agree_at_the_batch_limit(layout):
                              int(counts.max()), a.pt_h, a.et_h, a.sl_h)
     assert (st, stop) == (0, B)
     a.assert_state_equal()
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_staged_bulk_append_stops_at_a_stale_partial_page(layout):
+    """A bulk second call in which request 5's partly filled last page carries
+    a stale expected tag: the call serves requests 0-4, stops at 5 with
+    KV_ERR_TAG_MISMATCH (its index in ctl[KV_CTL_APPEND_STOP]) and leaves
+    request 5 and every later one untouched -- the same state as the oracle,
+    bit for bit."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    rng = np.random.default_rng(9300 + layout)
+    B = 12
+    if layout == 0:
+        P, H, Dk, Dv = 16, 8, 128, 128
+    else:
+        P, H, Dk, Dv = 64, 1, 576, 512
+    first = rng.integers(2 * P + 1, 5 * P, B)
+    first[first % P == 0] += 3                     # every request ends in a partial page
+    second = rng.integers(2 * P, 4 * P, B)
+    total = first + second
+    need = int((-(-total // P)).sum()) + 8
+    w = wl.Workload("stale_partial", 9300, total.astype(np.int32), 8 if layout == 0 else 16,
+                    H, Dk, Dv, P, 1, layout, need, float(np.float32(1 / np.sqrt(Dk))))
+    b = Both(w, 0)
+    g = torch.Generator(device="cuda").manual_seed(9300 + layout)
+
+    def rows(counts):
+        if layout == 0:
+            return ([_rows(g, int(c), H, Dk, [1.0]) for c in counts],
+                    [_rows(g, int(c), H, Dv, [1.0]) for c in counts])
+        ks = [_rows(g, int(c), None, Dk, [1.0]) for c in counts]
+        return ks, ks
+
+    st, stop = b.append(*rows(first), first)
+    assert (st, stop) == (0, B)
+    r, j = 5, int(first[5] // P)                   # request 5's partly filled page
+    b.et_h[r, j] = np.uint32(b.et_h[r, j]) - np.uint32(1)
+    b.et_d.copy_(torch.from_numpy(b.et_h.view(np.int32)))
+    st, stop = b.append(*rows(second), second)
+    assert (st, stop) == (oracle.ERR_TAG_MISMATCH, 5)
+    torch.cuda.synchronize()
+    assert b.dev.error() == kv.KV_ERR_TAG_MISMATCH
+    assert int(b.dev.ctl[kv.KV_CTL_APPEND_STOP].item()) == 5
+    b.assert_state_equal()
