@@ -10,7 +10,10 @@ Q and O counted, under `roofline.attn`).  The same line carries, under
 `roofline.points`, the other configurations: the 1..32-request points and the
 BF16 cache at 128k, the 32-request GQA batch (4k..32k), the skewed
 256-request stress step, the 96 q / 8 kv group, the latent tensor-core
-verify, the tag-check overhead and the bulk append.  `cpu_baseline` is the
+verify, the tag-check overhead (separate pass and fused), the bulk append and
+the handoff from a BF16 pool; each step line gives the attention's GB/s from
+CUDA events around an eager call and from its share of a CUDA-graph step
+(`frac_graph`).  `cpu_baseline` is the
 CPU oracle replaying sampled requests' first step, with the element-wise
 comparison of the GPU's outputs for those requests (`parity`).
 
