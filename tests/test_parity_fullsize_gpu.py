@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from pathrun import FullSize
 
@@ -128,3 +129,53 @@ def test_skewed_stress_steps_with_stale_tags():
     fs.assert_sampled_cache()
     assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == len(picks) * w.num_kv_heads
     assert fs.dev.error() == 0
+
+
+def test_one_call_step_at_the_headline_size():
+    """kv_decode_step -- tag check, append of one token per request, split-K
+    attention and combine in one call, as the benchmark's end-to-end line
+    runs it -- on 64 requests of 131,072 tokens (e4m3): bookkeeping of every
+    request and the abort mask bit-exact, cache bytes and attention output of
+    two sampled (request, kv head) pairs against the oracle."""
+    from pathrun import bf16_to_f64, close, gqa_oracle_attn
+
+    w = wl.concurrency(64)
+    w.steps = 2
+    fs = FullSize(w, 0, sample=[0, 37], heads=[3])
+    fs.fill(group=4)
+    B, dev = w.B, fs.dev
+    k, v = wl.step_rows(w, 0, device="cuda")
+    q = wl.queries(w, device="cuda")
+    ones = np.ones(B, np.int64)
+    ind = np.concatenate([[0], np.cumsum(ones)]).astype(np.int32)
+    out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), 7.0, dtype=torch.bfloat16,
+                     device="cuda")
+    mask = torch.full((B,), 0xEE, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(dev.step_workspace_size(B, w.num_q_heads, w.q_tokens), dtype=torch.uint8,
+                     device="cuda")
+    dev.step(B, w.num_q_heads, w.q_tokens, None, k.contiguous(), v.contiguous(),
+             torch.from_numpy(ind).cuda(), 1, fs.pt_d, fs.et_d, fs.sl_d, q, w.sm_scale, out,
+             mask, 0, ws)
+    # the oracle's side of the same step: every tag valid, so the check aborts
+    # nothing and the append serves every request
+    m_h = oracle.verify(fs.bk.num_pages, w.page_size, fs.bk.tags, fs.pt_h, fs.et_h, fs.sl_h)
+    assert not m_h.any()
+    st, stop = oracle.alloc(fs.bk, ind, 1, fs.pt_h, fs.et_h, fs.sl_h)
+    assert (st, stop) == (0, B)
+    for (r, h), (pool, pt, et, sl) in fs.twins.items():
+        s2, _ = oracle.append(pool, wl.bits_u16(k[r:r + 1, h:h + 1, :]),
+                              wl.bits_u16(v[r:r + 1, h:h + 1, :]), np.array([0, 1], np.int32),
+                              1, pt, et, sl)
+        assert s2 == 0
+    torch.cuda.synchronize()
+    assert dev.error() == 0
+    assert np.array_equal(mask.cpu().numpy(), m_h)
+    fs.assert_bookkeeping()
+    fs.assert_sampled_cache()
+    got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
+    G = w.num_q_heads // w.num_kv_heads
+    for (r, h), (pool, pt, et, sl) in fs.twins.items():
+        qs = wl.bits_u16(q[r:r + 1, :, h * G:(h + 1) * G, :].cpu())
+        ref = gqa_oracle_attn((pool, qs, pt, sl, w.sm_scale, G, w.q_tokens))
+        ok, mabs, mrel, _ = close(got[r, :, h * G:(h + 1) * G], ref)
+        assert ok, (r, h, mabs, mrel)
