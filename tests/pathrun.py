@@ -316,15 +316,25 @@ class FullSize:
                             self.et_h, self.sl_h)
         return m_d, m_h
 
-    def attn_check(self, q, abort_d, abort_h, sentinel=7.0):
-        """Attention on the device for the whole batch; oracle for the samples."""
+    def attn_check(self, q, abort_d, abort_h, sentinel=7.0, fused=False):
+        """Attention on the device for the whole batch; oracle for the samples.
+        fused: the call with the tag check inside its page reads
+        (paged_decode_attn_checked), whose abort mask must equal abort_h."""
         w, B = self.w, self.w.B
         out = torch.full((B, w.q_tokens, w.num_q_heads, w.head_dim_v), sentinel,
                          dtype=torch.bfloat16, device=self.device)
         ws = torch.empty(self.dev.workspace_size(B, w.num_q_heads, w.q_tokens), dtype=torch.uint8,
                          device=self.device)
-        self.dev.attn(B, w.num_q_heads, w.q_tokens, q, self.pt_d, self.sl_d, abort_d, w.sm_scale,
-                      out, ws)
+        if fused:
+            mask = torch.full((B,), 0xEE, dtype=torch.uint8, device=self.device)
+            self.kv.paged_decode_attn_checked(self.dev.handle, B, w.num_q_heads, w.q_tokens, q,
+                                              self.pt_d, self.et_d, self.sl_d, w.sm_scale, out,
+                                              mask, ws)
+            want = np.zeros(B, np.uint8) if abort_h is None else np.asarray(abort_h, np.uint8)
+            assert np.array_equal(mask.cpu().numpy(), want), "fused check's abort mask"
+        else:
+            self.dev.attn(B, w.num_q_heads, w.q_tokens, q, self.pt_d, self.sl_d, abort_d,
+                          w.sm_scale, out, ws)
         got = bf16_to_f64(out.cpu().view(torch.int16).numpy().view(np.uint16))
         G = w.num_q_heads // w.num_kv_heads
         qh = q.cpu()

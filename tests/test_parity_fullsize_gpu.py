@@ -105,7 +105,9 @@ def test_concurrency_128k_contexts(B, dtype):
 def test_skewed_stress_steps_with_stale_tags():
     """256 requests, lognormal contexts up to 256k; every step appends one
     token per request (pages come off a shuffled free list), then the tag
-    check and attention; the stale requests abort and are left untouched."""
+    check and attention; the stale requests abort and are left untouched.
+    The last step's attention runs twice: after the separate check, and with
+    the check fused into the page reads (paged_decode_attn_checked)."""
     w = wl.skewed(steps=4)
     rng = np.random.default_rng(5)
     live = [r for r in range(w.B) if r not in w.stale]
@@ -127,7 +129,11 @@ def test_skewed_stress_steps_with_stale_tags():
         torch.cuda.synchronize()
         fs.assert_bookkeeping()  # every step
     fs.assert_sampled_cache()
-    assert fs.attn_check(wl.queries(w, device="cuda"), m_d, m_h) == len(picks) * w.num_kv_heads
+    q = wl.queries(w, device="cuda")
+    assert fs.attn_check(q, m_d, m_h) == len(picks) * w.num_kv_heads
+    # the same step's attention with the check fused into its page reads:
+    # the same abort mask, the same outputs, the stale requests untouched
+    assert fs.attn_check(q, None, m_h, fused=True) == len(picks) * w.num_kv_heads
     assert fs.dev.error() == 0
 
 
