@@ -169,3 +169,31 @@ def test_handoff_full_gqa_batch_equals_append():
                  (a.k_scale, h.k_scale), (a.v_scale, h.v_scale), (a.k_cache, h.k_cache),
                  (a.v_cache, h.v_cache)):
         assert torch.equal(x, y)
+
+
+def test_handoff_full_latent_workload_equals_append():
+    """The whole latent workload (64 requests, 8k-64k rows of 576 values,
+    page 64): the handoff from a bf16 latent pool writes exactly what
+    kv_append_quantize of the same rows writes (same free list and tags),
+    codes, scales and bookkeeping alike."""
+    import paged_fp8_kv_append_gb300 as kv
+
+    w = wl.latent_verify()
+    ks = [wl.kv_rows(w, r, 0, int(w.lens[r]), device="cuda")[0] for r in range(w.B)]
+    src, spt, ssl = _source(w, ks, ks, check=False)
+    mk = lambda: kv.KVPool(w.num_pages, 64, 1, 576, 512, dtype=0, layout=1,  # noqa: E731
+                           device="cuda", tags=wl.initial_tags(w), free_list=wl.free_list(w))
+    tabs = lambda: (torch.full((w.B, w.max_pages), -1, dtype=torch.int32, device="cuda"),  # noqa: E731
+                    torch.zeros((w.B, w.max_pages), dtype=torch.int32, device="cuda"),
+                    torch.zeros(w.B, dtype=torch.int32, device="cuda"))
+    a, (apt, aet, asl) = mk(), tabs()
+    ind = torch.from_numpy(np.concatenate([[0], np.cumsum(w.lens)]).astype(np.int32)).cuda()
+    a.append(w.B, torch.cat(ks), None, ind, int(w.lens.max()), apt, aet, asl)
+    del ks
+    h, (hpt, het, hsl) = mk(), tabs()
+    h.append_from_pool(w.B, src, spt, ssl, hpt, het, hsl)
+    torch.cuda.synchronize()
+    assert a.error() == 0 and h.error() == 0
+    for x, y in ((apt, hpt), (aet, het), (asl, hsl), (a.tags, h.tags), (a.ctl, h.ctl),
+                 (a.k_scale, h.k_scale), (a.k_cache, h.k_cache)):
+        assert torch.equal(x, y)
